@@ -90,6 +90,7 @@ void tqo_quantize_group(const uint16_t* x, int n, uint8_t* codes,
         if (xi < mn) mn = xi;
         if (xi > mx) mx = xi;
     }
+    if (mn == 0.0f) mn = 0.0f;               /* a zero minimum is stored as +0 */
     volatile float range = mx - mn;          /* one binary32 subtraction */
     volatile float s32 = range / 15.0f;      /* one binary32 division */
     uint16_t sh = tqo_f32_to_f16(s32);

@@ -26,7 +26,9 @@
  *   - op order fixed for bit-exactness: min/max in fp32 (exact), r = fp32(max -
  *     min), s32 = fp32(r / 15), scale = fp16_rne(s32), bias = fp16(min) (exact),
  *     code = clamp(rint_rne(fp32(fp32(x - bias) / float(scale))), 0, 15), and
- *     code = 0 for every element when float(scale) == 0;
+ *     code = 0 for every element when float(scale) == 0; a group whose minimum
+ *     is zero stores bias +0 whatever the sign of its zeros (so that the bias
+ *     bits do not depend on the order in which the minimum is searched);
  *   - codes packed two per byte, element 2i in the low nibble of byte i;
  *   - dequantised value = (double)scale * code + (double)bias;
  *   - GQA: query head h reads KV head h / (Hq / Hkv);

@@ -156,6 +156,16 @@ def test_quantize_degenerate_groups():
     assert s == 0 and np.all(codes == 0) and b == 0
 
 
+def test_quantize_signed_zero_minimum_is_positive_zero():
+    # -0 and +0 both present at the minimum: the bias is +0 whichever comes first
+    for first in (-0.0, 0.0):
+        x = np.linspace(0, 3, 64).astype(np.float16)
+        x[0] = np.float16(first)
+        x[9] = np.float16(-first)
+        codes, s, b = oracle.quantize_group(x)
+        assert b == 0x0000 and codes[0] == 0 and codes[9] == 0
+
+
 def test_nibble_order_fixture():
     lines = [l.split() for l in open(os.path.join(GOLDEN, "nibble_order.txt"))
              if l.strip() and not l.startswith("#")]
