@@ -1,0 +1,210 @@
+/*
+ * tq.h -- C ABI of the int4 KV-cache decode path for NVIDIA GB300 (sm_103a).
+ *
+ * Two operations, as the pages describe the method:
+ *
+ *   quantize-on-store   fp16 K/V rows -> packed int4 codes + fp16 scale/bias,
+ *                       written in place into a preallocated cache
+ *                       ("turboquant-llama3.170B" README, decode-step listing:
+ *                        RoPE, then quantize K,V to int4, then fused sdpa_int4;
+ *                        "Fused int4 Attention for Gemma 4 31B", Background:
+ *                        MLX-style int4 with a per-group scale and bias).
+ *   fused decode attention (sdpa_int4)
+ *                       one query token per sequence attends over the int4
+ *                       cache; dequantisation happens in registers, softmax is
+ *                       online, the sequence is split into chunks (512 tokens by
+ *                       default) whose partial softmax states are merged by a
+ *                       log-sum-exp reduce ("turboquant-llama3.170B" README,
+ *                       kernel paragraph and split-K paragraph; Gemma page,
+ *                       "What I Built Instead": sdpa_int4(Q, K_int4, V_int4)).
+ *
+ * Conventions shared by every entry point
+ *   - All array pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates no device memory and keeps no per-call state between calls.
+ *   - fp16 values are passed as uint16_t holding IEEE binary16 bits.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream) and never synchronise the host.
+ *   - Host-side argument checks run before any launch and return a status;
+ *     nothing is launched when a check fails.  TQ_ERR_CUDA means a launch was
+ *     attempted and CUDA reported an error; tq_last_cuda_error() returns it.
+ *   - Kernels never trap.  Device-detected problems (a write position past the
+ *     cache capacity, a length outside [0, max_seq_len], a pipeline wait that
+ *     timed out) skip the offending work and OR a TQ_DEV_* bit into the
+ *     optional `status` word (device int32, may be NULL).  The caller zeroes it
+ *     when it wants to start afresh.
+ *   - Inputs containing NaN or Inf give unspecified (but finite-time) results.
+ *
+ * Cache layout (one cache = one attention layer), all row-major:
+ *   k_codes, v_codes  uint8  [batch][num_kv_heads][capacity][head_dim / 2]
+ *                     element 2i of a row is the low nibble of byte i
+ *                     (the Gemma page reads codes with masks 0xF, 0xF0, ...,
+ *                      low nibble first)
+ *   k_scale, k_bias,  fp16   [batch][num_kv_heads][capacity][head_dim / 64]
+ *   v_scale, v_bias          one (scale, bias) per group of 64 consecutive
+ *                            head_dim elements; value ~ scale * code + bias
+ * Requirements: head_dim in {64, 128, 256}; group_size == 64; capacity a
+ * positive multiple of 16; every array 16-byte aligned (256 recommended).
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TQ_ABI_VERSION 1
+#define TQ_GROUP_SIZE 64
+#define TQ_DEFAULT_CHUNK 512
+
+typedef enum tq_status {
+    TQ_OK = 0,
+    TQ_ERR_NULL = 1,        /* a required pointer is NULL */
+    TQ_ERR_SHAPE = 2,       /* inconsistent or out-of-range sizes */
+    TQ_ERR_CAPACITY = 3,    /* max_seq_len (or n_new) larger than the cache capacity */
+    TQ_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than required */
+    TQ_ERR_CUDA = 5,        /* CUDA reported an error (see tq_last_cuda_error) */
+    TQ_ERR_UNSUPPORTED = 6, /* head_dim / group / GQA ratio / impl not implemented */
+    TQ_ERR_ALIGN = 7        /* an array is not 16-byte (workspace: 256-byte) aligned */
+} tq_status;
+
+/* Bits ORed into the optional device status word. */
+#define TQ_DEV_WRITE_POS 0x1 /* append: write_pos[b] < 0 or write_pos[b] + n_new > capacity; rows skipped */
+#define TQ_DEV_SEQ_LEN 0x2   /* decode: seq_lens[b] < 0 or > max_seq_len; clamped into range */
+#define TQ_DEV_TIMEOUT 0x4   /* a pipeline wait exceeded its time limit; the CTA gave up */
+
+/* Decode implementations (tq_sdpa_int4_decode_impl and friends). */
+typedef enum tq_impl {
+    TQ_IMPL_AUTO = 0, /* the tensor-core path */
+    TQ_IMPL_MMA = 1,  /* mma.sync tensor-core tiles fed by TMA */
+    TQ_IMPL_SIMT = 2  /* CUDA-core fp32 path (comparison baseline) */
+} tq_impl;
+
+typedef struct tq_kv_cache {
+    uint8_t* k_codes;  /* [B][Hkv][cap][D/2] */
+    uint8_t* v_codes;  /* [B][Hkv][cap][D/2] */
+    uint16_t* k_scale; /* [B][Hkv][cap][D/64] fp16 */
+    uint16_t* k_bias;
+    uint16_t* v_scale;
+    uint16_t* v_bias;
+    int32_t batch;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t group_size; /* must be 64 */
+    int32_t capacity;   /* tokens per (sequence, kv head) */
+} tq_kv_cache;
+
+/* ABI version of the loaded library (TQ_ABI_VERSION it was built with). */
+int32_t tq_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* tq_status_string(tq_status s);
+
+/* The cudaError_t of the most recent TQ_ERR_CUDA on the calling host thread. */
+int32_t tq_last_cuda_error(void);
+
+/* Bytes of the six cache arrays together, each rounded up to 256 bytes, as
+ * laid out by tq_kv_cache_carve.  0 for invalid sizes.  Host-only. */
+size_t tq_kv_cache_bytes(int32_t batch, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t group_size, int32_t capacity);
+
+/* Point the six arrays of *cache into one caller-owned allocation `base` of
+ * at least tq_kv_cache_bytes(...) bytes (256-byte aligned), and fill in the
+ * sizes.  Order: k_codes, v_codes, k_scale, k_bias, v_scale, v_bias.
+ * Host-only (no device access). */
+tq_status tq_kv_cache_carve(tq_kv_cache* cache, void* base, int32_t batch,
+                            int32_t num_kv_heads, int32_t head_dim,
+                            int32_t group_size, int32_t capacity);
+
+/* Quantize-on-store.
+ * k_new, v_new: fp16 [batch][num_kv_heads][n_new][head_dim], contiguous.
+ * write_pos:    device int32 [batch]; token i of sequence b goes to cache row
+ *               write_pos[b] + i.  The caller advances its lengths afterwards.
+ * Per group of 64 elements x_0..x_63 (fp32 arithmetic, round-to-nearest-even):
+ *   mn, mx = min, max;  scale = fp16(fp32(mx - mn) / 15);  bias = fp16(mn)
+ *   code_i = clamp(rint(fp32(x_i - bias) / float(scale)), 0, 15), or 0 when
+ *   float(scale) == 0;  a zero minimum is stored as +0.
+ * Bit-identical to the CPU oracle.  Rows with an out-of-range write position
+ * are skipped and TQ_DEV_WRITE_POS is set. */
+tq_status tq_quantize_kv_append(const tq_kv_cache* cache, const uint16_t* k_new,
+                                const uint16_t* v_new, int32_t n_new,
+                                const int32_t* write_pos, int32_t* status,
+                                void* stream);
+
+/* Workspace bytes tq_sdpa_int4_decode needs for these sizes (an upper bound
+ * that does not depend on the device).  Host-only. */
+size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t num_q_heads,
+                               int32_t head_dim, int32_t max_seq_len,
+                               int32_t chunk);
+
+/* Fused int4 decode attention (Sq = 1, GQA).
+ * q:        fp16 [batch][num_q_heads][head_dim]; query head h reads KV head
+ *           h / (num_q_heads / num_kv_heads)  (num_q_heads / num_kv_heads <= 8)
+ * seq_lens: device int32 [batch]; sequence b attends to cache rows
+ *           [0, seq_lens[b]); 0 gives an all-zero output row
+ * max_seq_len: host bound on seq_lens (1 <= max_seq_len <= capacity); sizes the grid
+ * attn_scale: multiplies q.k (1/sqrt(head_dim) for Llama, 1.0 for Gemma)
+ * chunk:    split-K chunk in tokens (multiple of 16; TQ_DEFAULT_CHUNK = 512).
+ *           Each CTA takes a run of whole chunks and keeps one running softmax
+ *           state over them; the runs' states are merged by a log-sum-exp reduce.
+ * workspace: device scratch (256-byte aligned) of at least
+ *           tq_sdpa_workspace_bytes(...) bytes holding the fp32 partial states;
+ *           contents on entry are ignored.
+ * out:      fp16 [batch][num_q_heads][head_dim], round-to-nearest-even.
+ * Accumulation is fp32; result within 2e-3 abs / 1e-3 rel-L2 of fp64 attention
+ * over the dequantised cache. */
+tq_status tq_sdpa_int4_decode(const tq_kv_cache* cache, const uint16_t* q,
+                              int32_t num_q_heads, const int32_t* seq_lens,
+                              int32_t max_seq_len, float attn_scale,
+                              int32_t chunk, void* workspace,
+                              size_t workspace_bytes, uint16_t* out,
+                              int32_t* status, void* stream);
+
+/* Same as tq_sdpa_int4_decode with an explicit implementation choice. */
+tq_status tq_sdpa_int4_decode_impl(const tq_kv_cache* cache, const uint16_t* q,
+                                   int32_t num_q_heads, const int32_t* seq_lens,
+                                   int32_t max_seq_len, float attn_scale,
+                                   int32_t chunk, void* workspace,
+                                   size_t workspace_bytes, uint16_t* out,
+                                   int32_t* status, tq_impl impl, void* stream);
+
+/* The split plan tq_sdpa_int4_decode uses on the current device: each CTA
+ * takes *chunks_per_split consecutive chunks, and there are *n_splits runs per
+ * (sequence, kv head).  Host-side query (reads device attributes). */
+tq_status tq_sdpa_plan(const tq_kv_cache* cache, int32_t num_q_heads,
+                       int32_t max_seq_len, int32_t chunk, tq_impl impl,
+                       int32_t* chunks_per_split, int32_t* n_splits);
+
+/* Split-K phase 1 alone ("turboquant-llama3.170B" README, split-K paragraph:
+ * Phase 1 = partial attention over 512-token chunks processed in parallel).
+ * Each part covers `chunks_per_split` consecutive chunks (1 = one state per
+ * chunk, the pages' form; 0 = the plan tq_sdpa_int4_decode uses).  With
+ * np = ceil(ceil(max_seq_len / chunk) / chunks_per_split) parts, fp32 outputs:
+ *   part_m   [batch][num_q_heads][np]  max over the part of the scaled score
+ *            (natural-log units; -inf for an empty part)
+ *   part_l   [batch][num_q_heads][np]  sum of exp(score - m)  (0 if empty)
+ *   part_acc [batch][num_q_heads][np][head_dim]  sum of exp(score - m) * v
+ * Parts past seq_lens[b] are empty.  Arrays must hold np entries per (b, h). */
+tq_status tq_sdpa_int4_partial(const tq_kv_cache* cache, const uint16_t* q,
+                               int32_t num_q_heads, const int32_t* seq_lens,
+                               int32_t max_seq_len, float attn_scale,
+                               int32_t chunk, int32_t chunks_per_split,
+                               float* part_m, float* part_l, float* part_acc,
+                               int32_t* status, tq_impl impl, void* stream);
+
+/* Split-K phase 2 alone ("Phase 2 (reduce)" of the same paragraph): per (b, h),
+ *   M = max over parts with l > 0 of m,  w_c = exp(m_c - M),
+ *   out = sum_c w_c acc_c / sum_c w_c l_c   (fp16, RNE; all-empty rows -> 0).
+ * Inputs laid out as tq_sdpa_int4_partial writes them, n_parts per (b, h),
+ * 1 <= n_parts <= 12288. */
+tq_status tq_sdpa_int4_reduce(const float* part_m, const float* part_l,
+                              const float* part_acc, int32_t batch,
+                              int32_t num_q_heads, int32_t head_dim,
+                              int32_t n_parts, uint16_t* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TQ_H */

@@ -1,0 +1,263 @@
+"""int4 KV-cache quantize-on-store and fused decode attention for GB300.
+
+Thin Python binding over the C-ABI library ``libtq.so`` (see include/tq.h):
+argument marshalling only.  Every step of the path runs in the library's CUDA
+kernels; PyTorch supplies device memory and the current stream.  There is no
+fallback: if the compiled library is missing, every entry point raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "TQ_OK", "TQ_IMPL_AUTO", "TQ_IMPL_MMA", "TQ_IMPL_SIMT", "TQ_DEV_WRITE_POS", "TQ_DEV_SEQ_LEN",
+    "TQ_DEV_TIMEOUT", "TQError", "lib", "lib_path", "tq_kv_cache", "KVCache",
+    "tq_abi_version", "tq_status_string", "tq_kv_cache_bytes", "tq_sdpa_workspace_bytes",
+    "tq_quantize_kv_append", "tq_sdpa_int4_decode", "tq_sdpa_int4_partial", "tq_sdpa_int4_reduce",
+    "tq_sdpa_plan",
+]
+
+TQ_OK = 0
+TQ_IMPL_AUTO, TQ_IMPL_MMA, TQ_IMPL_SIMT = 0, 1, 2
+TQ_DEV_WRITE_POS, TQ_DEV_SEQ_LEN, TQ_DEV_TIMEOUT = 0x1, 0x2, 0x4
+GROUP_SIZE = 64
+DEFAULT_CHUNK = 512
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "_build", "libtq.so")
+
+
+class TQError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        msg = lib().tq_status_string(status).decode()
+        if status == 5:
+            msg += f" (cudaError {lib().tq_last_cuda_error()})"
+        super().__init__(f"{fn}: {msg} [status {status}]")
+        self.status = status
+
+
+class tq_kv_cache(ctypes.Structure):
+    _fields_ = [
+        ("k_codes", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
+        ("k_scale", ctypes.c_void_p), ("k_bias", ctypes.c_void_p),
+        ("v_scale", ctypes.c_void_p), ("v_bias", ctypes.c_void_p),
+        ("batch", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("group_size", ctypes.c_int32),
+        ("capacity", ctypes.c_int32),
+    ]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libtq.so (built by ``build.build()``); raises if it is not there."""
+    global _lib
+    if _lib is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise ImportError(f"libtq.so not built ({path}); run int4_kv_cache_gb300.build.build()")
+        L = ctypes.CDLL(path)
+        P, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+        C = ctypes.POINTER(tq_kv_cache)
+        sig = {
+            "tq_abi_version": ([], i32),
+            "tq_status_string": ([i32], ctypes.c_char_p),
+            "tq_last_cuda_error": ([], i32),
+            "tq_kv_cache_bytes": ([i32] * 5, sz),
+            "tq_kv_cache_carve": ([C, P, i32, i32, i32, i32, i32], i32),
+            "tq_quantize_kv_append": ([C, P, P, i32, P, P, P], i32),
+            "tq_sdpa_workspace_bytes": ([i32] * 5, sz),
+            "tq_sdpa_int4_decode": ([C, P, i32, P, i32, f32, i32, P, sz, P, P, P], i32),
+            "tq_sdpa_int4_decode_impl": ([C, P, i32, P, i32, f32, i32, P, sz, P, P, i32, P], i32),
+            "tq_sdpa_plan": ([C, i32, i32, i32, i32, P, P], i32),
+            "tq_sdpa_int4_partial": ([C, P, i32, P, i32, f32, i32, i32, P, P, P, P, i32, P], i32),
+            "tq_sdpa_int4_reduce": ([P, P, P, i32, i32, i32, i32, P, P], i32),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        if L.tq_abi_version() != 1:
+            raise ImportError("libtq.so ABI version mismatch")
+        _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != TQ_OK:
+        raise TQError(fn, status)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream]):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str) -> None:
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor, got {t.dtype} on {t.device}")
+
+
+# ------------------------------------------------------------------ host-only
+def tq_abi_version() -> int:
+    return int(lib().tq_abi_version())
+
+
+def tq_status_string(status: int) -> str:
+    return lib().tq_status_string(status).decode()
+
+
+def tq_kv_cache_bytes(batch: int, num_kv_heads: int, head_dim: int, group_size: int, capacity: int) -> int:
+    return int(lib().tq_kv_cache_bytes(batch, num_kv_heads, head_dim, group_size, capacity))
+
+
+def tq_sdpa_workspace_bytes(batch: int, num_q_heads: int, head_dim: int, max_seq_len: int,
+                            chunk: int = DEFAULT_CHUNK) -> int:
+    return int(lib().tq_sdpa_workspace_bytes(batch, num_q_heads, head_dim, max_seq_len, chunk))
+
+
+# ------------------------------------------------------------------ the cache
+class KVCache:
+    """One layer's int4 cache in a single device allocation (torch uint8).
+
+    Views: k_codes/v_codes uint8 [B, Hkv, cap, D/2]; k_scale/k_bias/v_scale/v_bias
+    fp16 [B, Hkv, cap, D/64].  ``struct`` is the tq_kv_cache handed to the ABI.
+    """
+
+    def __init__(self, batch: int, num_kv_heads: int, head_dim: int, capacity: int,
+                 device=None, group_size: int = GROUP_SIZE):
+        nbytes = tq_kv_cache_bytes(batch, num_kv_heads, head_dim, group_size, capacity)
+        if nbytes == 0:
+            raise ValueError("invalid cache sizes")
+        self.buffer = torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+        self.struct = tq_kv_cache()
+        _check("tq_kv_cache_carve", lib().tq_kv_cache_carve(ctypes.byref(self.struct), _ptr(self.buffer), batch,
+                                                             num_kv_heads, head_dim, group_size, capacity))
+        self.batch, self.num_kv_heads, self.head_dim, self.capacity = batch, num_kv_heads, head_dim, capacity
+        self.group_size = group_size
+        base = self.buffer.data_ptr()
+        rows = batch * num_kv_heads * capacity
+        ng = head_dim // group_size
+
+        def view(addr, n, dtype, shape):
+            off = addr - base
+            nb = n * torch.empty((), dtype=dtype).element_size()
+            return self.buffer[off: off + nb].view(dtype).view(shape)
+
+        cs = (batch, num_kv_heads, capacity, head_dim // 2)
+        ss = (batch, num_kv_heads, capacity, ng)
+        s = self.struct
+        self.k_codes = view(s.k_codes, rows * head_dim // 2, torch.uint8, cs)
+        self.v_codes = view(s.v_codes, rows * head_dim // 2, torch.uint8, cs)
+        self.k_scale = view(s.k_scale, rows * ng, torch.float16, ss)
+        self.k_bias = view(s.k_bias, rows * ng, torch.float16, ss)
+        self.v_scale = view(s.v_scale, rows * ng, torch.float16, ss)
+        self.v_bias = view(s.v_bias, rows * ng, torch.float16, ss)
+
+    @property
+    def nbytes(self) -> int:
+        return self.buffer.numel()
+
+    def ref(self):
+        return ctypes.byref(self.struct)
+
+
+# ------------------------------------------------------------------ device ops
+def tq_quantize_kv_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, write_pos: torch.Tensor,
+                          status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Quantize k_new/v_new [B, Hkv, n_new, D] fp16 into cache rows write_pos[b] + i."""
+    _need(k_new, torch.float16, "k_new")
+    _need(v_new, torch.float16, "v_new")
+    _need(write_pos, torch.int32, "write_pos")
+    if status is not None:
+        _need(status, torch.int32, "status")
+    n_new = k_new.shape[2] if k_new.dim() == 4 else 0
+    if tuple(k_new.shape) != (cache.batch, cache.num_kv_heads, n_new, cache.head_dim) or v_new.shape != k_new.shape:
+        raise ValueError(f"k_new/v_new must be [B, Hkv, n_new, D]; got {tuple(k_new.shape)}")
+    _check("tq_quantize_kv_append", lib().tq_quantize_kv_append(cache.ref(), _ptr(k_new), _ptr(v_new), n_new,
+                                                                _ptr(write_pos), _ptr(status), _stream(stream)))
+
+
+def tq_sdpa_int4_decode(cache: KVCache, q: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                        attn_scale: float, workspace: torch.Tensor, out: Optional[torch.Tensor] = None,
+                        chunk: int = DEFAULT_CHUNK, status: Optional[torch.Tensor] = None,
+                        impl: int = TQ_IMPL_AUTO, stream=None) -> torch.Tensor:
+    """Fused int4 decode attention; q [B, Hq, D] fp16 -> out [B, Hq, D] fp16."""
+    _need(q, torch.float16, "q")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(workspace, torch.uint8, "workspace")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.float16, "out")
+    if status is not None:
+        _need(status, torch.int32, "status")
+    if q.dim() != 3 or q.shape[0] != cache.batch or q.shape[2] != cache.head_dim or out.shape != q.shape:
+        raise ValueError(f"q must be [B, Hq, D]; got {tuple(q.shape)}")
+    _check("tq_sdpa_int4_decode", lib().tq_sdpa_int4_decode_impl(
+        cache.ref(), _ptr(q), q.shape[1], _ptr(seq_lens), int(max_seq_len), float(attn_scale), int(chunk),
+        _ptr(workspace), workspace.numel(), _ptr(out), _ptr(status), int(impl), _stream(stream)))
+    return out
+
+
+def tq_sdpa_plan(cache: KVCache, num_q_heads: int, max_seq_len: int, chunk: int = DEFAULT_CHUNK,
+                 impl: int = TQ_IMPL_AUTO):
+    """(chunks_per_split, n_splits) that tq_sdpa_int4_decode uses on this device."""
+    cps, ns = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check("tq_sdpa_plan", lib().tq_sdpa_plan(cache.ref(), num_q_heads, int(max_seq_len), int(chunk), int(impl),
+                                              ctypes.byref(cps), ctypes.byref(ns)))
+    return cps.value, ns.value
+
+
+def tq_sdpa_int4_partial(cache: KVCache, q: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                         attn_scale: float, chunk: int = DEFAULT_CHUNK, chunks_per_split: int = 1,
+                         status: Optional[torch.Tensor] = None, impl: int = TQ_IMPL_AUTO, stream=None,
+                         out=None):
+    """Phase 1 alone: (m, l, acc) fp32 per part of ``chunks_per_split`` chunks
+    (1 = per chunk; 0 = the decode plan), m in natural-log units."""
+    _need(q, torch.float16, "q")
+    _need(seq_lens, torch.int32, "seq_lens")
+    B, Hq, D = q.shape
+    nc = max(1, math.ceil(max_seq_len / chunk))
+    cps = chunks_per_split if chunks_per_split > 0 else tq_sdpa_plan(cache, Hq, max_seq_len, chunk, impl)[0]
+    n_parts = math.ceil(nc / cps)
+    if out is None:
+        m = torch.empty((B, Hq, n_parts), dtype=torch.float32, device=q.device)
+        l = torch.empty_like(m)
+        acc = torch.empty((B, Hq, n_parts, D), dtype=torch.float32, device=q.device)
+    else:
+        m, l, acc = out
+        if m.numel() < B * Hq * n_parts or acc.numel() < B * Hq * n_parts * D:
+            raise ValueError("partial output buffers too small")
+    _check("tq_sdpa_int4_partial", lib().tq_sdpa_int4_partial(
+        cache.ref(), _ptr(q), Hq, _ptr(seq_lens), int(max_seq_len), float(attn_scale), int(chunk), int(cps),
+        _ptr(m), _ptr(l), _ptr(acc), _ptr(status), int(impl), _stream(stream)))
+    return m, l, acc
+
+
+def tq_sdpa_int4_reduce(m: torch.Tensor, l: torch.Tensor, acc: torch.Tensor, out: Optional[torch.Tensor] = None,
+                        stream=None) -> torch.Tensor:
+    """Phase 2 alone: LSE merge of [B, Hq, n] partials -> fp16 [B, Hq, D]."""
+    for t, n in ((m, "m"), (l, "l"), (acc, "acc")):
+        _need(t, torch.float32, n)
+    B, Hq, n, D = acc.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float16, device=acc.device)
+    _need(out, torch.float16, "out")
+    _check("tq_sdpa_int4_reduce", lib().tq_sdpa_int4_reduce(_ptr(m), _ptr(l), _ptr(acc), B, Hq, D, n, _ptr(out),
+                                                            _stream(stream)))
+    return out

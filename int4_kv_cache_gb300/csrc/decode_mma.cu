@@ -1,0 +1,530 @@
+// decode_mma.cu -- split-K phase 1 of int4 decode attention on tensor cores.
+//
+// What it computes ("turboquant-llama3.170B" README, kernel + split-K
+// paragraphs; "Fused int4 Attention for Gemma 4 31B", What I Built Instead):
+// for one sequence b, one kv head and a run of whole chunks, the partial
+// softmax state of every query head of the GQA group,
+//     m = max_t s_t,  l = sum_t e^{s_t - m},  acc = sum_t e^{s_t - m} v_t,
+// with s_t = attn_scale * q . k_t and k_t, v_t the dequantised cache rows
+// (scale * code + bias per group of 64).  Dequantisation happens only in
+// registers; no float K/V and no score matrix is written anywhere.
+//
+// GB300 design (not the Metal kernel's):
+//  * A producer warp streams each tile (T tokens) of K codes, V codes and the
+//    four fp16 scale/bias arrays into a ring of shared-memory stages: the code
+//    tiles by 2-D TMA with the 128-byte swizzle, the scale/bias rows by 1-D
+//    bulk copies, completion on mbarriers.  Every byte of the cache is read
+//    from HBM once per step, with an evict-first L2 policy.
+//  * Consumer warps turn the nibbles into fp16 operands with one AND per
+//    register: a 4-bit code n in the low mantissa bits of a zero-exponent fp16
+//    is the subnormal n * 2^-24, and the high nibble of a byte gives
+//    16 n * 2^-24, so no integer->float conversion instruction is needed.
+//  * The grouped scores use mma.sync m16n8k16 with M = 16 tokens, N = the 8
+//    query heads of the GQA group (all heads share one read of K), K = 16
+//    head_dim elements; each 64-element group accumulates separately so its
+//    scale and bias are applied afterwards in fp32:
+//        s_t = attn * sum_g (scale_tg * sum_{d in g} q_d n_td + bias_tg * sum_{d in g} q_d).
+//    The high-nibble elements meet q/16 in the B operand (the pages' qdot
+//    "pre-divide the query" idea), so all products carry the same 2^-24.
+//  * P.V uses mma.sync with M = 16 head_dim elements, N = 8 heads, K = 16
+//    tokens.  B = (p_t * vscale_tg) in fp16, built from the score fragments
+//    with movmatrix (no shared-memory round trip); the bias part
+//    sum_t p_t * vbias_tg is accumulated in fp32 on the side.
+//  * Token order inside a 16-token tile and the head_dim order inside each
+//    operand are chosen so that every ldmatrix is bank-conflict free against
+//    the swizzled tile; the permutation is undone when the state is written.
+#include <math.h>
+
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+
+namespace {
+
+constexpr uint32_t kLoNib = 0x000F000Fu;  // nibbles at bits 0..3 / 16..19 -> n * 2^-24
+constexpr uint32_t kHiNib = 0x00F000F0u;  // nibbles at bits 4..7 / 20..23 -> 16 n * 2^-24
+
+template <int D>
+struct Cfg {
+    static constexpr int NG = D / kGroup;          // scale/bias groups per row
+    static constexpr int BPT = D / 2;              // code bytes per token
+    static constexpr int SPT = BPT / 16;           // 16-byte segments per token
+    static constexpr int TPR = 128 / BPT;          // tokens per 128-byte swizzle row (D=256: 1)
+    static constexpr int NWC = 4;                  // consumer warps
+    static constexpr int MT = (D == 256) ? 1 : 2;  // 16-token m-tiles per warp per stage
+    static constexpr int T = NWC * MT * 16;        // tokens per stage
+    static constexpr int STAGES = 4;
+    static constexpr int CODE_BYTES = T * BPT;     // one code tile (K or V)
+    static constexpr int SB_BYTES = T * NG * 2;    // one scale or bias tile
+    static constexpr int STAGE_BYTES = ((2 * CODE_BYTES + 4 * SB_BYTES + 1023) / 1024) * 1024;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // +1024 for base alignment
+    static constexpr int THREADS = (NWC + 1) * 32;
+    static constexpr int NKS = D / 16;             // k-steps of the score MMA = m-tiles of P.V
+    static constexpr bool EVEN_ODD = D <= 128;     // token order inside a 16-token tile
+    static_assert(CODE_BYTES % 1024 == 0, "code tiles must keep the 1024-byte swizzle period");
+    static_assert(STAGES * STAGE_BYTES >= NWC * 8 * D * 4, "merge buffer must fit in the stages");
+};
+
+// Token (within a 16-token tile) held by fragment row m.  For D <= 128 rows
+// 0..7 take the even tokens and rows 8..15 the odd ones, so that the eight
+// rows of every ldmatrix fall into eight different 16-byte bank groups of the
+// swizzled tile and a C-fragment row pair (m, m+8) is two adjacent tokens.
+template <int D>
+__device__ __forceinline__ int tok_of_row(int m) {
+    if constexpr (Cfg<D>::EVEN_ODD) return m < 8 ? 2 * m : 2 * (m - 8) + 1;
+    else return m;
+}
+
+// Shared address of 16-byte segment `seg` of token `tok` in a code tile laid
+// out by a TMA box of 128-byte rows with CU_TENSOR_MAP_SWIZZLE_128B.
+template <int D>
+__device__ __forceinline__ uint32_t code_addr(uint32_t tile, int tok, int seg) {
+    using C = Cfg<D>;
+    const int row = tok / C::TPR;
+    const int chunk = (tok % C::TPR) * C::SPT + seg;
+    return tile + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+struct alignas(8) Half4 {
+    __half2 a, b;
+};
+
+// NG fp16 values of one token row -> floats.
+template <int NG>
+__device__ __forceinline__ void load_row_sb(const uint16_t* base, int tok, float (&out)[NG]) {
+    const uint16_t* p = base + tok * NG;
+    if constexpr (NG == 1) {
+        out[0] = __half2float(__ushort_as_half(p[0]));
+    } else if constexpr (NG == 2) {
+        const __half2 h = *reinterpret_cast<const __half2*>(p);
+        out[0] = __low2float(h);
+        out[1] = __high2float(h);
+    } else {
+        const Half4 h = *reinterpret_cast<const Half4*>(p);
+        out[0] = __low2float(h.a);
+        out[1] = __high2float(h.a);
+        out[2] = __low2float(h.b);
+        out[3] = __high2float(h.b);
+    }
+}
+
+__device__ __forceinline__ int clamp_len(const DecodeParams& p, int b) {
+    int len = __ldg(p.seq_lens + b);
+    if (len < 0 || len > p.max_seq_len) {
+        if (p.status != nullptr && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+            atomicOr(p.status, TQ_DEV_SEQ_LEN);
+        len = min(max(len, 0), p.max_seq_len);
+    }
+    return len;
+}
+
+template <int D>
+__global__ void __launch_bounds__(Cfg<D>::THREADS)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const DecodeParams p) {
+    using C = Cfg<D>;
+    constexpr int NG = C::NG;
+    __shared__ uint64_t full_bar[C::STAGES];
+    __shared__ uint64_t empty_bar[C::STAGES];
+    __shared__ int abort_flag;
+    __shared__ float mrg_m[C::NWC][8], mrg_l[C::NWC][8];
+    extern __shared__ uint8_t dyn_smem[];
+    const uint32_t dyn_base = smem_u32(dyn_smem);
+    uint8_t* smem = dyn_smem + ((1024u - (dyn_base & 1023u)) & 1023u);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int G = p.group_q;
+    const int len = clamp_len(p, b);
+    const int t_begin = split * p.split_tokens;
+    const int t_end = min(t_begin + p.split_tokens, len);
+    const int n_tiles = t_end > t_begin ? (t_end - t_begin + C::T - 1) / C::T : 0;
+    const long long bh = static_cast<long long>(b) * p.num_kv_heads + kvh;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], C::NWC);
+        }
+        abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == C::NWC) {
+        // ------------------------------------------------------ producer warp
+        if (lane == 0 && n_tiles > 0) {
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+            const uint64_t policy = policy_evict_first();
+            const long long row_base = bh * p.capacity;  // cache row of token 0
+            int issued = 0;
+            for (int it = 0; it < n_tiles; ++it) {
+                const int stage = it % C::STAGES;
+                if (it >= C::STAGES) {
+                    if (!mbar_wait_bounded(&empty_bar[stage], ((it / C::STAGES) - 1) & 1)) {
+                        atomicExch(&abort_flag, 1);
+                        if (p.status) atomicOr(p.status, TQ_DEV_TIMEOUT);
+                        break;
+                    }
+                }
+                if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
+                const int t0 = t_begin + it * C::T;
+                const int avail = min(C::T, p.capacity - t0);  // rows left in this (b, kv head)
+                const uint32_t sb_bytes = static_cast<uint32_t>(avail) * NG * 2;
+                uint8_t* st = smem + stage * C::STAGE_BYTES;
+                mbar_arrive_expect_tx(&full_bar[stage], 2 * C::CODE_BYTES + 4 * sb_bytes);
+                const int y = static_cast<int>(((row_base + t0) * C::BPT) / 128);
+                tma_load_2d(st, &tm_k, 0, y, &full_bar[stage], policy);
+                tma_load_2d(st + C::CODE_BYTES, &tm_v, 0, y, &full_bar[stage], policy);
+                const long long sb_off = (row_base + t0) * NG;
+                uint8_t* sb = st + 2 * C::CODE_BYTES;
+                bulk_load(sb + 0 * C::SB_BYTES, p.k_scale + sb_off, sb_bytes, &full_bar[stage], policy);
+                bulk_load(sb + 1 * C::SB_BYTES, p.k_bias + sb_off, sb_bytes, &full_bar[stage], policy);
+                bulk_load(sb + 2 * C::SB_BYTES, p.v_scale + sb_off, sb_bytes, &full_bar[stage], policy);
+                bulk_load(sb + 3 * C::SB_BYTES, p.v_bias + sb_off, sb_bytes, &full_bar[stage], policy);
+                issued = it + 1;
+            }
+            // Do not leave while copies into this CTA's shared memory may be in
+            // flight: wait (bounded) for the fills of the last issued stages.
+            for (int it = max(0, issued - C::STAGES); it < issued; ++it)
+                mbar_wait_bounded(&full_bar[it % C::STAGES], (it / C::STAGES) & 1, 200000000ull);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumer warps
+    const int gid = lane >> 2, tig = lane & 3;
+    const float sl2 = p.score_scale_log2;
+
+    // Q operands: head gid of the group (zero rows pad G up to 8).
+    uint32_t qb[C::NKS][2];
+    float qsum_own[NG];
+    {
+        const bool hv = gid < G;
+        const uint16_t* qrow = p.q + (static_cast<long long>(b) * p.num_q_heads + kvh * G + (hv ? gid : 0)) * D;
+        const __half sixteenth = __float2half_rn(0.0625f);
+#pragma unroll
+        for (int g = 0; g < NG; ++g) qsum_own[g] = 0.0f;
+#pragma unroll
+        for (int s = 0; s < C::SPT; ++s) {
+            uint4 raw = hv ? *reinterpret_cast<const uint4*>(qrow + 32 * s + 8 * tig) : make_uint4(0, 0, 0, 0);
+            const __half* h = reinterpret_cast<const __half*>(&raw);
+            // k-step (s,0): k=2tig,2tig+1 <- dims +0,+4 ; k=2tig+8,+9 <- dims +1,+5 (x 1/16)
+            qb[2 * s][0] = pack_half2_bits(h[0], h[4]);
+            qb[2 * s][1] = pack_half2_bits(__hmul(h[1], sixteenth), __hmul(h[5], sixteenth));
+            // k-step (s,1): dims +2,+6 ; +3,+7 (x 1/16)
+            qb[2 * s + 1][0] = pack_half2_bits(h[2], h[6]);
+            qb[2 * s + 1][1] = pack_half2_bits(__hmul(h[3], sixteenth), __hmul(h[7], sixteenth));
+            float part = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) part += __half2float(h[j]);
+            qsum_own[(32 * s) / kGroup] += part;
+        }
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            qsum_own[g] += __shfl_xor_sync(0xffffffffu, qsum_own[g], 1);
+            qsum_own[g] += __shfl_xor_sync(0xffffffffu, qsum_own[g], 2);
+        }
+    }
+    // bias coefficients for this thread's two C columns (heads 2tig, 2tig+1), log2 units
+    float qs_l2[NG][2];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+        qs_l2[g][0] = __shfl_sync(0xffffffffu, qsum_own[g], (2 * tig) * 4) * sl2;
+        qs_l2[g][1] = __shfl_sync(0xffffffffu, qsum_own[g], (2 * tig + 1) * 4) * sl2;
+    }
+    const float k_coef = sl2 * 16777216.0f;  // undo the 2^-24 of the subnormal operands
+    const int r0 = tok_of_row<D>(gid), r1 = tok_of_row<D>(gid + 8);
+
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.0f, 0.0f};
+    float e_run[NG][2];
+    float acc[C::NKS][4];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) e_run[g][0] = e_run[g][1] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < C::NKS; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+
+    // ldmatrix row address pattern: lane -> (matrix, row)
+    const int lm_mat = lane >> 3, lm_row = lane & 7;
+    const int lm_tok = tok_of_row<D>((lm_mat & 1) * 8 + lm_row);  // token within the 16-token tile
+    const int lm_seg = lm_mat >> 1;                                // first or second segment
+
+    for (int it = 0; it < n_tiles; ++it) {
+        const int stage = it % C::STAGES;
+        if (!mbar_wait_bounded(&full_bar[stage], (it / C::STAGES) & 1)) {
+            if (p.status) atomicOr(p.status, TQ_DEV_TIMEOUT);
+            atomicExch(&abort_flag, 1);
+            break;
+        }
+        const int t0 = t_begin + it * C::T;
+        const uint8_t* st = smem + stage * C::STAGE_BYTES;
+        const uint32_t kc_s = smem_u32(st);
+        const uint32_t vc_s = smem_u32(st + C::CODE_BYTES);
+        const uint16_t* ks_s = reinterpret_cast<const uint16_t*>(st + 2 * C::CODE_BYTES);
+        const uint16_t* kb_s = ks_s + C::SB_BYTES / 2;
+        const uint16_t* vs_s = kb_s + C::SB_BYTES / 2;
+        const uint16_t* vb_s = vs_s + C::SB_BYTES / 2;
+
+        // ---- scores of this warp's m-tiles (log2 units)
+        float sc[C::MT][4];
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+            const int tb = (warp * C::MT + mt) * 16;
+            float cg[NG][4];
+#pragma unroll
+            for (int g = 0; g < NG; ++g) cg[g][0] = cg[g][1] = cg[g][2] = cg[g][3] = 0.0f;
+#pragma unroll
+            for (int sp = 0; sp < C::SPT / 2; ++sp) {
+                uint32_t x0, x1, x2, x3;
+                ldmatrix_x4(code_addr<D>(kc_s, tb + lm_tok, 2 * sp + lm_seg), x0, x1, x2, x3);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int s = 2 * sp + e;
+                    const int g = (32 * s) / kGroup;
+                    const uint32_t xa = e ? x2 : x0;  // rows 0..7
+                    const uint32_t xb = e ? x3 : x1;  // rows 8..15
+                    mma_16816(cg[g], xa & kLoNib, xb & kLoNib, xa & kHiNib, xb & kHiNib, qb[2 * s][0], qb[2 * s][1]);
+                    const uint32_t ya = xa >> 8, yb = xb >> 8;
+                    mma_16816(cg[g], ya & kLoNib, yb & kLoNib, ya & kHiNib, yb & kHiNib, qb[2 * s + 1][0],
+                              qb[2 * s + 1][1]);
+                }
+            }
+            float ksa[NG], kba[NG], ksb[NG], kbb[NG];
+            load_row_sb<NG>(ks_s, tb + r0, ksa);
+            load_row_sb<NG>(kb_s, tb + r0, kba);
+            load_row_sb<NG>(ks_s, tb + r1, ksb);
+            load_row_sb<NG>(kb_s, tb + r1, kbb);
+            const bool va = t0 + tb + r0 < t_end, vb = t0 + tb + r1 < t_end;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float sa = 0.0f, sb = 0.0f;
+#pragma unroll
+                for (int g = 0; g < NG; ++g) {
+                    sa = fmaf(ksa[g] * k_coef, cg[g][hh], fmaf(kba[g], qs_l2[g][hh], sa));
+                    sb = fmaf(ksb[g] * k_coef, cg[g][2 + hh], fmaf(kbb[g], qs_l2[g][hh], sb));
+                }
+                // masked rows may hold stale bits: select, never compute with them
+                sc[mt][hh] = va ? sa : -INFINITY;
+                sc[mt][2 + hh] = vb ? sb : -INFINITY;
+            }
+        }
+
+        // ---- online softmax update over this warp's tokens of the stage
+        float m_use[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) mx = fmaxf(mx, fmaxf(sc[mt][hh], sc[mt][2 + hh]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float m_new = fmaxf(m_run[hh], mx);
+            m_use[hh] = m_new == -INFINITY ? 0.0f : m_new;
+            if (m_new > m_run[hh]) {
+                const float alpha = m_run[hh] == -INFINITY ? 0.0f : exp2f(m_run[hh] - m_new);
+                l_run[hh] *= alpha;
+#pragma unroll
+                for (int g = 0; g < NG; ++g) e_run[g][hh] *= alpha;
+#pragma unroll
+                for (int i = 0; i < C::NKS; ++i) {
+                    acc[i][hh] *= alpha;
+                    acc[i][2 + hh] *= alpha;
+                }
+                m_run[hh] = m_new;
+            }
+        }
+
+        // ---- P.V for each m-tile of this warp
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+            const int tb = (warp * C::MT + mt) * 16;
+            const bool va = t0 + tb + r0 < t_end, vb = t0 + tb + r1 < t_end;
+            float pr[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) pr[c] = exp2f(sc[mt][c] - m_use[c & 1]);
+            l_run[0] += pr[0] + pr[2];
+            l_run[1] += pr[1] + pr[3];
+            float vsa[NG], vba[NG], vsb[NG], vbb[NG];
+            load_row_sb<NG>(vs_s, tb + r0, vsa);
+            load_row_sb<NG>(vb_s, tb + r0, vba);
+            load_row_sb<NG>(vs_s, tb + r1, vsb);
+            load_row_sb<NG>(vb_s, tb + r1, vbb);
+            uint32_t bfrag[NG][2];
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+                // masked rows may hold stale scale/bias bits: select, never multiply
+                const float sa = va ? vsa[g] : 0.0f, sb = vb ? vsb[g] : 0.0f;
+                const float ba = va ? vba[g] : 0.0f, bb = vb ? vbb[g] : 0.0f;
+                e_run[g][0] = fmaf(pr[0], ba, fmaf(pr[2], bb, e_run[g][0]));
+                e_run[g][1] = fmaf(pr[1], ba, fmaf(pr[3], bb, e_run[g][1]));
+                bfrag[g][0] = movmatrix_trans(pack_half2(pr[0] * sa, pr[1] * sa));
+                bfrag[g][1] = movmatrix_trans(pack_half2(pr[2] * sb, pr[3] * sb));
+            }
+#pragma unroll
+            for (int sp = 0; sp < C::SPT / 2; ++sp) {
+                uint32_t x0, x1, x2, x3;
+                ldmatrix_x4_trans(code_addr<D>(vc_s, tb + lm_tok, 2 * sp + lm_seg), x0, x1, x2, x3);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int s = 2 * sp + e;
+                    const int g = (32 * s) / kGroup;
+                    const uint32_t xa = e ? x2 : x0;  // tokens of rows 0..7  (k 0..7)
+                    const uint32_t xb = e ? x3 : x1;  // tokens of rows 8..15 (k 8..15)
+                    mma_16816(acc[2 * s], xa & kLoNib, xa & kHiNib, xb & kLoNib, xb & kHiNib, bfrag[g][0],
+                              bfrag[g][1]);
+                    const uint32_t ya = xa >> 8, yb = xb >> 8;
+                    mma_16816(acc[2 * s + 1], ya & kLoNib, ya & kHiNib, yb & kLoNib, yb & kHiNib, bfrag[g][0],
+                              bfrag[g][1]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[stage]);
+    }
+
+    // ---- reduce per-thread sums over the 8 token rows (lanes differing in gid)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], off);
+#pragma unroll
+            for (int g = 0; g < NG; ++g) e_run[g][hh] += __shfl_xor_sync(0xffffffffu, e_run[g][hh], off);
+        }
+    }
+
+    // ---- merge the consumer warps' states through shared memory
+    // (every stage has been consumed once all consumers pass this barrier)
+    asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
+    float* mrg_acc = reinterpret_cast<float*>(smem);  // [NWC][8][D]
+    {
+        float* wacc = mrg_acc + warp * 8 * D;
+#pragma unroll
+        for (int i = 0; i < C::NKS; ++i) {
+            const int s = i >> 1, j = i & 1;
+            const int d_lo = 32 * s + 4 * gid + 2 * j;  // fragment row gid
+            const int d_hi = d_lo + 1;                  // fragment row gid + 8 (x16 operand)
+            const int g = d_lo / kGroup;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int h = 2 * tig + hh;
+                wacc[h * D + d_lo] = fmaf(acc[i][hh], 16777216.0f, e_run[g][hh]);
+                wacc[h * D + d_hi] = fmaf(acc[i][2 + hh], 1048576.0f, e_run[g][hh]);
+            }
+        }
+        if (gid == 0) {
+            mrg_m[warp][2 * tig] = m_run[0];
+            mrg_m[warp][2 * tig + 1] = m_run[1];
+            mrg_l[warp][2 * tig] = l_run[0];
+            mrg_l[warp][2 * tig + 1] = l_run[1];
+        }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
+    const float ln2 = 0.69314718055994531f;
+    for (int idx = threadIdx.x; idx < G * D; idx += C::NWC * 32) {
+        const int h = idx / D, d = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < C::NWC; ++w) M = fmaxf(M, mrg_m[w][h]);
+        float L = 0.0f, A = 0.0f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < C::NWC; ++w) {
+                const float wt = mrg_m[w][h] == -INFINITY ? 0.0f : exp2f(mrg_m[w][h] - M);
+                L = fmaf(wt, mrg_l[w][h], L);
+                A = fmaf(wt, mrg_acc[(w * 8 + h) * D + d], A);
+            }
+        }
+        const long long ph = (static_cast<long long>(b) * p.num_q_heads + kvh * G + h) * p.n_splits + split;
+        p.part_acc[ph * D + d] = A;
+        if (d == 0) {
+            p.part_m[ph] = M == -INFINITY ? -INFINITY : M * ln2;
+            p.part_l[ph] = L;
+        }
+    }
+}
+
+template <int D>
+cudaError_t set_smem_attr() {
+    static bool done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_BYTES);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+    return e;
+}
+
+template <int D>
+cudaError_t launch_d(const DecodeParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v, cudaStream_t stream,
+                     bool pdl_secondary) {
+    using C = Cfg<D>;
+    cudaError_t e = set_smem_attr<D>();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_splits, p.num_kv_heads, p.batch);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_secondary ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D>, tm_k, tm_v, p);
+}
+
+template <int D>
+int ctas_per_sm_d() {
+    if (set_smem_attr<D>() != cudaSuccess) return 1;
+    int n = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D>, Cfg<D>::THREADS, Cfg<D>::SMEM_BYTES);
+    return n > 0 ? n : 1;
+}
+
+}  // namespace
+
+int mma_tile_tokens(int head_dim) {
+    switch (head_dim) {
+        case 64: return Cfg<64>::T;
+        case 128: return Cfg<128>::T;
+        case 256: return Cfg<256>::T;
+        default: return 0;
+    }
+}
+
+int mma_smem_bytes(int head_dim) {
+    switch (head_dim) {
+        case 64: return Cfg<64>::SMEM_BYTES;
+        case 128: return Cfg<128>::SMEM_BYTES;
+        case 256: return Cfg<256>::SMEM_BYTES;
+        default: return 0;
+    }
+}
+
+int mma_ctas_per_sm(int head_dim) {
+    switch (head_dim) {
+        case 64: return ctas_per_sm_d<64>();
+        case 128: return ctas_per_sm_d<128>();
+        case 256: return ctas_per_sm_d<256>();
+        default: return 1;
+    }
+}
+
+cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                              cudaStream_t stream, bool pdl_secondary) {
+    switch (head_dim) {
+        case 64: return launch_d<64>(p, tm_k, tm_v, stream, pdl_secondary);
+        case 128: return launch_d<128>(p, tm_k, tm_v, stream, pdl_secondary);
+        case 256: return launch_d<256>(p, tm_k, tm_v, stream, pdl_secondary);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace tq

@@ -1,0 +1,123 @@
+// quantize.cu -- quantize-on-store: fp16 K/V rows -> packed int4 codes plus
+// fp16 scale/bias per group of 64, written in place into the cache.
+//
+// Method: "turboquant-llama3.170B" README, decode-step listing (quantize K,V to
+// int4 after RoPE, then store) and the Gemma page, Background (MLX-style int4
+// with a per-group scale and bias).  The rounding rule is the one stated in
+// tq.h; every step is a single IEEE fp32 operation with round-to-nearest-even
+// (__fsub_rn / __fdiv_rn / __float2int_rn), so codes, scales and biases are
+// bit-identical to the CPU oracle.
+//
+// Work split: eight lanes own one group of 64 elements (16 bytes = 8 halves
+// each), which makes every global access a 16-byte (input) or 4-byte (codes)
+// coalesced transaction; min/max are reduced with three xor-shuffles.
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+
+namespace {
+
+struct GroupQ {
+    uint32_t codes;  // eight 4-bit codes, element 0 in bits 0..3
+    __half scale;
+    __half bias;
+};
+
+__device__ __forceinline__ GroupQ quantize_lane8(uint4 raw) {
+    float x[8];
+    const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 f = __half22float2(h2[i]);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+    float mn = x[0], mx = x[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) {
+        mn = fminf(mn, x[i]);
+        mx = fmaxf(mx, x[i]);
+    }
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) {  // the 8 lanes of a group differ in lane bits 0..2
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    }
+    if (mn == 0.0f) mn = 0.0f;  // a zero minimum is stored as +0
+    const float range = __fsub_rn(mx, mn);
+    GroupQ g;
+    g.scale = __float2half_rn(__fdiv_rn(range, 15.0f));
+    g.bias = __float2half_rn(mn);  // exact: mn is an fp16 value
+    const float s = __half2float(g.scale);
+    const float b = __half2float(g.bias);
+    uint32_t codes = 0;
+    if (s != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            int c = __float2int_rn(__fdiv_rn(__fsub_rn(x[i], b), s));
+            c = min(max(c, 0), 15);
+            codes |= static_cast<uint32_t>(c) << (4 * i);
+        }
+    }
+    g.codes = codes;
+    return g;
+}
+
+__global__ void __launch_bounds__(256) quantize_append_kernel(const AppendParams p) {
+    const int ng = p.head_dim / kGroup;
+    const long long n_groups = static_cast<long long>(p.batch) * p.num_kv_heads * p.n_new * ng;
+    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int part = static_cast<int>(tid & 7);
+    const long long gidx = tid >> 3;
+    const bool valid = gidx < n_groups;  // whole groups of 8 lanes agree
+    const long long gi = valid ? gidx : 0;
+    const int g = static_cast<int>(gi % ng);
+    const long long row = gi / ng;  // over [B][Hkv][n_new]
+    const int i = static_cast<int>(row % p.n_new);
+    const long long bh = row / p.n_new;  // b * Hkv + h
+    const int b = static_cast<int>(bh / p.num_kv_heads);
+
+    const long long src = row * p.head_dim + g * kGroup + part * 8;  // in halves
+    uint4 kr = make_uint4(0, 0, 0, 0), vr = make_uint4(0, 0, 0, 0);
+    int wp = 0;
+    if (valid) {
+        kr = __ldcs(reinterpret_cast<const uint4*>(p.k_new + src));
+        vr = __ldcs(reinterpret_cast<const uint4*>(p.v_new + src));
+        wp = __ldg(p.write_pos + b);
+    }
+    const GroupQ kq = quantize_lane8(kr);  // every lane takes part in the shuffles
+    const GroupQ vq = quantize_lane8(vr);
+    if (!valid) return;
+
+    const bool pos_ok = wp >= 0 && static_cast<long long>(wp) + p.n_new <= p.capacity;
+    if (!pos_ok) {
+        if (p.status != nullptr && part == 0 && g == 0 && i == 0) atomicOr(p.status, TQ_DEV_WRITE_POS);
+        return;
+    }
+    const long long dst_row = bh * p.capacity + wp + i;
+    const long long code_off = dst_row * (p.head_dim / 2) + g * (kGroup / 2) + part * 4;
+    *reinterpret_cast<uint32_t*>(p.k_codes + code_off) = kq.codes;
+    *reinterpret_cast<uint32_t*>(p.v_codes + code_off) = vq.codes;
+    if (part == 0) {
+        const long long sb = dst_row * ng + g;
+        p.k_scale[sb] = __half_as_ushort(kq.scale);
+        p.k_bias[sb] = __half_as_ushort(kq.bias);
+        p.v_scale[sb] = __half_as_ushort(vq.scale);
+        p.v_bias[sb] = __half_as_ushort(vq.bias);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_append(const AppendParams& p, cudaStream_t stream) {
+    const long long groups = static_cast<long long>(p.batch) * p.num_kv_heads * p.n_new * (p.head_dim / kGroup);
+    const long long threads = groups * 8;
+    const int block = 256;
+    const long long blocks = (threads + block - 1) / block;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    quantize_append_kernel<<<static_cast<unsigned>(blocks), block, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace tq

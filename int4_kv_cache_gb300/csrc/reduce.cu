@@ -1,0 +1,87 @@
+// reduce.cu -- split-K phase 2: log-sum-exp merge of partial softmax states
+// ("turboquant-llama3.170B" README, split-K paragraph: Phase 2 reduces the
+// partial softmax results of the chunks processed in parallel by Phase 1).
+//
+// Per (b, h):  M = max_c m_c over parts with l_c > 0,  w_c = e^{m_c - M},
+//              out = sum_c w_c acc_c / sum_c w_c l_c   (fp16, RNE; 0 if empty)
+// One CTA per (b, h); the weights go through shared memory once, then each
+// thread owns head_dim elements.  Launched as a programmatic dependent of
+// phase 1, it waits for phase 1's memory before the first read.
+#include <math.h>
+
+#include "tq_device.cuh"
+#include "tq_internal.h"
+
+namespace tq {
+
+namespace {
+
+constexpr int kReduceThreads = 128;
+
+__device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, v, off);
+        v = is_max ? fmaxf(v, o) : v + o;
+    }
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int w = 1; w < kReduceThreads / 32; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceParams p) {
+    extern __shared__ float w_s[];  // [n_parts]
+    __shared__ float red[kReduceThreads / 32];
+    pdl_wait_primary();
+
+    const long long bh = blockIdx.x;
+    const int n = p.n_parts, D = p.head_dim;
+    const float* pm = p.part_m + bh * n;
+    const float* pl = p.part_l + bh * n;
+    const float* pa = p.part_acc + bh * n * D;
+
+    float M = -INFINITY;
+    for (int c = threadIdx.x; c < n; c += kReduceThreads)
+        if (pl[c] > 0.0f) M = fmaxf(M, pm[c]);
+    M = block_reduce(M, red, true);
+
+    float L = 0.0f;
+    for (int c = threadIdx.x; c < n; c += kReduceThreads) {
+        const float w = (pl[c] > 0.0f) ? expf(pm[c] - M) : 0.0f;
+        w_s[c] = w;
+        L += w * pl[c];
+    }
+    L = block_reduce(L, red, false);  // its barriers also publish w_s
+
+    for (int d = threadIdx.x; d < D; d += kReduceThreads) {
+        float a = 0.0f;
+        for (int c = 0; c < n; ++c) {
+            const float w = w_s[c];
+            if (w != 0.0f) a = fmaf(w, pa[static_cast<long long>(c) * D + d], a);
+        }
+        p.out[bh * D + d] = __half_as_ushort(__float2half_rn(L > 0.0f ? __fdiv_rn(a, L) : 0.0f));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl_secondary) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.batch) * p.num_q_heads);
+    cfg.blockDim = dim3(kReduceThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(p.n_parts) * sizeof(float);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_secondary ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, reduce_kernel, p);
+}
+
+}  // namespace tq

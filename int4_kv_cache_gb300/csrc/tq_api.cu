@@ -1,0 +1,388 @@
+// tq_api.cu -- the extern "C" boundary of libtq: argument checks, split-K
+// planning, TMA descriptors and kernel dispatch.  No device allocation, no
+// host synchronisation.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "tq.h"
+#include "tq_internal.h"
+
+namespace {
+
+thread_local int32_t g_last_cuda_error = 0;
+
+tq_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return TQ_OK;
+    g_last_cuda_error = static_cast<int32_t>(e);
+    return TQ_ERR_CUDA;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_dim(int32_t d) { return d == 64 || d == 128 || d == 256; }
+
+bool valid_impl(tq_impl impl) { return impl == TQ_IMPL_AUTO || impl == TQ_IMPL_MMA || impl == TQ_IMPL_SIMT; }
+
+tq_status check_cache(const tq_kv_cache* c) {
+    if (c == nullptr) return TQ_ERR_NULL;
+    if (!c->k_codes || !c->v_codes || !c->k_scale || !c->k_bias || !c->v_scale || !c->v_bias) return TQ_ERR_NULL;
+    if (c->batch < 1 || c->num_kv_heads < 1 || c->capacity < 16 || c->capacity % 16 != 0) return TQ_ERR_SHAPE;
+    if (c->group_size != TQ_GROUP_SIZE || !supported_dim(c->head_dim)) return TQ_ERR_UNSUPPORTED;
+    if (!aligned16(c->k_codes) || !aligned16(c->v_codes) || !aligned16(c->k_scale) || !aligned16(c->k_bias) ||
+        !aligned16(c->v_scale) || !aligned16(c->v_bias))
+        return TQ_ERR_ALIGN;
+    // index arithmetic is 64-bit, but TMA row coordinates are int32
+    const long long rows128 =
+        static_cast<long long>(c->batch) * c->num_kv_heads * c->capacity * (c->head_dim / 2) / 128;
+    if (rows128 >= (1LL << 31)) return TQ_ERR_SHAPE;
+    return TQ_OK;
+}
+
+// ---------------------------------------------------------------- TMA maps --
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// The code array of a cache seen as [rows][128 bytes] (uint8), boxes of
+// `box_rows` rows with the 128-byte swizzle; reads past the end are zero-filled.
+tq_status make_code_map(CUtensorMap* map, const uint8_t* codes, const tq_kv_cache* c, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return cuda_status(cudaErrorNotSupported);
+    const cuuint64_t rows =
+        static_cast<cuuint64_t>(c->batch) * c->num_kv_heads * c->capacity * (c->head_dim / 2) / 128;
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_status(cudaErrorInvalidValue);
+    return TQ_OK;
+}
+
+// ------------------------------------------------------------ device facts --
+struct DeviceFacts {
+    int sms = 0;
+    int mma_ctas[3] = {0, 0, 0};  // per head_dim 64 / 128 / 256
+    int simt_ctas[3] = {0, 0, 0};
+};
+
+int dim_index(int d) { return d == 64 ? 0 : (d == 128 ? 1 : 2); }
+
+tq_status device_facts(DeviceFacts** out) {
+    static DeviceFacts facts[64];
+    static std::atomic<bool> ready[64];
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (dev < 0 || dev >= 64) return TQ_ERR_UNSUPPORTED;
+    if (!ready[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!ready[dev].load(std::memory_order_relaxed)) {
+            DeviceFacts f;
+            e = cudaDeviceGetAttribute(&f.sms, cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess) return cuda_status(e);
+            const int dims[3] = {64, 128, 256};
+            for (int i = 0; i < 3; ++i) {
+                f.mma_ctas[i] = tq::mma_ctas_per_sm(dims[i]);
+                f.simt_ctas[i] = tq::simt_ctas_per_sm(dims[i]);
+            }
+            cudaGetLastError();  // occupancy queries must leave no pending error
+            facts[dev] = f;
+            ready[dev].store(true, std::memory_order_release);
+        }
+    }
+    *out = &facts[dev];
+    return TQ_OK;
+}
+
+// ------------------------------------------------------------- decode plan --
+struct Plan {
+    int n_chunks, n_splits, split_tokens;
+};
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// Give each CTA a run of whole chunks so that the grid fills the GPU about
+// once: chunks_per_split = ceil(B * Hkv * n_chunks / resident CTAs).
+Plan make_plan(int batch, int hkv, int max_seq_len, int chunk, int resident) {
+    Plan pl;
+    pl.n_chunks = ceil_div(max_seq_len, chunk);
+    const long long units = static_cast<long long>(batch) * hkv * pl.n_chunks;
+    int cps = static_cast<int>((units + resident - 1) / resident);
+    if (cps < 1) cps = 1;
+    pl.n_splits = ceil_div(pl.n_chunks, cps);
+    pl.split_tokens = cps * chunk;
+    return pl;
+}
+
+tq_status device_plan(const tq_kv_cache* cache, int max_seq_len, int chunk, tq_impl impl, Plan* pl) {
+    DeviceFacts* f = nullptr;
+    tq_status s = device_facts(&f);
+    if (s != TQ_OK) return s;
+    const int di = dim_index(cache->head_dim);
+    const int per_sm = impl == TQ_IMPL_SIMT ? f->simt_ctas[di] : f->mma_ctas[di];
+    *pl = make_plan(cache->batch, cache->num_kv_heads, max_seq_len, chunk, f->sms * per_sm);
+    return TQ_OK;
+}
+
+tq_status check_decode_args(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
+                            int32_t max_seq_len, int32_t chunk, const void* out) {
+    tq_status s = check_cache(cache);
+    if (s != TQ_OK) return s;
+    if (q == nullptr || seq_lens == nullptr || out == nullptr) return TQ_ERR_NULL;
+    if (!aligned16(q)) return TQ_ERR_ALIGN;
+    if (hq < 1 || hq % cache->num_kv_heads != 0) return TQ_ERR_SHAPE;
+    if (hq / cache->num_kv_heads > 8) return TQ_ERR_UNSUPPORTED;
+    if (max_seq_len < 1) return TQ_ERR_SHAPE;
+    if (max_seq_len > cache->capacity) return TQ_ERR_CAPACITY;
+    if (chunk < 16 || chunk % 16 != 0) return TQ_ERR_SHAPE;
+    return TQ_OK;
+}
+
+tq_status run_phase1(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
+                     int32_t max_seq_len, float attn_scale, const Plan& pl, float* pm, float* plv, float* pa,
+                     int32_t* status, tq_impl impl, cudaStream_t stream) {
+    if (pl.n_splits > 65535 || cache->num_kv_heads > 65535 || cache->batch > 65535) return TQ_ERR_SHAPE;
+    tq::DecodeParams p;
+    p.q = q;
+    p.seq_lens = seq_lens;
+    p.k_scale = cache->k_scale;
+    p.k_bias = cache->k_bias;
+    p.v_scale = cache->v_scale;
+    p.v_bias = cache->v_bias;
+    p.k_codes = cache->k_codes;
+    p.v_codes = cache->v_codes;
+    p.part_m = pm;
+    p.part_l = plv;
+    p.part_acc = pa;
+    p.status = status;
+    p.batch = cache->batch;
+    p.num_q_heads = hq;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.group_q = hq / cache->num_kv_heads;
+    p.capacity = cache->capacity;
+    p.max_seq_len = max_seq_len;
+    p.split_tokens = pl.split_tokens;
+    p.n_splits = pl.n_splits;
+    p.score_scale_log2 = attn_scale * 1.4426950408889634f;
+    if (impl == TQ_IMPL_SIMT) return cuda_status(tq::launch_decode_simt(p, cache->head_dim, stream));
+    CUtensorMap tm_k, tm_v;
+    const int box_rows = tq::mma_tile_tokens(cache->head_dim) * (cache->head_dim / 2) / 128;
+    tq_status s = make_code_map(&tm_k, cache->k_codes, cache, box_rows);
+    if (s != TQ_OK) return s;
+    s = make_code_map(&tm_v, cache->v_codes, cache, box_rows);
+    if (s != TQ_OK) return s;
+    return cuda_status(tq::launch_decode_mma(p, cache->head_dim, tm_k, tm_v, stream, false));
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t tq_abi_version(void) { return TQ_ABI_VERSION; }
+
+const char* tq_status_string(tq_status s) {
+    switch (s) {
+        case TQ_OK: return "ok";
+        case TQ_ERR_NULL: return "null pointer";
+        case TQ_ERR_SHAPE: return "invalid shape";
+        case TQ_ERR_CAPACITY: return "exceeds cache capacity";
+        case TQ_ERR_WORKSPACE: return "workspace missing or too small";
+        case TQ_ERR_CUDA: return "CUDA error";
+        case TQ_ERR_UNSUPPORTED: return "unsupported configuration";
+        case TQ_ERR_ALIGN: return "misaligned array";
+    }
+    return "unknown status";
+}
+
+int32_t tq_last_cuda_error(void) { return g_last_cuda_error; }
+
+size_t tq_kv_cache_bytes(int32_t batch, int32_t hkv, int32_t head_dim, int32_t group_size, int32_t capacity) {
+    if (batch < 1 || hkv < 1 || capacity < 1 || head_dim < 2 || head_dim % 2 != 0 || group_size < 1 ||
+        head_dim % group_size != 0)
+        return 0;
+    const size_t rows = static_cast<size_t>(batch) * hkv * capacity;
+    const size_t codes = align256(rows * (head_dim / 2));
+    const size_t sb = align256(rows * (head_dim / group_size) * 2);
+    return 2 * codes + 4 * sb;
+}
+
+tq_status tq_kv_cache_carve(tq_kv_cache* cache, void* base, int32_t batch, int32_t hkv, int32_t head_dim,
+                            int32_t group_size, int32_t capacity) {
+    if (cache == nullptr || base == nullptr) return TQ_ERR_NULL;
+    if (tq_kv_cache_bytes(batch, hkv, head_dim, group_size, capacity) == 0) return TQ_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(base) & 255u) != 0) return TQ_ERR_ALIGN;
+    const size_t rows = static_cast<size_t>(batch) * hkv * capacity;
+    const size_t codes = align256(rows * (head_dim / 2));
+    const size_t sb = align256(rows * (head_dim / group_size) * 2);
+    uint8_t* p = static_cast<uint8_t*>(base);
+    cache->k_codes = p;
+    cache->v_codes = p + codes;
+    cache->k_scale = reinterpret_cast<uint16_t*>(p + 2 * codes);
+    cache->k_bias = reinterpret_cast<uint16_t*>(p + 2 * codes + sb);
+    cache->v_scale = reinterpret_cast<uint16_t*>(p + 2 * codes + 2 * sb);
+    cache->v_bias = reinterpret_cast<uint16_t*>(p + 2 * codes + 3 * sb);
+    cache->batch = batch;
+    cache->num_kv_heads = hkv;
+    cache->head_dim = head_dim;
+    cache->group_size = group_size;
+    cache->capacity = capacity;
+    return TQ_OK;
+}
+
+tq_status tq_quantize_kv_append(const tq_kv_cache* cache, const uint16_t* k_new, const uint16_t* v_new,
+                                int32_t n_new, const int32_t* write_pos, int32_t* status, void* stream) {
+    tq_status s = check_cache(cache);
+    if (s != TQ_OK) return s;
+    if (k_new == nullptr || v_new == nullptr || write_pos == nullptr) return TQ_ERR_NULL;
+    if (!aligned16(k_new) || !aligned16(v_new)) return TQ_ERR_ALIGN;
+    if (n_new < 0) return TQ_ERR_SHAPE;
+    if (n_new > cache->capacity) return TQ_ERR_CAPACITY;
+    if (n_new == 0) return TQ_OK;
+    tq::AppendParams p;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.write_pos = write_pos;
+    p.k_codes = cache->k_codes;
+    p.v_codes = cache->v_codes;
+    p.k_scale = cache->k_scale;
+    p.k_bias = cache->k_bias;
+    p.v_scale = cache->v_scale;
+    p.v_bias = cache->v_bias;
+    p.status = status;
+    p.batch = cache->batch;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.head_dim = cache->head_dim;
+    p.n_new = n_new;
+    p.capacity = cache->capacity;
+    return cuda_status(tq::launch_quantize_append(p, static_cast<cudaStream_t>(stream)));
+}
+
+size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t hq, int32_t head_dim, int32_t max_seq_len, int32_t chunk) {
+    if (batch < 1 || hq < 1 || head_dim < 1 || max_seq_len < 1 || chunk < 1) return 0;
+    const size_t nc = static_cast<size_t>((max_seq_len + chunk - 1) / chunk);
+    const size_t parts = static_cast<size_t>(batch) * hq * nc;
+    return 2 * align256(parts * sizeof(float)) + align256(parts * head_dim * sizeof(float));
+}
+
+tq_status tq_sdpa_int4_decode_impl(const tq_kv_cache* cache, const uint16_t* q, int32_t hq,
+                                   const int32_t* seq_lens, int32_t max_seq_len, float attn_scale, int32_t chunk,
+                                   void* workspace, size_t workspace_bytes, uint16_t* out, int32_t* status,
+                                   tq_impl impl, void* stream) {
+    tq_status s = check_decode_args(cache, q, hq, seq_lens, max_seq_len, chunk, out);
+    if (s != TQ_OK) return s;
+    if (!valid_impl(impl)) return TQ_ERR_UNSUPPORTED;
+    const size_t need = tq_sdpa_workspace_bytes(cache->batch, hq, cache->head_dim, max_seq_len, chunk);
+    if (workspace == nullptr || workspace_bytes < need) return TQ_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TQ_ERR_ALIGN;
+    Plan pl;
+    s = device_plan(cache, max_seq_len, chunk, impl, &pl);
+    if (s != TQ_OK) return s;
+    if (pl.n_splits > tq::kMaxReduceParts) return TQ_ERR_SHAPE;
+    const size_t parts = static_cast<size_t>(cache->batch) * hq * pl.n_splits;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* pm = reinterpret_cast<float*>(ws);
+    float* plv = reinterpret_cast<float*>(ws + align256(parts * sizeof(float)));
+    float* pa = reinterpret_cast<float*>(ws + 2 * align256(parts * sizeof(float)));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status,
+                   impl == TQ_IMPL_SIMT ? TQ_IMPL_SIMT : TQ_IMPL_MMA, st);
+    if (s != TQ_OK) return s;
+    tq::ReduceParams r;
+    r.part_m = pm;
+    r.part_l = plv;
+    r.part_acc = pa;
+    r.out = out;
+    r.batch = cache->batch;
+    r.num_q_heads = hq;
+    r.head_dim = cache->head_dim;
+    r.n_parts = pl.n_splits;
+    return cuda_status(tq::launch_reduce(r, st, true));
+}
+
+tq_status tq_sdpa_int4_decode(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
+                              int32_t max_seq_len, float attn_scale, int32_t chunk, void* workspace,
+                              size_t workspace_bytes, uint16_t* out, int32_t* status, void* stream) {
+    return tq_sdpa_int4_decode_impl(cache, q, hq, seq_lens, max_seq_len, attn_scale, chunk, workspace,
+                                    workspace_bytes, out, status, TQ_IMPL_AUTO, stream);
+}
+
+tq_status tq_sdpa_plan(const tq_kv_cache* cache, int32_t hq, int32_t max_seq_len, int32_t chunk, tq_impl impl,
+                       int32_t* chunks_per_split, int32_t* n_splits) {
+    if (cache == nullptr || chunks_per_split == nullptr || n_splits == nullptr) return TQ_ERR_NULL;
+    if (!supported_dim(cache->head_dim)) return TQ_ERR_UNSUPPORTED;
+    if (cache->batch < 1 || cache->num_kv_heads < 1 || hq < 1 || max_seq_len < 1 || chunk < 16 || chunk % 16)
+        return TQ_ERR_SHAPE;
+    if (!valid_impl(impl)) return TQ_ERR_UNSUPPORTED;
+    Plan pl;
+    tq_status s = device_plan(cache, max_seq_len, chunk, impl, &pl);
+    if (s != TQ_OK) return s;
+    *chunks_per_split = pl.split_tokens / chunk;
+    *n_splits = pl.n_splits;
+    return TQ_OK;
+}
+
+tq_status tq_sdpa_int4_partial(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
+                               int32_t max_seq_len, float attn_scale, int32_t chunk, int32_t chunks_per_split,
+                               float* part_m, float* part_l, float* part_acc, int32_t* status, tq_impl impl,
+                               void* stream) {
+    tq_status s = check_decode_args(cache, q, hq, seq_lens, max_seq_len, chunk, part_m);
+    if (s != TQ_OK) return s;
+    if (part_l == nullptr || part_acc == nullptr) return TQ_ERR_NULL;
+    if (!valid_impl(impl)) return TQ_ERR_UNSUPPORTED;
+    if (chunks_per_split < 0) return TQ_ERR_SHAPE;
+    if (chunks_per_split == 0) {
+        int32_t cps = 0, ns = 0;
+        s = tq_sdpa_plan(cache, hq, max_seq_len, chunk, impl, &cps, &ns);
+        if (s != TQ_OK) return s;
+        chunks_per_split = cps;
+    }
+    Plan pl;
+    pl.n_chunks = ceil_div(max_seq_len, chunk);
+    pl.n_splits = ceil_div(pl.n_chunks, chunks_per_split);
+    pl.split_tokens = chunks_per_split * chunk;
+    return run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, part_m, part_l, part_acc, status,
+                      impl == TQ_IMPL_SIMT ? TQ_IMPL_SIMT : TQ_IMPL_MMA, static_cast<cudaStream_t>(stream));
+}
+
+tq_status tq_sdpa_int4_reduce(const float* part_m, const float* part_l, const float* part_acc, int32_t batch,
+                              int32_t hq, int32_t head_dim, int32_t n_parts, uint16_t* out, void* stream) {
+    if (part_m == nullptr || part_l == nullptr || part_acc == nullptr || out == nullptr) return TQ_ERR_NULL;
+    if (batch < 1 || hq < 1 || head_dim < 1 || n_parts < 1 || n_parts > tq::kMaxReduceParts) return TQ_ERR_SHAPE;
+    if (!supported_dim(head_dim)) return TQ_ERR_UNSUPPORTED;
+    tq::ReduceParams r;
+    r.part_m = part_m;
+    r.part_l = part_l;
+    r.part_acc = part_acc;
+    r.out = out;
+    r.batch = batch;
+    r.num_q_heads = hq;
+    r.head_dim = head_dim;
+    r.n_parts = n_parts;
+    return cuda_status(tq::launch_reduce(r, static_cast<cudaStream_t>(stream), false));
+}
+
+}  // extern "C"

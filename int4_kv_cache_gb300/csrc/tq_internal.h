@@ -1,0 +1,74 @@
+// tq_internal.h -- launch parameters shared by the C-ABI layer and kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tq.h"
+
+namespace tq {
+
+constexpr int kGroup = 64;
+
+// Geometry of one phase-1 launch: grid (n_splits, Hkv, B); CTA (s, kvh, b)
+// covers tokens [s * split_tokens, (s + 1) * split_tokens) of sequence b,
+// clipped to seq_lens[b].
+struct DecodeParams {
+    const uint16_t* q;        // [B][Hq][D]
+    const int32_t* seq_lens;  // [B]
+    const uint16_t* k_scale;  // [B][Hkv][cap][NG]
+    const uint16_t* k_bias;
+    const uint16_t* v_scale;
+    const uint16_t* v_bias;
+    const uint8_t* k_codes;   // [B][Hkv][cap][D/2] (the SIMT path reads these directly)
+    const uint8_t* v_codes;
+    float* part_m;            // [B][Hq][n_splits]   natural-log units
+    float* part_l;            // [B][Hq][n_splits]
+    float* part_acc;          // [B][Hq][n_splits][D]
+    int32_t* status;          // optional device status word
+    int32_t batch, num_q_heads, num_kv_heads, group_q;  // group_q = Hq / Hkv
+    int32_t capacity, max_seq_len;
+    int32_t split_tokens, n_splits;
+    float score_scale_log2;   // attn_scale * log2(e)
+};
+
+struct ReduceParams {
+    const float* part_m;
+    const float* part_l;
+    const float* part_acc;
+    uint16_t* out;            // [B][Hq][D]
+    int32_t batch, num_q_heads, head_dim, n_parts;
+};
+
+struct AppendParams {
+    const uint16_t* k_new;    // [B][Hkv][n_new][D]
+    const uint16_t* v_new;
+    const int32_t* write_pos; // [B]
+    uint8_t* k_codes;
+    uint8_t* v_codes;
+    uint16_t* k_scale;
+    uint16_t* k_bias;
+    uint16_t* v_scale;
+    uint16_t* v_bias;
+    int32_t* status;
+    int32_t batch, num_kv_heads, head_dim, n_new, capacity;
+};
+
+// Launchers (return the cudaError_t of the launch).
+cudaError_t launch_quantize_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_decode_simt(const DecodeParams& p, int head_dim, cudaStream_t stream);
+cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, const CUtensorMap& tm_k,
+                              const CUtensorMap& tm_v, cudaStream_t stream, bool pdl_secondary);
+cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl_secondary);
+
+// Tokens per pipeline stage of the tensor-core kernel (tiles are TMA boxes).
+int mma_tile_tokens(int head_dim);
+int mma_smem_bytes(int head_dim);
+// Resident CTAs per SM of the phase-1 kernels (occupancy API).
+int mma_ctas_per_sm(int head_dim);
+int simt_ctas_per_sm(int head_dim);
+// Largest n_parts the reduce kernel takes (its weights live in shared memory).
+constexpr int kMaxReduceParts = 12288;
+
+}  // namespace tq

@@ -16,9 +16,9 @@ Recipe (one place, so that tests and bench agree):
   * every array is drawn as float32 N(0, 1) from ``numpy.random.default_rng``
     (PCG64) seeded with the workload seed, then rounded to fp16 (RNE);
   * order of draws: Q, then K, then V, each in C order of its shape;
-  * "outliers": one head_dim channel per KV head (round(0.01 * D) = 1 at
-    D = 128), chosen with ``rng.integers`` after V is drawn, multiplied by 20
-    in float32 before the fp16 rounding, for every token of that KV head;
+  * "outliers": round(0.01 * D) head_dim channels per KV head (1 at D = 128),
+    chosen with ``rng.choice`` (no replacement) after V is drawn, multiplied
+    by 20 in float32 before the fp16 rounding, for every token of that head;
   * "rms_qk": Q and K rows are divided by sqrt(mean(x^2)) in float32 before
     the fp16 rounding (unit RMS per head vector, eps 0);
   * ragged lengths: ``rng.integers(lo, hi + 1)`` from a generator seeded
@@ -164,3 +164,30 @@ WORKLOADS = {
     # ragged batch of 32 sequences, lengths uniform in [1K, 32K]
     "ragged32": Workload("ragged32", 4, 32, 64, 8, 128, 32768, _LLAMA_SCALE, outliers=True),
 }
+
+
+def torch_decode_inputs(seed: int, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                        seq_len: int, *, outliers: bool = False, rms_qk: bool = False, device="cuda"):
+    """Same recipe as ``decode_inputs`` drawn on the device with torch's
+    seeded generator (different numbers than numpy, same distributions).
+
+    Used where the host generator would be too slow (hundreds of millions of
+    elements); a test that needs the oracle copies the fp16 tensors to the host.
+    Returns (q, k, v, outlier_channels) with fp16 tensors on ``device``.
+    """
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    q = torch.randn((batch, num_q_heads, head_dim), generator=g, device=device, dtype=torch.float32)
+    k = torch.randn((batch, num_kv_heads, seq_len, head_dim), generator=g, device=device, dtype=torch.float32)
+    v = torch.randn((batch, num_kv_heads, seq_len, head_dim), generator=g, device=device, dtype=torch.float32)
+    chans = None
+    if outliers:
+        chans = np.random.default_rng(seed).integers(0, head_dim, size=num_kv_heads)
+        for h in range(num_kv_heads):
+            k[:, h, :, int(chans[h])] *= 20.0
+    if rms_qk:
+        q = q / torch.sqrt(torch.mean(q * q, dim=-1, keepdim=True))
+        k = k / torch.sqrt(torch.mean(k * k, dim=-1, keepdim=True))
+    return q.half(), k.half(), v.half(), chans

@@ -1,0 +1,161 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+include/tq.h declares, its host-only size helpers are right, and argument
+errors are reported before anything is launched."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import int4_kv_cache_gb300 as tq
+from int4_kv_cache_gb300 import build as tqbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def L():
+    tqbuild.build()
+    return tq.lib()
+
+
+def declared_functions():
+    names = set()
+    for fname in os.listdir(os.path.join(ROOT, "include")):
+        text = open(os.path.join(ROOT, "include", fname)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(tq_[a-z0-9_]+)\s*\(", text,
+                                flags=re.M))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("tq_quantize_kv_append", "tq_sdpa_int4_decode", "tq_sdpa_int4_partial", "tq_sdpa_int4_reduce",
+                 "tq_sdpa_workspace_bytes", "tq_kv_cache_bytes", "tq_status_string", "tq_sdpa_plan"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+    assert tq.tq_abi_version() == 1
+
+
+def test_status_strings(L):
+    for s in range(8):
+        assert isinstance(tq.tq_status_string(s), str) and tq.tq_status_string(s)
+
+
+def test_cache_bytes_closed_form(L):
+    # rows * (D/2 codes + 2 fp16 scale/bias per group) for K and V, each array 256-aligned
+    B, Hkv, D, cap = 1, 8, 128, 131072
+    rows = B * Hkv * cap
+    assert tq.tq_kv_cache_bytes(B, Hkv, D, 64, cap) == 2 * rows * (D // 2) + 4 * rows * (D // 64) * 2
+    assert tq.tq_kv_cache_bytes(0, 8, 128, 64, 16) == 0
+    assert tq.tq_kv_cache_bytes(1, 8, 100, 64, 16) == 0
+
+
+def test_memory_table_of_the_llama_page(L):
+    # FP16 column of the memory table: 80 layers x 8 kv heads x ctx x 128 x 2 B x 2 (K+V), in GiB
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "llama70b_kv_memory_table.txt"))
+            if l.strip() and not l.startswith("#")]
+    for ctx, fp16_gib, _int4_printed in rows:
+        ctx = int(ctx)
+        fp16 = 80 * 8 * ctx * 128 * 2 * 2
+        assert round(fp16 / 2**30, 1) == float(fp16_gib)
+        # int4 at group 64 with fp16 scale+bias: (64 + 8) bytes per 128-element row vs 256
+        int4 = 80 * tq.tq_kv_cache_bytes(1, 8, 128, 64, ctx)
+        assert int4 * 128 == fp16 * 36
+    assert 80 * tq.tq_kv_cache_bytes(1, 8, 128, 64, 131072) == 12_079_595_520
+
+
+def test_workspace_bytes(L):
+    nc = math.ceil(131072 / 512)
+    parts = 1 * 64 * nc
+    want = 2 * (-(-parts * 4 // 256) * 256) + (-(-parts * 128 * 4 // 256) * 256)
+    assert tq.tq_sdpa_workspace_bytes(1, 64, 128, 131072, 512) == want
+    assert tq.tq_sdpa_workspace_bytes(1, 64, 128, 0, 512) == 0
+
+
+def _fake_cache(B=1, Hkv=2, D=128, cap=256):
+    c = tq.tq_kv_cache()
+    base = 1 << 20
+    for i, f in enumerate(("k_codes", "v_codes", "k_scale", "k_bias", "v_scale", "v_bias")):
+        setattr(c, f, base + i * (1 << 20))
+    c.batch, c.num_kv_heads, c.head_dim, c.group_size, c.capacity = B, Hkv, D, 64, cap
+    return c
+
+
+def _decode(L, c, q=0x100000, hq=8, lens=0x200000, max_len=256, chunk=512, ws=0x300000, ws_bytes=1 << 30,
+            out=0x400000, impl=0):
+    return L.tq_sdpa_int4_decode_impl(ctypes.byref(c) if c is not None else None, q, hq, lens, max_len,
+                                      ctypes.c_float(0.1), chunk, ws, ws_bytes, out, None, impl, None)
+
+
+def test_decode_argument_errors_launch_nothing(L):
+    # Host-side checks fire before any CUDA call, so they work without a GPU.
+    c = _fake_cache()
+    assert _decode(L, None) == 1                                  # TQ_ERR_NULL
+    assert _decode(L, c, q=0) == 1
+    assert _decode(L, c, hq=7) == 2                               # Hq % Hkv != 0
+    assert _decode(L, c, hq=2 * 16) == 6                          # GQA ratio 16 > 8
+    assert _decode(L, c, max_len=0) == 2
+    assert _decode(L, c, max_len=257) == 3                        # beyond capacity
+    assert _decode(L, c, chunk=24) == 2                           # not a multiple of 16
+    assert _decode(L, c, ws_bytes=16) == 4                        # workspace too small
+    assert _decode(L, c, ws=0) == 4
+    assert _decode(L, c, ws=0x300010) == 7                        # workspace not 256-aligned
+    assert _decode(L, c, q=0x100002) == 7                         # misaligned q
+    assert _decode(L, c, impl=9) == 6
+    assert _decode(L, _fake_cache(D=96)) == 6
+    assert _decode(L, _fake_cache(cap=250), max_len=200) == 2
+    bad = _fake_cache()
+    bad.group_size = 32
+    assert _decode(L, bad) == 6
+    bad = _fake_cache()
+    bad.v_bias = 0
+    assert _decode(L, bad) == 1
+    bad = _fake_cache()
+    bad.k_scale += 2
+    assert _decode(L, bad) == 7
+
+
+def test_append_argument_errors_launch_nothing(L):
+    c = _fake_cache()
+    f = L.tq_quantize_kv_append
+    assert f(ctypes.byref(c), 0, 0x1000, 1, 0x2000, None, None) == 1
+    assert f(ctypes.byref(c), 0x1000, 0x1000, -1, 0x2000, None, None) == 2
+    assert f(ctypes.byref(c), 0x1000, 0x1000, 257, 0x2000, None, None) == 3
+    assert f(ctypes.byref(c), 0x1008, 0x1000, 1, 0x2000, None, None) == 7
+    assert f(ctypes.byref(c), 0x1000, 0x1000, 0, 0x2000, None, None) == 0  # nothing to do
+
+
+def test_reduce_partial_and_plan_argument_errors(L):
+    assert L.tq_sdpa_int4_reduce(0, 0x10, 0x10, 1, 1, 128, 1, 0x10, None) == 1
+    assert L.tq_sdpa_int4_reduce(0x10, 0x10, 0x10, 1, 1, 128, 0, 0x10, None) == 2
+    assert L.tq_sdpa_int4_reduce(0x10, 0x10, 0x10, 1, 1, 128, 20000, 0x10, None) == 2
+    assert L.tq_sdpa_int4_reduce(0x10, 0x10, 0x10, 1, 1, 96, 1, 0x10, None) == 6
+    c = _fake_cache()
+    f = L.tq_sdpa_int4_partial
+    assert f(ctypes.byref(c), 0x1000, 8, 0x2000, 256, ctypes.c_float(1.0), 512, 1, 0x3000, 0, 0x4000, None, 0,
+             None) == 1
+    assert f(ctypes.byref(c), 0x1000, 8, 0x2000, 256, ctypes.c_float(1.0), 512, -1, 0x3000, 0x3000, 0x4000, None,
+             0, None) == 2
+    cps, ns = ctypes.c_int32(), ctypes.c_int32()
+    assert L.tq_sdpa_plan(ctypes.byref(c), 8, 256, 500, 0, ctypes.byref(cps), ctypes.byref(ns)) == 2
+    assert L.tq_sdpa_plan(ctypes.byref(c), 8, 256, 512, 0, None, ctypes.byref(ns)) == 1
+    assert L.tq_sdpa_plan(ctypes.byref(c), 8, 256, 512, 7, ctypes.byref(cps), ctypes.byref(ns)) == 6
+
+
+def test_carve_layout(L):
+    c = tq.tq_kv_cache()
+    assert L.tq_kv_cache_carve(ctypes.byref(c), 0x10000, 2, 8, 128, 64, 64) == 0
+    rows = 2 * 8 * 64
+    assert c.v_codes - c.k_codes == rows * 64
+    assert c.k_scale - c.k_codes == 2 * rows * 64
+    assert c.k_bias - c.k_scale == rows * 2 * 2
+    assert (c.capacity, c.head_dim, c.num_kv_heads, c.batch) == (64, 128, 8, 2)
+    assert L.tq_kv_cache_carve(ctypes.byref(c), 0x10010, 2, 8, 128, 64, 64) == 7
