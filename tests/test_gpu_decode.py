@@ -1,0 +1,244 @@
+"""GPU fused int4 decode attention vs the fp64 CPU oracle.
+
+Bar: output within 2e-3 max-abs and 1e-3 relative L2 of fp64 attention over
+the dequantised cache (fp32 accumulation on the GPU, fp16 output).  The GPU
+side quantizes with its own kernel; the oracle quantizes the same fp16 inputs
+itself.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from int4_kv_cache_gb300 import synth
+from tests.gpu_helpers import ATOL, assert_close, decode, gpu_cache_from_fp16, gpu_cache_from_oracle, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+IMPLS = [1, 2]  # TQ_IMPL_MMA, TQ_IMPL_SIMT
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("name", ["tiny", "llama70b_1k", "gemma_33", "gemma_423", "gemma_786", "gemma_950"])
+def test_decode_matches_oracle(name, impl):
+    need_gpu()
+    w = synth.WORKLOADS[name]
+    x = w.draw()
+    cache = gpu_cache_from_fp16(x.k, x.v)
+    out = decode(cache, x.q, x.lens, int(x.lens.max()), w.attn_scale, impl=impl)
+    ref = oracle.attention(x.q, oracle.Cache.from_fp16(x.k, x.v), x.lens, w.attn_scale)
+    assert_close(out, ref, what=f"{name}/impl{impl}")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_decode_llama_16k_all_heads(impl):
+    need_gpu()
+    w = synth.WORKLOADS["llama70b_16k"]
+    x = w.draw()
+    cache = gpu_cache_from_fp16(x.k, x.v)
+    out = decode(cache, x.q, x.lens, w.seq_len, w.attn_scale, impl=impl)
+    ref = oracle.attention(x.q, oracle.Cache.from_fp16(x.k, x.v), x.lens, w.attn_scale)
+    assert_close(out, ref, what=f"llama16k/impl{impl}")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 8, 2), (64, 8, 8), (256, 16, 2), (128, 8, 1)])
+def test_ragged_lengths_and_tails(D, Hq, Hkv, impl):
+    """Lengths that are not multiples of 16 / 64 / 512, a zero-length
+    sequence, a single-token sequence, and the capacity itself, at several
+    chunk sizes (split-K invariance)."""
+    need_gpu()
+    lens = np.array([0, 1, 17, 511, 513, 1000, 1024, 1040], dtype=np.int32)
+    x = synth.decode_inputs(31 + D, len(lens), Hq, Hkv, D, 1040, lens=lens)
+    cache = gpu_cache_from_fp16(x.k, x.v)
+    a = 1 / math.sqrt(D)
+    ref = oracle.attention(x.q, oracle.Cache.from_fp16(x.k, x.v), lens, a)
+    for chunk in (16, 64, 512, 2048):
+        out = decode(cache, x.q, lens, int(lens.max()), a, chunk=chunk, impl=impl)
+        assert np.all(out[0] == 0.0)  # empty sequence -> zero row
+        assert_close(out, ref, what=f"D{D} chunk{chunk} impl{impl}")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_oracle_quantised_cache_decode(impl):
+    """Decode over a cache the oracle quantized (isolates attention from the
+    quantize kernel)."""
+    need_gpu()
+    w = synth.WORKLOADS["llama70b_1k"]
+    x = w.draw()
+    oc = oracle.Cache.from_fp16(x.k, x.v)
+    cache = gpu_cache_from_oracle(oc)
+    out = decode(cache, x.q, x.lens, int(x.lens.max()), w.attn_scale, impl=impl)
+    assert_close(out, oracle.attention(x.q, oc, x.lens, w.attn_scale), what="oracle cache")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_single_token_gives_value(impl):
+    need_gpu()
+    x = synth.decode_inputs(5, 2, 16, 2, 128, 1)
+    cache = gpu_cache_from_fp16(x.k, x.v)
+    out = decode(cache, x.q, x.lens, 1, 0.3, impl=impl)
+    oc = oracle.Cache.from_fp16(x.k, x.v)
+    vh = oracle.dequantize_rows(oc.vc, oc.vs, oc.vb)
+    for h in range(16):
+        np.testing.assert_allclose(out[:, h], vh[:, h // 8, 0], atol=ATOL, rtol=0)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_needles_at_chunk_edges(impl):
+    """One key per KV head aligned with its group's first query (score margin
+    >= 30): that head's output is the needle's value.  Placed at 0, 15/16,
+    511/512 and S-1."""
+    need_gpu()
+    B, Hq, Hkv, D, S = 1, 8, 2, 128, 1536
+    rng = np.random.default_rng(21)
+    q = rng.choice([-1.0, 1.0], size=(B, Hq, D)).astype(np.float16)
+    k = (rng.standard_normal((B, Hkv, S, D)) * 0.02).astype(np.float16)
+    v = rng.standard_normal((B, Hkv, S, D)).astype(np.float16)
+    for pos in (0, 15, 16, 511, 512, S - 1):
+        kk = k.copy()
+        for h in range(Hkv):
+            kk[0, h, pos] = q[0, h * (Hq // Hkv)]
+        cache = gpu_cache_from_fp16(kk, v)
+        out = decode(cache, q, [S], S, 1.0, impl=impl)
+        oc = oracle.Cache.from_fp16(kk, v)
+        ref = oracle.attention(q, oc, np.array([S]), 1.0)
+        assert_close(out, ref, what=f"needle@{pos}")
+        vh = oracle.dequantize_rows(oc.vc, oc.vs, oc.vb)
+        for h in range(Hkv):
+            np.testing.assert_allclose(out[0, h * (Hq // Hkv)], vh[0, h, pos], atol=ATOL)
+
+
+def test_partials_match_oracle_chunks():
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    lens = np.array([700, 1100], dtype=np.int32)
+    x = synth.decode_inputs(41, 2, 16, 2, 128, 1100, lens=lens, outliers=True)
+    cache = gpu_cache_from_fp16(x.k, x.v)
+    oc = oracle.Cache.from_fp16(x.k, x.v)
+    a = 1 / math.sqrt(128)
+    for chunk in (64, 512):
+        om, ol, oa = oracle.attention_partials(x.q, oc, lens, a, chunk)
+        for impl in IMPLS:
+            m, l, acc = tq.tq_sdpa_int4_partial(cache, torch.from_numpy(x.q).cuda(), torch.from_numpy(lens).cuda(),
+                                                1100, a, chunk=chunk, chunks_per_split=1, impl=impl)
+            torch.cuda.synchronize()
+            m, l, acc = m.cpu().numpy(), l.cpu().numpy(), acc.cpu().numpy()
+            empty = ol == 0
+            assert np.array_equal(l == 0, empty)
+            assert np.all(np.isneginf(m[empty]))
+            ne = ~empty
+            np.testing.assert_allclose(m[ne], om[ne], rtol=1e-5, atol=1e-5)
+            np.testing.assert_allclose(l[ne], ol[ne], rtol=1e-3)
+            # acc / l is the attention output over that chunk
+            assert_close(acc[ne] / l[ne][:, None], oa[ne] / ol[ne][:, None], what=f"chunk{chunk} impl{impl}")
+
+
+def test_decode_equals_partial_plan_plus_reduce():
+    """tq_sdpa_int4_decode == phase 1 with the decode's own plan + phase 2."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    w = synth.WORKLOADS["llama70b_16k"]
+    x = w.draw()
+    cache = gpu_cache_from_fp16(x.k, x.v)
+    q = torch.from_numpy(x.q).cuda()
+    lens = torch.from_numpy(x.lens).cuda()
+    full = decode(cache, x.q, x.lens, w.seq_len, w.attn_scale)
+    m, l, acc = tq.tq_sdpa_int4_partial(cache, q, lens, w.seq_len, w.attn_scale, chunks_per_split=0)
+    two = tq.tq_sdpa_int4_reduce(m, l, acc).float().cpu().numpy()
+    assert np.array_equal(full, two.astype(np.float64))
+
+
+def test_reduce_matches_oracle_merge():
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    rng = np.random.default_rng(8)
+    B, Hq, n, D = 2, 4, 37, 128
+    m = rng.normal(0, 3, (B, Hq, n)).astype(np.float32)
+    l = rng.uniform(0.5, 50, (B, Hq, n)).astype(np.float32)
+    acc = rng.normal(0, 5, (B, Hq, n, D)).astype(np.float32)
+    l[0, 1, 5:] = 0.0
+    m[0, 1, 5:] = -np.inf
+    l[1, 3, :] = 0.0  # every part empty -> zero row
+    m[1, 3, :] = -np.inf
+    out = tq.tq_sdpa_int4_reduce(torch.from_numpy(m).cuda(), torch.from_numpy(l).cuda(), torch.from_numpy(acc).cuda())
+    torch.cuda.synchronize()
+    ref = oracle.merge_partials(m.astype(np.float64), l.astype(np.float64), acc.astype(np.float64))
+    got = out.float().cpu().numpy()
+    assert np.all(got[1, 3] == 0)
+    np.testing.assert_allclose(got, ref, atol=1e-3 + 1e-3 * np.abs(ref))
+
+
+def test_determinism_and_impl_agreement():
+    need_gpu()
+    w = synth.WORKLOADS["llama70b_1k"]
+    x = w.draw()
+    cache = gpu_cache_from_fp16(x.k, x.v)
+    o1 = decode(cache, x.q, x.lens, 1024, w.attn_scale, impl=1)
+    o2 = decode(cache, x.q, x.lens, 1024, w.attn_scale, impl=1)
+    assert np.array_equal(o1, o2)
+    o3 = decode(cache, x.q, x.lens, 1024, w.attn_scale, impl=2)
+    assert np.abs(o1 - o3).max() <= 2 * ATOL
+
+
+def test_seq_len_beyond_bound_sets_status_and_clamps():
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    x = synth.decode_inputs(12, 2, 8, 2, 128, 64)
+    cache = gpu_cache_from_fp16(x.k, x.v)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = decode(cache, x.q, [64, 64], 48, 0.1, status=st)  # lens above max_seq_len = 48
+    assert int(st.item()) & tq.TQ_DEV_SEQ_LEN
+    oc = oracle.Cache.from_fp16(x.k, x.v)
+    assert_close(out, oracle.attention(x.q, oc, np.array([48, 48]), 0.1), what="clamped")
+
+
+def test_llama_128k_full_size_sampled():
+    """The headline shape at full size (one layer, 128K tokens, 64 q / 8 kv
+    heads) in the launch configuration the benchmark times; the oracle
+    computes a seeded sample of heads one by one."""
+    need_gpu()
+    w = synth.WORKLOADS["llama70b_128k"]
+    q, k, v, _ = synth.torch_decode_inputs(w.seed, 1, 64, 8, 128, w.seq_len, outliers=True)
+    cache = gpu_cache_from_fp16(k, v)
+    lens = np.array([w.seq_len], np.int32)
+    out = decode(cache, q, lens, w.seq_len, w.attn_scale)
+    qh = q.cpu().numpy()
+    for h in (0, 13, 27, 38, 45, 63):
+        kvh = h // 8
+        oc = oracle.Cache.from_fp16(np.ascontiguousarray(k[:, kvh:kvh + 1].cpu().numpy()),
+                                    np.ascontiguousarray(v[:, kvh:kvh + 1].cpu().numpy()))
+        ref = oracle.attention(np.ascontiguousarray(qh[:, h:h + 1]), oc, lens, w.attn_scale)
+        assert_close(out[:, h:h + 1], ref, what=f"128k head {h}")
+
+
+def test_ragged32_decode_step_full_size_sampled():
+    """32 sequences with lengths uniform in [1K, 32K]: append one token per
+    sequence at position len[b], then decode over len[b] + 1.  Sampled rows are
+    checked against the oracle, which quantizes the same fp16 inputs."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    w = synth.WORKLOADS["ragged32"]
+    lens = synth.ragged_lengths(w.seed, 32, 1024, 32768)
+    q, k, v, chans = synth.torch_decode_inputs(w.seed, 32, 64, 8, 128, 32768, outliers=True)
+    cache = gpu_cache_from_fp16(k, v, capacity=32768 + 16)
+    kn, vn = synth.append_tokens(w.seed, 0, 32, 8, 128, 1, outliers=chans)
+    tq.tq_quantize_kv_append(cache, torch.from_numpy(kn).cuda(), torch.from_numpy(vn).cuda(),
+                             torch.from_numpy(lens).cuda())
+    new_lens = lens + 1
+    out = decode(cache, q, new_lens, int(new_lens.max()), w.attn_scale)
+    qh = q.cpu().numpy()
+    rng = np.random.default_rng(5)
+    for b, h in zip(rng.choice(32, 6, replace=False), rng.integers(0, 64, 6)):
+        kvh, L = h // 8, int(lens[b])
+        kk = np.concatenate([k[b:b + 1, kvh:kvh + 1, :L].cpu().numpy(), kn[b:b + 1, kvh:kvh + 1]], axis=2)
+        vv = np.concatenate([v[b:b + 1, kvh:kvh + 1, :L].cpu().numpy(), vn[b:b + 1, kvh:kvh + 1]], axis=2)
+        oc = oracle.Cache.from_fp16(kk, vv)
+        ref = oracle.attention(np.ascontiguousarray(qh[b:b + 1, h:h + 1]), oc, np.array([L + 1]), w.attn_scale)
+        assert_close(out[b:b + 1, h:h + 1], ref, what=f"ragged b{b} h{h}")
