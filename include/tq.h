@@ -198,7 +198,7 @@ tq_status tq_sdpa_int4_partial(const tq_kv_cache* cache, const uint16_t* q,
  *   M = max over parts with l > 0 of m,  w_c = exp(m_c - M),
  *   out = sum_c w_c acc_c / sum_c w_c l_c   (fp16, RNE; all-empty rows -> 0).
  * Inputs laid out as tq_sdpa_int4_partial writes them, n_parts per (b, h),
- * 1 <= n_parts <= 12288. */
+ * 1 <= n_parts <= 8192. */
 tq_status tq_sdpa_int4_reduce(const float* part_m, const float* part_l,
                               const float* part_acc, int32_t batch,
                               int32_t num_q_heads, int32_t head_dim,

@@ -27,8 +27,9 @@
 //    The high-nibble elements meet q/16 in the B operand (the pages' qdot
 //    "pre-divide the query" idea), so all products carry the same 2^-24.
 //  * P.V uses mma.sync with M = 16 head_dim elements, N = 8 heads, K = 16
-//    tokens.  B = (p_t * vscale_tg) in fp16, built from the score fragments
-//    with movmatrix (no shared-memory round trip); the bias part
+//    tokens.  B = p_t * vscale_tg as an fp16 hi/lo pair (two MMAs into the same
+//    fp32 accumulator, ~2^-22 relative), built from the score fragments with
+//    movmatrix (no shared-memory round trip); the bias part
 //    sum_t p_t * vbias_tg is accumulated in fp32 on the side.
 //  * Token order inside a 16-token tile and the head_dim order inside each
 //    operand are chosen so that every ldmatrix is bank-conflict free against
@@ -354,7 +355,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
             load_row_sb<NG>(vb_s, tb + r0, vba);
             load_row_sb<NG>(vs_s, tb + r1, vsb);
             load_row_sb<NG>(vb_s, tb + r1, vbb);
-            uint32_t bfrag[NG][2];
+            // B operand p_t * vscale_tg as an fp16 pair hi + lo (hi = fp16(r), lo =
+            // fp16(r - hi)): one fp16 rounding of r would leave 2^-12 relative noise
+            // on every term of sum_t r_t n_t, which the code offset (n in 0..15, mean
+            // near 7.5) amplifies well past the 1e-3 output budget at long context.
+            uint32_t bhi[NG][2], blo[NG][2];
 #pragma unroll
             for (int g = 0; g < NG; ++g) {
                 // masked rows may hold stale scale/bias bits: select, never multiply
@@ -362,8 +367,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
                 const float ba = va ? vba[g] : 0.0f, bb = vb ? vbb[g] : 0.0f;
                 e_run[g][0] = fmaf(pr[0], ba, fmaf(pr[2], bb, e_run[g][0]));
                 e_run[g][1] = fmaf(pr[1], ba, fmaf(pr[3], bb, e_run[g][1]));
-                bfrag[g][0] = movmatrix_trans(pack_half2(pr[0] * sa, pr[1] * sa));
-                bfrag[g][1] = movmatrix_trans(pack_half2(pr[2] * sb, pr[3] * sb));
+                const float r0 = pr[0] * sa, r1 = pr[1] * sa, r2 = pr[2] * sb, r3 = pr[3] * sb;
+                const __half2 h01 = __floats2half2_rn(r0, r1), h23 = __floats2half2_rn(r2, r3);
+                const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+                bhi[g][0] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h01));
+                bhi[g][1] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h23));
+                blo[g][0] = movmatrix_trans(pack_half2(r0 - f01.x, r1 - f01.y));
+                blo[g][1] = movmatrix_trans(pack_half2(r2 - f23.x, r3 - f23.y));
             }
 #pragma unroll
             for (int sp = 0; sp < C::SPT / 2; ++sp) {
@@ -375,11 +385,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
                     const int g = (32 * s) / kGroup;
                     const uint32_t xa = e ? x2 : x0;  // tokens of rows 0..7  (k 0..7)
                     const uint32_t xb = e ? x3 : x1;  // tokens of rows 8..15 (k 8..15)
-                    mma_16816(acc[2 * s], xa & kLoNib, xa & kHiNib, xb & kLoNib, xb & kHiNib, bfrag[g][0],
-                              bfrag[g][1]);
+                    const uint32_t a0 = xa & kLoNib, a1 = xa & kHiNib, a2 = xb & kLoNib, a3 = xb & kHiNib;
+                    mma_16816(acc[2 * s], a0, a1, a2, a3, bhi[g][0], bhi[g][1]);
+                    mma_16816(acc[2 * s], a0, a1, a2, a3, blo[g][0], blo[g][1]);
                     const uint32_t ya = xa >> 8, yb = xb >> 8;
-                    mma_16816(acc[2 * s + 1], ya & kLoNib, ya & kHiNib, yb & kLoNib, yb & kHiNib, bfrag[g][0],
-                              bfrag[g][1]);
+                    const uint32_t c0 = ya & kLoNib, c1 = ya & kHiNib, c2 = yb & kLoNib, c3 = yb & kHiNib;
+                    mma_16816(acc[2 * s + 1], c0, c1, c2, c3, bhi[g][0], bhi[g][1]);
+                    mma_16816(acc[2 * s + 1], c0, c1, c2, c3, blo[g][0], blo[g][1]);
                 }
             }
         }

@@ -6,7 +6,8 @@
 // with a per-group scale and bias).  The rounding rule is the one stated in
 // tq.h; every step is a single IEEE fp32 operation with round-to-nearest-even
 // (__fsub_rn / __fdiv_rn / __float2int_rn), so codes, scales and biases are
-// bit-identical to the CPU oracle.
+// bit-identical to the CPU oracle.  The per-element division is replaced by a
+// multiply with the reciprocal wherever that provably rounds to the same code.
 //
 // Work split: eight lanes own one group of 64 elements (16 bytes = 8 halves
 // each), which makes every global access a 16-byte (input) or 4-byte (codes)
@@ -53,9 +54,17 @@ __device__ __forceinline__ GroupQ quantize_lane8(uint4 raw) {
     const float b = __half2float(g.bias);
     uint32_t codes = 0;
     if (s != 0.0f) {
+        // t = fp32(d / s) is rounded to an integer.  d * fp32(1/s) is within
+        // 2^-22 relative (< 4e-6 absolute, as t <= 15.01) of that quotient, so
+        // both round to the same integer unless a half-integer lies within 4e-6
+        // of the product: only then is the IEEE division itself evaluated.
+        const float rs = __frcp_rn(s);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            int c = __float2int_rn(__fdiv_rn(__fsub_rn(x[i], b), s));
+            const float d = __fsub_rn(x[i], b);  // >= 0: x >= the group minimum
+            float t = __fmul_rn(d, rs);
+            if (fabsf(t - floorf(t) - 0.5f) < 1.0e-5f) t = __fdiv_rn(d, s);
+            int c = __float2int_rn(t);
             c = min(max(c, 0), 15);
             codes |= static_cast<uint32_t>(c) << (4 * i);
         }

@@ -4,9 +4,9 @@
 //
 // Per (b, h):  M = max_c m_c over parts with l_c > 0,  w_c = e^{m_c - M},
 //              out = sum_c w_c acc_c / sum_c w_c l_c   (fp16, RNE; 0 if empty)
-// One CTA per (b, h); the weights go through shared memory once, then each
-// thread owns head_dim elements.  Launched as a programmatic dependent of
-// phase 1, it waits for phase 1's memory before the first read.
+// One CTA per (b, h); the weights go through shared memory once, then the
+// warps split the parts between them.  Launched as a programmatic dependent
+// of phase 1, it waits for phase 1's memory before the first read.
 #include <math.h>
 
 #include "tq_device.cuh"
@@ -16,7 +16,8 @@ namespace tq {
 
 namespace {
 
-constexpr int kReduceThreads = 128;
+constexpr int kReduceThreads = 256;
+constexpr int kReduceWarps = kReduceThreads / 32;
 
 __device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -29,18 +30,25 @@ __device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) 
     __syncthreads();
     float r = red[0];
 #pragma unroll
-    for (int w = 1; w < kReduceThreads / 32; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+    for (int w = 1; w < kReduceWarps; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
     __syncthreads();
     return r;
 }
 
+// Warp w sums parts w, w + 8, ...; lane owns head_dim elements
+// [lane * V, lane * V + V), read with vector loads; the eight warp sums are
+// combined through shared memory.
+template <int D>
 __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceParams p) {
+    constexpr int V = D / 32;
     extern __shared__ float w_s[];  // [n_parts]
-    __shared__ float red[kReduceThreads / 32];
+    __shared__ float red[kReduceWarps];
+    __shared__ float part_sum[kReduceWarps][D];
     pdl_wait_primary();
 
     const long long bh = blockIdx.x;
-    const int n = p.n_parts, D = p.head_dim;
+    const int n = p.n_parts;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float* pm = p.part_m + bh * n;
     const float* pl = p.part_l + bh * n;
     const float* pa = p.part_acc + bh * n * D;
@@ -58,13 +66,37 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReducePara
     }
     L = block_reduce(L, red, false);  // its barriers also publish w_s
 
-    for (int d = threadIdx.x; d < D; d += kReduceThreads) {
-        float a = 0.0f;
-        for (int c = 0; c < n; ++c) {
-            const float w = w_s[c];
-            if (w != 0.0f) a = fmaf(w, pa[static_cast<long long>(c) * D + d], a);
+    float a[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) a[i] = 0.0f;
+#pragma unroll 4
+    for (int c = warp; c < n; c += kReduceWarps) {
+        const float w = w_s[c];
+        if (w == 0.0f) continue;  // empty part (same branch for the whole warp)
+        const float* src = pa + static_cast<long long>(c) * D + lane * V;
+        if constexpr (V == 2) {
+            const float2 x = *reinterpret_cast<const float2*>(src);
+            a[0] = fmaf(w, x.x, a[0]);
+            a[1] = fmaf(w, x.y, a[1]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < V; i += 4) {
+                const float4 x = *reinterpret_cast<const float4*>(src + i);
+                a[i] = fmaf(w, x.x, a[i]);
+                a[i + 1] = fmaf(w, x.y, a[i + 1]);
+                a[i + 2] = fmaf(w, x.z, a[i + 2]);
+                a[i + 3] = fmaf(w, x.w, a[i + 3]);
+            }
         }
-        p.out[bh * D + d] = __half_as_ushort(__float2half_rn(L > 0.0f ? __fdiv_rn(a, L) : 0.0f));
+    }
+#pragma unroll
+    for (int i = 0; i < V; ++i) part_sum[warp][lane * V + i] = a[i];
+    __syncthreads();
+    for (int d = threadIdx.x; d < D; d += kReduceThreads) {
+        float t = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kReduceWarps; ++w) t += part_sum[w][d];
+        p.out[bh * D + d] = __half_as_ushort(__float2half_rn(L > 0.0f ? __fdiv_rn(t, L) : 0.0f));
     }
 }
 
@@ -81,7 +113,12 @@ cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl_s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_secondary ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, reduce_kernel, p);
+    switch (p.head_dim) {
+        case 64: return cudaLaunchKernelEx(&cfg, reduce_kernel<64>, p);
+        case 128: return cudaLaunchKernelEx(&cfg, reduce_kernel<128>, p);
+        case 256: return cudaLaunchKernelEx(&cfg, reduce_kernel<256>, p);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace tq

@@ -69,6 +69,6 @@ int mma_smem_bytes(int head_dim);
 int mma_ctas_per_sm(int head_dim);
 int simt_ctas_per_sm(int head_dim);
 // Largest n_parts the reduce kernel takes (its weights live in shared memory).
-constexpr int kMaxReduceParts = 12288;
+constexpr int kMaxReduceParts = 8192;
 
 }  // namespace tq

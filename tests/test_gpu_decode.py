@@ -170,7 +170,7 @@ def test_reduce_matches_oracle_merge():
     ref = oracle.merge_partials(m.astype(np.float64), l.astype(np.float64), acc.astype(np.float64))
     got = out.float().cpu().numpy()
     assert np.all(got[1, 3] == 0)
-    np.testing.assert_allclose(got, ref, atol=1e-3 + 1e-3 * np.abs(ref))
+    assert np.all(np.abs(got - ref) <= 1e-3 + 1e-3 * np.abs(ref))  # fp16 output rounding
 
 
 def test_determinism_and_impl_agreement():
