@@ -30,7 +30,9 @@
 //    tokens.  B = p_t * vscale_tg as an fp16 hi/lo pair (two MMAs into the same
 //    fp32 accumulator, ~2^-22 relative), built from the score fragments with
 //    movmatrix (no shared-memory round trip); the bias part
-//    sum_t p_t * vbias_tg is accumulated in fp32 on the side.
+//    sum_t p_t * vbias_tg is accumulated in fp32 on the side.  Each 16-token
+//    tile's code sum is formed in fresh tensor-core accumulators and added to
+//    the running state with round-to-nearest fp32 adds.
 //  * Token order inside a 16-token tile and the head_dim order inside each
 //    operand are chosen so that every ldmatrix is bank-conflict free against
 //    the swizzled tile; the permutation is undone when the state is written.
@@ -375,6 +377,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
                 blo[g][0] = movmatrix_trans(pack_half2(r0 - f01.x, r1 - f01.y));
                 blo[g][1] = movmatrix_trans(pack_half2(r2 - f23.x, r3 - f23.y));
             }
+            // This tile's sum_t r_t n_t goes into fresh tensor-core accumulators
+            // and is then added to the running state with round-to-nearest fp32
+            // adds.  The code sum is ~7.5 sum_t r_t while the attention output is
+            // what is left after the bias term cancels most of it, so a long
+            // chain of tensor-core accumulations (whose fp32 sums are not
+            // round-to-nearest) would leave a systematic error far above 1e-3
+            // of the output at long context.
+            float tile[C::NKS][4];
+#pragma unroll
+            for (int i = 0; i < C::NKS; ++i) tile[i][0] = tile[i][1] = tile[i][2] = tile[i][3] = 0.0f;
 #pragma unroll
             for (int sp = 0; sp < C::SPT / 2; ++sp) {
                 uint32_t x0, x1, x2, x3;
@@ -386,13 +398,18 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
                     const uint32_t xa = e ? x2 : x0;  // tokens of rows 0..7  (k 0..7)
                     const uint32_t xb = e ? x3 : x1;  // tokens of rows 8..15 (k 8..15)
                     const uint32_t a0 = xa & kLoNib, a1 = xa & kHiNib, a2 = xb & kLoNib, a3 = xb & kHiNib;
-                    mma_16816(acc[2 * s], a0, a1, a2, a3, bhi[g][0], bhi[g][1]);
-                    mma_16816(acc[2 * s], a0, a1, a2, a3, blo[g][0], blo[g][1]);
+                    mma_16816(tile[2 * s], a0, a1, a2, a3, bhi[g][0], bhi[g][1]);
+                    mma_16816(tile[2 * s], a0, a1, a2, a3, blo[g][0], blo[g][1]);
                     const uint32_t ya = xa >> 8, yb = xb >> 8;
                     const uint32_t c0 = ya & kLoNib, c1 = ya & kHiNib, c2 = yb & kLoNib, c3 = yb & kHiNib;
-                    mma_16816(acc[2 * s + 1], c0, c1, c2, c3, bhi[g][0], bhi[g][1]);
-                    mma_16816(acc[2 * s + 1], c0, c1, c2, c3, blo[g][0], blo[g][1]);
+                    mma_16816(tile[2 * s + 1], c0, c1, c2, c3, bhi[g][0], bhi[g][1]);
+                    mma_16816(tile[2 * s + 1], c0, c1, c2, c3, blo[g][0], blo[g][1]);
                 }
+            }
+#pragma unroll
+            for (int i = 0; i < C::NKS; ++i) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[i][c] = __fadd_rn(acc[i][c], tile[i][c]);
             }
         }
         __syncwarp();
