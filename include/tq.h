@@ -204,6 +204,35 @@ tq_status tq_sdpa_int4_reduce(const float* part_m, const float* part_l,
                               int32_t num_q_heads, int32_t head_dim,
                               int32_t n_parts, uint16_t* out, void* stream);
 
+/* Size of the library-owned device array tq_sdpa_int4_decode_noalloc keeps its
+ * partial states in (per GPU that loads the library, held until exit). */
+#define TQ_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* Fused int4 decode attention for callers that cannot allocate device memory.
+ * The pages have no counterpart of this entry point.  It is
+ * tq_sdpa_int4_decode (tensor-core path) without the workspace argument: the
+ * split-K partial states go to a fixed TQ_NOALLOC_SCRATCH_BYTES device array
+ * inside the library, so the call allocates nothing.  Meant for callers that
+ * have no allocator at hand or may not use one: code in host callbacks or
+ * other paths where cudaMalloc is forbidden, plugins of frameworks that own
+ * all device memory, plain C programs that link only this library.
+ *   - Same arguments, layouts and results as tq_sdpa_int4_decode.
+ *   - Requests whose partial states do not fit the array
+ *     (batch * num_q_heads * n_splits * (head_dim + 2) * 4 bytes, n_splits as
+ *     tq_sdpa_plan reports) return TQ_ERR_WORKSPACE before any launch.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents; nothing in it needs clearing (each call writes every element
+ *     it reads), but calls that overlap on the GPU (other streams, other host
+ *     threads) race on it and may return wrong results: serialise them. */
+tq_status tq_sdpa_int4_decode_noalloc(const tq_kv_cache* cache, const uint16_t* q,
+                                      int32_t num_q_heads, const int32_t* seq_lens,
+                                      int32_t max_seq_len, float attn_scale,
+                                      int32_t chunk, uint16_t* out,
+                                      int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -19,7 +19,7 @@ __all__ = [
     "TQ_DEV_TIMEOUT", "TQError", "lib", "lib_path", "tq_kv_cache", "KVCache",
     "tq_abi_version", "tq_status_string", "tq_kv_cache_bytes", "tq_sdpa_workspace_bytes",
     "tq_quantize_kv_append", "tq_sdpa_int4_decode", "tq_sdpa_int4_partial", "tq_sdpa_int4_reduce",
-    "tq_sdpa_plan",
+    "tq_sdpa_plan", "tq_sdpa_int4_decode_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 TQ_OK = 0
@@ -27,6 +27,7 @@ TQ_IMPL_AUTO, TQ_IMPL_MMA, TQ_IMPL_SIMT = 0, 1, 2
 TQ_DEV_WRITE_POS, TQ_DEV_SEQ_LEN, TQ_DEV_TIMEOUT = 0x1, 0x2, 0x4
 GROUP_SIZE = 64
 DEFAULT_CHUNK = 512
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -81,6 +82,7 @@ def lib() -> ctypes.CDLL:
             "tq_sdpa_plan": ([C, i32, i32, i32, i32, P, P], i32),
             "tq_sdpa_int4_partial": ([C, P, i32, P, i32, f32, i32, i32, P, P, P, P, i32, P], i32),
             "tq_sdpa_int4_reduce": ([P, P, P, i32, i32, i32, i32, P, P], i32),
+            "tq_sdpa_int4_decode_noalloc": ([C, P, i32, P, i32, f32, i32, P, P, P], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -260,4 +262,25 @@ def tq_sdpa_int4_reduce(m: torch.Tensor, l: torch.Tensor, acc: torch.Tensor, out
     _need(out, torch.float16, "out")
     _check("tq_sdpa_int4_reduce", lib().tq_sdpa_int4_reduce(_ptr(m), _ptr(l), _ptr(acc), B, Hq, D, n, _ptr(out),
                                                             _stream(stream)))
+    return out
+
+
+def tq_sdpa_int4_decode_noalloc(cache: KVCache, q: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                                attn_scale: float, out: Optional[torch.Tensor] = None, chunk: int = DEFAULT_CHUNK,
+                                status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """tq_sdpa_int4_decode without a workspace: the partial states live in a
+    fixed 4 MiB device array owned by the library (for callers that cannot
+    allocate).  Calls that overlap on the GPU share that array and race."""
+    _need(q, torch.float16, "q")
+    _need(seq_lens, torch.int32, "seq_lens")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.float16, "out")
+    if status is not None:
+        _need(status, torch.int32, "status")
+    if q.dim() != 3 or q.shape[0] != cache.batch or q.shape[2] != cache.head_dim or out.shape != q.shape:
+        raise ValueError(f"q must be [B, Hq, D]; got {tuple(q.shape)}")
+    _check("tq_sdpa_int4_decode_noalloc", lib().tq_sdpa_int4_decode_noalloc(
+        cache.ref(), _ptr(q), q.shape[1], _ptr(seq_lens), int(max_seq_len), float(attn_scale), int(chunk),
+        _ptr(out), _ptr(status), _stream(stream)))
     return out

@@ -200,6 +200,46 @@ tq_status run_phase1(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, co
 
 }  // namespace
 
+namespace tq {
+
+// Phase 1 + phase 2 with the partial states placed in `partials`
+// (`partials_bytes` long, 256-byte aligned) instead of a caller workspace.
+// Requests whose partial states do not fit are refused with TQ_ERR_WORKSPACE
+// before anything is launched.
+tq_status decode_into_partials(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
+                               int32_t max_seq_len, float attn_scale, int32_t chunk, uint8_t* partials,
+                               size_t partials_bytes, uint16_t* out, int32_t* status, cudaStream_t stream) {
+    tq_status s = check_decode_args(cache, q, hq, seq_lens, max_seq_len, chunk, out);
+    if (s != TQ_OK) return s;
+    if (partials == nullptr) return TQ_ERR_WORKSPACE;
+    Plan pl;
+    s = device_plan(cache, max_seq_len, chunk, TQ_IMPL_MMA, &pl);
+    if (s != TQ_OK) return s;
+    if (pl.n_splits > kMaxReduceParts) return TQ_ERR_SHAPE;
+    const size_t parts = static_cast<size_t>(cache->batch) * hq * pl.n_splits;
+    const size_t need = 2 * align256(parts * sizeof(float)) + parts * cache->head_dim * sizeof(float);
+    if (need > partials_bytes) return TQ_ERR_WORKSPACE;
+    float* pm = reinterpret_cast<float*>(partials);
+    float* plv = reinterpret_cast<float*>(partials + align256(parts * sizeof(float)));
+    float* pa = reinterpret_cast<float*>(partials + 2 * align256(parts * sizeof(float)));
+    s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, TQ_IMPL_MMA, stream);
+    if (s != TQ_OK) return s;
+    ReduceParams r;
+    r.part_m = pm;
+    r.part_l = plv;
+    r.part_acc = pa;
+    r.out = out;
+    r.batch = cache->batch;
+    r.num_q_heads = hq;
+    r.head_dim = cache->head_dim;
+    r.n_parts = pl.n_splits;
+    return cuda_status(launch_reduce(r, stream, true));
+}
+
+tq_status record_cuda_status(cudaError_t e) { return cuda_status(e); }
+
+}  // namespace tq
+
 extern "C" {
 
 int32_t tq_abi_version(void) { return TQ_ABI_VERSION; }

@@ -71,4 +71,12 @@ int simt_ctas_per_sm(int head_dim);
 // Largest n_parts the reduce kernel takes (its weights live in shared memory).
 constexpr int kMaxReduceParts = 8192;
 
+// Decode (tensor-core phase 1 + reduce) with the partial states written to
+// `partials` (partials_bytes long); TQ_ERR_WORKSPACE if they do not fit.
+tq_status decode_into_partials(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
+                               int32_t max_seq_len, float attn_scale, int32_t chunk, uint8_t* partials,
+                               size_t partials_bytes, uint16_t* out, int32_t* status, cudaStream_t stream);
+// Map a CUDA error to TQ_ERR_CUDA and remember it for tq_last_cuda_error().
+tq_status record_cuda_status(cudaError_t e);
+
 }  // namespace tq
