@@ -143,6 +143,29 @@ class ClockSampler:
                 "power_w_max": max(r[2] for r in rows), "reasons": reasons, "samples": len(rows)}
 
 
+# ------------------------------------------------------------ replicas
+def layer_seed(rank: int, layer: int, base: int = SEED) -> int:
+    """Seed of one rank's layer cache: every replica draws its own inputs."""
+    return base + 1000 * rank + layer
+
+
+def max_over_ranks(values, world: int, device=None):
+    """Element-wise max of per-rank timings: the slowest replica sets the job time."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_gbs(bytes_per_rank_step: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's bytes over the slowest rank's step time."""
+    return bytes_per_rank_step * world / (ms_per_step * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------- our arm
 def make_layer_caches(tq, synth, torch, dev, n_layers, seed0):
     """n_layers caches of the 128K workload, prefilled by the quantize kernel.
@@ -176,7 +199,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     nl = args.layers
-    caches, qs, chans_all, prefill_ms = make_layer_caches(tq, synth, torch, dev, nl, SEED + 1000 * rank)
+    caches, qs, chans_all, prefill_ms = make_layer_caches(tq, synth, torch, dev, nl, layer_seed(rank, 0))
     k_new, v_new = [torch.from_numpy(a).to(dev)
                     for a in synth.append_tokens(SEED + rank, 0, B, HKV, D, 1, outliers=chans_all[0])]
     write_pos = torch.full((B,), S - 1, dtype=torch.int32, device=dev)  # the step's token is row S-1
@@ -276,15 +299,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     # ---- reduce over ranks: max time, summed work
     ms_per_step = ms_total / args.steps
     e2e_ms_per_step = e2e_ms / args.steps
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([ms_per_step, e2e_ms_per_step, phase1_us], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step, e2e_ms_per_step, phase1_us = t.tolist()
-    nbytes = step_bytes(S) * world
-    value = nbytes / (ms_per_step * 1e-3) / 1e9
-    e2e_value = nbytes / (e2e_ms_per_step * 1e-3) / 1e9
+    ms_per_step, e2e_ms_per_step, phase1_us = max_over_ranks([ms_per_step, e2e_ms_per_step, phase1_us], world, dev)
+    value = job_gbs(step_bytes(S), world, ms_per_step)
+    e2e_value = job_gbs(step_bytes(S), world, e2e_ms_per_step)
     p1_gbs = phase1_bytes(S) / (phase1_us * 1e-6) / 1e9
     pages_gbs = step_bytes(S) / (PAGES_128K_MS * 1e-3) / 1e9
     result = {
