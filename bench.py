@@ -204,7 +204,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                     for a in synth.append_tokens(SEED + rank, 0, B, HKV, D, 1, outliers=chans_all[0])]
     write_pos = torch.full((B,), S - 1, dtype=torch.int32, device=dev)  # the step's token is row S-1
     seq_lens = torch.full((B,), S, dtype=torch.int32, device=dev)
-    ws = torch.empty(tq.tq_sdpa_workspace_bytes(B, HQ, D, S, CHUNK), dtype=torch.uint8, device=dev)
+    ws = torch.empty(tq.tq_sdpa_workspace_bytes(B, HQ, HKV, D, S, CHUNK), dtype=torch.uint8, device=dev)
     out = torch.empty((B, HQ, D), dtype=torch.float16, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
@@ -220,7 +220,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             dist.barrier()
         torch.cuda.synchronize()
 
-    cps, n_splits = tq.tq_sdpa_plan(caches[0], HQ, S, CHUNK)
+    n_splits, run_tokens = tq.tq_sdpa_plan(caches[0], HQ, S, CHUNK)
     pm = torch.empty((B, HQ, n_splits), dtype=torch.float32, device=dev)
     pl = torch.empty_like(pm)
     pa = torch.empty((B, HQ, n_splits, D), dtype=torch.float32, device=dev)
@@ -244,7 +244,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             ev[i][0].record()
             tq.tq_quantize_kv_append(c, k_new, v_new, write_pos, status=status)
             ev[i][1].record()
-            tq.tq_sdpa_int4_partial(c, qs[i % nl], seq_lens, S, ATTN, chunk=CHUNK, chunks_per_split=cps,
+            tq.tq_sdpa_int4_partial(c, qs[i % nl], seq_lens, S, ATTN, chunk=CHUNK, chunks_per_split=0,
                                     status=status, out=(pm, pl, pa))
             ev[i][2].record()
             tq.tq_sdpa_int4_reduce(pm, pl, pa, out=out)
@@ -328,7 +328,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "l2": f"inputs larger than L2: {nl} rotated layer cache(s) "
                   f"({nl * cache_bytes(S) / 1e9:.2f} GB > 129 MB L2)",
             "bytes_per_step": step_bytes(S),
-            "splits": {"chunks_per_split": cps, "n_splits": n_splits},
+            "splits": {"n_splits_per_head": n_splits, "max_run_tokens": run_tokens},
         },
         "kernels_us": {"quantize_append": round(append_us, 3), "sdpa_phase1": round(phase1_us, 3),
                        "sdpa_reduce": round(reduce_us, 3)},
@@ -406,7 +406,7 @@ def run_full_model(args, tq, synth, torch, dev, peak):
     k_new, v_new = [torch.from_numpy(a).to(dev) for a in synth.append_tokens(SEED, 1, B, HKV, D, 1, outliers=chans[0])]
     write_pos = torch.full((B,), S - 1, dtype=torch.int32, device=dev)
     seq_lens = torch.full((B,), S, dtype=torch.int32, device=dev)
-    ws = torch.empty(tq.tq_sdpa_workspace_bytes(B, HQ, D, S, CHUNK), dtype=torch.uint8, device=dev)
+    ws = torch.empty(tq.tq_sdpa_workspace_bytes(B, HQ, HKV, D, S, CHUNK), dtype=torch.uint8, device=dev)
     out = torch.empty((B, HQ, D), dtype=torch.float16, device=dev)
 
     def model_step(_):

@@ -136,8 +136,8 @@ tq_status tq_quantize_kv_append(const tq_kv_cache* cache, const uint16_t* k_new,
 /* Workspace bytes tq_sdpa_int4_decode needs for these sizes (an upper bound
  * that does not depend on the device).  Host-only. */
 size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t num_q_heads,
-                               int32_t head_dim, int32_t max_seq_len,
-                               int32_t chunk);
+                               int32_t num_kv_heads, int32_t head_dim,
+                               int32_t max_seq_len, int32_t chunk);
 
 /* Fused int4 decode attention (Sq = 1, GQA).
  * q:        fp16 [batch][num_q_heads][head_dim]; query head h reads KV head
@@ -147,8 +147,12 @@ size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t num_q_heads,
  * max_seq_len: host bound on seq_lens (1 <= max_seq_len <= capacity); sizes the grid
  * attn_scale: multiplies q.k (1/sqrt(head_dim) for Llama, 1.0 for Gemma)
  * chunk:    split-K chunk in tokens (multiple of 16; TQ_DEFAULT_CHUNK = 512).
- *           Each CTA takes a run of whole chunks and keeps one running softmax
- *           state over them; the runs' states are merged by a log-sum-exp reduce.
+ *           The sequence is split into balanced runs, one per CTA, of whole
+ *           units of min(chunk, pipeline tile) tokens (the tile is 128 tokens
+ *           for head_dim <= 128, 64 for 256); each run keeps one running softmax
+ *           state and the runs' states are merged by a log-sum-exp reduce.  The
+ *           result is the same as merging one state per chunk (see
+ *           tq_sdpa_int4_partial with chunks_per_split = 1).
  * workspace: device scratch (256-byte aligned) of at least
  *           tq_sdpa_workspace_bytes(...) bytes holding the fp32 partial states;
  *           contents on entry are ignored.
@@ -170,18 +174,19 @@ tq_status tq_sdpa_int4_decode_impl(const tq_kv_cache* cache, const uint16_t* q,
                                    size_t workspace_bytes, uint16_t* out,
                                    int32_t* status, tq_impl impl, void* stream);
 
-/* The split plan tq_sdpa_int4_decode uses on the current device: each CTA
- * takes *chunks_per_split consecutive chunks, and there are *n_splits runs per
- * (sequence, kv head).  Host-side query (reads device attributes). */
+/* The split plan tq_sdpa_int4_decode uses on the current device: *n_splits
+ * runs per (sequence, kv head), the longest *max_run_tokens tokens long.
+ * Host-side query (reads device attributes). */
 tq_status tq_sdpa_plan(const tq_kv_cache* cache, int32_t num_q_heads,
                        int32_t max_seq_len, int32_t chunk, tq_impl impl,
-                       int32_t* chunks_per_split, int32_t* n_splits);
+                       int32_t* n_splits, int32_t* max_run_tokens);
 
 /* Split-K phase 1 alone ("turboquant-llama3.170B" README, split-K paragraph:
  * Phase 1 = partial attention over 512-token chunks processed in parallel).
  * Each part covers `chunks_per_split` consecutive chunks (1 = one state per
- * chunk, the pages' form; 0 = the plan tq_sdpa_int4_decode uses).  With
- * np = ceil(ceil(max_seq_len / chunk) / chunks_per_split) parts, fp32 outputs:
+ * chunk, the pages' form), np = ceil(ceil(max_seq_len / chunk) /
+ * chunks_per_split); or, with chunks_per_split = 0, the runs
+ * tq_sdpa_int4_decode uses (np = n_splits of tq_sdpa_plan).  fp32 outputs:
  *   part_m   [batch][num_q_heads][np]  max over the part of the scaled score
  *            (natural-log units; -inf for an empty part)
  *   part_l   [batch][num_q_heads][np]  sum of exp(score - m)  (0 if empty)

@@ -76,7 +76,7 @@ def lib() -> ctypes.CDLL:
             "tq_kv_cache_bytes": ([i32] * 5, sz),
             "tq_kv_cache_carve": ([C, P, i32, i32, i32, i32, i32], i32),
             "tq_quantize_kv_append": ([C, P, P, i32, P, P, P], i32),
-            "tq_sdpa_workspace_bytes": ([i32] * 5, sz),
+            "tq_sdpa_workspace_bytes": ([i32] * 6, sz),
             "tq_sdpa_int4_decode": ([C, P, i32, P, i32, f32, i32, P, sz, P, P, P], i32),
             "tq_sdpa_int4_decode_impl": ([C, P, i32, P, i32, f32, i32, P, sz, P, P, i32, P], i32),
             "tq_sdpa_plan": ([C, i32, i32, i32, i32, P, P], i32),
@@ -128,9 +128,9 @@ def tq_kv_cache_bytes(batch: int, num_kv_heads: int, head_dim: int, group_size: 
     return int(lib().tq_kv_cache_bytes(batch, num_kv_heads, head_dim, group_size, capacity))
 
 
-def tq_sdpa_workspace_bytes(batch: int, num_q_heads: int, head_dim: int, max_seq_len: int,
+def tq_sdpa_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, max_seq_len: int,
                             chunk: int = DEFAULT_CHUNK) -> int:
-    return int(lib().tq_sdpa_workspace_bytes(batch, num_q_heads, head_dim, max_seq_len, chunk))
+    return int(lib().tq_sdpa_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len, chunk))
 
 
 # ------------------------------------------------------------------ the cache
@@ -218,11 +218,11 @@ def tq_sdpa_int4_decode(cache: KVCache, q: torch.Tensor, seq_lens: torch.Tensor,
 
 def tq_sdpa_plan(cache: KVCache, num_q_heads: int, max_seq_len: int, chunk: int = DEFAULT_CHUNK,
                  impl: int = TQ_IMPL_AUTO):
-    """(chunks_per_split, n_splits) that tq_sdpa_int4_decode uses on this device."""
-    cps, ns = ctypes.c_int32(0), ctypes.c_int32(0)
+    """(n_splits, max_run_tokens) of the runs tq_sdpa_int4_decode uses on this device."""
+    ns, run = ctypes.c_int32(0), ctypes.c_int32(0)
     _check("tq_sdpa_plan", lib().tq_sdpa_plan(cache.ref(), num_q_heads, int(max_seq_len), int(chunk), int(impl),
-                                              ctypes.byref(cps), ctypes.byref(ns)))
-    return cps.value, ns.value
+                                              ctypes.byref(ns), ctypes.byref(run)))
+    return ns.value, run.value
 
 
 def tq_sdpa_int4_partial(cache: KVCache, q: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
@@ -230,13 +230,15 @@ def tq_sdpa_int4_partial(cache: KVCache, q: torch.Tensor, seq_lens: torch.Tensor
                          status: Optional[torch.Tensor] = None, impl: int = TQ_IMPL_AUTO, stream=None,
                          out=None):
     """Phase 1 alone: (m, l, acc) fp32 per part of ``chunks_per_split`` chunks
-    (1 = per chunk; 0 = the decode plan), m in natural-log units."""
+    (1 = per chunk; 0 = the runs tq_sdpa_int4_decode uses), m in natural-log units."""
     _need(q, torch.float16, "q")
     _need(seq_lens, torch.int32, "seq_lens")
     B, Hq, D = q.shape
     nc = max(1, math.ceil(max_seq_len / chunk))
-    cps = chunks_per_split if chunks_per_split > 0 else tq_sdpa_plan(cache, Hq, max_seq_len, chunk, impl)[0]
-    n_parts = math.ceil(nc / cps)
+    if chunks_per_split > 0:
+        n_parts = math.ceil(nc / chunks_per_split)
+    else:
+        n_parts = tq_sdpa_plan(cache, Hq, max_seq_len, chunk, impl)[0]
     if out is None:
         m = torch.empty((B, Hq, n_parts), dtype=torch.float32, device=q.device)
         l = torch.empty_like(m)
@@ -246,7 +248,8 @@ def tq_sdpa_int4_partial(cache: KVCache, q: torch.Tensor, seq_lens: torch.Tensor
         if m.numel() < B * Hq * n_parts or acc.numel() < B * Hq * n_parts * D:
             raise ValueError("partial output buffers too small")
     _check("tq_sdpa_int4_partial", lib().tq_sdpa_int4_partial(
-        cache.ref(), _ptr(q), Hq, _ptr(seq_lens), int(max_seq_len), float(attn_scale), int(chunk), int(cps),
+        cache.ref(), _ptr(q), Hq, _ptr(seq_lens), int(max_seq_len), float(attn_scale), int(chunk),
+        int(chunks_per_split),
         _ptr(m), _ptr(l), _ptr(acc), _ptr(status), int(impl), _stream(stream)))
     return m, l, acc
 

@@ -10,11 +10,13 @@
 // registers; no float K/V and no score matrix is written anywhere.
 //
 // GB300 design (not the Metal kernel's):
-//  * A producer warp streams each tile (T tokens) of K codes, V codes and the
-//    four fp16 scale/bias arrays into a ring of shared-memory stages: the code
-//    tiles by 2-D TMA with the 128-byte swizzle, the scale/bias rows by 1-D
-//    bulk copies, completion on mbarriers.  Every byte of the cache is read
-//    from HBM once per step, with an evict-first L2 policy.
+//  * Each tile (T tokens) of K codes, V codes and the four fp16 scale/bias
+//    arrays streams into a ring of shared-memory stages: the code tiles by
+//    2-D TMA with the 128-byte swizzle, the scale/bias rows by 1-D bulk
+//    copies, completion on mbarriers.  There is no producer warp: the last
+//    warp to finish a stage issues its refill, so all four warps compute and
+//    four CTAs fit on an SM.  Every byte of the cache is read from HBM once
+//    per step, with an evict-first L2 policy.
 //  * Consumer warps turn the nibbles into fp16 operands with one AND per
 //    register: a 4-bit code n in the low mantissa bits of a zero-exponent fp16
 //    is the subnormal n * 2^-24, and the high nibble of a byte gives
@@ -38,6 +40,8 @@
 //    the swizzled tile; the permutation is undone when the state is written.
 #include <math.h>
 
+#include <type_traits>
+
 #include "tq_device.cuh"
 #include "tq_internal.h"
 
@@ -54,17 +58,20 @@ struct Cfg {
     static constexpr int BPT = D / 2;              // code bytes per token
     static constexpr int SPT = BPT / 16;           // 16-byte segments per token
     static constexpr int TPR = 128 / BPT;          // tokens per 128-byte swizzle row (D=256: 1)
-    static constexpr int NWC = 4;                  // consumer warps
+    static constexpr int NWC = 4;                  // warps (all consume; the last to finish a stage refills it)
     static constexpr int MT = (D == 256) ? 1 : 2;  // 16-token m-tiles per warp per stage
     static constexpr int T = NWC * MT * 16;        // tokens per stage
-    static constexpr int STAGES = 4;
+    static constexpr int STAGES = 3;
     static constexpr int CODE_BYTES = T * BPT;     // one code tile (K or V)
     static constexpr int SB_BYTES = T * NG * 2;    // one scale or bias tile
     static constexpr int STAGE_BYTES = ((2 * CODE_BYTES + 4 * SB_BYTES + 1023) / 1024) * 1024;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // +1024 for base alignment
-    static constexpr int THREADS = (NWC + 1) * 32;
+    static constexpr int THREADS = NWC * 32;
     static constexpr int NKS = D / 16;             // k-steps of the score MMA = m-tiles of P.V
     static constexpr bool EVEN_ODD = D <= 128;     // token order inside a 16-token tile
+    // 4 resident CTAs (16 warps) need <= 128 registers per thread: each SM
+    // sub-partition then holds 4 warps in its 16K registers.
+    static constexpr int MIN_CTAS = (D == 256) ? 2 : 4;
     static_assert(CODE_BYTES % 1024 == 0, "code tiles must keep the 1024-byte swizzle period");
     static_assert(STAGES * STAGE_BYTES >= NWC * 8 * D * 4, "merge buffer must fit in the stages");
 };
@@ -123,14 +130,13 @@ __device__ __forceinline__ int clamp_len(const DecodeParams& p, int b) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(Cfg<D>::THREADS)
+__global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const DecodeParams p) {
     using C = Cfg<D>;
     constexpr int NG = C::NG;
     __shared__ uint64_t full_bar[C::STAGES];
-    __shared__ uint64_t empty_bar[C::STAGES];
-    __shared__ int abort_flag;
+    __shared__ unsigned int done_cnt[C::STAGES];  // warps finished with the stage, cumulative
     __shared__ float mrg_m[C::NWC][8], mrg_l[C::NWC][8];
     extern __shared__ uint8_t dyn_smem[];
     const uint32_t dyn_base = smem_u32(dyn_smem);
@@ -140,65 +146,48 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int G = p.group_q;
     const int len = clamp_len(p, b);
-    const int t_begin = split * p.split_tokens;
-    const int t_end = min(t_begin + p.split_tokens, len);
+    const int t_begin = run_begin(split, p.units, p.n_splits, p.unit_tokens);
+    const int t_end = min(run_begin(split + 1, p.units, p.n_splits, p.unit_tokens), len);
     const int n_tiles = t_end > t_begin ? (t_end - t_begin + C::T - 1) / C::T : 0;
-    const long long bh = static_cast<long long>(b) * p.num_kv_heads + kvh;
+    const long long row_base = (static_cast<long long>(b) * p.num_kv_heads + kvh) * p.capacity;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], C::NWC);
+            done_cnt[s] = 0;
         }
-        abort_flag = 0;
         fence_mbarrier_init();
     }
     __syncthreads();
     pdl_launch_dependents();
 
-    if (warp == C::NWC) {
-        // ------------------------------------------------------ producer warp
-        if (lane == 0 && n_tiles > 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-            const uint64_t policy = policy_evict_first();
-            const long long row_base = bh * p.capacity;  // cache row of token 0
-            int issued = 0;
-            for (int it = 0; it < n_tiles; ++it) {
-                const int stage = it % C::STAGES;
-                if (it >= C::STAGES) {
-                    if (!mbar_wait_bounded(&empty_bar[stage], ((it / C::STAGES) - 1) & 1)) {
-                        atomicExch(&abort_flag, 1);
-                        if (p.status) atomicOr(p.status, TQ_DEV_TIMEOUT);
-                        break;
-                    }
-                }
-                if (*reinterpret_cast<volatile int*>(&abort_flag)) break;
-                const int t0 = t_begin + it * C::T;
-                const int avail = min(C::T, p.capacity - t0);  // rows left in this (b, kv head)
-                const uint32_t sb_bytes = static_cast<uint32_t>(avail) * NG * 2;
-                uint8_t* st = smem + stage * C::STAGE_BYTES;
-                mbar_arrive_expect_tx(&full_bar[stage], 2 * C::CODE_BYTES + 4 * sb_bytes);
-                const int y = static_cast<int>(((row_base + t0) * C::BPT) / 128);
-                tma_load_2d(st, &tm_k, 0, y, &full_bar[stage], policy);
-                tma_load_2d(st + C::CODE_BYTES, &tm_v, 0, y, &full_bar[stage], policy);
-                const long long sb_off = (row_base + t0) * NG;
-                uint8_t* sb = st + 2 * C::CODE_BYTES;
-                bulk_load(sb + 0 * C::SB_BYTES, p.k_scale + sb_off, sb_bytes, &full_bar[stage], policy);
-                bulk_load(sb + 1 * C::SB_BYTES, p.k_bias + sb_off, sb_bytes, &full_bar[stage], policy);
-                bulk_load(sb + 2 * C::SB_BYTES, p.v_scale + sb_off, sb_bytes, &full_bar[stage], policy);
-                bulk_load(sb + 3 * C::SB_BYTES, p.v_bias + sb_off, sb_bytes, &full_bar[stage], policy);
-                issued = it + 1;
-            }
-            // Do not leave while copies into this CTA's shared memory may be in
-            // flight: wait (bounded) for the fills of the last issued stages.
-            for (int it = max(0, issued - C::STAGES); it < issued; ++it)
-                mbar_wait_bounded(&full_bar[it % C::STAGES], (it / C::STAGES) & 1, 200000000ull);
-        }
-        return;
+    // Fill stage it % STAGES with tile it: both code tiles by TMA, the four
+    // scale/bias rows by bulk copies; completion counted in bytes on full_bar.
+    auto issue_tile = [&](int it, uint64_t policy) {
+        const int stage = it % C::STAGES;
+        const int t0 = t_begin + it * C::T;
+        const int avail = min(C::T, p.capacity - t0);  // rows left in this (b, kv head)
+        const uint32_t sb_bytes = static_cast<uint32_t>(avail) * NG * 2;
+        uint8_t* st = smem + stage * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&full_bar[stage], 2 * C::CODE_BYTES + 4 * sb_bytes);
+        const int y = static_cast<int>(((row_base + t0) * C::BPT) / 128);
+        tma_load_2d(st, &tm_k, 0, y, &full_bar[stage], policy);
+        tma_load_2d(st + C::CODE_BYTES, &tm_v, 0, y, &full_bar[stage], policy);
+        const long long sb_off = (row_base + t0) * NG;
+        uint8_t* sb = st + 2 * C::CODE_BYTES;
+        bulk_load(sb + 0 * C::SB_BYTES, p.k_scale + sb_off, sb_bytes, &full_bar[stage], policy);
+        bulk_load(sb + 1 * C::SB_BYTES, p.k_bias + sb_off, sb_bytes, &full_bar[stage], policy);
+        bulk_load(sb + 2 * C::SB_BYTES, p.v_scale + sb_off, sb_bytes, &full_bar[stage], policy);
+        bulk_load(sb + 3 * C::SB_BYTES, p.v_bias + sb_off, sb_bytes, &full_bar[stage], policy);
+    };
+    if (threadIdx.x == 0 && n_tiles > 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        const uint64_t policy = policy_evict_first();
+        for (int it = 0; it < min(n_tiles, C::STAGES); ++it) issue_tile(it, policy);
     }
 
-    // ---------------------------------------------------------- consumer warps
+    // ------------------------------------------------------------ all warps
     const int gid = lane >> 2, tig = lane & 3;
     const float sl2 = p.score_scale_log2;
 
@@ -255,12 +244,20 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
     const int lm_mat = lane >> 3, lm_row = lane & 7;
     const int lm_tok = tok_of_row<D>((lm_mat & 1) * 8 + lm_row);  // token within the 16-token tile
     const int lm_seg = lm_mat >> 1;                                // first or second segment
+    // per-lane ldmatrix offset inside a 16-token tile for each segment pair.
+    // A tile starting at token tb begins at swizzle row tb / TPR; its phase
+    // (that row mod 8) is XORed into the 16-byte chunk bits at use (always 0
+    // for D >= 128, where a tile covers a multiple of 8 rows).
+    uint32_t lm_off[C::SPT / 2];
+#pragma unroll
+    for (int sp = 0; sp < C::SPT / 2; ++sp) lm_off[sp] = code_addr<D>(0u, lm_tok, 2 * sp + lm_seg);
 
     for (int it = 0; it < n_tiles; ++it) {
         const int stage = it % C::STAGES;
         if (!mbar_wait_bounded(&full_bar[stage], (it / C::STAGES) & 1)) {
+            // the fill never completed: report, stop consuming (no further
+            // refills are issued, so the other warps give up the same way)
             if (p.status) atomicOr(p.status, TQ_DEV_TIMEOUT);
-            atomicExch(&abort_flag, 1);
             break;
         }
         const int t0 = t_begin + it * C::T;
@@ -272,148 +269,164 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
         const uint16_t* vs_s = kb_s + C::SB_BYTES / 2;
         const uint16_t* vb_s = vs_s + C::SB_BYTES / 2;
 
-        // ---- scores of this warp's m-tiles (log2 units)
-        float sc[C::MT][4];
-#pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt) {
-            const int tb = (warp * C::MT + mt) * 16;
-            float cg[NG][4];
-#pragma unroll
-            for (int g = 0; g < NG; ++g) cg[g][0] = cg[g][1] = cg[g][2] = cg[g][3] = 0.0f;
-#pragma unroll
-            for (int sp = 0; sp < C::SPT / 2; ++sp) {
-                uint32_t x0, x1, x2, x3;
-                ldmatrix_x4(code_addr<D>(kc_s, tb + lm_tok, 2 * sp + lm_seg), x0, x1, x2, x3);
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int s = 2 * sp + e;
-                    const int g = (32 * s) / kGroup;
-                    const uint32_t xa = e ? x2 : x0;  // rows 0..7
-                    const uint32_t xb = e ? x3 : x1;  // rows 8..15
-                    mma_16816(cg[g], xa & kLoNib, xb & kLoNib, xa & kHiNib, xb & kHiNib, qb[2 * s][0], qb[2 * s][1]);
-                    const uint32_t ya = xa >> 8, yb = xb >> 8;
-                    mma_16816(cg[g], ya & kLoNib, yb & kLoNib, ya & kHiNib, yb & kHiNib, qb[2 * s + 1][0],
-                              qb[2 * s + 1][1]);
+        // Only the last tile of a run can be partial; full tiles take a copy of
+        // the body without the masking selects.
+        auto stage_body = [&](auto tail_tag) {
+            constexpr bool kTail = decltype(tail_tag)::value;
+            // ---- scores of this warp's m-tiles (log2 units)
+            float sc[C::MT][4];
+    #pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                const int tb = (warp * C::MT + mt) * 16;
+                const uint32_t sw = static_cast<uint32_t>((tb / C::TPR) & 7) << 4;
+                float cg[NG][4];
+    #pragma unroll
+                for (int g = 0; g < NG; ++g) cg[g][0] = cg[g][1] = cg[g][2] = cg[g][3] = 0.0f;
+    #pragma unroll
+                for (int sp = 0; sp < C::SPT / 2; ++sp) {
+                    uint32_t x0, x1, x2, x3;
+                    ldmatrix_x4(kc_s + tb * C::BPT + (lm_off[sp] ^ sw), x0, x1, x2, x3);
+    #pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int s = 2 * sp + e;
+                        const int g = (32 * s) / kGroup;
+                        const uint32_t xa = e ? x2 : x0;  // rows 0..7
+                        const uint32_t xb = e ? x3 : x1;  // rows 8..15
+                        mma_16816(cg[g], xa & kLoNib, xb & kLoNib, xa & kHiNib, xb & kHiNib, qb[2 * s][0], qb[2 * s][1]);
+                        const uint32_t ya = xa >> 8, yb = xb >> 8;
+                        mma_16816(cg[g], ya & kLoNib, yb & kLoNib, ya & kHiNib, yb & kHiNib, qb[2 * s + 1][0],
+                                  qb[2 * s + 1][1]);
+                    }
+                }
+                float ksa[NG], kba[NG], ksb[NG], kbb[NG];
+                load_row_sb<NG>(ks_s, tb + r0, ksa);
+                load_row_sb<NG>(kb_s, tb + r0, kba);
+                load_row_sb<NG>(ks_s, tb + r1, ksb);
+                load_row_sb<NG>(kb_s, tb + r1, kbb);
+                const bool va = !kTail || t0 + tb + r0 < t_end, vb = !kTail || t0 + tb + r1 < t_end;
+    #pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float sa = 0.0f, sb = 0.0f;
+    #pragma unroll
+                    for (int g = 0; g < NG; ++g) {
+                        sa = fmaf(ksa[g] * k_coef, cg[g][hh], fmaf(kba[g], qs_l2[g][hh], sa));
+                        sb = fmaf(ksb[g] * k_coef, cg[g][2 + hh], fmaf(kbb[g], qs_l2[g][hh], sb));
+                    }
+                    // masked rows may hold stale bits: select, never compute with them
+                    sc[mt][hh] = va ? sa : -INFINITY;
+                    sc[mt][2 + hh] = vb ? sb : -INFINITY;
                 }
             }
-            float ksa[NG], kba[NG], ksb[NG], kbb[NG];
-            load_row_sb<NG>(ks_s, tb + r0, ksa);
-            load_row_sb<NG>(kb_s, tb + r0, kba);
-            load_row_sb<NG>(ks_s, tb + r1, ksb);
-            load_row_sb<NG>(kb_s, tb + r1, kbb);
-            const bool va = t0 + tb + r0 < t_end, vb = t0 + tb + r1 < t_end;
-#pragma unroll
+
+            // ---- online softmax update over this warp's tokens of the stage
+            float m_use[2];
+    #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                float sa = 0.0f, sb = 0.0f;
-#pragma unroll
+                float mx = -INFINITY;
+    #pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) mx = fmaxf(mx, fmaxf(sc[mt][hh], sc[mt][2 + hh]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float m_new = fmaxf(m_run[hh], mx);
+                m_use[hh] = m_new == -INFINITY ? 0.0f : m_new;
+                if (m_new > m_run[hh]) {
+                    const float alpha = m_run[hh] == -INFINITY ? 0.0f : ex2_approx(m_run[hh] - m_new);
+                    l_run[hh] *= alpha;
+    #pragma unroll
+                    for (int g = 0; g < NG; ++g) e_run[g][hh] *= alpha;
+    #pragma unroll
+                    for (int i = 0; i < C::NKS; ++i) {
+                        acc[i][hh] *= alpha;
+                        acc[i][2 + hh] *= alpha;
+                    }
+                    m_run[hh] = m_new;
+                }
+            }
+
+            // ---- P.V for each m-tile of this warp
+    #pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                const int tb = (warp * C::MT + mt) * 16;
+                const uint32_t sw = static_cast<uint32_t>((tb / C::TPR) & 7) << 4;
+                const bool va = !kTail || t0 + tb + r0 < t_end, vb = !kTail || t0 + tb + r1 < t_end;
+                float pr[4];
+    #pragma unroll
+                for (int c = 0; c < 4; ++c) pr[c] = ex2_approx(sc[mt][c] - m_use[c & 1]);
+                l_run[0] += pr[0] + pr[2];
+                l_run[1] += pr[1] + pr[3];
+                float vsa[NG], vba[NG], vsb[NG], vbb[NG];
+                load_row_sb<NG>(vs_s, tb + r0, vsa);
+                load_row_sb<NG>(vb_s, tb + r0, vba);
+                load_row_sb<NG>(vs_s, tb + r1, vsb);
+                load_row_sb<NG>(vb_s, tb + r1, vbb);
+                // B operand p_t * vscale_tg as an fp16 pair hi + lo (hi = fp16(r), lo =
+                // fp16(r - hi)): one fp16 rounding of r would leave 2^-12 relative noise
+                // on every term of sum_t r_t n_t, which the code offset (n in 0..15, mean
+                // near 7.5) amplifies well past the 1e-3 output budget at long context.
+                uint32_t bhi[NG][2], blo[NG][2];
+    #pragma unroll
                 for (int g = 0; g < NG; ++g) {
-                    sa = fmaf(ksa[g] * k_coef, cg[g][hh], fmaf(kba[g], qs_l2[g][hh], sa));
-                    sb = fmaf(ksb[g] * k_coef, cg[g][2 + hh], fmaf(kbb[g], qs_l2[g][hh], sb));
+                    // masked rows may hold stale scale/bias bits: select, never multiply
+                    const float sa = va ? vsa[g] : 0.0f, sb = vb ? vsb[g] : 0.0f;
+                    const float ba = va ? vba[g] : 0.0f, bb = vb ? vbb[g] : 0.0f;
+                    e_run[g][0] = fmaf(pr[0], ba, fmaf(pr[2], bb, e_run[g][0]));
+                    e_run[g][1] = fmaf(pr[1], ba, fmaf(pr[3], bb, e_run[g][1]));
+                    const float r0 = pr[0] * sa, r1 = pr[1] * sa, r2 = pr[2] * sb, r3 = pr[3] * sb;
+                    const __half2 h01 = __floats2half2_rn(r0, r1), h23 = __floats2half2_rn(r2, r3);
+                    const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+                    bhi[g][0] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h01));
+                    bhi[g][1] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h23));
+                    blo[g][0] = movmatrix_trans(pack_half2(r0 - f01.x, r1 - f01.y));
+                    blo[g][1] = movmatrix_trans(pack_half2(r2 - f23.x, r3 - f23.y));
                 }
-                // masked rows may hold stale bits: select, never compute with them
-                sc[mt][hh] = va ? sa : -INFINITY;
-                sc[mt][2 + hh] = vb ? sb : -INFINITY;
+                // This tile's sum_t r_t n_t goes into fresh tensor-core accumulators
+                // and is then added to the running state with round-to-nearest fp32
+                // adds.  The code sum is ~7.5 sum_t r_t while the attention output is
+                // what is left after the bias term cancels most of it, so a long
+                // chain of tensor-core accumulations (whose fp32 sums are not
+                // round-to-nearest) would leave a systematic error far above 1e-3
+                // of the output at long context.
+    #pragma unroll
+                for (int sp = 0; sp < C::SPT / 2; ++sp) {
+                    uint32_t x0, x1, x2, x3;
+                    ldmatrix_x4_trans(vc_s + tb * C::BPT + (lm_off[sp] ^ sw), x0, x1, x2, x3);
+    #pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int s = 2 * sp + e;
+                        const int g = (32 * s) / kGroup;
+                        const uint32_t xa = e ? x2 : x0;  // tokens of rows 0..7  (k 0..7)
+                        const uint32_t xb = e ? x3 : x1;  // tokens of rows 8..15 (k 8..15)
+    #pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const uint32_t ua = j ? (xa >> 8) : xa, ub = j ? (xb >> 8) : xb;
+                            float t[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                            mma_16816(t, ua & kLoNib, ua & kHiNib, ub & kLoNib, ub & kHiNib, bhi[g][0], bhi[g][1]);
+                            mma_16816(t, ua & kLoNib, ua & kHiNib, ub & kLoNib, ub & kHiNib, blo[g][0], blo[g][1]);
+    #pragma unroll
+                            for (int c = 0; c < 4; ++c) acc[2 * s + j][c] = __fadd_rn(acc[2 * s + j][c], t[c]);
+                        }
+                    }
+                }
             }
-        }
+        };
+        if (t0 + C::T <= t_end) stage_body(std::false_type{});
+        else stage_body(std::true_type{});
 
-        // ---- online softmax update over this warp's tokens of the stage
-        float m_use[2];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) mx = fmaxf(mx, fmaxf(sc[mt][hh], sc[mt][2 + hh]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float m_new = fmaxf(m_run[hh], mx);
-            m_use[hh] = m_new == -INFINITY ? 0.0f : m_new;
-            if (m_new > m_run[hh]) {
-                const float alpha = m_run[hh] == -INFINITY ? 0.0f : exp2f(m_run[hh] - m_new);
-                l_run[hh] *= alpha;
-#pragma unroll
-                for (int g = 0; g < NG; ++g) e_run[g][hh] *= alpha;
-#pragma unroll
-                for (int i = 0; i < C::NKS; ++i) {
-                    acc[i][hh] *= alpha;
-                    acc[i][2 + hh] *= alpha;
-                }
-                m_run[hh] = m_new;
-            }
-        }
-
-        // ---- P.V for each m-tile of this warp
-#pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt) {
-            const int tb = (warp * C::MT + mt) * 16;
-            const bool va = t0 + tb + r0 < t_end, vb = t0 + tb + r1 < t_end;
-            float pr[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) pr[c] = exp2f(sc[mt][c] - m_use[c & 1]);
-            l_run[0] += pr[0] + pr[2];
-            l_run[1] += pr[1] + pr[3];
-            float vsa[NG], vba[NG], vsb[NG], vbb[NG];
-            load_row_sb<NG>(vs_s, tb + r0, vsa);
-            load_row_sb<NG>(vb_s, tb + r0, vba);
-            load_row_sb<NG>(vs_s, tb + r1, vsb);
-            load_row_sb<NG>(vb_s, tb + r1, vbb);
-            // B operand p_t * vscale_tg as an fp16 pair hi + lo (hi = fp16(r), lo =
-            // fp16(r - hi)): one fp16 rounding of r would leave 2^-12 relative noise
-            // on every term of sum_t r_t n_t, which the code offset (n in 0..15, mean
-            // near 7.5) amplifies well past the 1e-3 output budget at long context.
-            uint32_t bhi[NG][2], blo[NG][2];
-#pragma unroll
-            for (int g = 0; g < NG; ++g) {
-                // masked rows may hold stale scale/bias bits: select, never multiply
-                const float sa = va ? vsa[g] : 0.0f, sb = vb ? vsb[g] : 0.0f;
-                const float ba = va ? vba[g] : 0.0f, bb = vb ? vbb[g] : 0.0f;
-                e_run[g][0] = fmaf(pr[0], ba, fmaf(pr[2], bb, e_run[g][0]));
-                e_run[g][1] = fmaf(pr[1], ba, fmaf(pr[3], bb, e_run[g][1]));
-                const float r0 = pr[0] * sa, r1 = pr[1] * sa, r2 = pr[2] * sb, r3 = pr[3] * sb;
-                const __half2 h01 = __floats2half2_rn(r0, r1), h23 = __floats2half2_rn(r2, r3);
-                const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-                bhi[g][0] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h01));
-                bhi[g][1] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h23));
-                blo[g][0] = movmatrix_trans(pack_half2(r0 - f01.x, r1 - f01.y));
-                blo[g][1] = movmatrix_trans(pack_half2(r2 - f23.x, r3 - f23.y));
-            }
-            // This tile's sum_t r_t n_t goes into fresh tensor-core accumulators
-            // and is then added to the running state with round-to-nearest fp32
-            // adds.  The code sum is ~7.5 sum_t r_t while the attention output is
-            // what is left after the bias term cancels most of it, so a long
-            // chain of tensor-core accumulations (whose fp32 sums are not
-            // round-to-nearest) would leave a systematic error far above 1e-3
-            // of the output at long context.
-            float tile[C::NKS][4];
-#pragma unroll
-            for (int i = 0; i < C::NKS; ++i) tile[i][0] = tile[i][1] = tile[i][2] = tile[i][3] = 0.0f;
-#pragma unroll
-            for (int sp = 0; sp < C::SPT / 2; ++sp) {
-                uint32_t x0, x1, x2, x3;
-                ldmatrix_x4_trans(code_addr<D>(vc_s, tb + lm_tok, 2 * sp + lm_seg), x0, x1, x2, x3);
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int s = 2 * sp + e;
-                    const int g = (32 * s) / kGroup;
-                    const uint32_t xa = e ? x2 : x0;  // tokens of rows 0..7  (k 0..7)
-                    const uint32_t xb = e ? x3 : x1;  // tokens of rows 8..15 (k 8..15)
-                    const uint32_t a0 = xa & kLoNib, a1 = xa & kHiNib, a2 = xb & kLoNib, a3 = xb & kHiNib;
-                    mma_16816(tile[2 * s], a0, a1, a2, a3, bhi[g][0], bhi[g][1]);
-                    mma_16816(tile[2 * s], a0, a1, a2, a3, blo[g][0], blo[g][1]);
-                    const uint32_t ya = xa >> 8, yb = xb >> 8;
-                    const uint32_t c0 = ya & kLoNib, c1 = ya & kHiNib, c2 = yb & kLoNib, c3 = yb & kHiNib;
-                    mma_16816(tile[2 * s + 1], c0, c1, c2, c3, bhi[g][0], bhi[g][1]);
-                    mma_16816(tile[2 * s + 1], c0, c1, c2, c3, blo[g][0], blo[g][1]);
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < C::NKS; ++i) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) acc[i][c] = __fadd_rn(acc[i][c], tile[i][c]);
-            }
-        }
+        // Release the stage.  The last warp to finish it refills it with tile
+        // it + STAGES: its fence orders every warp's reads of the stage (made
+        // visible by their fences before the counter update) before the
+        // asynchronous copies that overwrite it.
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[stage]);
+        if (lane == 0) {
+            __threadfence_block();
+            const unsigned int before = atomicAdd(&done_cnt[stage], 1u);
+            if (before % C::NWC == C::NWC - 1 && it + C::STAGES < n_tiles) {
+                __threadfence_block();
+                fence_proxy_async_shared();
+                issue_tile(it + C::STAGES, policy_evict_first());
+            }
+        }
     }
 
     // ---- reduce per-thread sums over the 8 token rows (lanes differing in gid)
@@ -428,8 +441,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
     }
 
     // ---- merge the consumer warps' states through shared memory
-    // (every stage has been consumed once all consumers pass this barrier)
-    asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
+    // (every issued fill has been waited for by every warp once all pass this barrier)
+    __syncthreads();
     float* mrg_acc = reinterpret_cast<float*>(smem);  // [NWC][8][D]
     {
         float* wacc = mrg_acc + warp * 8 * D;
@@ -453,7 +466,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
             mrg_l[warp][2 * tig + 1] = l_run[1];
         }
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
+    __syncthreads();
     const float ln2 = 0.69314718055994531f;
     for (int idx = threadIdx.x; idx < G * D; idx += C::NWC * 32) {
         const int h = idx / D, d = idx % D;
@@ -464,7 +477,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < C::NWC; ++w) {
-                const float wt = mrg_m[w][h] == -INFINITY ? 0.0f : exp2f(mrg_m[w][h] - M);
+                const float wt = mrg_m[w][h] == -INFINITY ? 0.0f : ex2_approx(mrg_m[w][h] - M);
                 L = fmaf(wt, mrg_l[w][h], L);
                 A = fmaf(wt, mrg_acc[(w * 8 + h) * D + d], A);
             }

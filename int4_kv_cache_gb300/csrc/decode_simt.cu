@@ -21,7 +21,7 @@ namespace tq {
 namespace {
 
 constexpr int kSimtThreads = 128;
-constexpr int kSimtTile = 64;
+constexpr int kSimtTile = kSimtTileTokens;
 constexpr int kGMax = 8;
 
 __device__ __forceinline__ int clamp_len(const DecodeParams& p, int b) {
@@ -48,8 +48,8 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const DecodeP
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int G = p.group_q;
     const int len = clamp_len(p, b);
-    const int t_begin = split * p.split_tokens;
-    const int t_end = min(t_begin + p.split_tokens, len);
+    const int t_begin = run_begin(split, p.units, p.n_splits, p.unit_tokens);
+    const int t_end = min(run_begin(split + 1, p.units, p.n_splits, p.unit_tokens), len);
 
     pdl_launch_dependents();
 

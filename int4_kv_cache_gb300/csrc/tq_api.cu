@@ -120,21 +120,34 @@ tq_status device_facts(DeviceFacts** out) {
 
 // ------------------------------------------------------------- decode plan --
 struct Plan {
-    int n_chunks, n_splits, split_tokens;
+    int n_splits, unit_tokens, units;
 };
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
-// Give each CTA a run of whole chunks so that the grid fills the GPU about
-// once: chunks_per_split = ceil(B * Hkv * n_chunks / resident CTAs).
-Plan make_plan(int batch, int hkv, int max_seq_len, int chunk, int resident) {
+// Balanced runs of whole units, about one CTA per resident slot: the unit is
+// the kernel's pipeline tile, or the chunk if that is smaller, so that runs
+// cover the sequence evenly whatever its length in chunks.
+Plan make_plan(int batch, int hkv, int max_seq_len, int chunk, int tile_tokens, int resident) {
     Plan pl;
-    pl.n_chunks = ceil_div(max_seq_len, chunk);
-    const long long units = static_cast<long long>(batch) * hkv * pl.n_chunks;
-    int cps = static_cast<int>((units + resident - 1) / resident);
-    if (cps < 1) cps = 1;
-    pl.n_splits = ceil_div(pl.n_chunks, cps);
-    pl.split_tokens = cps * chunk;
+    pl.unit_tokens = chunk < tile_tokens ? chunk : tile_tokens;
+    pl.units = ceil_div(max_seq_len, pl.unit_tokens);
+    const long long heads = static_cast<long long>(batch) * hkv;
+    long long ns = resident / heads;
+    const long long cap = tq::kMaxDecodeCtas / heads;
+    if (ns > cap) ns = cap;
+    if (ns > pl.units) ns = pl.units;
+    if (ns < 1) ns = 1;
+    pl.n_splits = static_cast<int>(ns);
+    return pl;
+}
+
+// Fixed runs of `cps` whole chunks (the pages' per-chunk states when cps = 1).
+Plan chunk_plan(int max_seq_len, int chunk, int cps) {
+    Plan pl;
+    pl.unit_tokens = cps * chunk;
+    pl.units = ceil_div(max_seq_len, pl.unit_tokens);
+    pl.n_splits = pl.units;
     return pl;
 }
 
@@ -143,8 +156,10 @@ tq_status device_plan(const tq_kv_cache* cache, int max_seq_len, int chunk, tq_i
     tq_status s = device_facts(&f);
     if (s != TQ_OK) return s;
     const int di = dim_index(cache->head_dim);
-    const int per_sm = impl == TQ_IMPL_SIMT ? f->simt_ctas[di] : f->mma_ctas[di];
-    *pl = make_plan(cache->batch, cache->num_kv_heads, max_seq_len, chunk, f->sms * per_sm);
+    const bool simt = impl == TQ_IMPL_SIMT;
+    const int per_sm = simt ? f->simt_ctas[di] : f->mma_ctas[di];
+    const int tile = simt ? tq::kSimtTileTokens : tq::mma_tile_tokens(cache->head_dim);
+    *pl = make_plan(cache->batch, cache->num_kv_heads, max_seq_len, chunk, tile, f->sms * per_sm);
     return TQ_OK;
 }
 
@@ -185,7 +200,8 @@ tq_status run_phase1(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, co
     p.group_q = hq / cache->num_kv_heads;
     p.capacity = cache->capacity;
     p.max_seq_len = max_seq_len;
-    p.split_tokens = pl.split_tokens;
+    p.unit_tokens = pl.unit_tokens;
+    p.units = pl.units;
     p.n_splits = pl.n_splits;
     p.score_scale_log2 = attn_scale * 1.4426950408889634f;
     if (impl == TQ_IMPL_SIMT) return cuda_status(tq::launch_decode_simt(p, cache->head_dim, stream));
@@ -321,10 +337,16 @@ tq_status tq_quantize_kv_append(const tq_kv_cache* cache, const uint16_t* k_new,
     return cuda_status(tq::launch_quantize_append(p, static_cast<cudaStream_t>(stream)));
 }
 
-size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t hq, int32_t head_dim, int32_t max_seq_len, int32_t chunk) {
-    if (batch < 1 || hq < 1 || head_dim < 1 || max_seq_len < 1 || chunk < 1) return 0;
-    const size_t nc = static_cast<size_t>((max_seq_len + chunk - 1) / chunk);
-    const size_t parts = static_cast<size_t>(batch) * hq * nc;
+size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t hq, int32_t hkv, int32_t head_dim, int32_t max_seq_len,
+                               int32_t chunk) {
+    if (batch < 1 || hq < 1 || hkv < 1 || head_dim < 1 || max_seq_len < 1 || chunk < 1) return 0;
+    // n_splits <= min(units of the smallest unit (16 or chunk tokens), kMaxDecodeCtas / (batch * hkv))
+    const long long unit = chunk < 16 ? chunk : 16;
+    long long ns = (max_seq_len + unit - 1) / unit;
+    long long cap = tq::kMaxDecodeCtas / (static_cast<long long>(batch) * hkv);
+    if (cap < 1) cap = 1;
+    if (ns > cap) ns = cap;
+    const size_t parts = static_cast<size_t>(batch) * hq * static_cast<size_t>(ns);
     return 2 * align256(parts * sizeof(float)) + align256(parts * head_dim * sizeof(float));
 }
 
@@ -335,7 +357,8 @@ tq_status tq_sdpa_int4_decode_impl(const tq_kv_cache* cache, const uint16_t* q, 
     tq_status s = check_decode_args(cache, q, hq, seq_lens, max_seq_len, chunk, out);
     if (s != TQ_OK) return s;
     if (!valid_impl(impl)) return TQ_ERR_UNSUPPORTED;
-    const size_t need = tq_sdpa_workspace_bytes(cache->batch, hq, cache->head_dim, max_seq_len, chunk);
+    const size_t need =
+        tq_sdpa_workspace_bytes(cache->batch, hq, cache->num_kv_heads, cache->head_dim, max_seq_len, chunk);
     if (workspace == nullptr || workspace_bytes < need) return TQ_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TQ_ERR_ALIGN;
     Plan pl;
@@ -371,8 +394,8 @@ tq_status tq_sdpa_int4_decode(const tq_kv_cache* cache, const uint16_t* q, int32
 }
 
 tq_status tq_sdpa_plan(const tq_kv_cache* cache, int32_t hq, int32_t max_seq_len, int32_t chunk, tq_impl impl,
-                       int32_t* chunks_per_split, int32_t* n_splits) {
-    if (cache == nullptr || chunks_per_split == nullptr || n_splits == nullptr) return TQ_ERR_NULL;
+                       int32_t* n_splits, int32_t* max_run_tokens) {
+    if (cache == nullptr || n_splits == nullptr || max_run_tokens == nullptr) return TQ_ERR_NULL;
     if (!supported_dim(cache->head_dim)) return TQ_ERR_UNSUPPORTED;
     if (cache->batch < 1 || cache->num_kv_heads < 1 || hq < 1 || max_seq_len < 1 || chunk < 16 || chunk % 16)
         return TQ_ERR_SHAPE;
@@ -380,8 +403,8 @@ tq_status tq_sdpa_plan(const tq_kv_cache* cache, int32_t hq, int32_t max_seq_len
     Plan pl;
     tq_status s = device_plan(cache, max_seq_len, chunk, impl, &pl);
     if (s != TQ_OK) return s;
-    *chunks_per_split = pl.split_tokens / chunk;
     *n_splits = pl.n_splits;
+    *max_run_tokens = ceil_div(pl.units, pl.n_splits) * pl.unit_tokens;
     return TQ_OK;
 }
 
@@ -394,16 +417,13 @@ tq_status tq_sdpa_int4_partial(const tq_kv_cache* cache, const uint16_t* q, int3
     if (part_l == nullptr || part_acc == nullptr) return TQ_ERR_NULL;
     if (!valid_impl(impl)) return TQ_ERR_UNSUPPORTED;
     if (chunks_per_split < 0) return TQ_ERR_SHAPE;
-    if (chunks_per_split == 0) {
-        int32_t cps = 0, ns = 0;
-        s = tq_sdpa_plan(cache, hq, max_seq_len, chunk, impl, &cps, &ns);
-        if (s != TQ_OK) return s;
-        chunks_per_split = cps;
-    }
     Plan pl;
-    pl.n_chunks = ceil_div(max_seq_len, chunk);
-    pl.n_splits = ceil_div(pl.n_chunks, chunks_per_split);
-    pl.split_tokens = chunks_per_split * chunk;
+    if (chunks_per_split == 0) {
+        s = device_plan(cache, max_seq_len, chunk, impl, &pl);
+        if (s != TQ_OK) return s;
+    } else {
+        pl = chunk_plan(max_seq_len, chunk, chunks_per_split);
+    }
     return run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, part_m, part_l, part_acc, status,
                       impl == TQ_IMPL_SIMT ? TQ_IMPL_SIMT : TQ_IMPL_MMA, static_cast<cudaStream_t>(stream));
 }

@@ -11,9 +11,10 @@ namespace tq {
 
 constexpr int kGroup = 64;
 
-// Geometry of one phase-1 launch: grid (n_splits, Hkv, B); CTA (s, kvh, b)
-// covers tokens [s * split_tokens, (s + 1) * split_tokens) of sequence b,
-// clipped to seq_lens[b].
+// Geometry of one phase-1 launch: grid (n_splits, Hkv, B).  The sequence is
+// cut into `units` units of `unit_tokens` tokens; CTA (s, kvh, b) covers units
+// [floor(s * units / n_splits), floor((s + 1) * units / n_splits)) of sequence b
+// (balanced runs), clipped to seq_lens[b].
 struct DecodeParams {
     const uint16_t* q;        // [B][Hq][D]
     const int32_t* seq_lens;  // [B]
@@ -29,7 +30,7 @@ struct DecodeParams {
     int32_t* status;          // optional device status word
     int32_t batch, num_q_heads, num_kv_heads, group_q;  // group_q = Hq / Hkv
     int32_t capacity, max_seq_len;
-    int32_t split_tokens, n_splits;
+    int32_t unit_tokens, units, n_splits;
     float score_scale_log2;   // attn_scale * log2(e)
 };
 
@@ -70,6 +71,15 @@ int mma_ctas_per_sm(int head_dim);
 int simt_ctas_per_sm(int head_dim);
 // Largest n_parts the reduce kernel takes (its weights live in shared memory).
 constexpr int kMaxReduceParts = 8192;
+// Most CTAs a decode plan launches (bounds the workspace independently of the device).
+constexpr int kMaxDecodeCtas = 2048;
+// Tokens per work unit of the SIMT phase-1 kernel.
+constexpr int kSimtTileTokens = 64;
+
+// First token of run s of a phase-1 launch (runs are balanced over units).
+__host__ __device__ inline int run_begin(int s, int units, int n_splits, int unit_tokens) {
+    return static_cast<int>(static_cast<long long>(s) * units / n_splits) * unit_tokens;
+}
 
 // Decode (tensor-core phase 1 + reduce) with the partial states written to
 // `partials` (partials_bytes long); TQ_ERR_WORKSPACE if they do not fit.

@@ -52,12 +52,12 @@ def gpu_cache_from_oracle(oc, capacity=None):
     return cache
 
 
-def workspace_for(B, Hq, D, max_len, chunk=512):
+def workspace_for(B, Hq, Hkv, D, max_len, chunk=512):
     import torch
 
     import int4_kv_cache_gb300 as tq
 
-    return torch.empty(tq.tq_sdpa_workspace_bytes(B, Hq, D, max_len, chunk), dtype=torch.uint8, device="cuda")
+    return torch.empty(tq.tq_sdpa_workspace_bytes(B, Hq, Hkv, D, max_len, chunk), dtype=torch.uint8, device="cuda")
 
 
 def decode(cache, q, lens, max_len, attn_scale, chunk=512, impl=0, status=None):
@@ -68,7 +68,7 @@ def decode(cache, q, lens, max_len, attn_scale, chunk=512, impl=0, status=None):
 
     qt = q if isinstance(q, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(q)).cuda()
     lt = torch.from_numpy(np.asarray(lens, dtype=np.int32)).cuda()
-    ws = workspace_for(cache.batch, qt.shape[1], cache.head_dim, max_len, chunk)
+    ws = workspace_for(cache.batch, qt.shape[1], cache.num_kv_heads, cache.head_dim, max_len, chunk)
     out = tq.tq_sdpa_int4_decode(cache, qt, lt, max_len, attn_scale, ws, chunk=chunk, impl=impl, status=status)
     torch.cuda.synchronize()
     return out.float().cpu().numpy().astype(np.float64)

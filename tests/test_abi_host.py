@@ -73,11 +73,17 @@ def test_memory_table_of_the_llama_page(L):
 
 
 def test_workspace_bytes(L):
-    nc = math.ceil(131072 / 512)
-    parts = 1 * 64 * nc
-    want = 2 * (-(-parts * 4 // 256) * 256) + (-(-parts * 128 * 4 // 256) * 256)
-    assert tq.tq_sdpa_workspace_bytes(1, 64, 128, 131072, 512) == want
-    assert tq.tq_sdpa_workspace_bytes(1, 64, 128, 0, 512) == 0
+    # runs per (sequence, kv head) are bounded by 2048 CTAs / (B * Hkv) and by
+    # the sequence length in 16-token units
+    def want(B, Hq, Hkv, D, S):
+        ns = min(math.ceil(S / 16), max(1, 2048 // (B * Hkv)))
+        parts = B * Hq * ns
+        return 2 * (-(-parts * 4 // 256) * 256) + (-(-parts * D * 4 // 256) * 256)
+
+    assert tq.tq_sdpa_workspace_bytes(1, 64, 8, 128, 131072, 512) == want(1, 64, 8, 128, 131072)
+    assert tq.tq_sdpa_workspace_bytes(32, 64, 8, 128, 32768, 512) == want(32, 64, 8, 128, 32768)
+    assert tq.tq_sdpa_workspace_bytes(1, 8, 2, 128, 40, 512) == want(1, 8, 2, 128, 40)
+    assert tq.tq_sdpa_workspace_bytes(1, 64, 8, 128, 0, 512) == 0
 
 
 def _fake_cache(B=1, Hkv=2, D=128, cap=256):
@@ -144,10 +150,10 @@ def test_reduce_partial_and_plan_argument_errors(L):
              None) == 1
     assert f(ctypes.byref(c), 0x1000, 8, 0x2000, 256, ctypes.c_float(1.0), 512, -1, 0x3000, 0x3000, 0x4000, None,
              0, None) == 2
-    cps, ns = ctypes.c_int32(), ctypes.c_int32()
-    assert L.tq_sdpa_plan(ctypes.byref(c), 8, 256, 500, 0, ctypes.byref(cps), ctypes.byref(ns)) == 2
-    assert L.tq_sdpa_plan(ctypes.byref(c), 8, 256, 512, 0, None, ctypes.byref(ns)) == 1
-    assert L.tq_sdpa_plan(ctypes.byref(c), 8, 256, 512, 7, ctypes.byref(cps), ctypes.byref(ns)) == 6
+    ns, run = ctypes.c_int32(), ctypes.c_int32()
+    assert L.tq_sdpa_plan(ctypes.byref(c), 8, 256, 500, 0, ctypes.byref(ns), ctypes.byref(run)) == 2
+    assert L.tq_sdpa_plan(ctypes.byref(c), 8, 256, 512, 0, None, ctypes.byref(run)) == 1
+    assert L.tq_sdpa_plan(ctypes.byref(c), 8, 256, 512, 7, ctypes.byref(ns), ctypes.byref(run)) == 6
 
 
 def test_carve_layout(L):

@@ -46,7 +46,7 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls():
         lens = torch.from_numpy(x.lens).cuda()
         max_len = int(x.lens.max())
         ref = tq.tq_sdpa_int4_decode(cache, q, lens, max_len, w.attn_scale,
-                                     workspace_for(2, 64, 128, max_len), chunk=512)
+                                     workspace_for(2, 64, 8, 128, max_len), chunk=512)
         out = torch.full_like(q, float("nan"))
         assert _noalloc(L, cache, q, lens, max_len, w.attn_scale, out) == 0
         assert_close(out.float().cpu().numpy(), ref.float().cpu().numpy(), what="noalloc vs workspace")
