@@ -2,8 +2,8 @@
 """Benchmark of the int4 KV-cache decode step on GB300.
 
 One step = the whole hot path over one batch: quantize-on-store of the new
-token's K/V into the int4 cache (tq_quantize_kv_append), then fused split-K
-decode attention over the cache (tq_sdpa_int4_decode: phase 1 + LSE reduce).
+token's K/V into the int4 cache, then fused split-K decode attention over the
+cache (phase 1 + LSE reduce), issued as one tq_decode_step call.
 
 Workload (default): Llama-3.1-70B single-layer decode shape at 128K tokens --
 batch 1, 64 query heads, 8 KV heads, head_dim 128, 131072 cached tokens, int4
@@ -209,9 +209,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def step(i):
-        c = caches[i % nl]
-        tq.tq_quantize_kv_append(c, k_new, v_new, write_pos, status=status)
-        tq.tq_sdpa_int4_decode(c, qs[i % nl], seq_lens, S, ATTN, ws, out=out, chunk=CHUNK, status=status)
+        # one call: append the new token at row S-1, then decode over S rows
+        tq.tq_decode_step(caches[i % nl], k_new, v_new, write_pos, qs[i % nl], seq_lens, S, ATTN, ws, out=out,
+                          chunk=CHUNK, status=status)
 
     def barrier():
         if world > 1:
@@ -268,9 +268,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         d_q.copy_(h_q[i % nl], non_blocking=True)
         d_k.copy_(h_k, non_blocking=True)
         d_v.copy_(h_v, non_blocking=True)
-        c = caches[i % nl]
-        tq.tq_quantize_kv_append(c, d_k, d_v, write_pos, status=status)
-        tq.tq_sdpa_int4_decode(c, d_q, seq_lens, S, ATTN, ws, out=out, chunk=CHUNK, status=status)
+        tq.tq_decode_step(caches[i % nl], d_k, d_v, write_pos, d_q, seq_lens, S, ATTN, ws, out=out, chunk=CHUNK,
+                          status=status)
         h_out.copy_(out, non_blocking=True)
 
     for i in range(args.warmup):
@@ -411,8 +410,7 @@ def run_full_model(args, tq, synth, torch, dev, peak):
 
     def model_step(_):
         for c, q in zip(caches, qs):
-            tq.tq_quantize_kv_append(c, k_new, v_new, write_pos)
-            tq.tq_sdpa_int4_decode(c, q, seq_lens, S, ATTN, ws, out=out, chunk=CHUNK)
+            tq.tq_decode_step(c, k_new, v_new, write_pos, q, seq_lens, S, ATTN, ws, out=out, chunk=CHUNK)
 
     us = time_loop(torch, model_step, max(5, args.steps // 5))
     nbytes = FULL_MODEL_LAYERS * step_bytes(S)

@@ -174,6 +174,22 @@ tq_status tq_sdpa_int4_decode_impl(const tq_kv_cache* cache, const uint16_t* q,
                                    size_t workspace_bytes, uint16_t* out,
                                    int32_t* status, tq_impl impl, void* stream);
 
+/* One decode step: quantize-on-store of the new tokens, then fused int4 decode
+ * attention over the cache that now holds them ("turboquant-llama3.170B"
+ * README, decode-step listing: quantize K,V to int4, then fused sdpa_int4).
+ * Arguments as tq_quantize_kv_append and tq_sdpa_int4_decode (tensor-core
+ * path); results identical to calling the two in order on `stream`.  The
+ * decode launch may start while the append still runs and waits for it only
+ * in the CTAs whose runs read an appended row.  seq_lens must already count
+ * the new tokens (typically write_pos[b] + n_new). */
+tq_status tq_decode_step(const tq_kv_cache* cache, const uint16_t* k_new,
+                         const uint16_t* v_new, int32_t n_new,
+                         const int32_t* write_pos, const uint16_t* q,
+                         int32_t num_q_heads, const int32_t* seq_lens,
+                         int32_t max_seq_len, float attn_scale, int32_t chunk,
+                         void* workspace, size_t workspace_bytes,
+                         uint16_t* out, int32_t* status, void* stream);
+
 /* The split plan tq_sdpa_int4_decode uses on the current device: *n_splits
  * runs per (sequence, kv head), the longest *max_run_tokens tokens long.
  * Host-side query (reads device attributes). */

@@ -19,7 +19,7 @@ __all__ = [
     "TQ_DEV_TIMEOUT", "TQError", "lib", "lib_path", "tq_kv_cache", "KVCache",
     "tq_abi_version", "tq_status_string", "tq_kv_cache_bytes", "tq_sdpa_workspace_bytes",
     "tq_quantize_kv_append", "tq_sdpa_int4_decode", "tq_sdpa_int4_partial", "tq_sdpa_int4_reduce",
-    "tq_sdpa_plan", "tq_sdpa_int4_decode_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "tq_sdpa_plan", "tq_sdpa_int4_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "tq_decode_step",
 ]
 
 TQ_OK = 0
@@ -83,6 +83,7 @@ def lib() -> ctypes.CDLL:
             "tq_sdpa_int4_partial": ([C, P, i32, P, i32, f32, i32, i32, P, P, P, P, i32, P], i32),
             "tq_sdpa_int4_reduce": ([P, P, P, i32, i32, i32, i32, P, P], i32),
             "tq_sdpa_int4_decode_noalloc": ([C, P, i32, P, i32, f32, i32, P, P, P], i32),
+            "tq_decode_step": ([C, P, P, i32, P, P, i32, P, i32, f32, i32, P, sz, P, P, P], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -213,6 +214,33 @@ def tq_sdpa_int4_decode(cache: KVCache, q: torch.Tensor, seq_lens: torch.Tensor,
     _check("tq_sdpa_int4_decode", lib().tq_sdpa_int4_decode_impl(
         cache.ref(), _ptr(q), q.shape[1], _ptr(seq_lens), int(max_seq_len), float(attn_scale), int(chunk),
         _ptr(workspace), workspace.numel(), _ptr(out), _ptr(status), int(impl), _stream(stream)))
+    return out
+
+
+def tq_decode_step(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, write_pos: torch.Tensor,
+                   q: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int, attn_scale: float,
+                   workspace: torch.Tensor, out: Optional[torch.Tensor] = None, chunk: int = DEFAULT_CHUNK,
+                   status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Append k_new/v_new [B, Hkv, n_new, D] at write_pos, then decode q [B, Hq, D]
+    over seq_lens (which must already count the new tokens)."""
+    for t, n, dt in ((k_new, "k_new", torch.float16), (v_new, "v_new", torch.float16), (q, "q", torch.float16),
+                     (write_pos, "write_pos", torch.int32), (seq_lens, "seq_lens", torch.int32),
+                     (workspace, "workspace", torch.uint8)):
+        _need(t, dt, n)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.float16, "out")
+    if status is not None:
+        _need(status, torch.int32, "status")
+    n_new = k_new.shape[2] if k_new.dim() == 4 else 0
+    if tuple(k_new.shape) != (cache.batch, cache.num_kv_heads, n_new, cache.head_dim) or v_new.shape != k_new.shape:
+        raise ValueError(f"k_new/v_new must be [B, Hkv, n_new, D]; got {tuple(k_new.shape)}")
+    if q.dim() != 3 or q.shape[0] != cache.batch or q.shape[2] != cache.head_dim or out.shape != q.shape:
+        raise ValueError(f"q must be [B, Hq, D]; got {tuple(q.shape)}")
+    _check("tq_decode_step", lib().tq_decode_step(
+        cache.ref(), _ptr(k_new), _ptr(v_new), n_new, _ptr(write_pos), _ptr(q), q.shape[1], _ptr(seq_lens),
+        int(max_seq_len), float(attn_scale), int(chunk), _ptr(workspace), workspace.numel(), _ptr(out),
+        _ptr(status), _stream(stream)))
     return out
 
 

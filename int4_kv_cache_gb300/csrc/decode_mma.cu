@@ -181,6 +181,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
         bulk_load(sb + 3 * C::SB_BYTES, p.v_bias + sb_off, sb_bytes, &full_bar[stage], policy);
     };
     if (threadIdx.x == 0 && n_tiles > 0) {
+        if (p.dep_write_pos != nullptr) {
+            // launched while the append of this step may still run: wait for
+            // it only if this run reads a row it writes (later refills are
+            // issued after this point, so they see its rows as well)
+            const int wp = __ldg(p.dep_write_pos + b);
+            if (wp < t_end && wp + p.dep_n_new > t_begin) pdl_wait_primary();
+        }
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         const uint64_t policy = policy_evict_first();

@@ -74,6 +74,7 @@ __device__ __forceinline__ GroupQ quantize_lane8(uint4 raw) {
 }
 
 __global__ void __launch_bounds__(256) quantize_append_kernel(const AppendParams p) {
+    pdl_launch_dependents();  // no effect unless the next launch is a programmatic dependent
     const int ng = p.head_dim / kGroup;
     const long long n_groups = static_cast<long long>(p.batch) * p.num_kv_heads * p.n_new * ng;
     const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -127,6 +128,10 @@ cudaError_t launch_quantize_append(const AppendParams& p, cudaStream_t stream) {
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     quantize_append_kernel<<<static_cast<unsigned>(blocks), block, 0, stream>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_append_primary(const AppendParams& p, cudaStream_t stream) {
+    return launch_quantize_append(p, stream);
 }
 
 }  // namespace tq

@@ -179,7 +179,8 @@ tq_status check_decode_args(const tq_kv_cache* cache, const uint16_t* q, int32_t
 
 tq_status run_phase1(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
                      int32_t max_seq_len, float attn_scale, const Plan& pl, float* pm, float* plv, float* pa,
-                     int32_t* status, tq_impl impl, cudaStream_t stream) {
+                     int32_t* status, tq_impl impl, cudaStream_t stream, const int32_t* dep_write_pos = nullptr,
+                     int32_t dep_n_new = 0) {
     if (pl.n_splits > 65535 || cache->num_kv_heads > 65535 || cache->batch > 65535) return TQ_ERR_SHAPE;
     tq::DecodeParams p;
     p.q = q;
@@ -204,6 +205,8 @@ tq_status run_phase1(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, co
     p.units = pl.units;
     p.n_splits = pl.n_splits;
     p.score_scale_log2 = attn_scale * 1.4426950408889634f;
+    p.dep_write_pos = dep_write_pos;
+    p.dep_n_new = dep_n_new;
     if (impl == TQ_IMPL_SIMT) return cuda_status(tq::launch_decode_simt(p, cache->head_dim, stream));
     CUtensorMap tm_k, tm_v;
     const int box_rows = tq::mma_tile_tokens(cache->head_dim) * (cache->head_dim / 2) / 128;
@@ -211,7 +214,7 @@ tq_status run_phase1(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, co
     if (s != TQ_OK) return s;
     s = make_code_map(&tm_v, cache->v_codes, cache, box_rows);
     if (s != TQ_OK) return s;
-    return cuda_status(tq::launch_decode_mma(p, cache->head_dim, tm_k, tm_v, stream, false));
+    return cuda_status(tq::launch_decode_mma(p, cache->head_dim, tm_k, tm_v, stream, dep_write_pos != nullptr));
 }
 
 }  // namespace
@@ -309,15 +312,23 @@ tq_status tq_kv_cache_carve(tq_kv_cache* cache, void* base, int32_t batch, int32
     return TQ_OK;
 }
 
-tq_status tq_quantize_kv_append(const tq_kv_cache* cache, const uint16_t* k_new, const uint16_t* v_new,
-                                int32_t n_new, const int32_t* write_pos, int32_t* status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+tq_status check_append_args(const tq_kv_cache* cache, const uint16_t* k_new, const uint16_t* v_new, int32_t n_new,
+                            const int32_t* write_pos) {
     tq_status s = check_cache(cache);
     if (s != TQ_OK) return s;
     if (k_new == nullptr || v_new == nullptr || write_pos == nullptr) return TQ_ERR_NULL;
     if (!aligned16(k_new) || !aligned16(v_new)) return TQ_ERR_ALIGN;
     if (n_new < 0) return TQ_ERR_SHAPE;
     if (n_new > cache->capacity) return TQ_ERR_CAPACITY;
-    if (n_new == 0) return TQ_OK;
+    return TQ_OK;
+}
+
+tq::AppendParams append_params(const tq_kv_cache* cache, const uint16_t* k_new, const uint16_t* v_new,
+                               int32_t n_new, const int32_t* write_pos, int32_t* status) {
     tq::AppendParams p;
     p.k_new = k_new;
     p.v_new = v_new;
@@ -334,7 +345,62 @@ tq_status tq_quantize_kv_append(const tq_kv_cache* cache, const uint16_t* k_new,
     p.head_dim = cache->head_dim;
     p.n_new = n_new;
     p.capacity = cache->capacity;
-    return cuda_status(tq::launch_quantize_append(p, static_cast<cudaStream_t>(stream)));
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+tq_status tq_quantize_kv_append(const tq_kv_cache* cache, const uint16_t* k_new, const uint16_t* v_new,
+                                int32_t n_new, const int32_t* write_pos, int32_t* status, void* stream) {
+    tq_status s = check_append_args(cache, k_new, v_new, n_new, write_pos);
+    if (s != TQ_OK) return s;
+    if (n_new == 0) return TQ_OK;
+    return cuda_status(tq::launch_quantize_append(append_params(cache, k_new, v_new, n_new, write_pos, status),
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
+tq_status tq_decode_step(const tq_kv_cache* cache, const uint16_t* k_new, const uint16_t* v_new, int32_t n_new,
+                         const int32_t* write_pos, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
+                         int32_t max_seq_len, float attn_scale, int32_t chunk, void* workspace,
+                         size_t workspace_bytes, uint16_t* out, int32_t* status, void* stream) {
+    tq_status s = check_append_args(cache, k_new, v_new, n_new, write_pos);
+    if (s != TQ_OK) return s;
+    s = check_decode_args(cache, q, hq, seq_lens, max_seq_len, chunk, out);
+    if (s != TQ_OK) return s;
+    const size_t need =
+        tq_sdpa_workspace_bytes(cache->batch, hq, cache->num_kv_heads, cache->head_dim, max_seq_len, chunk);
+    if (workspace == nullptr || workspace_bytes < need) return TQ_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TQ_ERR_ALIGN;
+    Plan pl;
+    s = device_plan(cache, max_seq_len, chunk, TQ_IMPL_MMA, &pl);
+    if (s != TQ_OK) return s;
+    if (pl.n_splits > tq::kMaxReduceParts) return TQ_ERR_SHAPE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n_new > 0) {
+        s = cuda_status(tq::launch_quantize_append_primary(
+            append_params(cache, k_new, v_new, n_new, write_pos, status), st));
+        if (s != TQ_OK) return s;
+    }
+    const size_t parts = static_cast<size_t>(cache->batch) * hq * pl.n_splits;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* pm = reinterpret_cast<float*>(ws);
+    float* plv = reinterpret_cast<float*>(ws + align256(parts * sizeof(float)));
+    float* pa = reinterpret_cast<float*>(ws + 2 * align256(parts * sizeof(float)));
+    s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, TQ_IMPL_MMA, st,
+                   n_new > 0 ? write_pos : nullptr, n_new);
+    if (s != TQ_OK) return s;
+    tq::ReduceParams r;
+    r.part_m = pm;
+    r.part_l = plv;
+    r.part_acc = pa;
+    r.out = out;
+    r.batch = cache->batch;
+    r.num_q_heads = hq;
+    r.head_dim = cache->head_dim;
+    r.n_parts = pl.n_splits;
+    return cuda_status(tq::launch_reduce(r, st, true));
 }
 
 size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t hq, int32_t hkv, int32_t head_dim, int32_t max_seq_len,

@@ -32,6 +32,11 @@ struct DecodeParams {
     int32_t capacity, max_seq_len;
     int32_t unit_tokens, units, n_splits;
     float score_scale_log2;   // attn_scale * log2(e)
+    // Set when the launch is a programmatic dependent of an append that wrote
+    // rows [dep_write_pos[b], dep_write_pos[b] + dep_n_new): a CTA whose run
+    // covers any of them waits for the append before reading the cache.
+    const int32_t* dep_write_pos;
+    int32_t dep_n_new;
 };
 
 struct ReduceParams {
@@ -61,6 +66,9 @@ cudaError_t launch_quantize_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_decode_simt(const DecodeParams& p, int head_dim, cudaStream_t stream);
 cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, const CUtensorMap& tm_k,
                               const CUtensorMap& tm_v, cudaStream_t stream, bool pdl_secondary);
+// The append kernel, optionally letting the next launch start early (the
+// decode kernel then waits only where it reads the appended rows).
+cudaError_t launch_quantize_append_primary(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl_secondary);
 
 // Tokens per pipeline stage of the tensor-core kernel (tiles are TMA boxes).

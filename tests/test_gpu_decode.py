@@ -12,7 +12,8 @@ import pytest
 
 import oracle
 from int4_kv_cache_gb300 import synth
-from tests.gpu_helpers import ATOL, assert_close, decode, gpu_cache_from_fp16, gpu_cache_from_oracle, need_gpu
+from tests.gpu_helpers import (ATOL, assert_close, decode, gpu_cache_from_fp16, gpu_cache_from_oracle, need_gpu,
+                               workspace_for)
 
 pytestmark = pytest.mark.gpu
 
@@ -242,3 +243,37 @@ def test_ragged32_decode_step_full_size_sampled():
         oc = oracle.Cache.from_fp16(kk, vv)
         ref = oracle.attention(np.ascontiguousarray(qh[b:b + 1, h:h + 1]), oc, np.array([L + 1]), w.attn_scale)
         assert_close(out[b:b + 1, h:h + 1], ref, what=f"ragged b{b} h{h}")
+
+
+def test_fused_step_equals_append_then_decode():
+    """tq_decode_step (append, then a decode launched before the append ends)
+    gives what the two calls give in order, with the appended rows at the
+    start, in the middle and at the end of a CTA's run, and in a ragged batch."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    B, Hq, Hkv, D, S = 3, 64, 8, 128, 20000
+    x = synth.decode_inputs(61, B, Hq, Hkv, D, S, outliers=True)
+    pos = np.array([0, 9001, S - 2], np.int32)  # the new tokens go to rows pos[b], pos[b] + 1
+    kn, vn = synth.append_tokens(61, 3, B, Hkv, D, 2, outliers=x.outlier_channels)
+    lens = pos + 2
+    q = torch.from_numpy(x.q).cuda()
+    wp = torch.from_numpy(pos).cuda()
+    lt = torch.from_numpy(lens).cuda()
+    knt, vnt = torch.from_numpy(kn).cuda(), torch.from_numpy(vn).cuda()
+    ws = workspace_for(B, Hq, Hkv, D, S)
+    c1 = gpu_cache_from_fp16(x.k, x.v)
+    tq.tq_quantize_kv_append(c1, knt, vnt, wp)
+    ref = tq.tq_sdpa_int4_decode(c1, q, lt, S, 0.088, ws).float().cpu().numpy()
+    c2 = gpu_cache_from_fp16(x.k, x.v)
+    for _ in range(2):  # a second step rewrites the same rows: same result
+        got = tq.tq_decode_step(c2, knt, vnt, wp, q, lt, S, 0.088, ws).float().cpu().numpy()
+        assert np.array_equal(got, ref)
+    assert torch.equal(c1.buffer, c2.buffer)
+    # and against the oracle on the appended cache
+    kk, vv = x.k.copy(), x.v.copy()
+    for b in range(B):
+        kk[b, :, pos[b]:pos[b] + 2] = kn[b]
+        vv[b, :, pos[b]:pos[b] + 2] = vn[b]
+    oref = oracle.attention(x.q, oracle.Cache.from_fp16(kk, vv), lens, 0.088)
+    assert_close(got, oref, what="fused step")
