@@ -51,6 +51,7 @@ namespace {
 
 constexpr uint32_t kLoNib = 0x000F000Fu;  // nibbles at bits 0..3 / 16..19 -> n * 2^-24
 constexpr uint32_t kHiNib = 0x00F000F0u;  // nibbles at bits 4..7 / 20..23 -> 16 n * 2^-24
+constexpr float kLazyMax = 8.0f;          // slack of the running softmax max (log2 units)
 
 template <int D>
 struct Cfg {
@@ -119,6 +120,27 @@ __device__ __forceinline__ void load_row_sb(const uint16_t* base, int tok, float
     }
 }
 
+// NG fp16 values of two token rows; for D <= 128 the rows are adjacent and one
+// load brings both.
+template <int D, int NG>
+__device__ __forceinline__ void load_pair_sb(const uint16_t* base, int tok_a, int tok_b, float (&a)[NG],
+                                             float (&bb)[NG]) {
+    if constexpr (Cfg<D>::EVEN_ODD && NG == 2) {  // tok_b == tok_a + 1
+        const Half4 h = *reinterpret_cast<const Half4*>(base + tok_a * 2);
+        a[0] = __low2float(h.a);
+        a[1] = __high2float(h.a);
+        bb[0] = __low2float(h.b);
+        bb[1] = __high2float(h.b);
+    } else if constexpr (Cfg<D>::EVEN_ODD && NG == 1) {
+        const __half2 h = *reinterpret_cast<const __half2*>(base + tok_a);
+        a[0] = __low2float(h);
+        bb[0] = __high2float(h);
+    } else {
+        load_row_sb<NG>(base, tok_a, a);
+        load_row_sb<NG>(base, tok_b, bb);
+    }
+}
+
 __device__ __forceinline__ int clamp_len(const DecodeParams& p, int b) {
     int len = __ldg(p.seq_lens + b);
     if (len < 0 || len > p.max_seq_len) {
@@ -137,7 +159,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
     constexpr int NG = C::NG;
     __shared__ uint64_t full_bar[C::STAGES];
     __shared__ unsigned int done_cnt[C::STAGES];  // warps finished with the stage, cumulative
-    __shared__ float mrg_m[C::NWC][8], mrg_l[C::NWC][8];
+    __shared__ float mrg_m[C::NWC][8], mrg_l[C::NWC][8], mrg_t[C::NWC][8];
     extern __shared__ uint8_t dyn_smem[];
     const uint32_t dyn_base = smem_u32(dyn_smem);
     uint8_t* smem = dyn_smem + ((1024u - (dyn_base & 1023u)) & 1023u);
@@ -238,7 +260,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
     const float k_coef = sl2 * 16777216.0f;  // undo the 2^-24 of the subnormal operands
     const int r0 = tok_of_row<D>(gid), r1 = tok_of_row<D>(gid + 8);
 
-    float m_run[2] = {-INFINITY, -INFINITY};
+    float m_run[2] = {-INFINITY, -INFINITY};  // reference max of l, acc (lazy)
+    float m_true[2] = {-INFINITY, -INFINITY}; // this thread's largest score so far
     float l_run[2] = {0.0f, 0.0f};
     float e_run[NG][2];
     float acc[C::NKS][4];
@@ -306,10 +329,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
                     }
                 }
                 float ksa[NG], kba[NG], ksb[NG], kbb[NG];
-                load_row_sb<NG>(ks_s, tb + r0, ksa);
-                load_row_sb<NG>(kb_s, tb + r0, kba);
-                load_row_sb<NG>(ks_s, tb + r1, ksb);
-                load_row_sb<NG>(kb_s, tb + r1, kbb);
+                load_pair_sb<D, NG>(ks_s, tb + r0, tb + r1, ksa, ksb);
+                load_pair_sb<D, NG>(kb_s, tb + r0, tb + r1, kba, kbb);
                 const bool va = !kTail || t0 + tb + r0 < t_end, vb = !kTail || t0 + tb + r1 < t_end;
     #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
@@ -325,31 +346,45 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
                 }
             }
 
-            // ---- online softmax update over this warp's tokens of the stage
-            float m_use[2];
+            // ---- online softmax update over this warp's tokens of the stage.
+            // The running max only moves when a score exceeds it by more than
+            // kLazyMax (log2 units): until then p = 2^(s - m) <= 2^kLazyMax,
+            // harmless for the fp32 sums and the fp16 B operand, and the
+            // cross-lane reduction and rescale are skipped for the stage.
+            float mx[2];
+            bool grow = false;
     #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                float mx = -INFINITY;
+                mx[hh] = -INFINITY;
     #pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt) mx = fmaxf(mx, fmaxf(sc[mt][hh], sc[mt][2 + hh]));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float m_new = fmaxf(m_run[hh], mx);
-                m_use[hh] = m_new == -INFINITY ? 0.0f : m_new;
-                if (m_new > m_run[hh]) {
-                    const float alpha = m_run[hh] == -INFINITY ? 0.0f : ex2_approx(m_run[hh] - m_new);
-                    l_run[hh] *= alpha;
+                for (int mt = 0; mt < C::MT; ++mt) mx[hh] = fmaxf(mx[hh], fmaxf(sc[mt][hh], sc[mt][2 + hh]));
+                grow |= mx[hh] > m_run[hh] + kLazyMax;
+                m_true[hh] = fmaxf(m_true[hh], mx[hh]);
+            }
+            if (__any_sync(0xffffffffu, grow)) {
     #pragma unroll
-                    for (int g = 0; g < NG; ++g) e_run[g][hh] *= alpha;
+                for (int hh = 0; hh < 2; ++hh) {
+                    float m = mx[hh];
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+                    if (m > m_run[hh]) {
+                        const float alpha = m_run[hh] == -INFINITY ? 0.0f : ex2_approx(m_run[hh] - m);
+                        l_run[hh] *= alpha;
     #pragma unroll
-                    for (int i = 0; i < C::NKS; ++i) {
-                        acc[i][hh] *= alpha;
-                        acc[i][2 + hh] *= alpha;
+                        for (int g = 0; g < NG; ++g) e_run[g][hh] *= alpha;
+    #pragma unroll
+                        for (int i = 0; i < C::NKS; ++i) {
+                            acc[i][hh] *= alpha;
+                            acc[i][2 + hh] *= alpha;
+                        }
+                        m_run[hh] = m;
                     }
-                    m_run[hh] = m_new;
                 }
             }
+            float m_use[2];
+    #pragma unroll
+            for (int hh = 0; hh < 2; ++hh) m_use[hh] = m_run[hh] == -INFINITY ? 0.0f : m_run[hh];
 
             // ---- P.V for each m-tile of this warp
     #pragma unroll
@@ -363,10 +398,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
                 l_run[0] += pr[0] + pr[2];
                 l_run[1] += pr[1] + pr[3];
                 float vsa[NG], vba[NG], vsb[NG], vbb[NG];
-                load_row_sb<NG>(vs_s, tb + r0, vsa);
-                load_row_sb<NG>(vb_s, tb + r0, vba);
-                load_row_sb<NG>(vs_s, tb + r1, vsb);
-                load_row_sb<NG>(vb_s, tb + r1, vbb);
+                load_pair_sb<D, NG>(vs_s, tb + r0, tb + r1, vsa, vsb);
+                load_pair_sb<D, NG>(vb_s, tb + r0, tb + r1, vba, vbb);
                 // B operand p_t * vscale_tg as an fp16 pair hi + lo (hi = fp16(r), lo =
                 // fp16(r - hi)): one fp16 rounding of r would leave 2^-12 relative noise
                 // on every term of sum_t r_t n_t, which the code offset (n in 0..15, mean
@@ -379,13 +412,13 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
                     const float ba = va ? vba[g] : 0.0f, bb = vb ? vbb[g] : 0.0f;
                     e_run[g][0] = fmaf(pr[0], ba, fmaf(pr[2], bb, e_run[g][0]));
                     e_run[g][1] = fmaf(pr[1], ba, fmaf(pr[3], bb, e_run[g][1]));
-                    const float r0 = pr[0] * sa, r1 = pr[1] * sa, r2 = pr[2] * sb, r3 = pr[3] * sb;
-                    const __half2 h01 = __floats2half2_rn(r0, r1), h23 = __floats2half2_rn(r2, r3);
+                    const float q0 = pr[0] * sa, q1 = pr[1] * sa, q2 = pr[2] * sb, q3 = pr[3] * sb;
+                    const __half2 h01 = __floats2half2_rn(q0, q1), h23 = __floats2half2_rn(q2, q3);
                     const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
                     bhi[g][0] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h01));
                     bhi[g][1] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h23));
-                    blo[g][0] = movmatrix_trans(pack_half2(r0 - f01.x, r1 - f01.y));
-                    blo[g][1] = movmatrix_trans(pack_half2(r2 - f23.x, r3 - f23.y));
+                    blo[g][0] = movmatrix_trans(pack_half2(q0 - f01.x, q1 - f01.y));
+                    blo[g][1] = movmatrix_trans(pack_half2(q2 - f23.x, q3 - f23.y));
                 }
                 // This tile's sum_t r_t n_t goes into fresh tensor-core accumulators
                 // and is then added to the running state with round-to-nearest fp32
@@ -436,7 +469,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
         }
     }
 
-    // ---- reduce per-thread sums over the 8 token rows (lanes differing in gid)
+    // ---- reduce per-thread sums and maxima over the 8 token rows (lanes differing in gid)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) m_true[hh] = fmaxf(m_true[hh], __shfl_xor_sync(0xffffffffu, m_true[hh], off));
+    }
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
@@ -469,6 +507,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
         if (gid == 0) {
             mrg_m[warp][2 * tig] = m_run[0];
             mrg_m[warp][2 * tig + 1] = m_run[1];
+            mrg_t[warp][2 * tig] = m_true[0];
+            mrg_t[warp][2 * tig + 1] = m_true[1];
             mrg_l[warp][2 * tig] = l_run[0];
             mrg_l[warp][2 * tig + 1] = l_run[1];
         }
@@ -479,7 +519,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
         const int h = idx / D, d = idx % D;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < C::NWC; ++w) M = fmaxf(M, mrg_m[w][h]);
+        for (int w = 0; w < C::NWC; ++w) M = fmaxf(M, mrg_t[w][h]);  // the run's largest score
         float L = 0.0f, A = 0.0f;
         if (M != -INFINITY) {
 #pragma unroll
