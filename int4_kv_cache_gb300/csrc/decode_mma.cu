@@ -386,11 +386,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
     #pragma unroll
             for (int hh = 0; hh < 2; ++hh) m_use[hh] = m_run[hh] == -INFINITY ? 0.0f : m_run[hh];
 
-            // ---- P.V for each m-tile of this warp
+            // ---- P.V.  B operand p_t * vscale_tg as an fp16 pair hi + lo (hi =
+            // fp16(r), lo = fp16(r - hi)): one fp16 rounding of r would leave 2^-12
+            // relative noise on every term of sum_t r_t n_t, which the code offset
+            // (n in 0..15, mean near 7.5) amplifies past the 1e-3 output budget at
+            // long context.
+            uint32_t bhi[C::MT][NG][2], blo[C::MT][NG][2];
     #pragma unroll
             for (int mt = 0; mt < C::MT; ++mt) {
                 const int tb = (warp * C::MT + mt) * 16;
-                const uint32_t sw = static_cast<uint32_t>((tb / C::TPR) & 7) << 4;
                 const bool va = !kTail || t0 + tb + r0 < t_end, vb = !kTail || t0 + tb + r1 < t_end;
                 float pr[4];
     #pragma unroll
@@ -400,11 +404,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
                 float vsa[NG], vba[NG], vsb[NG], vbb[NG];
                 load_pair_sb<D, NG>(vs_s, tb + r0, tb + r1, vsa, vsb);
                 load_pair_sb<D, NG>(vb_s, tb + r0, tb + r1, vba, vbb);
-                // B operand p_t * vscale_tg as an fp16 pair hi + lo (hi = fp16(r), lo =
-                // fp16(r - hi)): one fp16 rounding of r would leave 2^-12 relative noise
-                // on every term of sum_t r_t n_t, which the code offset (n in 0..15, mean
-                // near 7.5) amplifies well past the 1e-3 output budget at long context.
-                uint32_t bhi[NG][2], blo[NG][2];
     #pragma unroll
                 for (int g = 0; g < NG; ++g) {
                     // masked rows may hold stale scale/bias bits: select, never multiply
@@ -415,37 +414,46 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
                     const float q0 = pr[0] * sa, q1 = pr[1] * sa, q2 = pr[2] * sb, q3 = pr[3] * sb;
                     const __half2 h01 = __floats2half2_rn(q0, q1), h23 = __floats2half2_rn(q2, q3);
                     const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-                    bhi[g][0] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h01));
-                    bhi[g][1] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h23));
-                    blo[g][0] = movmatrix_trans(pack_half2(q0 - f01.x, q1 - f01.y));
-                    blo[g][1] = movmatrix_trans(pack_half2(q2 - f23.x, q3 - f23.y));
+                    bhi[mt][g][0] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h01));
+                    bhi[mt][g][1] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h23));
+                    blo[mt][g][0] = movmatrix_trans(pack_half2(q0 - f01.x, q1 - f01.y));
+                    blo[mt][g][1] = movmatrix_trans(pack_half2(q2 - f23.x, q3 - f23.y));
                 }
-                // This tile's sum_t r_t n_t goes into fresh tensor-core accumulators
-                // and is then added to the running state with round-to-nearest fp32
-                // adds.  The code sum is ~7.5 sum_t r_t while the attention output is
-                // what is left after the bias term cancels most of it, so a long
-                // chain of tensor-core accumulations (whose fp32 sums are not
-                // round-to-nearest) would leave a systematic error far above 1e-3
-                // of the output at long context.
+            }
+            // The stage's sum_t r_t n_t (all MT tiles) goes into fresh tensor-core
+            // accumulators and is then added to the running state with
+            // round-to-nearest fp32 adds.  The code sum is ~7.5 sum_t r_t while the
+            // attention output is what is left after the bias term cancels most
+            // of it, so a long chain of tensor-core accumulations (whose fp32 sums
+            // are not round-to-nearest) would leave a systematic error far above
+            // 1e-3 of the output at long context.
     #pragma unroll
-                for (int sp = 0; sp < C::SPT / 2; ++sp) {
-                    uint32_t x0, x1, x2, x3;
-                    ldmatrix_x4_trans(vc_s + tb * C::BPT + (lm_off[sp] ^ sw), x0, x1, x2, x3);
+            for (int sp = 0; sp < C::SPT / 2; ++sp) {
+                uint32_t x[C::MT][4];
     #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int s = 2 * sp + e;
-                        const int g = (32 * s) / kGroup;
-                        const uint32_t xa = e ? x2 : x0;  // tokens of rows 0..7  (k 0..7)
-                        const uint32_t xb = e ? x3 : x1;  // tokens of rows 8..15 (k 8..15)
+                for (int mt = 0; mt < C::MT; ++mt) {
+                    const int tb = (warp * C::MT + mt) * 16;
+                    const uint32_t sw = static_cast<uint32_t>((tb / C::TPR) & 7) << 4;
+                    ldmatrix_x4_trans(vc_s + tb * C::BPT + (lm_off[sp] ^ sw), x[mt][0], x[mt][1], x[mt][2], x[mt][3]);
+                }
     #pragma unroll
-                        for (int j = 0; j < 2; ++j) {
+                for (int e = 0; e < 2; ++e) {
+                    const int s = 2 * sp + e;
+                    const int g = (32 * s) / kGroup;
+    #pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        float t[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    #pragma unroll
+                        for (int mt = 0; mt < C::MT; ++mt) {
+                            const uint32_t xa = e ? x[mt][2] : x[mt][0];  // tokens of rows 0..7  (k 0..7)
+                            const uint32_t xb = e ? x[mt][3] : x[mt][1];  // tokens of rows 8..15 (k 8..15)
                             const uint32_t ua = j ? (xa >> 8) : xa, ub = j ? (xb >> 8) : xb;
-                            float t[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                            mma_16816(t, ua & kLoNib, ua & kHiNib, ub & kLoNib, ub & kHiNib, bhi[g][0], bhi[g][1]);
-                            mma_16816(t, ua & kLoNib, ua & kHiNib, ub & kLoNib, ub & kHiNib, blo[g][0], blo[g][1]);
-    #pragma unroll
-                            for (int c = 0; c < 4; ++c) acc[2 * s + j][c] = __fadd_rn(acc[2 * s + j][c], t[c]);
+                            const uint32_t a0 = ua & kLoNib, a1 = ua & kHiNib, a2 = ub & kLoNib, a3 = ub & kHiNib;
+                            mma_16816(t, a0, a1, a2, a3, bhi[mt][g][0], bhi[mt][g][1]);
+                            mma_16816(t, a0, a1, a2, a3, blo[mt][g][0], blo[mt][g][1]);
                         }
+    #pragma unroll
+                        for (int c = 0; c < 4; ++c) acc[2 * s + j][c] = __fadd_rn(acc[2 * s + j][c], t[c]);
                     }
                 }
             }
