@@ -29,12 +29,12 @@
 //    The high-nibble elements meet q/16 in the B operand (the pages' qdot
 //    "pre-divide the query" idea), so all products carry the same 2^-24.
 //  * P.V uses mma.sync with M = 16 head_dim elements, N = 8 heads, K = 16
-//    tokens.  B = p_t * vscale_tg as an fp16 hi/lo pair (two MMAs into the same
-//    fp32 accumulator, ~2^-22 relative), built from the score fragments with
+//    tokens.  B = fp16(p_t * vscale_tg), built from the score fragments with
 //    movmatrix (no shared-memory round trip); the bias part
-//    sum_t p_t * vbias_tg is accumulated in fp32 on the side.  Each 16-token
-//    tile's code sum is formed in fresh tensor-core accumulators and added to
-//    the running state with round-to-nearest fp32 adds.
+//    sum_t p_t * vbias_tg, and the mean-code share of the fp16 rounding
+//    error of B, are accumulated in fp32 on the side.  Each stage's code sum
+//    is formed in fresh tensor-core accumulators and added to the running
+//    state with round-to-nearest fp32 adds.
 //  * Token order inside a 16-token tile and the head_dim order inside each
 //    operand are chosen so that every ldmatrix is bank-conflict free against
 //    the swizzled tile; the permutation is undone when the state is written.
@@ -44,6 +44,7 @@
 
 #include "tq_device.cuh"
 #include "tq_internal.h"
+#include "tq_quant.cuh"
 
 namespace tq {
 
@@ -52,6 +53,7 @@ namespace {
 constexpr uint32_t kLoNib = 0x000F000Fu;  // nibbles at bits 0..3 / 16..19 -> n * 2^-24
 constexpr uint32_t kHiNib = 0x00F000F0u;  // nibbles at bits 4..7 / 20..23 -> 16 n * 2^-24
 constexpr float kLazyMax = 8.0f;          // slack of the running softmax max (log2 units)
+constexpr float kCodeMean = 7.5f;         // mean of a code uniform on 0..15
 
 template <int D>
 struct Cfg {
@@ -62,7 +64,7 @@ struct Cfg {
     static constexpr int NWC = 4;                  // warps (all consume; the last to finish a stage refills it)
     static constexpr int MT = (D == 256) ? 1 : 2;  // 16-token m-tiles per warp per stage
     static constexpr int T = NWC * MT * 16;        // tokens per stage
-    static constexpr int STAGES = 3;
+    static constexpr int STAGES = 4;
     static constexpr int CODE_BYTES = T * BPT;     // one code tile (K or V)
     static constexpr int SB_BYTES = T * NG * 2;    // one scale or bias tile
     static constexpr int STAGE_BYTES = ((2 * CODE_BYTES + 4 * SB_BYTES + 1023) / 1024) * 1024;
@@ -70,9 +72,9 @@ struct Cfg {
     static constexpr int THREADS = NWC * 32;
     static constexpr int NKS = D / 16;             // k-steps of the score MMA = m-tiles of P.V
     static constexpr bool EVEN_ODD = D <= 128;     // token order inside a 16-token tile
-    // 4 resident CTAs (16 warps) need <= 128 registers per thread: each SM
-    // sub-partition then holds 4 warps in its 16K registers.
-    static constexpr int MIN_CTAS = (D == 256) ? 2 : 4;
+    // Resident CTAs per SM: 3 for D = 128 (shared memory: 4 stages of 18 KB
+    // each), 4 for D = 64 (whose stages are half as large), 2 for D = 256.
+    static constexpr int MIN_CTAS = (D == 256) ? 2 : (D == 128 ? 3 : 4);
     static_assert(CODE_BYTES % 1024 == 0, "code tiles must keep the 1024-byte swizzle period");
     static_assert(STAGES * STAGE_BYTES >= NWC * 8 * D * 4, "merge buffer must fit in the stages");
 };
@@ -183,11 +185,41 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
     __syncthreads();
     pdl_launch_dependents();
 
+    // Rows the append of this step writes while this grid may already run
+    // (programmatic dependent launch): a tile that uses any of them is issued
+    // only after the append grid has completed.  Other tiles do not wait.
+    int dep_lo = 0, dep_hi = 0;
+    if (p.dep_write_pos != nullptr) {
+        dep_lo = __ldg(p.dep_write_pos + b);
+        dep_hi = dep_lo + p.dep_n_new;
+    }
+
+    // Fused append: rows [app_lo, app_hi) of this (b, kv head) are owned by
+    // this run and quantized here before any tile that uses them is loaded.
+    int app_lo = 0, app_hi = 0, app_wp = 0;
+    if (p.app.n_new > 0) {
+        const int wp = app_wp = __ldg(p.app.write_pos + b);
+        if (wp < 0 || static_cast<long long>(wp) + p.app.n_new > p.capacity) {
+            if (p.status != nullptr && threadIdx.x == 0 && split == 0 && kvh == 0)
+                atomicOr(p.status, TQ_DEV_WRITE_POS);
+        } else {
+            const int own_end =
+                split + 1 == p.n_splits ? p.capacity : run_begin(split + 1, p.units, p.n_splits, p.unit_tokens);
+            app_lo = max(wp, run_begin(split, p.units, p.n_splits, p.unit_tokens));
+            app_hi = min(wp + p.app.n_new, own_end);
+        }
+    }
+    auto tile_uses = [&](int it, int lo, int hi) {
+        const int t0 = t_begin + it * C::T;
+        return lo < min(t0 + C::T, t_end) && hi > t0;
+    };
+
     // Fill stage it % STAGES with tile it: both code tiles by TMA, the four
     // scale/bias rows by bulk copies; completion counted in bytes on full_bar.
     auto issue_tile = [&](int it, uint64_t policy) {
         const int stage = it % C::STAGES;
         const int t0 = t_begin + it * C::T;
+        if (tile_uses(it, dep_lo, dep_hi)) pdl_wait_primary();
         const int avail = min(C::T, p.capacity - t0);  // rows left in this (b, kv head)
         const uint32_t sb_bytes = static_cast<uint32_t>(avail) * NG * 2;
         uint8_t* st = smem + stage * C::STAGE_BYTES;
@@ -203,18 +235,25 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
         bulk_load(sb + 3 * C::SB_BYTES, p.v_bias + sb_off, sb_bytes, &full_bar[stage], policy);
     };
     if (threadIdx.x == 0 && n_tiles > 0) {
-        if (p.dep_write_pos != nullptr) {
-            // launched while the append of this step may still run: wait for
-            // it only if this run reads a row it writes (later refills are
-            // issued after this point, so they see its rows as well)
-            const int wp = __ldg(p.dep_write_pos + b);
-            if (wp < t_end && wp + p.dep_n_new > t_begin) pdl_wait_primary();
-        }
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         const uint64_t policy = policy_evict_first();
-        for (int it = 0; it < min(n_tiles, C::STAGES); ++it) issue_tile(it, policy);
+        for (int it = 0; it < min(n_tiles, C::STAGES); ++it)
+            if (!tile_uses(it, app_lo, app_hi)) issue_tile(it, policy);
     }
+    // The fused append, part 1: the first pass of new-row loads is issued now
+    // so that its latency overlaps the Q loads below.
+    const int app_tasks = (app_hi - app_lo) * NG * 2;  // eight lanes per (row, group, K|V)
+    const int app_part = threadIdx.x & 7;
+    auto app_src = [&](int task) {
+        const int kv = task & 1, g = (task >> 1) % NG, r = app_lo + (task >> 1) / NG;
+        return (kv ? p.app.v_new : p.app.k_new) +
+               (((static_cast<long long>(b) * p.num_kv_heads + kvh) * p.app.n_new + (r - app_wp)) * D + g * kGroup +
+                app_part * 8);
+    };
+    uint4 app_raw = make_uint4(0, 0, 0, 0);
+    if (static_cast<int>(threadIdx.x >> 3) < app_tasks)
+        app_raw = __ldcs(reinterpret_cast<const uint4*>(app_src(threadIdx.x >> 3)));
 
     // ------------------------------------------------------------ all warps
     const int gid = lane >> 2, tig = lane & 3;
@@ -269,6 +308,44 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
     for (int g = 0; g < NG; ++g) e_run[g][0] = e_run[g][1] = 0.0f;
 #pragma unroll
     for (int i = 0; i < C::NKS; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+
+    // The fused append, part 2: quantize the rows this run owns, publish them
+    // to the async proxy, then load the first tiles that use them.
+    if (app_lo < app_hi) {  // the same for the whole CTA
+        for (int t0 = 0; t0 < app_tasks; t0 += C::THREADS / 8) {  // uniform trip count: shuffles inside
+            const int task = t0 + (threadIdx.x >> 3);
+            const bool valid = task < app_tasks;
+            uint4 raw = app_raw;
+            if (t0 > 0 && valid) raw = __ldcs(reinterpret_cast<const uint4*>(app_src(task)));
+            const GroupQ gq = quantize_lane8(raw);
+            if (valid) {
+                const int kv = task & 1, g = (task >> 1) % NG, r = app_lo + (task >> 1) / NG;
+                const long long row = row_base + r;
+                *reinterpret_cast<uint32_t*>((kv ? p.app.v_codes : p.app.k_codes) + row * (D / 2) +
+                                             g * (kGroup / 2) + app_part * 4) = gq.codes;
+                if (app_part == 0) {
+                    (kv ? p.app.v_scale : p.app.k_scale)[row * NG + g] = __half_as_ushort(gq.scale);
+                    (kv ? p.app.v_bias : p.app.k_bias)[row * NG + g] = __half_as_ushort(gq.bias);
+                }
+            }
+        }
+        // Ordering: the proxy fence makes the stores visible to later TMA /
+        // bulk reads; the reads are issued after a CTA-scope synchronisation
+        // with every writer -- the barrier below for the first STAGES tiles,
+        // the per-stage release count (each warp's fence and counter update
+        // after its stores) for a later refill.
+        fence_proxy_async_global();
+        bool early = false;
+        for (int it = 0; it < min(n_tiles, C::STAGES); ++it) early |= tile_uses(it, app_lo, app_hi);
+        if (early) {  // the same for the whole CTA
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                const uint64_t policy = policy_evict_first();
+                for (int it = 0; it < min(n_tiles, C::STAGES); ++it)
+                    if (tile_uses(it, app_lo, app_hi)) issue_tile(it, policy);
+            }
+        }
+    }
 
     // ldmatrix row address pattern: lane -> (matrix, row)
     const int lm_mat = lane >> 3, lm_row = lane & 7;
@@ -386,12 +463,14 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
     #pragma unroll
             for (int hh = 0; hh < 2; ++hh) m_use[hh] = m_run[hh] == -INFINITY ? 0.0f : m_run[hh];
 
-            // ---- P.V.  B operand p_t * vscale_tg as an fp16 pair hi + lo (hi =
-            // fp16(r), lo = fp16(r - hi)): one fp16 rounding of r would leave 2^-12
-            // relative noise on every term of sum_t r_t n_t, which the code offset
-            // (n in 0..15, mean near 7.5) amplifies past the 1e-3 output budget at
-            // long context.
-            uint32_t bhi[C::MT][NG][2], blo[C::MT][NG][2];
+            // ---- P.V.  B operand r_t = p_t * vscale_tg rounded to fp16.  Its
+            // rounding error e_t = r_t - fp16(r_t) (up to 2^-11 relative) meets
+            // codes n in 0..15 whose mean is near 7.5, so sum_t e_t n_t would
+            // be a visible bias next to the small attention output at long
+            // context.  Most of it is the mean part 7.5 * sum_t e_t, which is
+            // added back in fp32 together with the bias term; what is left,
+            // sum_t e_t (n_t - 7.5), is at most half as large and averages out.
+            uint32_t bhi[C::MT][NG][2];
     #pragma unroll
             for (int mt = 0; mt < C::MT; ++mt) {
                 const int tb = (warp * C::MT + mt) * 16;
@@ -409,15 +488,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
                     // masked rows may hold stale scale/bias bits: select, never multiply
                     const float sa = va ? vsa[g] : 0.0f, sb = vb ? vsb[g] : 0.0f;
                     const float ba = va ? vba[g] : 0.0f, bb = vb ? vbb[g] : 0.0f;
-                    e_run[g][0] = fmaf(pr[0], ba, fmaf(pr[2], bb, e_run[g][0]));
-                    e_run[g][1] = fmaf(pr[1], ba, fmaf(pr[3], bb, e_run[g][1]));
                     const float q0 = pr[0] * sa, q1 = pr[1] * sa, q2 = pr[2] * sb, q3 = pr[3] * sb;
                     const __half2 h01 = __floats2half2_rn(q0, q1), h23 = __floats2half2_rn(q2, q3);
                     const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+                    e_run[g][0] = fmaf(pr[0], ba, fmaf(pr[2], bb, e_run[g][0]));
+                    e_run[g][1] = fmaf(pr[1], ba, fmaf(pr[3], bb, e_run[g][1]));
+                    e_run[g][0] = fmaf(kCodeMean, (q0 - f01.x) + (q2 - f23.x), e_run[g][0]);
+                    e_run[g][1] = fmaf(kCodeMean, (q1 - f01.y) + (q3 - f23.y), e_run[g][1]);
                     bhi[mt][g][0] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h01));
                     bhi[mt][g][1] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h23));
-                    blo[mt][g][0] = movmatrix_trans(pack_half2(q0 - f01.x, q1 - f01.y));
-                    blo[mt][g][1] = movmatrix_trans(pack_half2(q2 - f23.x, q3 - f23.y));
                 }
             }
             // The stage's sum_t r_t n_t (all MT tiles) goes into fresh tensor-core
@@ -450,7 +529,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
                             const uint32_t ua = j ? (xa >> 8) : xa, ub = j ? (xb >> 8) : xb;
                             const uint32_t a0 = ua & kLoNib, a1 = ua & kHiNib, a2 = ub & kLoNib, a3 = ub & kHiNib;
                             mma_16816(t, a0, a1, a2, a3, bhi[mt][g][0], bhi[mt][g][1]);
-                            mma_16816(t, a0, a1, a2, a3, blo[mt][g][0], blo[mt][g][1]);
                         }
     #pragma unroll
                         for (int c = 0; c < 4; ++c) acc[2 * s + j][c] = __fadd_rn(acc[2 * s + j][c], t[c]);
@@ -507,9 +585,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
             const int g = d_lo / kGroup;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
+                // element d of head h sits at h * D + (d ^ (h >> 1 & 3)): the XOR
+                // spreads the four tig lanes of a store over different banks
                 const int h = 2 * tig + hh;
-                wacc[h * D + d_lo] = fmaf(acc[i][hh], 16777216.0f, e_run[g][hh]);
-                wacc[h * D + d_hi] = fmaf(acc[i][2 + hh], 1048576.0f, e_run[g][hh]);
+                wacc[h * D + (d_lo ^ tig)] = fmaf(acc[i][hh], 16777216.0f, e_run[g][hh]);
+                wacc[h * D + (d_hi ^ tig)] = fmaf(acc[i][2 + hh], 1048576.0f, e_run[g][hh]);
             }
         }
         if (gid == 0) {
@@ -534,7 +614,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
             for (int w = 0; w < C::NWC; ++w) {
                 const float wt = mrg_m[w][h] == -INFINITY ? 0.0f : ex2_approx(mrg_m[w][h] - M);
                 L = fmaf(wt, mrg_l[w][h], L);
-                A = fmaf(wt, mrg_acc[(w * 8 + h) * D + d], A);
+                A = fmaf(wt, mrg_acc[(w * 8 + h) * D + (d ^ (h >> 1 & 3))], A);
             }
         }
         const long long ph = (static_cast<long long>(b) * p.num_q_heads + kvh * G + h) * p.n_splits + split;

@@ -37,55 +37,74 @@ __device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) 
 
 // Warp w sums parts w, w + 8, ...; lane owns head_dim elements
 // [lane * V, lane * V + V), read with vector loads; the eight warp sums are
-// combined through shared memory.
+// combined through shared memory.  The first R rows of every warp are loaded
+// before the weights are known, so the row reads overlap the max / sum
+// reductions instead of following them.
 template <int D>
 __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceParams p) {
-    constexpr int V = D / 32;
-    extern __shared__ float w_s[];  // [n_parts]
+    constexpr int V = D / 32;  // floats per lane per row
+    constexpr int R = 48 / V;  // rows per warp in flight
+    extern __shared__ float w_s[];  // [n_parts]: m, then the weight of each part
     __shared__ float red[kReduceWarps];
     __shared__ float part_sum[kReduceWarps][D];
     pdl_wait_primary();
-
     const long long bh = blockIdx.x;
     const int n = p.n_parts;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float* pm = p.part_m + bh * n;
     const float* pl = p.part_l + bh * n;
     const float* pa = p.part_acc + bh * n * D;
-
+    float x[R][V];
+    auto load_rows = [&](int base) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int c = base + warp + r * kReduceWarps;
+            if (c < n) {
+                const float* src = pa + static_cast<long long>(c) * D + lane * V;
+                if constexpr (V == 2) {
+                    const float2 v = *reinterpret_cast<const float2*>(src);
+                    x[r][0] = v.x; x[r][1] = v.y;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < V; i += 4) {
+                        const float4 v = *reinterpret_cast<const float4*>(src + i);
+                        x[r][i] = v.x; x[r][i + 1] = v.y; x[r][i + 2] = v.z; x[r][i + 3] = v.w;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < V; ++i) x[r][i] = 0.0f;
+            }
+        }
+    };
+    load_rows(0);
     float M = -INFINITY;
-    for (int c = threadIdx.x; c < n; c += kReduceThreads)
-        if (pl[c] > 0.0f) M = fmaxf(M, pm[c]);
+    for (int c = threadIdx.x; c < n; c += kReduceThreads) {
+        const float m = pl[c] > 0.0f ? pm[c] : -INFINITY;  // empty parts carry no weight
+        w_s[c] = m;
+        M = fmaxf(M, m);
+    }
     M = block_reduce(M, red, true);
-
     float L = 0.0f;
     for (int c = threadIdx.x; c < n; c += kReduceThreads) {
-        const float w = (pl[c] > 0.0f) ? expf(pm[c] - M) : 0.0f;
+        const float m = w_s[c];
+        const float w = m == -INFINITY ? 0.0f : expf(m - M);
         w_s[c] = w;
-        L += w * pl[c];
+        L = fmaf(w, pl[c], L);
     }
     L = block_reduce(L, red, false);  // its barriers also publish w_s
-
     float a[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) a[i] = 0.0f;
-#pragma unroll 4
-    for (int c = warp; c < n; c += kReduceWarps) {
-        const float w = w_s[c];
-        if (w == 0.0f) continue;  // empty part (same branch for the whole warp)
-        const float* src = pa + static_cast<long long>(c) * D + lane * V;
-        if constexpr (V == 2) {
-            const float2 x = *reinterpret_cast<const float2*>(src);
-            a[0] = fmaf(w, x.x, a[0]);
-            a[1] = fmaf(w, x.y, a[1]);
-        } else {
+    for (int base = 0; base < n; base += R * kReduceWarps) {
+        if (base > 0) load_rows(base);
 #pragma unroll
-            for (int i = 0; i < V; i += 4) {
-                const float4 x = *reinterpret_cast<const float4*>(src + i);
-                a[i] = fmaf(w, x.x, a[i]);
-                a[i + 1] = fmaf(w, x.y, a[i + 1]);
-                a[i + 2] = fmaf(w, x.z, a[i + 2]);
-                a[i + 3] = fmaf(w, x.w, a[i + 3]);
+        for (int r = 0; r < R; ++r) {
+            const int c = base + warp + r * kReduceWarps;
+            const float w = c < n ? w_s[c] : 0.0f;
+            if (w != 0.0f) {  // same branch for the whole warp
+#pragma unroll
+                for (int i = 0; i < V; ++i) a[i] = fmaf(w, x[r][i], a[i]);
             }
         }
     }

@@ -180,7 +180,7 @@ tq_status check_decode_args(const tq_kv_cache* cache, const uint16_t* q, int32_t
 tq_status run_phase1(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
                      int32_t max_seq_len, float attn_scale, const Plan& pl, float* pm, float* plv, float* pa,
                      int32_t* status, tq_impl impl, cudaStream_t stream, const int32_t* dep_write_pos = nullptr,
-                     int32_t dep_n_new = 0) {
+                     int32_t dep_n_new = 0, const tq::AppendParams* fused_append = nullptr) {
     if (pl.n_splits > 65535 || cache->num_kv_heads > 65535 || cache->batch > 65535) return TQ_ERR_SHAPE;
     tq::DecodeParams p;
     p.q = q;
@@ -207,6 +207,11 @@ tq_status run_phase1(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, co
     p.score_scale_log2 = attn_scale * 1.4426950408889634f;
     p.dep_write_pos = dep_write_pos;
     p.dep_n_new = dep_n_new;
+    p.app = {};
+    if (fused_append != nullptr) {
+        if (impl == TQ_IMPL_SIMT) return TQ_ERR_UNSUPPORTED;
+        p.app = *fused_append;
+    }
     if (impl == TQ_IMPL_SIMT) return cuda_status(tq::launch_decode_simt(p, cache->head_dim, stream));
     CUtensorMap tm_k, tm_v;
     const int box_rows = tq::mma_tile_tokens(cache->head_dim) * (cache->head_dim / 2) / 128;
@@ -378,9 +383,14 @@ tq_status tq_decode_step(const tq_kv_cache* cache, const uint16_t* k_new, const 
     if (s != TQ_OK) return s;
     if (pl.n_splits > tq::kMaxReduceParts) return TQ_ERR_SHAPE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (n_new > 0) {
-        s = cuda_status(tq::launch_quantize_append_primary(
-            append_params(cache, k_new, v_new, n_new, write_pos, status), st));
+    // A few new rows per sequence are quantized by the decode kernel itself
+    // (the CTA that reads them writes them first); longer appends run the
+    // append kernel, and the decode starts early and waits only for the tiles
+    // that hold the new rows.
+    const tq::AppendParams ap = append_params(cache, k_new, v_new, n_new, write_pos, status);
+    const bool fused = n_new > 0 && n_new <= tq::kFusedAppendMaxRows;
+    if (n_new > 0 && !fused) {
+        s = cuda_status(tq::launch_quantize_append_primary(ap, st));
         if (s != TQ_OK) return s;
     }
     const size_t parts = static_cast<size_t>(cache->batch) * hq * pl.n_splits;
@@ -389,7 +399,7 @@ tq_status tq_decode_step(const tq_kv_cache* cache, const uint16_t* k_new, const 
     float* plv = reinterpret_cast<float*>(ws + align256(parts * sizeof(float)));
     float* pa = reinterpret_cast<float*>(ws + 2 * align256(parts * sizeof(float)));
     s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, TQ_IMPL_MMA, st,
-                   n_new > 0 ? write_pos : nullptr, n_new);
+                   n_new > 0 && !fused ? write_pos : nullptr, fused ? 0 : n_new, fused ? &ap : nullptr);
     if (s != TQ_OK) return s;
     tq::ReduceParams r;
     r.part_m = pm;

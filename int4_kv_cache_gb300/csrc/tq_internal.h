@@ -11,6 +11,20 @@ namespace tq {
 
 constexpr int kGroup = 64;
 
+struct AppendParams {
+    const uint16_t* k_new;    // [B][Hkv][n_new][D]
+    const uint16_t* v_new;
+    const int32_t* write_pos; // [B]
+    uint8_t* k_codes;
+    uint8_t* v_codes;
+    uint16_t* k_scale;
+    uint16_t* k_bias;
+    uint16_t* v_scale;
+    uint16_t* v_bias;
+    int32_t* status;
+    int32_t batch, num_kv_heads, head_dim, n_new, capacity;
+};
+
 // Geometry of one phase-1 launch: grid (n_splits, Hkv, B).  The sequence is
 // cut into `units` units of `unit_tokens` tokens; CTA (s, kvh, b) covers units
 // [floor(s * units / n_splits), floor((s + 1) * units / n_splits)) of sequence b
@@ -33,11 +47,20 @@ struct DecodeParams {
     int32_t unit_tokens, units, n_splits;
     float score_scale_log2;   // attn_scale * log2(e)
     // Set when the launch is a programmatic dependent of an append that wrote
-    // rows [dep_write_pos[b], dep_write_pos[b] + dep_n_new): a CTA whose run
-    // covers any of them waits for the append before reading the cache.
+    // rows [dep_write_pos[b], dep_write_pos[b] + dep_n_new): a tile that
+    // uses any of them waits for the append before it is loaded.
     const int32_t* dep_write_pos;
     int32_t dep_n_new;
+    // Fused append (tensor-core kernel only, app.n_new > 0): before reading
+    // them, the CTA whose run owns rows [write_pos[b], write_pos[b] + n_new)
+    // quantizes k_new / v_new into those rows itself.  A run owns
+    // [run_begin(s), run_begin(s + 1)); the last run also owns the rows up to
+    // the capacity.
+    AppendParams app;
 };
+// Most rows per sequence the decode kernel appends itself; longer appends
+// run the append kernel first.
+constexpr int kFusedAppendMaxRows = 16;
 
 struct ReduceParams {
     const float* part_m;
@@ -47,19 +70,6 @@ struct ReduceParams {
     int32_t batch, num_q_heads, head_dim, n_parts;
 };
 
-struct AppendParams {
-    const uint16_t* k_new;    // [B][Hkv][n_new][D]
-    const uint16_t* v_new;
-    const int32_t* write_pos; // [B]
-    uint8_t* k_codes;
-    uint8_t* v_codes;
-    uint16_t* k_scale;
-    uint16_t* k_bias;
-    uint16_t* v_scale;
-    uint16_t* v_bias;
-    int32_t* status;
-    int32_t batch, num_kv_heads, head_dim, n_new, capacity;
-};
 
 // Launchers (return the cudaError_t of the launch).
 cudaError_t launch_quantize_append(const AppendParams& p, cudaStream_t stream);
@@ -77,7 +87,7 @@ int mma_smem_bytes(int head_dim);
 // Resident CTAs per SM of the phase-1 kernels (occupancy API).
 int mma_ctas_per_sm(int head_dim);
 int simt_ctas_per_sm(int head_dim);
-// Largest n_parts the reduce kernel takes (its weights live in shared memory).
+// Largest n_parts the reduce kernel takes.
 constexpr int kMaxReduceParts = 8192;
 // Most CTAs a decode plan launches (bounds the workspace independently of the device).
 constexpr int kMaxDecodeCtas = 2048;

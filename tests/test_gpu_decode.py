@@ -277,3 +277,74 @@ def test_fused_step_equals_append_then_decode():
         vv[b, :, pos[b]:pos[b] + 2] = vn[b]
     oref = oracle.attention(x.q, oracle.Cache.from_fp16(kk, vv), lens, 0.088)
     assert_close(got, oref, what="fused step")
+
+
+def _run_begins(n_splits, max_len, unit=128):
+    units = -(-max_len // unit)
+    return [(s * units // n_splits) * unit for s in range(n_splits + 1)]
+
+
+@pytest.mark.parametrize("n_new", [1, 16, 17, 40])
+def test_fused_step_rows_across_run_boundaries(n_new):
+    """Up to 16 new rows per sequence are quantized by the decode kernel (each
+    CTA writes the rows its run owns, then reads them); longer appends run the
+    append kernel first.  Rows straddling a run boundary, at the start of the
+    cache and at its end give the same cache bytes and the same output as the
+    append kernel followed by the decode."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    B, Hq, Hkv, D, S = 3, 64, 8, 128, 20000
+    x = synth.decode_inputs(71, B, Hq, Hkv, D, S, outliers=True)
+    c1 = gpu_cache_from_fp16(x.k, x.v)
+    ns, run = tq.tq_sdpa_plan(c1, Hq, S)
+    rb = _run_begins(ns, S)
+    assert max(b - a for a, b in zip(rb, rb[1:])) == run  # the boundaries the kernel uses
+    pos = np.array([0, rb[ns // 2] - n_new // 2, S - n_new], np.int32)
+    kn, vn = synth.append_tokens(71, n_new, B, Hkv, D, n_new, outliers=x.outlier_channels)
+    lens = pos + n_new
+    q = torch.from_numpy(x.q).cuda()
+    wp, lt = torch.from_numpy(pos).cuda(), torch.from_numpy(lens).cuda()
+    knt, vnt = torch.from_numpy(kn).cuda(), torch.from_numpy(vn).cuda()
+    ws = workspace_for(B, Hq, Hkv, D, S)
+    tq.tq_quantize_kv_append(c1, knt, vnt, wp)
+    ref = tq.tq_sdpa_int4_decode(c1, q, lt, S, 0.088, ws).float().cpu().numpy()
+    c2 = gpu_cache_from_fp16(x.k, x.v)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = tq.tq_decode_step(c2, knt, vnt, wp, q, lt, S, 0.088, ws, status=st).float().cpu().numpy()
+    assert int(st.item()) == 0
+    assert torch.equal(c1.buffer, c2.buffer)
+    assert np.array_equal(got, ref)
+
+
+def test_fused_step_write_pos_out_of_range():
+    """A fused append whose rows would pass the capacity writes nothing and sets
+    TQ_DEV_WRITE_POS; the decode over the unchanged cache still runs."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    B, Hq, Hkv, D, S = 2, 16, 2, 128, 1024
+    x = synth.decode_inputs(73, B, Hq, Hkv, D, S)
+    c = gpu_cache_from_fp16(x.k, x.v)
+    before = c.buffer.clone()
+    kn, vn = synth.append_tokens(73, 0, B, Hkv, D, 2)
+    pos = np.array([S - 1, 5], np.int32)  # b = 0 overflows, b = 1 is in range
+    lens = np.array([S, S], np.int32)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = workspace_for(B, Hq, Hkv, D, S)
+    got = tq.tq_decode_step(c, torch.from_numpy(kn).cuda(), torch.from_numpy(vn).cuda(),
+                            torch.from_numpy(pos).cuda(), torch.from_numpy(x.q).cuda(), torch.from_numpy(lens).cuda(),
+                            S, 0.088, ws, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & tq.TQ_DEV_WRITE_POS
+    after = c.buffer
+    # sequence 0's rows are untouched; sequence 1's rows 5, 6 were written
+    ref_c = gpu_cache_from_fp16(x.k, x.v)
+    kk, vv = x.k.copy(), x.v.copy()
+    kk[1, :, 5:7] = kn[1]
+    vv[1, :, 5:7] = vn[1]
+    ref_c2 = gpu_cache_from_fp16(kk, vv)
+    assert not torch.equal(before, after)
+    assert torch.equal(after, ref_c2.buffer)
+    oref = oracle.attention(x.q, oracle.Cache.from_fp16(kk, vv), lens, 0.088)
+    assert_close(got.float().cpu().numpy(), oref, what="fused step, one row out of range")
