@@ -3,7 +3,8 @@
 
 One step = the whole hot path over one batch: quantize-on-store of the new
 token's K/V into the int4 cache, then fused split-K decode attention over the
-cache (phase 1 + LSE reduce), issued as one tq_decode_step call.
+cache (phase 1 + LSE reduce), issued as one tq_decode_step call; the new
+row is quantized by the phase-1 CTA that later reads it.
 
 Workload (default): Llama-3.1-70B single-layer decode shape at 128K tokens --
 batch 1, 64 query heads, 8 KV heads, head_dim 128, 131072 cached tokens, int4
@@ -225,34 +226,40 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     pl = torch.empty_like(pm)
     pa = torch.empty((B, HQ, n_splits, D), dtype=torch.float32, device=dev)
 
-    # ---- headline: K steps with device-resident inputs
+    # ---- headline: K steps with device-resident inputs, replayed from one
+    # CUDA graph of exactly K tq_decode_step calls (the serving-loop form:
+    # no host launch gaps inside the step sequence)
     for i in range(args.warmup):
         step(i)
     barrier()
+    g_steps = capture_graph(torch, step, args.steps)
+    g_steps.replay()  # untimed: first replay of the captured graph
+    barrier()
     with ClockSampler(local_rank) as clk:
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        g_steps.replay()
+        t1.record()
+        barrier()
+        ms_total = t0.elapsed_time(t1)
+        # ---- the same K steps issued eagerly, one host call each (information)
         t0.record()
         for i in range(args.steps):
             step(i)
         t1.record()
         barrier()
-        ms_total = t0.elapsed_time(t1)
-        # ---- per-kernel durations on the same stream: append | phase 1 | reduce
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-        for i in range(args.steps):
-            c = caches[i % nl]
-            ev[i][0].record()
-            tq.tq_quantize_kv_append(c, k_new, v_new, write_pos, status=status)
-            ev[i][1].record()
-            tq.tq_sdpa_int4_partial(c, qs[i % nl], seq_lens, S, ATTN, chunk=CHUNK, chunks_per_split=0,
-                                    status=status, out=(pm, pl, pa))
-            ev[i][2].record()
-            tq.tq_sdpa_int4_reduce(pm, pl, pa, out=out)
-            ev[i][3].record()
+        eager_ms = t0.elapsed_time(t1)
+        # ---- per-kernel average durations on the same stream, each kernel
+        # replayed K times back to back from its own graph: append | phase 1 | reduce
+        append_us = time_graph(torch, lambda i: tq.tq_quantize_kv_append(caches[i % nl], k_new, v_new, write_pos,
+                                                                          status=status), args.steps)
+        phase1_us = time_graph(torch, lambda i: tq.tq_sdpa_int4_partial(
+            caches[i % nl], qs[i % nl], seq_lens, S, ATTN, chunk=CHUNK, chunks_per_split=0, status=status,
+            out=(pm, pl, pa)), args.steps)
+        reduce_us = time_graph(torch, lambda i: tq.tq_sdpa_int4_reduce(pm, pl, pa, out=out), args.steps)
         barrier()
+    del g_steps
     clocks = clk.summary()
-    k_ms = np.array([[ev[i][j].elapsed_time(ev[i][j + 1]) for j in range(3)] for i in range(args.steps)])
-    append_us, phase1_us, reduce_us = (k_ms.mean(axis=0) * 1e3).tolist()
 
     # ---- e2e: through the C ABI from pinned host buffers, result read back every step
     h_q = [torch.empty((B, HQ, D), dtype=torch.float16).pin_memory() for _ in range(nl)]
@@ -329,8 +336,12 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "bytes_per_step": step_bytes(S),
             "splits": {"n_splits_per_head": n_splits, "max_run_tokens": run_tokens},
         },
-        "kernels_us": {"quantize_append": round(append_us, 3), "sdpa_phase1": round(phase1_us, 3),
-                       "sdpa_reduce": round(reduce_us, 3)},
+        "launch": f"one CUDA graph of the {args.steps} timed tq_decode_step calls",
+        "eager_us_per_step": round(eager_ms / args.steps * 1e3, 3),
+        "kernels_us": {"sdpa_phase1": round(phase1_us, 3), "sdpa_reduce": round(reduce_us, 3),
+                       "quantize_append_kernel": round(append_us, 3),
+                       "how": ("each kernel alone, K launches replayed back to back from one CUDA graph; the step "
+                               "fuses its 1-row append into phase 1, the append kernel serves longer appends")},
         "roofline": {
             "kernel": "decode_mma_kernel<128> (sdpa phase 1)",
             "bound": "hbm",
@@ -346,7 +357,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         },
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_per_step, 6)},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,  # per step: phase 1 (with the 1-row append fused in) + reduce
         "device_status": st,
         "clocks": clocks,
         "prefill_quantize_128k": prefill_summary(prefill_ms, peak),
@@ -366,17 +377,31 @@ def prefill_summary(ms_list, peak):
             "bytes_per_layer": rd + wr, "layers_timed": len(ms_list)}
 
 
-def time_loop(torch, fn, reps):
+def capture_graph(torch, fn, n):
+    """One CUDA graph holding fn(0) .. fn(n - 1) (fn was already run eagerly)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n):
+            fn(i)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(torch, fn, n):
+    """Average device time of fn(i) over n calls replayed from one CUDA graph
+    (no host launch gaps), in microseconds; one untimed replay first."""
     for i in range(3):
         fn(i)
     torch.cuda.synchronize()
+    g = capture_graph(torch, fn, n)
+    g.replay()
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for i in range(reps):
-        fn(i)
+    g.replay()
     e1.record()
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) * 1e3 / reps  # microseconds
+    return e0.elapsed_time(e1) * 1e3 / n
 
 
 def run_extras(args, tq, synth, torch, dev, caches, qs, ws, out, peak):
@@ -390,8 +415,8 @@ def run_extras(args, tq, synth, torch, dev, caches, qs, ws, out, peak):
         for impl, tag in ((1, "mma"), (2, "simt")):
             if impl == 2 and n not in (16384, 131072):
                 continue
-            us = time_loop(torch, lambda i: tq.tq_sdpa_int4_decode(caches[i % nl], qs[i % nl], lens, n, ATTN, ws,
-                                                                   out=out, chunk=CHUNK, impl=impl), reps)
+            us = time_graph(torch, lambda i: tq.tq_sdpa_int4_decode(caches[i % nl], qs[i % nl], lens, n, ATTN, ws,
+                                                                    out=out, chunk=CHUNK, impl=impl), reps)
             gbs = (cache_bytes(n) + B * HQ * D * 4) / (us * 1e-6) / 1e9
             res["sweep_decode_only"][f"{n // 1024}k_{tag}"] = {"us": round(us, 3), "GB_per_s": round(gbs, 1),
                                                                "frac": round(gbs / peak, 4)}
@@ -412,7 +437,7 @@ def run_full_model(args, tq, synth, torch, dev, peak):
         for c, q in zip(caches, qs):
             tq.tq_decode_step(c, k_new, v_new, write_pos, q, seq_lens, S, ATTN, ws, out=out, chunk=CHUNK)
 
-    us = time_loop(torch, model_step, max(5, args.steps // 5))
+    us = time_graph(torch, model_step, max(5, args.steps // 5))
     nbytes = FULL_MODEL_LAYERS * step_bytes(S)
     gbs = nbytes / (us * 1e-6) / 1e9
     res = {"ms_per_step": round(us / 1e3, 4), "GB_per_s": round(gbs, 1), "frac": round(gbs / peak, 4),
