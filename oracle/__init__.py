@@ -36,6 +36,7 @@ def lib() -> ctypes.CDLL:
         L.tqo_quantize_group.argtypes = [P, i32, P, P, P]
         L.tqo_quantize_rows.argtypes = [P, i64, i32, i32, P, P, P]
         L.tqo_dequantize_rows.argtypes = [P, P, P, i64, i32, i32, P]
+        L.tqo_dequantize_rows_f16.argtypes = [P, P, P, i64, i32, i32, P]
         L.tqo_attention.argtypes = [P, i32, i32, i32, i32, i32, i64, P, P, P, P, P, P, P, f64,
                                     P, i64, P]
         L.tqo_attention_partials.argtypes = [P, i32, i32, i32, i32, i32, i64, P, P, P, P, P, P,
@@ -109,6 +110,17 @@ def dequantize_rows(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray, grou
     rows = codes.size // (D // 2)
     out = np.empty(codes.shape[:-1] + (D,), dtype=np.float64)
     lib().tqo_dequantize_rows(_ptr(codes), _ptr(scale), _ptr(bias), rows, D, group, _ptr(out))
+    return out
+
+
+def dequantize_rows_f16(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray, group: int = 64):
+    """fp16 bits [.., D] of fp16_rne(fp32(scale * code + bias)) per element."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scale, bias = _bits16(scale), _bits16(bias)
+    D = codes.shape[-1] * 2
+    rows = codes.size // (D // 2)
+    out = np.empty(codes.shape[:-1] + (D,), dtype=np.uint16)
+    lib().tqo_dequantize_rows_f16(_ptr(codes), _ptr(scale), _ptr(bias), rows, D, group, _ptr(out))
     return out
 
 

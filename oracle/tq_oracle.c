@@ -151,6 +151,28 @@ void tqo_dequantize_rows(const uint8_t* codes_packed, const uint16_t* scale,
                                          bias + r * ng, d, group);
 }
 
+/* fp16 dequantisation: the float K/V a dequantize-then-SDPA baseline builds
+ * before attention ([G4] What I Built Instead: the MLX path expands the int4
+ * cache to float K/V and runs ordinary SDPA).  Reading: one fp32 rounding of
+ * scale * code + bias (the product is exact in fp32: 11 x 4 significant bits),
+ * then RNE to binary16. */
+void tqo_dequantize_rows_f16(const uint8_t* codes_packed, const uint16_t* scale,
+                             const uint16_t* bias, int64_t rows, int D, int group,
+                             uint16_t* out) {
+    int ng = D / group;
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint8_t* rc = codes_packed + r * (D / 2);
+        for (int d = 0; d < D; ++d) {
+            uint8_t byte = rc[d / 2];
+            int code = (d & 1) ? (byte >> 4) : (byte & 0xf);
+            int g = d / group;
+            float sc = (float)tqo_f16_to_f64(scale[r * ng + g]);
+            float bi = (float)tqo_f16_to_f64(bias[r * ng + g]);
+            out[r * D + d] = tqo_f32_to_f16(fmaf(sc, (float)code, bi));
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Decode attention ([L70] kernel paragraph: scores from the int4 data,       */
 /* softmax, weighted sum of values; GQA with Hq/Hkv query heads per KV head). */

@@ -68,6 +68,12 @@ void tqo_dequantize_rows(const uint8_t* codes_packed, const uint16_t* scale,
                          const uint16_t* bias, int64_t rows, int D, int group,
                          double* out);
 
+/* Dequantize rows to fp16 bits: out[rows][D] = fp16_rne(fp32(scale * code + bias)),
+ * the float cache of a dequantize-then-attend baseline. */
+void tqo_dequantize_rows_f16(const uint8_t* codes_packed, const uint16_t* scale,
+                             const uint16_t* bias, int64_t rows, int D, int group,
+                             uint16_t* out);
+
 /* Single-token decode attention over a quantised cache.
  * q:    [B][Hq][D] fp16 bits
  * kc,vc:[B][Hkv][cap][D/2] packed codes; ks,kb,vs,vb: [B][Hkv][cap][D/group]

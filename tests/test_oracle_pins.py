@@ -142,6 +142,40 @@ def test_quantize_round_trip_bound_and_ends():
     assert np.all(np.diff(np.take_along_axis(codes.astype(int), order, axis=1), axis=1) >= 0)
 
 
+def _ulp16(v):
+    """Spacing of binary16 numbers at |v| (2^-24 in the subnormal range)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0**-14)))
+    return 2.0 ** (e - 10)
+
+
+def test_dequantize_f16_pins():
+    """fp16 dequantisation (the float cache of the dequantize-then-attend
+    baseline): grid values exact, code 0 gives the bias bits, within half an
+    fp16 ulp (plus the fp32 step) of the exact fp64 value, monotone in the code."""
+    x, ks = _grid_group()
+    codes_p, sc, bi = oracle.quantize_rows(x.reshape(1, 64))
+    assert np.array_equal(oracle.dequantize_rows_f16(codes_p, sc, bi).view(np.float16).ravel(), x)
+
+    rng = np.random.default_rng(9)
+    xs = _random_groups(rng, 2000)
+    codes_p, sc, bi = oracle.quantize_rows(xs)
+    h = oracle.dequantize_rows_f16(codes_p, sc, bi)
+    got = h.view(np.float16).astype(np.float64)
+    exact = oracle.dequantize_rows(codes_p, sc, bi)          # fp64, exact
+    err = np.abs(got - exact)
+    assert np.all(err <= 0.5 * _ulp16(np.maximum(np.abs(got), np.abs(exact))) + np.abs(exact) * 2.0**-24)
+    codes = np.stack([(codes_p & 0xF), (codes_p >> 4)], axis=-1).reshape(xs.shape)
+    zero = codes == 0
+    assert np.array_equal(h[zero], np.broadcast_to(bi[:, :1], codes.shape)[zero])  # code 0 -> bias bits
+    # every code of every group: monotone non-decreasing in the code (scale >= 0)
+    all_codes = np.tile(np.arange(16, dtype=np.uint8), 4)
+    packed = (all_codes[0::2] | (all_codes[1::2] << 4)).astype(np.uint8)
+    grid = oracle.dequantize_rows_f16(np.broadcast_to(packed, (sc.shape[0], 32)), sc, bi)
+    g = grid.view(np.float16).astype(np.float64)[:, :16]
+    assert np.all(np.diff(g, axis=1) >= 0)
+
+
 def test_quantize_degenerate_groups():
     for v in (0.0, 1.5, -7.25, 65504.0, -2.0**-24):
         x = np.full(64, v, dtype=np.float16)
