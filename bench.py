@@ -420,6 +420,38 @@ def run_extras(args, tq, synth, torch, dev, caches, qs, ws, out, peak):
             gbs = (cache_bytes(n) + B * HQ * D * 4) / (us * 1e-6) / 1e9
             res["sweep_decode_only"][f"{n // 1024}k_{tag}"] = {"us": round(us, 3), "GB_per_s": round(gbs, 1),
                                                                "frac": round(gbs / peak, 4)}
+    res["dequant_sdpa_baseline_128k"] = run_dequant_baseline(args, tq, torch, dev, caches, qs, peak)
+    return res
+
+
+def run_dequant_baseline(args, tq, torch, dev, caches, qs, peak):
+    """The decode the fused kernel replaces, at the same 128K shape: expand
+    the int4 cache to fp16 K/V (tq_dequantize_kv), then torch's SDPA with GQA.
+    Timed per part and together, same layer rotation; GB/s in the fused path's
+    algorithmic bytes so the two read side by side."""
+    nl = len(caches)
+    k16 = torch.empty((B, HKV, S, D), dtype=torch.float16, device=dev)
+    v16 = torch.empty_like(k16)
+    sdpa = torch.nn.functional.scaled_dot_product_attention
+
+    def deq(i):
+        tq.tq_dequantize_kv(caches[i % nl], S, out=(k16, v16))
+
+    def att(i):
+        sdpa(qs[i % nl].unsqueeze(2), k16, v16, scale=ATTN, enable_gqa=True)
+
+    def both(i):
+        deq(i)
+        att(i)
+
+    reps = max(10, args.steps // 2)
+    deq_us, att_us, both_us = (time_graph(torch, f, reps) for f in (deq, att, both))
+    deq_bytes = cache_bytes(S) + 2 * B * HKV * S * D * 2  # int4 cache read + fp16 K/V written
+    res = {"dequant_us": round(deq_us, 3), "sdpa_us": round(att_us, 3), "total_us": round(both_us, 3),
+           "dequant_GB_per_s": round(deq_bytes / (deq_us * 1e-6) / 1e9, 1),
+           "total_GB_per_s_fused_bytes": round(step_bytes(S) / (both_us * 1e-6) / 1e9, 1),
+           "sdpa": "torch.nn.functional.scaled_dot_product_attention(enable_gqa=True) over fp16 K/V"}
+    del k16, v16
     return res
 
 

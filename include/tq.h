@@ -215,6 +215,20 @@ tq_status tq_sdpa_int4_partial(const tq_kv_cache* cache, const uint16_t* q,
                                float* part_m, float* part_l, float* part_acc,
                                int32_t* status, tq_impl impl, void* stream);
 
+/* Expand rows [0, n_rows) of every (sequence, KV head) of the cache into fp16
+ * K and V, k_out / v_out [batch][num_kv_heads][n_rows][head_dim] (device,
+ * caller-owned, 16-byte aligned):
+ *   value = fp16_rne(fp32(scale * code + bias))
+ * (one fp32 rounding -- the product is exact -- then RNE to binary16).  This
+ * is the float cache of the dequantize-then-attend decode that the fused
+ * kernel replaces ("Fused int4 Attention for Gemma 4 31B on Apple Silicon",
+ * What I Built Instead); it is here as that comparison point, not as a step of
+ * the fused path.  Errors: TQ_ERR_NULL, TQ_ERR_SHAPE (n_rows < 0),
+ * TQ_ERR_CAPACITY (n_rows > capacity), TQ_ERR_ALIGN, plus the cache checks.
+ * n_rows = 0 launches nothing. */
+tq_status tq_dequantize_kv(const tq_kv_cache* cache, int32_t n_rows,
+                           uint16_t* k_out, uint16_t* v_out, void* stream);
+
 /* Split-K phase 2 alone ("Phase 2 (reduce)" of the same paragraph): per (b, h),
  *   M = max over parts with l > 0 of m,  w_c = exp(m_c - M),
  *   out = sum_c w_c acc_c / sum_c w_c l_c   (fp16, RNE; all-empty rows -> 0).

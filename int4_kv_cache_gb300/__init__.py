@@ -20,6 +20,7 @@ __all__ = [
     "tq_abi_version", "tq_status_string", "tq_kv_cache_bytes", "tq_sdpa_workspace_bytes",
     "tq_quantize_kv_append", "tq_sdpa_int4_decode", "tq_sdpa_int4_partial", "tq_sdpa_int4_reduce",
     "tq_sdpa_plan", "tq_sdpa_int4_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "tq_decode_step",
+    "tq_dequantize_kv",
 ]
 
 TQ_OK = 0
@@ -84,6 +85,7 @@ def lib() -> ctypes.CDLL:
             "tq_sdpa_int4_reduce": ([P, P, P, i32, i32, i32, i32, P, P], i32),
             "tq_sdpa_int4_decode_noalloc": ([C, P, i32, P, i32, f32, i32, P, P, P], i32),
             "tq_decode_step": ([C, P, P, i32, P, P, i32, P, i32, f32, i32, P, sz, P, P, P], i32),
+            "tq_dequantize_kv": ([C, i32, P, P, P], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -315,3 +317,20 @@ def tq_sdpa_int4_decode_noalloc(cache: KVCache, q: torch.Tensor, seq_lens: torch
         cache.ref(), _ptr(q), q.shape[1], _ptr(seq_lens), int(max_seq_len), float(attn_scale), int(chunk),
         _ptr(out), _ptr(status), _stream(stream)))
     return out
+
+
+def tq_dequantize_kv(cache: KVCache, n_rows: int, out=None, stream=None):
+    """fp16 K and V [B, Hkv, n_rows, D] of rows [0, n_rows) of the cache:
+    fp16_rne(fp32(scale * code + bias)).  The float cache of the
+    dequantize-then-attend comparison path; the fused decode never uses it."""
+    shape = (cache.batch, cache.num_kv_heads, int(n_rows), cache.head_dim)
+    if out is None:
+        dev = cache.buffer.device
+        out = (torch.empty(shape, dtype=torch.float16, device=dev), torch.empty(shape, dtype=torch.float16, device=dev))
+    k, v = out
+    for t, n in ((k, "k_out"), (v, "v_out")):
+        _need(t, torch.float16, n)
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{n} must be {shape}; got {tuple(t.shape)}")
+    _check("tq_dequantize_kv", lib().tq_dequantize_kv(cache.ref(), int(n_rows), _ptr(k), _ptr(v), _stream(stream)))
+    return k, v

@@ -521,4 +521,33 @@ tq_status tq_sdpa_int4_reduce(const float* part_m, const float* part_l, const fl
     return cuda_status(tq::launch_reduce(r, static_cast<cudaStream_t>(stream), false));
 }
 
+tq_status tq_dequantize_kv(const tq_kv_cache* cache, int32_t n_rows, uint16_t* k_out, uint16_t* v_out,
+                           void* stream) {
+    tq_status s = check_cache(cache);
+    if (s != TQ_OK) return s;
+    if (k_out == nullptr || v_out == nullptr) return TQ_ERR_NULL;
+    if (n_rows < 0) return TQ_ERR_SHAPE;
+    if (n_rows > cache->capacity) return TQ_ERR_CAPACITY;
+    if (!aligned16(k_out) || !aligned16(v_out)) return TQ_ERR_ALIGN;
+    if (n_rows == 0) return TQ_OK;
+    DeviceFacts* f = nullptr;
+    s = device_facts(&f);
+    if (s != TQ_OK) return s;
+    tq::DequantParams p;
+    p.k_codes = cache->k_codes;
+    p.v_codes = cache->v_codes;
+    p.k_scale = cache->k_scale;
+    p.k_bias = cache->k_bias;
+    p.v_scale = cache->v_scale;
+    p.v_bias = cache->v_bias;
+    p.k_out = k_out;
+    p.v_out = v_out;
+    p.batch = cache->batch;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.head_dim = cache->head_dim;
+    p.capacity = cache->capacity;
+    p.n_rows = n_rows;
+    return cuda_status(tq::launch_dequant(p, f->sms, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

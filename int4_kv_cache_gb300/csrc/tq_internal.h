@@ -62,6 +62,19 @@ struct DecodeParams {
 // run the append kernel first.
 constexpr int kFusedAppendMaxRows = 16;
 
+// Expansion of the cache into fp16 K/V [B][Hkv][n_rows][D] (comparison path).
+struct DequantParams {
+    const uint8_t* k_codes;
+    const uint8_t* v_codes;
+    const uint16_t* k_scale;
+    const uint16_t* k_bias;
+    const uint16_t* v_scale;
+    const uint16_t* v_bias;
+    uint16_t* k_out;
+    uint16_t* v_out;
+    int32_t batch, num_kv_heads, head_dim, capacity, n_rows;
+};
+
 struct ReduceParams {
     const float* part_m;
     const float* part_l;
@@ -80,6 +93,7 @@ cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, const CUtenso
 // decode kernel then waits only where it reads the appended rows).
 cudaError_t launch_quantize_append_primary(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl_secondary);
+cudaError_t launch_dequant(const DequantParams& p, int sm_count, cudaStream_t stream);
 
 // Tokens per pipeline stage of the tensor-core kernel (tiles are TMA boxes).
 int mma_tile_tokens(int head_dim);

@@ -165,3 +165,14 @@ def test_carve_layout(L):
     assert c.k_bias - c.k_scale == rows * 2 * 2
     assert (c.capacity, c.head_dim, c.num_kv_heads, c.batch) == (64, 128, 8, 2)
     assert L.tq_kv_cache_carve(ctypes.byref(c), 0x10010, 2, 8, 128, 64, 64) == 7
+
+
+def test_dequantize_argument_errors_launch_nothing(L):
+    c = _fake_cache()
+    f = L.tq_dequantize_kv
+    assert f(None, 16, 0x1000, 0x2000, None) == 1
+    assert f(ctypes.byref(c), 16, 0, 0x2000, None) == 1
+    assert f(ctypes.byref(c), -1, 0x1000, 0x2000, None) == 2
+    assert f(ctypes.byref(c), 257, 0x1000, 0x2000, None) == 3
+    assert f(ctypes.byref(c), 16, 0x1008, 0x2000, None) == 7
+    assert f(ctypes.byref(c), 0, 0x1000, 0x2000, None) == 0  # nothing to do
