@@ -4,14 +4,16 @@
 // Method: "turboquant-llama3.170B" README, decode-step listing (quantize K,V to
 // int4 after RoPE, then store) and the Gemma page, Background (MLX-style int4
 // with a per-group scale and bias).  The rounding rule is the one stated in
-// tq.h; every step is a single IEEE fp32 operation with round-to-nearest-even
-// (__fsub_rn / __fdiv_rn / __float2int_rn), so codes, scales and biases are
-// bit-identical to the CPU oracle.  The per-element division is replaced by a
-// multiply with the reciprocal wherever that provably rounds to the same code.
+// tq.h; every step is a single IEEE fp32 operation with round-to-nearest-even,
+// so codes, scales and biases are bit-identical to the CPU oracle.  The
+// per-element division is replaced by a multiply with the reciprocal wherever
+// that provably rounds to the same code (tq_quant.cuh).
 //
-// Work split: eight lanes own one group of 64 elements (16 bytes = 8 halves
-// each), which makes every global access a 16-byte (input) or 4-byte (codes)
-// coalesced transaction; min/max are reduced with three xor-shuffles.
+// Work split: one thread per (row, group of 64): it loads the group of K and
+// the group of V (eight 16-byte words each, all issued before any use), and
+// writes 32 bytes of codes per tensor and the four scale / bias halves.  With
+// no cross-lane reductions the per-group work (min/max, the scale division,
+// the reciprocal) is spread over 64 elements.
 #include "tq_device.cuh"
 #include "tq_internal.h"
 #include "tq_quant.cuh"
@@ -20,48 +22,67 @@ namespace tq {
 
 namespace {
 
-__global__ void __launch_bounds__(256) quantize_append_kernel(const AppendParams p) {
+constexpr int kQuantThreads = 128;
+
+__global__ void __launch_bounds__(kQuantThreads) quantize_append_kernel(const AppendParams p) {
+    // staging: per warp and tensor, 32 groups x 8 words of 16 bytes; word w of
+    // group r sits at slot w ^ (r & 7), so that the eight lanes of each phase of
+    // a 16-byte shared access hit eight different bank groups
+    __shared__ uint4 stage[kQuantThreads / 32][2][32][8];
     pdl_launch_dependents();  // no effect unless the next launch is a programmatic dependent
     const int ng = p.head_dim / kGroup;
     const long long n_groups = static_cast<long long>(p.batch) * p.num_kv_heads * p.n_new * ng;
-    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int part = static_cast<int>(tid & 7);
-    const long long gidx = tid >> 3;
-    const bool valid = gidx < n_groups;  // whole groups of 8 lanes agree
-    const long long gi = valid ? gidx : 0;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long long warp_base = static_cast<long long>(blockIdx.x) * kQuantThreads + warp * 32;
+    if (warp_base >= n_groups) return;  // the whole warp
+
+    // coalesced loads of the warp's 32 consecutive groups (4 KB per tensor:
+    // group gi starts at element gi * 64 of k_new / v_new)
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const uint4* src = reinterpret_cast<const uint4*>(t ? p.v_new : p.k_new) + warp_base * 8;
+        uint4 w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int r = 4 * j + (lane >> 3);  // group within the warp's 32
+            w[j] = warp_base + r < n_groups ? __ldcs(src + 32 * j + lane) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int r = 4 * j + (lane >> 3), word = lane & 7;
+            stage[warp][t][r][word ^ (r & 7)] = w[j];
+        }
+    }
+    __syncwarp();
+
+    const long long gi = warp_base + lane;
+    if (gi >= n_groups) return;
     const int g = static_cast<int>(gi % ng);
     const long long row = gi / ng;  // over [B][Hkv][n_new]
     const int i = static_cast<int>(row % p.n_new);
     const long long bh = row / p.n_new;  // b * Hkv + h
     const int b = static_cast<int>(bh / p.num_kv_heads);
-
-    const long long src = row * p.head_dim + g * kGroup + part * 8;  // in halves
-    uint4 kr = make_uint4(0, 0, 0, 0), vr = make_uint4(0, 0, 0, 0);
-    int wp = 0;
-    if (valid) {
-        kr = __ldcs(reinterpret_cast<const uint4*>(p.k_new + src));
-        vr = __ldcs(reinterpret_cast<const uint4*>(p.v_new + src));
-        wp = __ldg(p.write_pos + b);
-    }
-    const GroupQ kq = quantize_lane8(kr);  // every lane takes part in the shuffles
-    const GroupQ vq = quantize_lane8(vr);
-    if (!valid) return;
-
-    const bool pos_ok = wp >= 0 && static_cast<long long>(wp) + p.n_new <= p.capacity;
-    if (!pos_ok) {
-        if (p.status != nullptr && part == 0 && g == 0 && i == 0) atomicOr(p.status, TQ_DEV_WRITE_POS);
+    const int wp = __ldg(p.write_pos + b);
+    if (wp < 0 || static_cast<long long>(wp) + p.n_new > p.capacity) {
+        if (p.status != nullptr && g == 0 && i == 0) atomicOr(p.status, TQ_DEV_WRITE_POS);
         return;
     }
     const long long dst_row = bh * p.capacity + wp + i;
-    const long long code_off = dst_row * (p.head_dim / 2) + g * (kGroup / 2) + part * 4;
-    *reinterpret_cast<uint32_t*>(p.k_codes + code_off) = kq.codes;
-    *reinterpret_cast<uint32_t*>(p.v_codes + code_off) = vq.codes;
-    if (part == 0) {
-        const long long sb = dst_row * ng + g;
-        p.k_scale[sb] = __half_as_ushort(kq.scale);
-        p.k_bias[sb] = __half_as_ushort(kq.bias);
-        p.v_scale[sb] = __half_as_ushort(vq.scale);
-        p.v_bias[sb] = __half_as_ushort(vq.bias);
+    const long long code_off = dst_row * (p.head_dim / 2) + g * (kGroup / 2);  // 32-byte aligned
+    const long long sb = dst_row * ng + g;
+#pragma unroll 1
+    for (int t = 0; t < 2; ++t) {
+        uint4 x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = stage[warp][t][lane][j ^ (lane & 7)];
+        uint32_t c[8];
+        __half sc, bi;
+        quantize_group64(x, c, sc, bi);
+        uint4* dst = reinterpret_cast<uint4*>((t ? p.v_codes : p.k_codes) + code_off);
+        dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+        dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+        (t ? p.v_scale : p.k_scale)[sb] = __half_as_ushort(sc);
+        (t ? p.v_bias : p.k_bias)[sb] = __half_as_ushort(bi);
     }
 }
 
@@ -69,9 +90,8 @@ __global__ void __launch_bounds__(256) quantize_append_kernel(const AppendParams
 
 cudaError_t launch_quantize_append(const AppendParams& p, cudaStream_t stream) {
     const long long groups = static_cast<long long>(p.batch) * p.num_kv_heads * p.n_new * (p.head_dim / kGroup);
-    const long long threads = groups * 8;
-    const int block = 256;
-    const long long blocks = (threads + block - 1) / block;
+    const int block = kQuantThreads;
+    const long long blocks = (groups + block - 1) / block;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     quantize_append_kernel<<<static_cast<unsigned>(blocks), block, 0, stream>>>(p);
     return cudaGetLastError();

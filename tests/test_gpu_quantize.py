@@ -45,6 +45,8 @@ def test_quantize_edge_groups_bit_exact(D):
     flat[7] = np.round(flat[7] * 4) / 4                                 # repeated values
     flat[8, :] = 0.0
     flat[8, 5] = 2.0**-24                                               # scale rounds to zero
+    flat[9, :] = 0.0
+    flat[9, ::3] = 21 * 2.0**-24                  # scale 1.4 * 2^-24 rounds to 2^-24: codes up to 21, clamped
     kh, vh = k.astype(np.float16), v.astype(np.float16)
     _compare(gpu_cache_from_fp16(kh, vh), kh, vh)
 
