@@ -37,6 +37,9 @@ def lib() -> ctypes.CDLL:
         L.tqo_quantize_rows.argtypes = [P, i64, i32, i32, P, P, P]
         L.tqo_dequantize_rows.argtypes = [P, P, P, i64, i32, i32, P]
         L.tqo_dequantize_rows_f16.argtypes = [P, P, P, i64, i32, i32, P]
+        L.tqo_hadamard_f64.argtypes = [P, i32]
+        L.tqo_hadamard_f32.argtypes = [P, i32]
+        L.tqo_rotate_rows_f16.argtypes = [P, i64, i32, P]
         L.tqo_attention.argtypes = [P, i32, i32, i32, i32, i32, i64, P, P, P, P, P, P, P, f64,
                                     P, i64, P]
         L.tqo_attention_partials.argtypes = [P, i32, i32, i32, i32, i32, i64, P, P, P, P, P, P,
@@ -122,6 +125,30 @@ def dequantize_rows_f16(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray, 
     out = np.empty(codes.shape[:-1] + (D,), dtype=np.uint16)
     lib().tqo_dequantize_rows_f16(_ptr(codes), _ptr(scale), _ptr(bias), rows, D, group, _ptr(out))
     return out
+
+
+def hadamard(x: np.ndarray) -> np.ndarray:
+    """(1/sqrt(n)) H_n x along the last axis: float64 in, float64 out; float32 in,
+    the fp32 fast transform out."""
+    x = np.array(x, copy=True, order="C")
+    n = x.shape[-1]
+    fn = lib().tqo_hadamard_f32 if x.dtype == np.float32 else lib().tqo_hadamard_f64
+    if x.dtype not in (np.float32, np.float64):
+        x = x.astype(np.float64)
+        fn = lib().tqo_hadamard_f64
+    flat = x.reshape(-1, n)
+    for r in range(flat.shape[0]):
+        fn(flat[r].ctypes.data_as(ctypes.c_void_p), n)
+    return x
+
+
+def rotate_rows_f16(x: np.ndarray) -> np.ndarray:
+    """fp16 rows rotated by the fp32 transform, rounded to fp16 (same shape, float16)."""
+    xb = _bits16(np.asarray(x))
+    n = xb.shape[-1]
+    out = np.empty_like(xb)
+    lib().tqo_rotate_rows_f16(_ptr(xb), xb.size // n, n, _ptr(out))
+    return out.view(np.float16)
 
 
 class Cache:

@@ -174,6 +174,59 @@ void tqo_dequantize_rows_f16(const uint8_t* codes_packed, const uint16_t* scale,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Hadamard rotation ([TQ] "Running and Evaluating TurboQuant optimized       */
+/* Gemma 4": the key breakthrough paragraph and the worked example -- a       */
+/* normalised Sylvester Hadamard matrix H / sqrt(n) spreads an outlier over  */
+/* all coordinates before quantisation and, being its own inverse, brings    */
+/* the vector back).  y = (1/sqrt(n)) * H_n x with H_1 = [1], H_2m =          */
+/* [[H_m, H_m], [H_m, -H_m]], evaluated as the fast transform: for h = 1, 2,  */
+/* 4, ..., n/2, every pair (i, i + h) with bit h of i clear becomes           */
+/* (x_i + x_{i+h}, x_i - x_{i+h}); then every element is multiplied by        */
+/* 1/sqrt(n).  Readings: the fp32 variant performs exactly these operations  */
+/* in fp32 (the stage order fixes the rounding), with 1/sqrt(n) taken as the */
+/* fp32 value nearest to the fp64 1/sqrt(n); the rows variant converts fp16  */
+/* input to fp32 and rounds the result to fp16 (RNE).                        */
+/* ------------------------------------------------------------------------ */
+
+static int is_pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
+
+void tqo_hadamard_f64(double* x, int n) {
+    if (!is_pow2(n)) return;
+    for (int h = 1; h < n; h <<= 1)
+        for (int i = 0; i < n; ++i)
+            if ((i & h) == 0) {
+                double u = x[i], v = x[i + h];
+                x[i] = u + v;
+                x[i + h] = u - v;
+            }
+    double c = 1.0 / sqrt((double)n);
+    for (int i = 0; i < n; ++i) x[i] *= c;
+}
+
+void tqo_hadamard_f32(float* x, int n) {
+    if (!is_pow2(n)) return;
+    for (int h = 1; h < n; h <<= 1)
+        for (int i = 0; i < n; ++i)
+            if ((i & h) == 0) {
+                float u = x[i], v = x[i + h];
+                x[i] = u + v;
+                x[i + h] = u - v;
+            }
+    float c = (float)(1.0 / sqrt((double)n));
+    for (int i = 0; i < n; ++i) x[i] *= c;
+}
+
+void tqo_rotate_rows_f16(const uint16_t* x, int64_t rows, int n, uint16_t* out) {
+    float buf[1024];
+    if (!is_pow2(n) || n > 1024) return;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int i = 0; i < n; ++i) buf[i] = (float)tqo_f16_to_f64(x[r * n + i]);
+        tqo_hadamard_f32(buf, n);
+        for (int i = 0; i < n; ++i) out[r * n + i] = tqo_f32_to_f16(buf[i]);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Decode attention ([L70] kernel paragraph: scores from the int4 data,       */
 /* softmax, weighted sum of values; GQA with Hq/Hkv query heads per KV head). */
 /* The oracle simply dequantises and runs ordinary attention in fp64.         */

@@ -74,6 +74,15 @@ void tqo_dequantize_rows_f16(const uint8_t* codes_packed, const uint16_t* scale,
                              const uint16_t* bias, int64_t rows, int D, int group,
                              uint16_t* out);
 
+/* Normalised Sylvester Hadamard transform in place, n a power of two:
+ * x <- (1/sqrt(n)) H_n x by the fast transform (stages h = 1, 2, ..., n/2).
+ * The f64 form is the reference; the f32 form performs the same operations in
+ * fp32 (the rotation applied to K and Q before quantisation / attention). */
+void tqo_hadamard_f64(double* x, int n);
+void tqo_hadamard_f32(float* x, int n);
+/* Rotate fp16 rows: out = fp16_rne(fp32 transform of the fp16 row), n <= 1024. */
+void tqo_rotate_rows_f16(const uint16_t* x, int64_t rows, int n, uint16_t* out);
+
 /* Single-token decode attention over a quantised cache.
  * q:    [B][Hq][D] fp16 bits
  * kc,vc:[B][Hkv][cap][D/2] packed codes; ks,kb,vs,vb: [B][Hkv][cap][D/group]

@@ -376,3 +376,66 @@ def test_partial_state_definition():
         np.testing.assert_allclose(l[0, h, 0], np.exp(s - s.max()).sum(), rtol=1e-13)
         np.testing.assert_allclose(acc[0, h, 0], np.exp(s - s.max()) @ vh[0, h // 4], rtol=1e-12,
                                    atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# Hadamard rotation ("Running and Evaluating TurboQuant optimized Gemma 4")
+# --------------------------------------------------------------------------
+
+def _hadamard_fixture():
+    rows = {l.split()[0]: np.array([float(v) for v in l.split()[1:]])
+            for l in open(os.path.join(GOLDEN, "hadamard_worked_example.txt")) if l.strip() and not l.startswith("#")}
+    return rows["input"], rows["rotated"]
+
+
+def test_hadamard_worked_example():
+    x, want = _hadamard_fixture()
+    for dt in (np.float64, np.float32):
+        y = oracle.hadamard(x.astype(dt))
+        assert np.allclose(y, want, atol=5e-4, rtol=0)           # the page prints three decimals
+        assert np.allclose(oracle.hadamard(y), x, atol=1e-6, rtol=0)  # its own inverse
+    assert np.allclose(oracle.hadamard(x), want, atol=1e-15, rtol=0)  # the printed values are exact here
+
+
+def test_hadamard_matches_sylvester_matrix():
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    rng = np.random.default_rng(21)
+    for n in (2, 4, 64, 128, 256):
+        H = scipy_linalg.hadamard(n) / math.sqrt(n)
+        x = rng.standard_normal((5, n))
+        x[:, 3 % n] *= 20.0                                          # an outlier channel
+        ref = x @ H.T
+        assert np.allclose(oracle.hadamard(x), ref, atol=1e-12, rtol=0)
+        # fp32 fast transform: log2(n) rounded adds and one rounded scale
+        y32 = oracle.hadamard(x.astype(np.float32)).astype(np.float64)
+        ref32 = x.astype(np.float32).astype(np.float64) @ H.T
+        bound = (math.log2(n) + 2) * 2.0**-24 * np.abs(x).sum(axis=1, keepdims=True)
+        assert np.all(np.abs(y32 - ref32) <= bound)
+
+
+def test_hadamard_norm_inverse_and_spreading():
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((20, 128))
+    y = oracle.hadamard(x)
+    assert np.allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-13)
+    assert np.allclose(oracle.hadamard(y), x, atol=1e-13)
+    q = rng.standard_normal(128)
+    assert np.allclose(oracle.hadamard(q) @ y.T, q @ x.T, atol=1e-11)  # dot products kept
+    spike = np.zeros(128)
+    spike[17] = 1.0
+    assert np.allclose(np.abs(oracle.hadamard(spike)), 1 / math.sqrt(128), atol=1e-15)  # an outlier spread evenly
+
+
+def test_rotate_rows_f16_is_rounded_fp32_transform():
+    rng = np.random.default_rng(23)
+    x = (rng.standard_normal((50, 128)) * 3).astype(np.float16)
+    got = oracle.rotate_rows_f16(x).astype(np.float64)
+    exact = oracle.hadamard(x.astype(np.float64))
+    # fp32 transform error (bound above) plus one fp16 rounding
+    bound = 0.5 * _ulp16(np.maximum(np.abs(got), np.abs(exact))) + 9 * 2.0**-24 * np.abs(x.astype(np.float64)).sum(
+        axis=1, keepdims=True)
+    assert np.all(np.abs(got - exact) <= bound)
+    # exactly representable results come back exactly: +-1 entries of a scaled Hadamard column
+    e = np.zeros((1, 64), np.float16)
+    e[0, 5] = 8.0                                                    # 8 / sqrt(64) = 1
+    assert np.array_equal(np.abs(oracle.rotate_rows_f16(e).astype(np.float64)), np.ones((1, 64)))
