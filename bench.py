@@ -421,7 +421,34 @@ def run_extras(args, tq, synth, torch, dev, caches, qs, ws, out, peak):
             res["sweep_decode_only"][f"{n // 1024}k_{tag}"] = {"us": round(us, 3), "GB_per_s": round(gbs, 1),
                                                                "frac": round(gbs / peak, 4)}
     res["dequant_sdpa_baseline_128k"] = run_dequant_baseline(args, tq, torch, dev, caches, qs, peak)
+    res["hadamard_rotated_128k"] = run_rotation(args, tq, synth, torch, dev, caches, qs, ws, out, peak)
     return res
+
+
+def run_rotation(args, tq, synth, torch, dev, caches, qs, ws, out, peak):
+    """Hadamard-rotated int4 at the same shape: the decode step with K and V
+    rotated (query rotated before phase 1, output rotated back in the reduce;
+    the rotated one-row append runs the append kernel) and the 128K prefill
+    quantize with the rotation fused in."""
+    nl = len(caches)
+    flags = tq.TQ_ROTATE_K | tq.TQ_ROTATE_V
+    k_new = torch.randn((B, HKV, 1, D), device=dev).half()
+    v_new = torch.randn((B, HKV, 1, D), device=dev).half()
+    write_pos = torch.full((B,), S - 1, dtype=torch.int32, device=dev)
+    seq_lens = torch.full((B,), S, dtype=torch.int32, device=dev)
+    step_us = time_graph(torch, lambda i: tq.tq_decode_step(caches[i % nl], k_new, v_new, write_pos, qs[i % nl],
+                                                            seq_lens, S, ATTN, ws, out=out, chunk=CHUNK,
+                                                            flags=flags), max(20, args.steps))
+    _, k, v, _ = synth.torch_decode_inputs(SEED + 77, B, HQ, HKV, D, S, outliers=True, device=dev)
+    zero = torch.zeros((B,), dtype=torch.int32, device=dev)
+    pre_us = time_graph(torch, lambda i: tq.tq_quantize_kv_append(caches[i % nl], k, v, zero, flags=flags), 4)
+    del k, v
+    rd = B * HKV * S * D * 2 * 2
+    pre_gbs = (rd + cache_bytes(S)) / (pre_us * 1e-6) / 1e9
+    return {"decode_step_us": round(step_us, 3),
+            "decode_step_GB_per_s": round(step_bytes(S) / (step_us * 1e-6) / 1e9, 1),
+            "prefill_quantize_ms_per_layer": round(pre_us / 1e3, 4), "prefill_GB_per_s": round(pre_gbs, 1),
+            "prefill_frac": round(pre_gbs / peak, 4), "flags": "TQ_ROTATE_K | TQ_ROTATE_V"}
 
 
 def run_dequant_baseline(args, tq, torch, dev, caches, qs, peak):

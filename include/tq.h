@@ -75,6 +75,18 @@ typedef enum tq_status {
 #define TQ_DEV_SEQ_LEN 0x2   /* decode: seq_lens[b] < 0 or > max_seq_len; clamped into range */
 #define TQ_DEV_TIMEOUT 0x4   /* a pipeline wait exceeded its time limit; the CTA gave up */
 
+/* Rotation flags ("Running and Evaluating TurboQuant optimized Gemma 4",
+ * TurboQuant section: vectors are rotated by the normalised Sylvester Hadamard
+ * matrix H = H_n / sqrt(n) before quantisation, which spreads outliers over
+ * all coordinates; H is its own inverse).  In this library H is applied by an
+ * fp32 fast transform (stages h = 1, 2, ..., n/2) and rounded to fp16.
+ *   TQ_ROTATE_K  keys are stored as quantize(H k); decode then uses H q, and
+ *                (H q).(H k) = q.k leaves the scores unchanged.
+ *   TQ_ROTATE_V  values are stored as quantize(H v); decode returns H o of the
+ *                attention output o over them, which is the output over v. */
+#define TQ_ROTATE_K 0x1u
+#define TQ_ROTATE_V 0x2u
+
 /* Decode implementations (tq_sdpa_int4_decode_impl and friends). */
 typedef enum tq_impl {
     TQ_IMPL_AUTO = 0, /* the tensor-core path */
@@ -133,6 +145,22 @@ tq_status tq_quantize_kv_append(const tq_kv_cache* cache, const uint16_t* k_new,
                                 const int32_t* write_pos, int32_t* status,
                                 void* stream);
 
+/* tq_quantize_kv_append with rotation: flags TQ_ROTATE_K / TQ_ROTATE_V rotate
+ * each new K / V row by H (see the rotation flags above) before it is
+ * quantized; the rotation is fused into the same kernel (no extra pass over
+ * the rows).  Rotated rows are fp16_rne(fp32 transform), then quantized by the
+ * rule above.  Other flag bits: TQ_ERR_UNSUPPORTED. */
+tq_status tq_quantize_kv_append_ex(const tq_kv_cache* cache, const uint16_t* k_new,
+                                   const uint16_t* v_new, int32_t n_new,
+                                   const int32_t* write_pos, uint32_t flags,
+                                   int32_t* status, void* stream);
+
+/* out[r] = fp16_rne(H x[r]) for `rows` rows of `dim` fp16 values (dim 64, 128
+ * or 256; device pointers, 16-byte aligned; out may equal x).  H as for the
+ * rotation flags.  rows = 0 launches nothing. */
+tq_status tq_hadamard_rotate(const uint16_t* x, int64_t rows, int32_t dim,
+                             uint16_t* out, void* stream);
+
 /* Workspace bytes tq_sdpa_int4_decode needs for these sizes (an upper bound
  * that does not depend on the device).  Host-only. */
 size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t num_q_heads,
@@ -154,7 +182,8 @@ size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t num_q_heads,
  *           result is the same as merging one state per chunk (see
  *           tq_sdpa_int4_partial with chunks_per_split = 1).
  * workspace: device scratch (256-byte aligned) of at least
- *           tq_sdpa_workspace_bytes(...) bytes holding the fp32 partial states;
+ *           tq_sdpa_workspace_bytes(...) bytes holding the fp32 partial states
+ *           (and the rotated query of tq_sdpa_int4_decode_ex / tq_decode_step_ex);
  *           contents on entry are ignored.
  * out:      fp16 [batch][num_q_heads][head_dim], round-to-nearest-even.
  * Accumulation is fp32; result within 2e-3 abs / 1e-3 rel-L2 of fp64 attention
@@ -189,6 +218,24 @@ tq_status tq_decode_step(const tq_kv_cache* cache, const uint16_t* k_new,
                          int32_t max_seq_len, float attn_scale, int32_t chunk,
                          void* workspace, size_t workspace_bytes,
                          uint16_t* out, int32_t* status, void* stream);
+
+/* Decode over a cache written with rotation flags (the same flags as its
+ * appends): TQ_ROTATE_K rotates the query (into the workspace) before phase
+ * 1; TQ_ROTATE_V applies H to the merged output before its fp16 rounding.
+ * Otherwise as tq_sdpa_int4_decode / tq_decode_step (a rotated append always
+ * runs the append kernel, with the decode as its programmatic dependent). */
+tq_status tq_sdpa_int4_decode_ex(const tq_kv_cache* cache, const uint16_t* q,
+                                 int32_t num_q_heads, const int32_t* seq_lens,
+                                 int32_t max_seq_len, float attn_scale, int32_t chunk,
+                                 uint32_t flags, void* workspace, size_t workspace_bytes,
+                                 uint16_t* out, int32_t* status, void* stream);
+tq_status tq_decode_step_ex(const tq_kv_cache* cache, const uint16_t* k_new,
+                            const uint16_t* v_new, int32_t n_new,
+                            const int32_t* write_pos, const uint16_t* q,
+                            int32_t num_q_heads, const int32_t* seq_lens,
+                            int32_t max_seq_len, float attn_scale, int32_t chunk,
+                            uint32_t flags, void* workspace, size_t workspace_bytes,
+                            uint16_t* out, int32_t* status, void* stream);
 
 /* The split plan tq_sdpa_int4_decode uses on the current device: *n_splits
  * runs per (sequence, kv head), the longest *max_run_tokens tokens long.

@@ -20,12 +20,13 @@ __all__ = [
     "tq_abi_version", "tq_status_string", "tq_kv_cache_bytes", "tq_sdpa_workspace_bytes",
     "tq_quantize_kv_append", "tq_sdpa_int4_decode", "tq_sdpa_int4_partial", "tq_sdpa_int4_reduce",
     "tq_sdpa_plan", "tq_sdpa_int4_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "tq_decode_step",
-    "tq_dequantize_kv",
+    "tq_dequantize_kv", "tq_hadamard_rotate", "TQ_ROTATE_K", "TQ_ROTATE_V",
 ]
 
 TQ_OK = 0
 TQ_IMPL_AUTO, TQ_IMPL_MMA, TQ_IMPL_SIMT = 0, 1, 2
 TQ_DEV_WRITE_POS, TQ_DEV_SEQ_LEN, TQ_DEV_TIMEOUT = 0x1, 0x2, 0x4
+TQ_ROTATE_K, TQ_ROTATE_V = 0x1, 0x2
 GROUP_SIZE = 64
 DEFAULT_CHUNK = 512
 NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -68,7 +69,7 @@ def lib() -> ctypes.CDLL:
         if not os.path.exists(path):
             raise ImportError(f"libtq.so not built ({path}); run int4_kv_cache_gb300.build.build()")
         L = ctypes.CDLL(path)
-        P, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+        P, i32, sz, f32, u32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float, ctypes.c_uint32
         C = ctypes.POINTER(tq_kv_cache)
         sig = {
             "tq_abi_version": ([], i32),
@@ -86,6 +87,10 @@ def lib() -> ctypes.CDLL:
             "tq_sdpa_int4_decode_noalloc": ([C, P, i32, P, i32, f32, i32, P, P, P], i32),
             "tq_decode_step": ([C, P, P, i32, P, P, i32, P, i32, f32, i32, P, sz, P, P, P], i32),
             "tq_dequantize_kv": ([C, i32, P, P, P], i32),
+            "tq_quantize_kv_append_ex": ([C, P, P, i32, P, u32, P, P], i32),
+            "tq_hadamard_rotate": ([P, ctypes.c_int64, i32, P, P], i32),
+            "tq_sdpa_int4_decode_ex": ([C, P, i32, P, i32, f32, i32, u32, P, sz, P, P, P], i32),
+            "tq_decode_step_ex": ([C, P, P, i32, P, P, i32, P, i32, f32, i32, u32, P, sz, P, P, P], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -184,8 +189,9 @@ class KVCache:
 
 # ------------------------------------------------------------------ device ops
 def tq_quantize_kv_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, write_pos: torch.Tensor,
-                          status: Optional[torch.Tensor] = None, stream=None) -> None:
-    """Quantize k_new/v_new [B, Hkv, n_new, D] fp16 into cache rows write_pos[b] + i."""
+                          status: Optional[torch.Tensor] = None, stream=None, flags: int = 0) -> None:
+    """Quantize k_new/v_new [B, Hkv, n_new, D] fp16 into cache rows write_pos[b] + i
+    (flags TQ_ROTATE_K / TQ_ROTATE_V: Hadamard-rotate the rows first)."""
     _need(k_new, torch.float16, "k_new")
     _need(v_new, torch.float16, "v_new")
     _need(write_pos, torch.int32, "write_pos")
@@ -194,6 +200,10 @@ def tq_quantize_kv_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tens
     n_new = k_new.shape[2] if k_new.dim() == 4 else 0
     if tuple(k_new.shape) != (cache.batch, cache.num_kv_heads, n_new, cache.head_dim) or v_new.shape != k_new.shape:
         raise ValueError(f"k_new/v_new must be [B, Hkv, n_new, D]; got {tuple(k_new.shape)}")
+    if flags:
+        _check("tq_quantize_kv_append_ex", lib().tq_quantize_kv_append_ex(
+            cache.ref(), _ptr(k_new), _ptr(v_new), n_new, _ptr(write_pos), int(flags), _ptr(status), _stream(stream)))
+        return
     _check("tq_quantize_kv_append", lib().tq_quantize_kv_append(cache.ref(), _ptr(k_new), _ptr(v_new), n_new,
                                                                 _ptr(write_pos), _ptr(status), _stream(stream)))
 
@@ -201,8 +211,9 @@ def tq_quantize_kv_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tens
 def tq_sdpa_int4_decode(cache: KVCache, q: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
                         attn_scale: float, workspace: torch.Tensor, out: Optional[torch.Tensor] = None,
                         chunk: int = DEFAULT_CHUNK, status: Optional[torch.Tensor] = None,
-                        impl: int = TQ_IMPL_AUTO, stream=None) -> torch.Tensor:
-    """Fused int4 decode attention; q [B, Hq, D] fp16 -> out [B, Hq, D] fp16."""
+                        impl: int = TQ_IMPL_AUTO, stream=None, flags: int = 0) -> torch.Tensor:
+    """Fused int4 decode attention; q [B, Hq, D] fp16 -> out [B, Hq, D] fp16
+    (flags: the rotation flags the cache was written with)."""
     _need(q, torch.float16, "q")
     _need(seq_lens, torch.int32, "seq_lens")
     _need(workspace, torch.uint8, "workspace")
@@ -213,6 +224,13 @@ def tq_sdpa_int4_decode(cache: KVCache, q: torch.Tensor, seq_lens: torch.Tensor,
         _need(status, torch.int32, "status")
     if q.dim() != 3 or q.shape[0] != cache.batch or q.shape[2] != cache.head_dim or out.shape != q.shape:
         raise ValueError(f"q must be [B, Hq, D]; got {tuple(q.shape)}")
+    if flags:
+        if impl != TQ_IMPL_AUTO:
+            raise ValueError("rotation flags take the default implementation")
+        _check("tq_sdpa_int4_decode_ex", lib().tq_sdpa_int4_decode_ex(
+            cache.ref(), _ptr(q), q.shape[1], _ptr(seq_lens), int(max_seq_len), float(attn_scale), int(chunk),
+            int(flags), _ptr(workspace), workspace.numel(), _ptr(out), _ptr(status), _stream(stream)))
+        return out
     _check("tq_sdpa_int4_decode", lib().tq_sdpa_int4_decode_impl(
         cache.ref(), _ptr(q), q.shape[1], _ptr(seq_lens), int(max_seq_len), float(attn_scale), int(chunk),
         _ptr(workspace), workspace.numel(), _ptr(out), _ptr(status), int(impl), _stream(stream)))
@@ -222,9 +240,9 @@ def tq_sdpa_int4_decode(cache: KVCache, q: torch.Tensor, seq_lens: torch.Tensor,
 def tq_decode_step(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, write_pos: torch.Tensor,
                    q: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int, attn_scale: float,
                    workspace: torch.Tensor, out: Optional[torch.Tensor] = None, chunk: int = DEFAULT_CHUNK,
-                   status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                   status: Optional[torch.Tensor] = None, stream=None, flags: int = 0) -> torch.Tensor:
     """Append k_new/v_new [B, Hkv, n_new, D] at write_pos, then decode q [B, Hq, D]
-    over seq_lens (which must already count the new tokens)."""
+    over seq_lens (which must already count the new tokens); flags: rotation."""
     for t, n, dt in ((k_new, "k_new", torch.float16), (v_new, "v_new", torch.float16), (q, "q", torch.float16),
                      (write_pos, "write_pos", torch.int32), (seq_lens, "seq_lens", torch.int32),
                      (workspace, "workspace", torch.uint8)):
@@ -239,6 +257,12 @@ def tq_decode_step(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, wri
         raise ValueError(f"k_new/v_new must be [B, Hkv, n_new, D]; got {tuple(k_new.shape)}")
     if q.dim() != 3 or q.shape[0] != cache.batch or q.shape[2] != cache.head_dim or out.shape != q.shape:
         raise ValueError(f"q must be [B, Hq, D]; got {tuple(q.shape)}")
+    if flags:
+        _check("tq_decode_step_ex", lib().tq_decode_step_ex(
+            cache.ref(), _ptr(k_new), _ptr(v_new), n_new, _ptr(write_pos), _ptr(q), q.shape[1], _ptr(seq_lens),
+            int(max_seq_len), float(attn_scale), int(chunk), int(flags), _ptr(workspace), workspace.numel(),
+            _ptr(out), _ptr(status), _stream(stream)))
+        return out
     _check("tq_decode_step", lib().tq_decode_step(
         cache.ref(), _ptr(k_new), _ptr(v_new), n_new, _ptr(write_pos), _ptr(q), q.shape[1], _ptr(seq_lens),
         int(max_seq_len), float(attn_scale), int(chunk), _ptr(workspace), workspace.numel(), _ptr(out),
@@ -334,3 +358,18 @@ def tq_dequantize_kv(cache: KVCache, n_rows: int, out=None, stream=None):
             raise ValueError(f"{n} must be {shape}; got {tuple(t.shape)}")
     _check("tq_dequantize_kv", lib().tq_dequantize_kv(cache.ref(), int(n_rows), _ptr(k), _ptr(v), _stream(stream)))
     return k, v
+
+
+def tq_hadamard_rotate(x: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """fp16 rows [..., D] (D = 64, 128, 256) -> fp16_rne(H x) per row, H the
+    normalised Sylvester Hadamard matrix (out may be x)."""
+    _need(x, torch.float16, "x")
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, torch.float16, "out")
+    if out.shape != x.shape:
+        raise ValueError("out must have the shape of x")
+    dim = x.shape[-1]
+    _check("tq_hadamard_rotate", lib().tq_hadamard_rotate(_ptr(x), x.numel() // dim, dim, _ptr(out),
+                                                          _stream(stream)))
+    return out

@@ -15,6 +15,7 @@
 // no cross-lane reductions the per-group work (min/max, the scale division,
 // the reciprocal) is spread over 64 elements.
 #include "tq_device.cuh"
+#include "tq_hadamard.cuh"
 #include "tq_internal.h"
 #include "tq_quant.cuh"
 
@@ -23,6 +24,21 @@ namespace tq {
 namespace {
 
 constexpr int kQuantThreads = 128;
+
+// Rotate the rows held in one warp's staging tile in place (32 groups = 32 /
+// ng whole rows): lane l takes elements E*l .. E*l+E-1 of each row in turn.
+template <int E>
+__device__ __forceinline__ void rotate_staged(uint4 (&tile)[32][8], int lane, int ng, float scale) {
+    const int d = E * lane;
+    for (int rr = 0; rr < 32 / ng; ++rr) {
+        const int r = rr * ng + d / kGroup, w = (d % kGroup) / 8;
+        uint16_t* ptr = reinterpret_cast<uint16_t*>(&tile[r][w ^ (r & 7)]) + (d % 8);
+        float v[E];
+        halves_to_floats<E>(ptr, v);
+        hadamard_warp<E>(v, lane, scale);
+        floats_to_halves<E>(v, ptr);
+    }
+}
 
 __global__ void __launch_bounds__(kQuantThreads) quantize_append_kernel(const AppendParams p) {
     // staging: per warp and tensor, 32 groups x 8 words of 16 bytes; word w of
@@ -54,6 +70,18 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_append_kernel(const Ap
         }
     }
     __syncwarp();
+    if (p.flags & (TQ_ROTATE_K | TQ_ROTATE_V)) {  // the same for the whole launch
+#pragma unroll 1
+        for (int t = 0; t < 2; ++t) {
+            if (!(p.flags & (t ? TQ_ROTATE_V : TQ_ROTATE_K))) continue;
+            switch (p.head_dim) {
+                case 64: rotate_staged<2>(stage[warp][t], lane, ng, p.rot_scale); break;
+                case 128: rotate_staged<4>(stage[warp][t], lane, ng, p.rot_scale); break;
+                default: rotate_staged<8>(stage[warp][t], lane, ng, p.rot_scale); break;
+            }
+        }
+        __syncwarp();
+    }
 
     const long long gi = warp_base + lane;
     if (gi >= n_groups) return;

@@ -10,6 +10,7 @@
 #include <math.h>
 
 #include "tq_device.cuh"
+#include "tq_hadamard.cuh"
 #include "tq_internal.h"
 
 namespace tq {
@@ -111,11 +112,29 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReducePara
 #pragma unroll
     for (int i = 0; i < V; ++i) part_sum[warp][lane * V + i] = a[i];
     __syncthreads();
-    for (int d = threadIdx.x; d < D; d += kReduceThreads) {
-        float t = 0.0f;
+    if (!p.rotate_out) {
+        for (int d = threadIdx.x; d < D; d += kReduceThreads) {
+            float t = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kReduceWarps; ++w) t += part_sum[w][d];
-        p.out[bh * D + d] = __half_as_ushort(__float2half_rn(L > 0.0f ? __fdiv_rn(t, L) : 0.0f));
+            for (int w = 0; w < kReduceWarps; ++w) t += part_sum[w][d];
+            p.out[bh * D + d] = __half_as_ushort(__float2half_rn(L > 0.0f ? __fdiv_rn(t, L) : 0.0f));
+        }
+        return;
+    }
+    // values were stored rotated: the output is H applied to the merged fp32
+    // output (warp 0, V consecutive elements per lane), rounded once to fp16
+    if (warp == 0) {
+        float o[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            float t = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kReduceWarps; ++w) t += part_sum[w][lane * V + i];
+            o[i] = L > 0.0f ? __fdiv_rn(t, L) : 0.0f;
+        }
+        hadamard_warp<V>(o, lane, p.rot_scale);
+#pragma unroll
+        for (int i = 0; i < V; ++i) p.out[bh * D + lane * V + i] = __half_as_ushort(__float2half_rn(o[i]));
     }
 }
 

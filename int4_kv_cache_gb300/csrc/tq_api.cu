@@ -182,7 +182,7 @@ tq_status run_phase1(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, co
                      int32_t* status, tq_impl impl, cudaStream_t stream, const int32_t* dep_write_pos = nullptr,
                      int32_t dep_n_new = 0, const tq::AppendParams* fused_append = nullptr) {
     if (pl.n_splits > 65535 || cache->num_kv_heads > 65535 || cache->batch > 65535) return TQ_ERR_SHAPE;
-    tq::DecodeParams p;
+    tq::DecodeParams p{};
     p.q = q;
     p.seq_lens = seq_lens;
     p.k_scale = cache->k_scale;
@@ -248,7 +248,7 @@ tq_status decode_into_partials(const tq_kv_cache* cache, const uint16_t* q, int3
     float* pa = reinterpret_cast<float*>(partials + 2 * align256(parts * sizeof(float)));
     s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, TQ_IMPL_MMA, stream);
     if (s != TQ_OK) return s;
-    ReduceParams r;
+    ReduceParams r{};
     r.part_m = pm;
     r.part_l = plv;
     r.part_acc = pa;
@@ -333,8 +333,10 @@ tq_status check_append_args(const tq_kv_cache* cache, const uint16_t* k_new, con
 }
 
 tq::AppendParams append_params(const tq_kv_cache* cache, const uint16_t* k_new, const uint16_t* v_new,
-                               int32_t n_new, const int32_t* write_pos, int32_t* status) {
-    tq::AppendParams p;
+                               int32_t n_new, const int32_t* write_pos, int32_t* status, uint32_t flags = 0) {
+    tq::AppendParams p{};
+    p.flags = flags;
+    p.rot_scale = tq::rotation_scale(cache->head_dim);
     p.k_new = k_new;
     p.v_new = v_new;
     p.write_pos = write_pos;
@@ -351,6 +353,74 @@ tq::AppendParams append_params(const tq_kv_cache* cache, const uint16_t* k_new, 
     p.n_new = n_new;
     p.capacity = cache->capacity;
     return p;
+}
+
+bool valid_rotation(uint32_t flags) { return (flags & ~(TQ_ROTATE_K | TQ_ROTATE_V)) == 0; }
+
+// Decode (optionally preceded by an append of n_new rows) with the workspace
+// laid out as [m][l][acc][rotated q]; the one path behind tq_decode_step*,
+// tq_sdpa_int4_decode*.
+tq_status decode_path(const tq_kv_cache* cache, const uint16_t* k_new, const uint16_t* v_new, int32_t n_new,
+                      const int32_t* write_pos, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
+                      int32_t max_seq_len, float attn_scale, int32_t chunk, uint32_t flags, void* workspace,
+                      size_t workspace_bytes, uint16_t* out, int32_t* status, tq_impl impl, cudaStream_t st) {
+    tq_status s = check_decode_args(cache, q, hq, seq_lens, max_seq_len, chunk, out);
+    if (s != TQ_OK) return s;
+    if (n_new != 0) {
+        s = check_append_args(cache, k_new, v_new, n_new, write_pos);
+        if (s != TQ_OK) return s;
+    }
+    if (!valid_impl(impl) || !valid_rotation(flags)) return TQ_ERR_UNSUPPORTED;
+    const size_t need =
+        tq_sdpa_workspace_bytes(cache->batch, hq, cache->num_kv_heads, cache->head_dim, max_seq_len, chunk);
+    if (workspace == nullptr || workspace_bytes < need) return TQ_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TQ_ERR_ALIGN;
+    Plan pl;
+    s = device_plan(cache, max_seq_len, chunk, impl, &pl);
+    if (s != TQ_OK) return s;
+    if (pl.n_splits > tq::kMaxReduceParts) return TQ_ERR_SHAPE;
+    const size_t parts = static_cast<size_t>(cache->batch) * hq * pl.n_splits;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* pm = reinterpret_cast<float*>(ws);
+    float* plv = reinterpret_cast<float*>(ws + align256(parts * sizeof(float)));
+    float* pa = reinterpret_cast<float*>(ws + 2 * align256(parts * sizeof(float)));
+    uint16_t* q_rot = reinterpret_cast<uint16_t*>(ws + 2 * align256(parts * sizeof(float)) +
+                                                  align256(parts * cache->head_dim * sizeof(float)));
+    const float rs = tq::rotation_scale(cache->head_dim);
+    // keys stored rotated: attend with the rotated query, (H q).(H k) = q.k
+    if (flags & TQ_ROTATE_K) {
+        s = cuda_status(tq::launch_rotate_rows(q, static_cast<long long>(cache->batch) * hq, cache->head_dim, q_rot,
+                                               rs, st));
+        if (s != TQ_OK) return s;
+        q = q_rot;
+    }
+    // A few new rows per sequence are quantized by the decode kernel itself
+    // (the CTA that reads them writes them first); longer or rotated appends
+    // run the append kernel, and the decode starts early and waits only for
+    // the tiles that hold the new rows.
+    const tq::AppendParams ap = append_params(cache, k_new, v_new, n_new, write_pos, status, flags);
+    const bool fused = n_new > 0 && n_new <= tq::kFusedAppendMaxRows && flags == 0 && impl != TQ_IMPL_SIMT;
+    if (n_new > 0 && !fused) {
+        s = cuda_status(tq::launch_quantize_append_primary(ap, st));
+        if (s != TQ_OK) return s;
+    }
+    const tq_impl ph1 = impl == TQ_IMPL_SIMT ? TQ_IMPL_SIMT : TQ_IMPL_MMA;
+    const bool dep = n_new > 0 && !fused && ph1 == TQ_IMPL_MMA;
+    s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, ph1, st,
+                   dep ? write_pos : nullptr, dep ? n_new : 0, fused ? &ap : nullptr);
+    if (s != TQ_OK) return s;
+    tq::ReduceParams r{};
+    r.part_m = pm;
+    r.part_l = plv;
+    r.part_acc = pa;
+    r.out = out;
+    r.batch = cache->batch;
+    r.num_q_heads = hq;
+    r.head_dim = cache->head_dim;
+    r.n_parts = pl.n_splits;
+    r.rotate_out = (flags & TQ_ROTATE_V) ? 1 : 0;
+    r.rot_scale = rs;
+    return cuda_status(tq::launch_reduce(r, st, true));
 }
 
 }  // namespace
@@ -370,47 +440,38 @@ tq_status tq_decode_step(const tq_kv_cache* cache, const uint16_t* k_new, const 
                          const int32_t* write_pos, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
                          int32_t max_seq_len, float attn_scale, int32_t chunk, void* workspace,
                          size_t workspace_bytes, uint16_t* out, int32_t* status, void* stream) {
+    return tq_decode_step_ex(cache, k_new, v_new, n_new, write_pos, q, hq, seq_lens, max_seq_len, attn_scale, chunk,
+                             0u, workspace, workspace_bytes, out, status, stream);
+}
+
+tq_status tq_decode_step_ex(const tq_kv_cache* cache, const uint16_t* k_new, const uint16_t* v_new, int32_t n_new,
+                            const int32_t* write_pos, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
+                            int32_t max_seq_len, float attn_scale, int32_t chunk, uint32_t flags, void* workspace,
+                            size_t workspace_bytes, uint16_t* out, int32_t* status, void* stream) {
     tq_status s = check_append_args(cache, k_new, v_new, n_new, write_pos);
     if (s != TQ_OK) return s;
-    s = check_decode_args(cache, q, hq, seq_lens, max_seq_len, chunk, out);
+    return decode_path(cache, k_new, v_new, n_new, write_pos, q, hq, seq_lens, max_seq_len, attn_scale, chunk, flags,
+                       workspace, workspace_bytes, out, status, TQ_IMPL_MMA, static_cast<cudaStream_t>(stream));
+}
+
+tq_status tq_quantize_kv_append_ex(const tq_kv_cache* cache, const uint16_t* k_new, const uint16_t* v_new,
+                                   int32_t n_new, const int32_t* write_pos, uint32_t flags, int32_t* status,
+                                   void* stream) {
+    tq_status s = check_append_args(cache, k_new, v_new, n_new, write_pos);
     if (s != TQ_OK) return s;
-    const size_t need =
-        tq_sdpa_workspace_bytes(cache->batch, hq, cache->num_kv_heads, cache->head_dim, max_seq_len, chunk);
-    if (workspace == nullptr || workspace_bytes < need) return TQ_ERR_WORKSPACE;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TQ_ERR_ALIGN;
-    Plan pl;
-    s = device_plan(cache, max_seq_len, chunk, TQ_IMPL_MMA, &pl);
-    if (s != TQ_OK) return s;
-    if (pl.n_splits > tq::kMaxReduceParts) return TQ_ERR_SHAPE;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // A few new rows per sequence are quantized by the decode kernel itself
-    // (the CTA that reads them writes them first); longer appends run the
-    // append kernel, and the decode starts early and waits only for the tiles
-    // that hold the new rows.
-    const tq::AppendParams ap = append_params(cache, k_new, v_new, n_new, write_pos, status);
-    const bool fused = n_new > 0 && n_new <= tq::kFusedAppendMaxRows;
-    if (n_new > 0 && !fused) {
-        s = cuda_status(tq::launch_quantize_append_primary(ap, st));
-        if (s != TQ_OK) return s;
-    }
-    const size_t parts = static_cast<size_t>(cache->batch) * hq * pl.n_splits;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    float* pm = reinterpret_cast<float*>(ws);
-    float* plv = reinterpret_cast<float*>(ws + align256(parts * sizeof(float)));
-    float* pa = reinterpret_cast<float*>(ws + 2 * align256(parts * sizeof(float)));
-    s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, TQ_IMPL_MMA, st,
-                   n_new > 0 && !fused ? write_pos : nullptr, fused ? 0 : n_new, fused ? &ap : nullptr);
-    if (s != TQ_OK) return s;
-    tq::ReduceParams r;
-    r.part_m = pm;
-    r.part_l = plv;
-    r.part_acc = pa;
-    r.out = out;
-    r.batch = cache->batch;
-    r.num_q_heads = hq;
-    r.head_dim = cache->head_dim;
-    r.n_parts = pl.n_splits;
-    return cuda_status(tq::launch_reduce(r, st, true));
+    if (!valid_rotation(flags)) return TQ_ERR_UNSUPPORTED;
+    if (n_new == 0) return TQ_OK;
+    return cuda_status(tq::launch_quantize_append(append_params(cache, k_new, v_new, n_new, write_pos, status, flags),
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
+tq_status tq_hadamard_rotate(const uint16_t* x, int64_t rows, int32_t dim, uint16_t* out, void* stream) {
+    if (x == nullptr || out == nullptr) return TQ_ERR_NULL;
+    if (rows < 0) return TQ_ERR_SHAPE;
+    if (!supported_dim(dim)) return TQ_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(out)) return TQ_ERR_ALIGN;
+    return cuda_status(tq::launch_rotate_rows(x, rows, dim, out, tq::rotation_scale(dim),
+                                              static_cast<cudaStream_t>(stream)));
 }
 
 size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t hq, int32_t hkv, int32_t head_dim, int32_t max_seq_len,
@@ -423,43 +484,25 @@ size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t hq, int32_t hkv, int32_t h
     if (cap < 1) cap = 1;
     if (ns > cap) ns = cap;
     const size_t parts = static_cast<size_t>(batch) * hq * static_cast<size_t>(ns);
-    return 2 * align256(parts * sizeof(float)) + align256(parts * head_dim * sizeof(float));
+    // m, l, acc of every part, then the rotated query (TQ_ROTATE_K)
+    return 2 * align256(parts * sizeof(float)) + align256(parts * head_dim * sizeof(float)) +
+           align256(static_cast<size_t>(batch) * hq * head_dim * sizeof(uint16_t));
 }
 
 tq_status tq_sdpa_int4_decode_impl(const tq_kv_cache* cache, const uint16_t* q, int32_t hq,
                                    const int32_t* seq_lens, int32_t max_seq_len, float attn_scale, int32_t chunk,
                                    void* workspace, size_t workspace_bytes, uint16_t* out, int32_t* status,
                                    tq_impl impl, void* stream) {
-    tq_status s = check_decode_args(cache, q, hq, seq_lens, max_seq_len, chunk, out);
-    if (s != TQ_OK) return s;
-    if (!valid_impl(impl)) return TQ_ERR_UNSUPPORTED;
-    const size_t need =
-        tq_sdpa_workspace_bytes(cache->batch, hq, cache->num_kv_heads, cache->head_dim, max_seq_len, chunk);
-    if (workspace == nullptr || workspace_bytes < need) return TQ_ERR_WORKSPACE;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TQ_ERR_ALIGN;
-    Plan pl;
-    s = device_plan(cache, max_seq_len, chunk, impl, &pl);
-    if (s != TQ_OK) return s;
-    if (pl.n_splits > tq::kMaxReduceParts) return TQ_ERR_SHAPE;
-    const size_t parts = static_cast<size_t>(cache->batch) * hq * pl.n_splits;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    float* pm = reinterpret_cast<float*>(ws);
-    float* plv = reinterpret_cast<float*>(ws + align256(parts * sizeof(float)));
-    float* pa = reinterpret_cast<float*>(ws + 2 * align256(parts * sizeof(float)));
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status,
-                   impl == TQ_IMPL_SIMT ? TQ_IMPL_SIMT : TQ_IMPL_MMA, st);
-    if (s != TQ_OK) return s;
-    tq::ReduceParams r;
-    r.part_m = pm;
-    r.part_l = plv;
-    r.part_acc = pa;
-    r.out = out;
-    r.batch = cache->batch;
-    r.num_q_heads = hq;
-    r.head_dim = cache->head_dim;
-    r.n_parts = pl.n_splits;
-    return cuda_status(tq::launch_reduce(r, st, true));
+    return decode_path(cache, nullptr, nullptr, 0, nullptr, q, hq, seq_lens, max_seq_len, attn_scale, chunk, 0u,
+                       workspace, workspace_bytes, out, status, impl, static_cast<cudaStream_t>(stream));
+}
+
+tq_status tq_sdpa_int4_decode_ex(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
+                                 int32_t max_seq_len, float attn_scale, int32_t chunk, uint32_t flags,
+                                 void* workspace, size_t workspace_bytes, uint16_t* out, int32_t* status,
+                                 void* stream) {
+    return decode_path(cache, nullptr, nullptr, 0, nullptr, q, hq, seq_lens, max_seq_len, attn_scale, chunk, flags,
+                       workspace, workspace_bytes, out, status, TQ_IMPL_AUTO, static_cast<cudaStream_t>(stream));
 }
 
 tq_status tq_sdpa_int4_decode(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
@@ -509,7 +552,7 @@ tq_status tq_sdpa_int4_reduce(const float* part_m, const float* part_l, const fl
     if (part_m == nullptr || part_l == nullptr || part_acc == nullptr || out == nullptr) return TQ_ERR_NULL;
     if (batch < 1 || hq < 1 || head_dim < 1 || n_parts < 1 || n_parts > tq::kMaxReduceParts) return TQ_ERR_SHAPE;
     if (!supported_dim(head_dim)) return TQ_ERR_UNSUPPORTED;
-    tq::ReduceParams r;
+    tq::ReduceParams r{};
     r.part_m = part_m;
     r.part_l = part_l;
     r.part_acc = part_acc;
@@ -533,7 +576,7 @@ tq_status tq_dequantize_kv(const tq_kv_cache* cache, int32_t n_rows, uint16_t* k
     DeviceFacts* f = nullptr;
     s = device_facts(&f);
     if (s != TQ_OK) return s;
-    tq::DequantParams p;
+    tq::DequantParams p{};
     p.k_codes = cache->k_codes;
     p.v_codes = cache->v_codes;
     p.k_scale = cache->k_scale;

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cmath>
+
 #include "tq.h"
 
 namespace tq {
@@ -23,6 +25,8 @@ struct AppendParams {
     uint16_t* v_bias;
     int32_t* status;
     int32_t batch, num_kv_heads, head_dim, n_new, capacity;
+    uint32_t flags;    // TQ_ROTATE_K / TQ_ROTATE_V: rotate the rows before quantizing them
+    float rot_scale;   // fp32 value nearest 1 / sqrt(head_dim)
 };
 
 // Geometry of one phase-1 launch: grid (n_splits, Hkv, B).  The sequence is
@@ -81,6 +85,8 @@ struct ReduceParams {
     const float* part_acc;
     uint16_t* out;            // [B][Hq][D]
     int32_t batch, num_q_heads, head_dim, n_parts;
+    int32_t rotate_out;       // nonzero: out = H (merged output), for a cache whose V rows were rotated
+    float rot_scale;
 };
 
 
@@ -94,6 +100,11 @@ cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, const CUtenso
 cudaError_t launch_quantize_append_primary(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl_secondary);
 cudaError_t launch_dequant(const DequantParams& p, int sm_count, cudaStream_t stream);
+// out[r] = fp16(H x[r]) for rows of `dim` fp16 values (dim 64 / 128 / 256); out may be x.
+cudaError_t launch_rotate_rows(const uint16_t* x, long long rows, int dim, uint16_t* out, float scale,
+                               cudaStream_t stream);
+// fp32 value nearest 1 / sqrt(dim), the rotation's normalisation.
+inline float rotation_scale(int dim) { return static_cast<float>(1.0 / std::sqrt(static_cast<double>(dim))); }
 
 // Tokens per pipeline stage of the tensor-core kernel (tiles are TMA boxes).
 int mma_tile_tokens(int head_dim);

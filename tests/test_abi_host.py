@@ -78,7 +78,9 @@ def test_workspace_bytes(L):
     def want(B, Hq, Hkv, D, S):
         ns = min(math.ceil(S / 16), max(1, 2048 // (B * Hkv)))
         parts = B * Hq * ns
-        return 2 * (-(-parts * 4 // 256) * 256) + (-(-parts * D * 4 // 256) * 256)
+        a256 = lambda n: -(-n // 256) * 256
+        # m, l, acc per part, then room for the rotated query (B * Hq * D fp16)
+        return 2 * a256(parts * 4) + a256(parts * D * 4) + a256(B * Hq * D * 2)
 
     assert tq.tq_sdpa_workspace_bytes(1, 64, 8, 128, 131072, 512) == want(1, 64, 8, 128, 131072)
     assert tq.tq_sdpa_workspace_bytes(32, 64, 8, 128, 32768, 512) == want(32, 64, 8, 128, 32768)
@@ -176,3 +178,20 @@ def test_dequantize_argument_errors_launch_nothing(L):
     assert f(ctypes.byref(c), 257, 0x1000, 0x2000, None) == 3
     assert f(ctypes.byref(c), 16, 0x1008, 0x2000, None) == 7
     assert f(ctypes.byref(c), 0, 0x1000, 0x2000, None) == 0  # nothing to do
+
+
+def test_rotation_argument_errors_launch_nothing(L):
+    c = _fake_cache()
+    assert L.tq_hadamard_rotate(None, 4, 128, 0x2000, None) == 1
+    assert L.tq_hadamard_rotate(0x1000, -1, 128, 0x2000, None) == 2
+    assert L.tq_hadamard_rotate(0x1000, 4, 96, 0x2000, None) == 6
+    assert L.tq_hadamard_rotate(0x1008, 4, 128, 0x2000, None) == 7
+    assert L.tq_hadamard_rotate(0x1000, 0, 128, 0x2000, None) == 0  # nothing to do
+    f = L.tq_quantize_kv_append_ex
+    assert f(ctypes.byref(c), 0x1000, 0x1000, 1, 0x2000, 4, None, None) == 6   # unknown flag bit
+    assert f(ctypes.byref(c), 0x1000, 0x1000, 0, 0x2000, 3, None, None) == 0
+    d = L.tq_sdpa_int4_decode_ex
+    assert d(ctypes.byref(c), 0x100000, 8, 0x200000, 256, ctypes.c_float(0.1), 512, 8, 0x300000, 1 << 30,
+             0x400000, None, None) == 6
+    assert d(ctypes.byref(c), 0x100000, 8, 0x200000, 256, ctypes.c_float(0.1), 512, 1, 0x300000, 16, 0x400000,
+             None, None) == 4

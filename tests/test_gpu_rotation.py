@@ -1,0 +1,99 @@
+"""GPU Hadamard-rotated int4 ("Running and Evaluating TurboQuant optimized
+Gemma 4", TurboQuant section) against the oracle: the rotation kernel and the
+rotated append bit for bit, the rotated decode within the output tolerance."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from int4_kv_cache_gb300 import synth
+from tests.gpu_helpers import assert_close, cache_arrays, gpu_cache_from_fp16, need_gpu, workspace_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_rotate_rows_bit_exact(D):
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    rng = np.random.default_rng(100 + D)
+    x = (rng.standard_normal((37, 3, D)) * 2).astype(np.float16)
+    x[:, :, 5] *= 20
+    xt = torch.from_numpy(x).cuda()
+    got = tq.tq_hadamard_rotate(xt).cpu().numpy()
+    assert np.array_equal(got.view(np.uint16), oracle.rotate_rows_f16(x).view(np.uint16))
+    tq.tq_hadamard_rotate(xt, out=xt)  # in place
+    assert np.array_equal(xt.cpu().numpy().view(np.uint16), got.view(np.uint16))
+
+
+@pytest.mark.parametrize("D,flags", [(128, 1), (128, 3), (64, 3), (256, 2)])
+def test_rotated_append_bit_exact(D, flags):
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    x = synth.decode_inputs(110 + D, 2, 2, 2, D, 300, outliers=True)
+    cache = tq.KVCache(2, 2, D, 304)
+    wp = torch.zeros(2, dtype=torch.int32, device="cuda")
+    tq.tq_quantize_kv_append(cache, torch.from_numpy(x.k).cuda(), torch.from_numpy(x.v).cuda(), wp, flags=flags)
+    torch.cuda.synchronize()
+    kk = oracle.rotate_rows_f16(x.k) if flags & tq.TQ_ROTATE_K else x.k
+    vv = oracle.rotate_rows_f16(x.v) if flags & tq.TQ_ROTATE_V else x.v
+    oc = oracle.Cache.from_fp16(kk, vv)
+    kc, ks, kb, vc, vs, vb = cache_arrays(cache)
+    S = 300
+    for got, want in ((kc, oc.kc), (ks, oc.ks), (kb, oc.kb), (vc, oc.vc), (vs, oc.vs), (vb, oc.vb)):
+        assert np.array_equal(got[:, :, :S], want)
+
+
+def _rotated_reference(x, lens, scale, flags):
+    kk = oracle.rotate_rows_f16(x.k) if flags & 1 else x.k
+    vv = oracle.rotate_rows_f16(x.v) if flags & 2 else x.v
+    qq = oracle.rotate_rows_f16(x.q) if flags & 1 else x.q
+    out = oracle.attention(qq, oracle.Cache.from_fp16(kk, vv), lens, scale)
+    return oracle.hadamard(out) if flags & 2 else out
+
+
+@pytest.mark.parametrize("flags", [1, 2, 3])
+def test_rotated_decode_matches_oracle(flags):
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    B, Hq, Hkv, D, S = 3, 16, 2, 128, 3000
+    lens = np.array([3000, 1, 1377], np.int32)
+    x = synth.decode_inputs(120 + flags, B, Hq, Hkv, D, S, lens=lens, outliers=True)
+    cache = tq.KVCache(B, Hkv, D, S + 8)
+    wp = torch.zeros(B, dtype=torch.int32, device="cuda")
+    tq.tq_quantize_kv_append(cache, torch.from_numpy(x.k).cuda(), torch.from_numpy(x.v).cuda(), wp, flags=flags)
+    ws = workspace_for(B, Hq, Hkv, D, S)
+    out = tq.tq_sdpa_int4_decode(cache, torch.from_numpy(x.q).cuda(), torch.from_numpy(lens).cuda(), S,
+                                 1 / math.sqrt(D), ws, flags=flags)
+    torch.cuda.synchronize()
+    assert_close(out.float().cpu().numpy(), _rotated_reference(x, lens, 1 / math.sqrt(D), flags),
+                 what=f"rotated decode flags={flags}")
+
+
+def test_rotated_step_equals_append_then_decode():
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    B, Hq, Hkv, D, S, flags = 2, 64, 8, 128, 4992, 3
+    x = synth.decode_inputs(131, B, Hq, Hkv, D, S, outliers=True)
+    kn, vn = synth.append_tokens(131, 0, B, Hkv, D, 1, outliers=x.outlier_channels)
+    pos = np.array([S - 1, 2500], np.int32)
+    lens = pos + 1
+    q, wp, lt = (torch.from_numpy(a).cuda() for a in (x.q, pos, lens))
+    knt, vnt = torch.from_numpy(kn).cuda(), torch.from_numpy(vn).cuda()
+    ws = workspace_for(B, Hq, Hkv, D, S)
+    zero = torch.zeros(B, dtype=torch.int32, device="cuda")
+    caches = []
+    for _ in range(2):
+        c = tq.KVCache(B, Hkv, D, S)
+        tq.tq_quantize_kv_append(c, torch.from_numpy(x.k).cuda(), torch.from_numpy(x.v).cuda(), zero, flags=flags)
+        caches.append(c)
+    tq.tq_quantize_kv_append(caches[0], knt, vnt, wp, flags=flags)
+    ref = tq.tq_sdpa_int4_decode(caches[0], q, lt, S, 0.088, ws, flags=flags).float().cpu().numpy()
+    got = tq.tq_decode_step(caches[1], knt, vnt, wp, q, lt, S, 0.088, ws, flags=flags).float().cpu().numpy()
+    assert torch.equal(caches[0].buffer, caches[1].buffer)
+    assert np.array_equal(got, ref)
