@@ -74,6 +74,7 @@ typedef enum tq_status {
 #define TQ_DEV_WRITE_POS 0x1 /* append: write_pos[b] < 0 or write_pos[b] + n_new > capacity; rows skipped */
 #define TQ_DEV_SEQ_LEN 0x2   /* decode: seq_lens[b] < 0 or > max_seq_len; clamped into range */
 #define TQ_DEV_TIMEOUT 0x4   /* a pipeline wait exceeded its time limit; the CTA gave up */
+#define TQ_DEV_PAGE 0x8      /* paged cache: a block-table entry outside [0, num_pages); page 0 used instead */
 
 /* Rotation flags ("Running and Evaluating TurboQuant optimized Gemma 4",
  * TurboQuant section: vectors are rotated by the normalised Sylvester Hadamard
@@ -86,6 +87,14 @@ typedef enum tq_status {
  *                attention output o over them, which is the output over v. */
 #define TQ_ROTATE_K 0x1u
 #define TQ_ROTATE_V 0x2u
+
+/* tq_decode_step_ex / tq_paged_decode_step: after the step, add n_new to
+ * write_pos[b] and to seq_lens[b] on the device (both arrays are written;
+ * they must not overlap).  A step captured once in a CUDA graph can then be
+ * replayed token after token with no host work; the graph keeps the
+ * max_seq_len it was captured with, which must stay an upper bound of the
+ * advancing lengths. */
+#define TQ_STEP_ADVANCE 0x100u
 
 /* Decode implementations (tq_sdpa_int4_decode_impl and friends). */
 typedef enum tq_impl {
@@ -107,6 +116,32 @@ typedef struct tq_kv_cache {
     int32_t group_size; /* must be 64 */
     int32_t capacity;   /* tokens per (sequence, kv head) */
 } tq_kv_cache;
+
+/* Paged cache: a pool of pages, each holding page_tokens consecutive tokens of
+ * one sequence for every kv head, and a block table mapping each sequence's
+ * logical pages to pool pages (the survey's paged-cache option for ragged
+ * batches; the Llama page's 18% concatenation gap is what a cache that grows
+ * by reallocation costs).  Row t of (sequence b, kv head h) is row
+ * t % page_tokens of head h in page block_table[b * max_pages_per_seq +
+ * t / page_tokens].  The caller owns the pool and the table and allocates
+ * pages before appending into them; a table entry outside [0, num_pages) sets
+ * TQ_DEV_PAGE and page 0 is used instead (no fault). */
+typedef struct tq_paged_kv_cache {
+    uint8_t* k_codes;  /* [num_pages][Hkv][page_tokens][D/2] */
+    uint8_t* v_codes;
+    uint16_t* k_scale; /* [num_pages][Hkv][page_tokens][D/64] fp16 */
+    uint16_t* k_bias;
+    uint16_t* v_scale;
+    uint16_t* v_bias;
+    const int32_t* block_table; /* device [batch][max_pages_per_seq] */
+    int32_t batch;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t group_size;  /* must be 64 */
+    int32_t page_tokens; /* a multiple of 128 */
+    int32_t num_pages;
+    int32_t max_pages_per_seq; /* logical capacity = max_pages_per_seq * page_tokens */
+} tq_paged_kv_cache;
 
 /* ABI version of the loaded library (TQ_ABI_VERSION it was built with). */
 int32_t tq_abi_version(void);
@@ -160,6 +195,42 @@ tq_status tq_quantize_kv_append_ex(const tq_kv_cache* cache, const uint16_t* k_n
  * rotation flags.  rows = 0 launches nothing. */
 tq_status tq_hadamard_rotate(const uint16_t* x, int64_t rows, int32_t dim,
                              uint16_t* out, void* stream);
+
+/* ------------------------------------------------------------ paged cache --
+ * Bytes of a page pool for these sizes (the six arrays, each 256-aligned),
+ * 0 for invalid sizes.  Host-only. */
+size_t tq_paged_kv_cache_bytes(int32_t num_pages, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t group_size, int32_t page_tokens);
+
+/* Fill *cache with the arrays carved from `base` (device, 256-byte aligned,
+ * tq_paged_kv_cache_bytes long) and the given block table.  Host-only. */
+tq_status tq_paged_kv_cache_carve(tq_paged_kv_cache* cache, void* base, const int32_t* block_table,
+                                  int32_t batch, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t group_size, int32_t page_tokens, int32_t num_pages,
+                                  int32_t max_pages_per_seq);
+
+/* tq_quantize_kv_append_ex into a paged cache (rows through the block table). */
+tq_status tq_paged_quantize_kv_append(const tq_paged_kv_cache* cache, const uint16_t* k_new,
+                                      const uint16_t* v_new, int32_t n_new,
+                                      const int32_t* write_pos, uint32_t flags,
+                                      int32_t* status, void* stream);
+
+/* tq_sdpa_int4_decode_ex / tq_decode_step_ex over a paged cache: the same
+ * arithmetic and, for chunk >= 128, the same split plan as the contiguous
+ * cache (runs start on page-aligned tile boundaries; smaller chunks are
+ * raised to the tile), so the results are identical to a contiguous cache
+ * holding the same rows.  Tensor-core path only. */
+tq_status tq_paged_sdpa_int4_decode(const tq_paged_kv_cache* cache, const uint16_t* q,
+                                    int32_t num_q_heads, const int32_t* seq_lens,
+                                    int32_t max_seq_len, float attn_scale, int32_t chunk,
+                                    uint32_t flags, void* workspace, size_t workspace_bytes,
+                                    uint16_t* out, int32_t* status, void* stream);
+tq_status tq_paged_decode_step(const tq_paged_kv_cache* cache, const uint16_t* k_new,
+                               const uint16_t* v_new, int32_t n_new, const int32_t* write_pos,
+                               const uint16_t* q, int32_t num_q_heads, const int32_t* seq_lens,
+                               int32_t max_seq_len, float attn_scale, int32_t chunk, uint32_t flags,
+                               void* workspace, size_t workspace_bytes, uint16_t* out,
+                               int32_t* status, void* stream);
 
 /* Workspace bytes tq_sdpa_int4_decode needs for these sizes (an upper bound
  * that does not depend on the device).  Host-only. */

@@ -20,13 +20,16 @@ __all__ = [
     "tq_abi_version", "tq_status_string", "tq_kv_cache_bytes", "tq_sdpa_workspace_bytes",
     "tq_quantize_kv_append", "tq_sdpa_int4_decode", "tq_sdpa_int4_partial", "tq_sdpa_int4_reduce",
     "tq_sdpa_plan", "tq_sdpa_int4_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "tq_decode_step",
-    "tq_dequantize_kv", "tq_hadamard_rotate", "TQ_ROTATE_K", "TQ_ROTATE_V",
+    "tq_dequantize_kv", "tq_hadamard_rotate", "TQ_ROTATE_K", "TQ_ROTATE_V", "TQ_STEP_ADVANCE", "TQ_DEV_PAGE",
+    "tq_paged_kv_cache", "PagedKVCache",
 ]
 
 TQ_OK = 0
 TQ_IMPL_AUTO, TQ_IMPL_MMA, TQ_IMPL_SIMT = 0, 1, 2
 TQ_DEV_WRITE_POS, TQ_DEV_SEQ_LEN, TQ_DEV_TIMEOUT = 0x1, 0x2, 0x4
 TQ_ROTATE_K, TQ_ROTATE_V = 0x1, 0x2
+TQ_STEP_ADVANCE = 0x100
+TQ_DEV_PAGE = 0x8
 GROUP_SIZE = 64
 DEFAULT_CHUNK = 512
 NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -58,6 +61,19 @@ class tq_kv_cache(ctypes.Structure):
     ]
 
 
+class tq_paged_kv_cache(ctypes.Structure):
+    _fields_ = [
+        ("k_codes", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
+        ("k_scale", ctypes.c_void_p), ("k_bias", ctypes.c_void_p),
+        ("v_scale", ctypes.c_void_p), ("v_bias", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p),
+        ("batch", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("group_size", ctypes.c_int32),
+        ("page_tokens", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+        ("max_pages_per_seq", ctypes.c_int32),
+    ]
+
+
 _lib = None
 
 
@@ -71,6 +87,7 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(path)
         P, i32, sz, f32, u32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float, ctypes.c_uint32
         C = ctypes.POINTER(tq_kv_cache)
+        PC = ctypes.POINTER(tq_paged_kv_cache)
         sig = {
             "tq_abi_version": ([], i32),
             "tq_status_string": ([i32], ctypes.c_char_p),
@@ -91,6 +108,11 @@ def lib() -> ctypes.CDLL:
             "tq_hadamard_rotate": ([P, ctypes.c_int64, i32, P, P], i32),
             "tq_sdpa_int4_decode_ex": ([C, P, i32, P, i32, f32, i32, u32, P, sz, P, P, P], i32),
             "tq_decode_step_ex": ([C, P, P, i32, P, P, i32, P, i32, f32, i32, u32, P, sz, P, P, P], i32),
+            "tq_paged_kv_cache_bytes": ([i32] * 5, sz),
+            "tq_paged_kv_cache_carve": ([PC, P, P] + [i32] * 7, i32),
+            "tq_paged_quantize_kv_append": ([PC, P, P, i32, P, u32, P, P], i32),
+            "tq_paged_sdpa_int4_decode": ([PC, P, i32, P, i32, f32, i32, u32, P, sz, P, P, P], i32),
+            "tq_paged_decode_step": ([PC, P, P, i32, P, P, i32, P, i32, f32, i32, u32, P, sz, P, P, P], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -187,6 +209,57 @@ class KVCache:
         return ctypes.byref(self.struct)
 
 
+class PagedKVCache:
+    """A page pool (one device allocation) plus a device block table.
+
+    Views: k_codes/v_codes uint8 [num_pages, Hkv, page_tokens, D/2];
+    k_scale/k_bias/v_scale/v_bias fp16 [num_pages, Hkv, page_tokens, D/64];
+    block_table int32 [B, max_pages_per_seq] (the caller fills it: page of
+    logical page j of sequence b).  Every call of this binding that takes a
+    ``KVCache`` takes a ``PagedKVCache`` as well.
+    """
+
+    paged = True
+
+    def __init__(self, batch: int, num_kv_heads: int, head_dim: int, page_tokens: int, num_pages: int,
+                 max_pages_per_seq: int, device=None, group_size: int = GROUP_SIZE):
+        nbytes = int(lib().tq_paged_kv_cache_bytes(num_pages, num_kv_heads, head_dim, group_size, page_tokens))
+        if nbytes == 0:
+            raise ValueError("invalid page pool sizes")
+        dev = device or "cuda"
+        self.buffer = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.block_table = torch.zeros((batch, max_pages_per_seq), dtype=torch.int32, device=dev)
+        self.struct = tq_paged_kv_cache()
+        _check("tq_paged_kv_cache_carve", lib().tq_paged_kv_cache_carve(
+            ctypes.byref(self.struct), _ptr(self.buffer), _ptr(self.block_table), batch, num_kv_heads, head_dim,
+            group_size, page_tokens, num_pages, max_pages_per_seq))
+        self.batch, self.num_kv_heads, self.head_dim = batch, num_kv_heads, head_dim
+        self.page_tokens, self.num_pages, self.max_pages_per_seq = page_tokens, num_pages, max_pages_per_seq
+        self.capacity = page_tokens * max_pages_per_seq
+        self.group_size = group_size
+        base = self.buffer.data_ptr()
+        rows = num_pages * num_kv_heads * page_tokens
+        ng = head_dim // group_size
+
+        def view(addr, n, dtype, shape):
+            off = addr - base
+            nb = n * torch.empty((), dtype=dtype).element_size()
+            return self.buffer[off: off + nb].view(dtype).view(shape)
+
+        cs = (num_pages, num_kv_heads, page_tokens, head_dim // 2)
+        ss = (num_pages, num_kv_heads, page_tokens, ng)
+        st = self.struct
+        self.k_codes = view(st.k_codes, rows * head_dim // 2, torch.uint8, cs)
+        self.v_codes = view(st.v_codes, rows * head_dim // 2, torch.uint8, cs)
+        self.k_scale = view(st.k_scale, rows * ng, torch.float16, ss)
+        self.k_bias = view(st.k_bias, rows * ng, torch.float16, ss)
+        self.v_scale = view(st.v_scale, rows * ng, torch.float16, ss)
+        self.v_bias = view(st.v_bias, rows * ng, torch.float16, ss)
+
+    def ref(self):
+        return ctypes.byref(self.struct)
+
+
 # ------------------------------------------------------------------ device ops
 def tq_quantize_kv_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, write_pos: torch.Tensor,
                           status: Optional[torch.Tensor] = None, stream=None, flags: int = 0) -> None:
@@ -200,6 +273,10 @@ def tq_quantize_kv_append(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tens
     n_new = k_new.shape[2] if k_new.dim() == 4 else 0
     if tuple(k_new.shape) != (cache.batch, cache.num_kv_heads, n_new, cache.head_dim) or v_new.shape != k_new.shape:
         raise ValueError(f"k_new/v_new must be [B, Hkv, n_new, D]; got {tuple(k_new.shape)}")
+    if getattr(cache, "paged", False):
+        _check("tq_paged_quantize_kv_append", lib().tq_paged_quantize_kv_append(
+            cache.ref(), _ptr(k_new), _ptr(v_new), n_new, _ptr(write_pos), int(flags), _ptr(status), _stream(stream)))
+        return
     if flags:
         _check("tq_quantize_kv_append_ex", lib().tq_quantize_kv_append_ex(
             cache.ref(), _ptr(k_new), _ptr(v_new), n_new, _ptr(write_pos), int(flags), _ptr(status), _stream(stream)))
@@ -224,6 +301,13 @@ def tq_sdpa_int4_decode(cache: KVCache, q: torch.Tensor, seq_lens: torch.Tensor,
         _need(status, torch.int32, "status")
     if q.dim() != 3 or q.shape[0] != cache.batch or q.shape[2] != cache.head_dim or out.shape != q.shape:
         raise ValueError(f"q must be [B, Hq, D]; got {tuple(q.shape)}")
+    if getattr(cache, "paged", False):
+        if impl == TQ_IMPL_SIMT:
+            raise ValueError("a paged cache takes the tensor-core implementation")
+        _check("tq_paged_sdpa_int4_decode", lib().tq_paged_sdpa_int4_decode(
+            cache.ref(), _ptr(q), q.shape[1], _ptr(seq_lens), int(max_seq_len), float(attn_scale), int(chunk),
+            int(flags), _ptr(workspace), workspace.numel(), _ptr(out), _ptr(status), _stream(stream)))
+        return out
     if flags:
         if impl != TQ_IMPL_AUTO:
             raise ValueError("rotation flags take the default implementation")
@@ -257,6 +341,12 @@ def tq_decode_step(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, wri
         raise ValueError(f"k_new/v_new must be [B, Hkv, n_new, D]; got {tuple(k_new.shape)}")
     if q.dim() != 3 or q.shape[0] != cache.batch or q.shape[2] != cache.head_dim or out.shape != q.shape:
         raise ValueError(f"q must be [B, Hq, D]; got {tuple(q.shape)}")
+    if getattr(cache, "paged", False):
+        _check("tq_paged_decode_step", lib().tq_paged_decode_step(
+            cache.ref(), _ptr(k_new), _ptr(v_new), n_new, _ptr(write_pos), _ptr(q), q.shape[1], _ptr(seq_lens),
+            int(max_seq_len), float(attn_scale), int(chunk), int(flags), _ptr(workspace), workspace.numel(),
+            _ptr(out), _ptr(status), _stream(stream)))
+        return out
     if flags:
         _check("tq_decode_step_ex", lib().tq_decode_step_ex(
             cache.ref(), _ptr(k_new), _ptr(v_new), n_new, _ptr(write_pos), _ptr(q), q.shape[1], _ptr(seq_lens),

@@ -153,7 +153,7 @@ __device__ __forceinline__ int clamp_len(const DecodeParams& p, int b) {
     return len;
 }
 
-template <int D>
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const DecodeParams p) {
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
     const int t_begin = run_begin(split, p.units, p.n_splits, p.unit_tokens);
     const int t_end = min(run_begin(split + 1, p.units, p.n_splits, p.unit_tokens), len);
     const int n_tiles = t_end > t_begin ? (t_end - t_begin + C::T - 1) / C::T : 0;
-    const long long row_base = (static_cast<long long>(b) * p.num_kv_heads + kvh) * p.capacity;
+    const long long row_base = (static_cast<long long>(b) * p.num_kv_heads + kvh) * p.capacity;  // contiguous
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -220,14 +220,23 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
         const int stage = it % C::STAGES;
         const int t0 = t_begin + it * C::T;
         if (tile_uses(it, dep_lo, dep_hi)) pdl_wait_primary();
-        const int avail = min(C::T, p.capacity - t0);  // rows left in this (b, kv head)
+        // the tile's first row and its rows (a tile never crosses a page: pages hold whole tiles)
+        long long row;
+        int avail;
+        if constexpr (PAGED) {
+            row = kv_row(p.map, p.num_kv_heads, b, kvh, t0, p.status);
+            avail = C::T;
+        } else {
+            row = row_base + t0;
+            avail = min(C::T, p.capacity - t0);  // rows left in this (b, kv head)
+        }
         const uint32_t sb_bytes = static_cast<uint32_t>(avail) * NG * 2;
         uint8_t* st = smem + stage * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&full_bar[stage], 2 * C::CODE_BYTES + 4 * sb_bytes);
-        const int y = static_cast<int>(((row_base + t0) * C::BPT) / 128);
+        const int y = static_cast<int>((row * C::BPT) / 128);
         tma_load_2d(st, &tm_k, 0, y, &full_bar[stage], policy);
         tma_load_2d(st + C::CODE_BYTES, &tm_v, 0, y, &full_bar[stage], policy);
-        const long long sb_off = (row_base + t0) * NG;
+        const long long sb_off = row * NG;
         uint8_t* sb = st + 2 * C::CODE_BYTES;
         bulk_load(sb + 0 * C::SB_BYTES, p.k_scale + sb_off, sb_bytes, &full_bar[stage], policy);
         bulk_load(sb + 1 * C::SB_BYTES, p.k_bias + sb_off, sb_bytes, &full_bar[stage], policy);
@@ -320,7 +329,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
             const GroupQ gq = quantize_lane8(raw);
             if (valid) {
                 const int kv = task & 1, g = (task >> 1) % NG, r = app_lo + (task >> 1) / NG;
-                const long long row = row_base + r;
+                long long row;
+                if constexpr (PAGED) row = kv_row(p.map, p.num_kv_heads, b, kvh, r, p.status);
+                else row = row_base + r;
                 *reinterpret_cast<uint32_t*>((kv ? p.app.v_codes : p.app.k_codes) + row * (D / 2) +
                                              g * (kGroup / 2) + app_part * 4) = gq.codes;
                 if (app_part == 0) {
@@ -626,14 +637,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
     }
 }
 
-template <int D>
+template <int D, bool PAGED>
 cudaError_t set_smem_attr() {
     static bool done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
     cudaError_t e =
-        cudaFuncSetAttribute(decode_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_BYTES);
+        cudaFuncSetAttribute(decode_mma_kernel<D, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<D>::SMEM_BYTES);
     if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
     return e;
 }
@@ -642,7 +654,8 @@ template <int D>
 cudaError_t launch_d(const DecodeParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v, cudaStream_t stream,
                      bool pdl_secondary) {
     using C = Cfg<D>;
-    cudaError_t e = set_smem_attr<D>();
+    const bool paged = p.map.block_table != nullptr;
+    cudaError_t e = paged ? set_smem_attr<D, true>() : set_smem_attr<D, false>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_splits, p.num_kv_heads, p.batch);
@@ -654,14 +667,16 @@ cudaError_t launch_d(const DecodeParams& p, const CUtensorMap& tm_k, const CUten
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_secondary ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D>, tm_k, tm_v, p);
+    if (paged) return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, true>, tm_k, tm_v, p);
+    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, false>, tm_k, tm_v, p);
 }
 
 template <int D>
 int ctas_per_sm_d() {
-    if (set_smem_attr<D>() != cudaSuccess) return 1;
+    if (set_smem_attr<D, false>() != cudaSuccess) return 1;
     int n = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D>, Cfg<D>::THREADS, Cfg<D>::SMEM_BYTES);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D, false>, Cfg<D>::THREADS,
+                                                  Cfg<D>::SMEM_BYTES);
     return n > 0 ? n : 1;
 }
 

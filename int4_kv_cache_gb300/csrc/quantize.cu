@@ -95,7 +95,9 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_append_kernel(const Ap
         if (p.status != nullptr && g == 0 && i == 0) atomicOr(p.status, TQ_DEV_WRITE_POS);
         return;
     }
-    const long long dst_row = bh * p.capacity + wp + i;
+    const long long dst_row =
+        kv_row(p.map, p.num_kv_heads, b, static_cast<int>(bh - static_cast<long long>(b) * p.num_kv_heads), wp + i,
+               p.status);
     const long long code_off = dst_row * (p.head_dim / 2) + g * (kGroup / 2);  // 32-byte aligned
     const long long sb = dst_row * ng + g;
 #pragma unroll 1

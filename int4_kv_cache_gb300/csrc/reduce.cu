@@ -50,6 +50,11 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReducePara
     __shared__ float part_sum[kReduceWarps][D];
     pdl_wait_primary();
     const long long bh = blockIdx.x;
+    if (p.adv_n != 0 && threadIdx.x == 0 && bh % p.num_q_heads == 0) {  // phase 1 has read the lengths
+        const long long b = bh / p.num_q_heads;
+        p.adv_seq_lens[b] += p.adv_n;
+        p.adv_write_pos[b] += p.adv_n;
+    }
     const int n = p.n_parts;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float* pm = p.part_m + bh * n;
@@ -138,7 +143,22 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReducePara
     }
 }
 
+// TQ_STEP_ADVANCE after a step whose append ran as its own kernel: a plain
+// launch after the reduce, so stream order covers the append as well.
+__global__ void advance_lengths_kernel(int32_t* seq_lens, int32_t* write_pos, int batch, int n) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < batch) {
+        seq_lens[b] += n;
+        write_pos[b] += n;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_advance(int32_t* seq_lens, int32_t* write_pos, int batch, int n, cudaStream_t stream) {
+    advance_lengths_kernel<<<(batch + 127) / 128, 128, 0, stream>>>(seq_lens, write_pos, batch, n);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl_secondary) {
     cudaLaunchConfig_t cfg = {};

@@ -44,6 +44,86 @@ tq_status check_cache(const tq_kv_cache* c) {
     return TQ_OK;
 }
 
+// The cache as the kernels see it: the arrays, the sizes, and where each
+// logical row lives (tq::RowMap).  A contiguous cache is one page per
+// sequence; `capacity` is the logical capacity (max_pages * page_tokens when
+// paged).  Field names follow tq_kv_cache so the code below reads the same
+// for both layouts.
+struct Store {
+    uint8_t* k_codes;
+    uint8_t* v_codes;
+    uint16_t* k_scale;
+    uint16_t* k_bias;
+    uint16_t* v_scale;
+    uint16_t* v_bias;
+    int32_t batch, num_kv_heads, head_dim, group_size, capacity;
+    tq::RowMap map;
+    bool paged;
+};
+
+// Sizes and pointers only (no checks): for planning queries.
+Store shape_of(const tq_kv_cache* c) {
+    Store st{};
+    st.k_codes = c->k_codes;
+    st.v_codes = c->v_codes;
+    st.k_scale = c->k_scale;
+    st.k_bias = c->k_bias;
+    st.v_scale = c->v_scale;
+    st.v_bias = c->v_bias;
+    st.batch = c->batch;
+    st.num_kv_heads = c->num_kv_heads;
+    st.head_dim = c->head_dim;
+    st.group_size = c->group_size;
+    st.capacity = c->capacity;
+    st.map = {nullptr, c->capacity, 1, c->batch};
+    st.paged = false;
+    return st;
+}
+
+tq_status store_of(const tq_kv_cache* c, Store* st) {
+    tq_status s = check_cache(c);
+    if (s != TQ_OK) return s;
+    *st = shape_of(c);
+    return TQ_OK;
+}
+
+// Pages hold whole pipeline tiles (128 tokens; 64 for head_dim 256), so a
+// tile never crosses a page.
+constexpr int kPageTokenMultiple = 128;
+
+tq_status store_of(const tq_paged_kv_cache* c, Store* st) {
+    if (c == nullptr) return TQ_ERR_NULL;
+    if (!c->k_codes || !c->v_codes || !c->k_scale || !c->k_bias || !c->v_scale || !c->v_bias || !c->block_table)
+        return TQ_ERR_NULL;
+    if (c->batch < 1 || c->num_kv_heads < 1 || c->num_pages < 1 || c->max_pages_per_seq < 1) return TQ_ERR_SHAPE;
+    if (c->page_tokens < kPageTokenMultiple || c->page_tokens % kPageTokenMultiple != 0) return TQ_ERR_SHAPE;
+    if (c->group_size != TQ_GROUP_SIZE || !supported_dim(c->head_dim)) return TQ_ERR_UNSUPPORTED;
+    if (!aligned16(c->k_codes) || !aligned16(c->v_codes) || !aligned16(c->k_scale) || !aligned16(c->k_bias) ||
+        !aligned16(c->v_scale) || !aligned16(c->v_bias))
+        return TQ_ERR_ALIGN;
+    const long long cap = static_cast<long long>(c->max_pages_per_seq) * c->page_tokens;
+    if (cap >= (1LL << 31)) return TQ_ERR_SHAPE;
+    const long long rows128 =
+        static_cast<long long>(c->num_pages) * c->num_kv_heads * c->page_tokens * (c->head_dim / 2) / 128;
+    if (rows128 >= (1LL << 31)) return TQ_ERR_SHAPE;
+    Store& t = *st;
+    t = Store{};
+    t.k_codes = c->k_codes;
+    t.v_codes = c->v_codes;
+    t.k_scale = c->k_scale;
+    t.k_bias = c->k_bias;
+    t.v_scale = c->v_scale;
+    t.v_bias = c->v_bias;
+    t.batch = c->batch;
+    t.num_kv_heads = c->num_kv_heads;
+    t.head_dim = c->head_dim;
+    t.group_size = c->group_size;
+    t.capacity = static_cast<int32_t>(cap);
+    t.map = {c->block_table, c->page_tokens, c->max_pages_per_seq, c->num_pages};
+    t.paged = true;
+    return TQ_OK;
+}
+
 // ---------------------------------------------------------------- TMA maps --
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -65,11 +145,11 @@ EncodeTiledFn encode_fn() {
 
 // The code array of a cache seen as [rows][128 bytes] (uint8), boxes of
 // `box_rows` rows with the 128-byte swizzle; reads past the end are zero-filled.
-tq_status make_code_map(CUtensorMap* map, const uint8_t* codes, const tq_kv_cache* c, int box_rows) {
+tq_status make_code_map(CUtensorMap* map, const uint8_t* codes, const Store* c, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return cuda_status(cudaErrorNotSupported);
     const cuuint64_t rows =
-        static_cast<cuuint64_t>(c->batch) * c->num_kv_heads * c->capacity * (c->head_dim / 2) / 128;
+        static_cast<cuuint64_t>(c->map.num_pages) * c->num_kv_heads * c->map.page_tokens * (c->head_dim / 2) / 128;
     cuuint64_t dims[2] = {128, rows};
     cuuint64_t strides[1] = {128};
     cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
@@ -151,7 +231,7 @@ Plan chunk_plan(int max_seq_len, int chunk, int cps) {
     return pl;
 }
 
-tq_status device_plan(const tq_kv_cache* cache, int max_seq_len, int chunk, tq_impl impl, Plan* pl) {
+tq_status device_plan(const Store* cache, int max_seq_len, int chunk, tq_impl impl, Plan* pl) {
     DeviceFacts* f = nullptr;
     tq_status s = device_facts(&f);
     if (s != TQ_OK) return s;
@@ -159,14 +239,13 @@ tq_status device_plan(const tq_kv_cache* cache, int max_seq_len, int chunk, tq_i
     const bool simt = impl == TQ_IMPL_SIMT;
     const int per_sm = simt ? f->simt_ctas[di] : f->mma_ctas[di];
     const int tile = simt ? tq::kSimtTileTokens : tq::mma_tile_tokens(cache->head_dim);
+    if (cache->paged && chunk < tile) chunk = tile;  // runs start on tile (hence page-aligned) boundaries
     *pl = make_plan(cache->batch, cache->num_kv_heads, max_seq_len, chunk, tile, f->sms * per_sm);
     return TQ_OK;
 }
 
-tq_status check_decode_args(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
+tq_status check_decode_args(const Store* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
                             int32_t max_seq_len, int32_t chunk, const void* out) {
-    tq_status s = check_cache(cache);
-    if (s != TQ_OK) return s;
     if (q == nullptr || seq_lens == nullptr || out == nullptr) return TQ_ERR_NULL;
     if (!aligned16(q)) return TQ_ERR_ALIGN;
     if (hq < 1 || hq % cache->num_kv_heads != 0) return TQ_ERR_SHAPE;
@@ -177,7 +256,7 @@ tq_status check_decode_args(const tq_kv_cache* cache, const uint16_t* q, int32_t
     return TQ_OK;
 }
 
-tq_status run_phase1(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
+tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
                      int32_t max_seq_len, float attn_scale, const Plan& pl, float* pm, float* plv, float* pa,
                      int32_t* status, tq_impl impl, cudaStream_t stream, const int32_t* dep_write_pos = nullptr,
                      int32_t dep_n_new = 0, const tq::AppendParams* fused_append = nullptr) {
@@ -207,12 +286,16 @@ tq_status run_phase1(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, co
     p.score_scale_log2 = attn_scale * 1.4426950408889634f;
     p.dep_write_pos = dep_write_pos;
     p.dep_n_new = dep_n_new;
+    p.map = cache->map;
     p.app = {};
     if (fused_append != nullptr) {
         if (impl == TQ_IMPL_SIMT) return TQ_ERR_UNSUPPORTED;
         p.app = *fused_append;
     }
-    if (impl == TQ_IMPL_SIMT) return cuda_status(tq::launch_decode_simt(p, cache->head_dim, stream));
+    if (impl == TQ_IMPL_SIMT) {
+        if (cache->paged) return TQ_ERR_UNSUPPORTED;  // the CUDA-core comparison path reads contiguous caches
+        return cuda_status(tq::launch_decode_simt(p, cache->head_dim, stream));
+    }
     CUtensorMap tm_k, tm_v;
     const int box_rows = tq::mma_tile_tokens(cache->head_dim) * (cache->head_dim / 2) / 128;
     tq_status s = make_code_map(&tm_k, cache->k_codes, cache, box_rows);
@@ -230,10 +313,14 @@ namespace tq {
 // (`partials_bytes` long, 256-byte aligned) instead of a caller workspace.
 // Requests whose partial states do not fit are refused with TQ_ERR_WORKSPACE
 // before anything is launched.
-tq_status decode_into_partials(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
+tq_status decode_into_partials(const tq_kv_cache* raw, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
                                int32_t max_seq_len, float attn_scale, int32_t chunk, uint8_t* partials,
                                size_t partials_bytes, uint16_t* out, int32_t* status, cudaStream_t stream) {
-    tq_status s = check_decode_args(cache, q, hq, seq_lens, max_seq_len, chunk, out);
+    Store st;
+    tq_status s = store_of(raw, &st);
+    if (s != TQ_OK) return s;
+    const Store* cache = &st;
+    s = check_decode_args(cache, q, hq, seq_lens, max_seq_len, chunk, out);
     if (s != TQ_OK) return s;
     if (partials == nullptr) return TQ_ERR_WORKSPACE;
     Plan pl;
@@ -321,10 +408,8 @@ tq_status tq_kv_cache_carve(tq_kv_cache* cache, void* base, int32_t batch, int32
 
 namespace {
 
-tq_status check_append_args(const tq_kv_cache* cache, const uint16_t* k_new, const uint16_t* v_new, int32_t n_new,
+tq_status check_append_args(const Store* cache, const uint16_t* k_new, const uint16_t* v_new, int32_t n_new,
                             const int32_t* write_pos) {
-    tq_status s = check_cache(cache);
-    if (s != TQ_OK) return s;
     if (k_new == nullptr || v_new == nullptr || write_pos == nullptr) return TQ_ERR_NULL;
     if (!aligned16(k_new) || !aligned16(v_new)) return TQ_ERR_ALIGN;
     if (n_new < 0) return TQ_ERR_SHAPE;
@@ -332,7 +417,7 @@ tq_status check_append_args(const tq_kv_cache* cache, const uint16_t* k_new, con
     return TQ_OK;
 }
 
-tq::AppendParams append_params(const tq_kv_cache* cache, const uint16_t* k_new, const uint16_t* v_new,
+tq::AppendParams append_params(const Store* cache, const uint16_t* k_new, const uint16_t* v_new,
                                int32_t n_new, const int32_t* write_pos, int32_t* status, uint32_t flags = 0) {
     tq::AppendParams p{};
     p.flags = flags;
@@ -352,15 +437,17 @@ tq::AppendParams append_params(const tq_kv_cache* cache, const uint16_t* k_new, 
     p.head_dim = cache->head_dim;
     p.n_new = n_new;
     p.capacity = cache->capacity;
+    p.map = cache->map;
     return p;
 }
 
 bool valid_rotation(uint32_t flags) { return (flags & ~(TQ_ROTATE_K | TQ_ROTATE_V)) == 0; }
+bool valid_step_flags(uint32_t flags) { return valid_rotation(flags & ~TQ_STEP_ADVANCE); }
 
 // Decode (optionally preceded by an append of n_new rows) with the workspace
 // laid out as [m][l][acc][rotated q]; the one path behind tq_decode_step*,
 // tq_sdpa_int4_decode*.
-tq_status decode_path(const tq_kv_cache* cache, const uint16_t* k_new, const uint16_t* v_new, int32_t n_new,
+tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t* v_new, int32_t n_new,
                       const int32_t* write_pos, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
                       int32_t max_seq_len, float attn_scale, int32_t chunk, uint32_t flags, void* workspace,
                       size_t workspace_bytes, uint16_t* out, int32_t* status, tq_impl impl, cudaStream_t st) {
@@ -370,7 +457,10 @@ tq_status decode_path(const tq_kv_cache* cache, const uint16_t* k_new, const uin
         s = check_append_args(cache, k_new, v_new, n_new, write_pos);
         if (s != TQ_OK) return s;
     }
-    if (!valid_impl(impl) || !valid_rotation(flags)) return TQ_ERR_UNSUPPORTED;
+    if (!valid_impl(impl) || !valid_step_flags(flags)) return TQ_ERR_UNSUPPORTED;
+    const bool advance = (flags & TQ_STEP_ADVANCE) != 0;
+    flags &= ~TQ_STEP_ADVANCE;
+    if (advance && (write_pos == nullptr || write_pos == seq_lens)) return TQ_ERR_SHAPE;
     const size_t need =
         tq_sdpa_workspace_bytes(cache->batch, hq, cache->num_kv_heads, cache->head_dim, max_seq_len, chunk);
     if (workspace == nullptr || workspace_bytes < need) return TQ_ERR_WORKSPACE;
@@ -420,7 +510,18 @@ tq_status decode_path(const tq_kv_cache* cache, const uint16_t* k_new, const uin
     r.n_parts = pl.n_splits;
     r.rotate_out = (flags & TQ_ROTATE_V) ? 1 : 0;
     r.rot_scale = rs;
-    return cuda_status(tq::launch_reduce(r, st, true));
+    // TQ_STEP_ADVANCE: the reduce advances the lengths once phase 1 is done
+    // (which covers a fused append); after a separate append kernel a plain
+    // launch after the reduce does it, so that stream order covers that kernel
+    if (advance && (fused || n_new == 0)) {
+        r.adv_seq_lens = const_cast<int32_t*>(seq_lens);
+        r.adv_write_pos = const_cast<int32_t*>(write_pos);
+        r.adv_n = n_new;
+    }
+    s = cuda_status(tq::launch_reduce(r, st, true));
+    if (s != TQ_OK || !advance || fused || n_new == 0) return s;
+    return cuda_status(tq::launch_advance(const_cast<int32_t*>(seq_lens), const_cast<int32_t*>(write_pos),
+                                          cache->batch, n_new, st));
 }
 
 }  // namespace
@@ -429,11 +530,7 @@ extern "C" {
 
 tq_status tq_quantize_kv_append(const tq_kv_cache* cache, const uint16_t* k_new, const uint16_t* v_new,
                                 int32_t n_new, const int32_t* write_pos, int32_t* status, void* stream) {
-    tq_status s = check_append_args(cache, k_new, v_new, n_new, write_pos);
-    if (s != TQ_OK) return s;
-    if (n_new == 0) return TQ_OK;
-    return cuda_status(tq::launch_quantize_append(append_params(cache, k_new, v_new, n_new, write_pos, status),
-                                                  static_cast<cudaStream_t>(stream)));
+    return tq_quantize_kv_append_ex(cache, k_new, v_new, n_new, write_pos, 0u, status, stream);
 }
 
 tq_status tq_decode_step(const tq_kv_cache* cache, const uint16_t* k_new, const uint16_t* v_new, int32_t n_new,
@@ -444,20 +541,28 @@ tq_status tq_decode_step(const tq_kv_cache* cache, const uint16_t* k_new, const 
                              0u, workspace, workspace_bytes, out, status, stream);
 }
 
-tq_status tq_decode_step_ex(const tq_kv_cache* cache, const uint16_t* k_new, const uint16_t* v_new, int32_t n_new,
+tq_status tq_decode_step_ex(const tq_kv_cache* raw, const uint16_t* k_new, const uint16_t* v_new, int32_t n_new,
                             const int32_t* write_pos, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
                             int32_t max_seq_len, float attn_scale, int32_t chunk, uint32_t flags, void* workspace,
                             size_t workspace_bytes, uint16_t* out, int32_t* status, void* stream) {
-    tq_status s = check_append_args(cache, k_new, v_new, n_new, write_pos);
+    Store st;
+    tq_status s = store_of(raw, &st);
+    if (s != TQ_OK) return s;
+    const Store* cache = &st;
+    s = check_append_args(cache, k_new, v_new, n_new, write_pos);
     if (s != TQ_OK) return s;
     return decode_path(cache, k_new, v_new, n_new, write_pos, q, hq, seq_lens, max_seq_len, attn_scale, chunk, flags,
                        workspace, workspace_bytes, out, status, TQ_IMPL_MMA, static_cast<cudaStream_t>(stream));
 }
 
-tq_status tq_quantize_kv_append_ex(const tq_kv_cache* cache, const uint16_t* k_new, const uint16_t* v_new,
+tq_status tq_quantize_kv_append_ex(const tq_kv_cache* raw, const uint16_t* k_new, const uint16_t* v_new,
                                    int32_t n_new, const int32_t* write_pos, uint32_t flags, int32_t* status,
                                    void* stream) {
-    tq_status s = check_append_args(cache, k_new, v_new, n_new, write_pos);
+    Store st;
+    tq_status s = store_of(raw, &st);
+    if (s != TQ_OK) return s;
+    const Store* cache = &st;
+    s = check_append_args(cache, k_new, v_new, n_new, write_pos);
     if (s != TQ_OK) return s;
     if (!valid_rotation(flags)) return TQ_ERR_UNSUPPORTED;
     if (n_new == 0) return TQ_OK;
@@ -489,20 +594,97 @@ size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t hq, int32_t hkv, int32_t h
            align256(static_cast<size_t>(batch) * hq * head_dim * sizeof(uint16_t));
 }
 
-tq_status tq_sdpa_int4_decode_impl(const tq_kv_cache* cache, const uint16_t* q, int32_t hq,
+tq_status tq_sdpa_int4_decode_impl(const tq_kv_cache* raw, const uint16_t* q, int32_t hq,
                                    const int32_t* seq_lens, int32_t max_seq_len, float attn_scale, int32_t chunk,
                                    void* workspace, size_t workspace_bytes, uint16_t* out, int32_t* status,
                                    tq_impl impl, void* stream) {
-    return decode_path(cache, nullptr, nullptr, 0, nullptr, q, hq, seq_lens, max_seq_len, attn_scale, chunk, 0u,
+    Store st;
+    tq_status s = store_of(raw, &st);
+    if (s != TQ_OK) return s;
+    return decode_path(&st, nullptr, nullptr, 0, nullptr, q, hq, seq_lens, max_seq_len, attn_scale, chunk, 0u,
                        workspace, workspace_bytes, out, status, impl, static_cast<cudaStream_t>(stream));
 }
 
-tq_status tq_sdpa_int4_decode_ex(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
+tq_status tq_sdpa_int4_decode_ex(const tq_kv_cache* raw, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
                                  int32_t max_seq_len, float attn_scale, int32_t chunk, uint32_t flags,
                                  void* workspace, size_t workspace_bytes, uint16_t* out, int32_t* status,
                                  void* stream) {
-    return decode_path(cache, nullptr, nullptr, 0, nullptr, q, hq, seq_lens, max_seq_len, attn_scale, chunk, flags,
+    Store st;
+    tq_status s = store_of(raw, &st);
+    if (s != TQ_OK) return s;
+    if (!valid_rotation(flags)) return TQ_ERR_UNSUPPORTED;
+    return decode_path(&st, nullptr, nullptr, 0, nullptr, q, hq, seq_lens, max_seq_len, attn_scale, chunk, flags,
                        workspace, workspace_bytes, out, status, TQ_IMPL_AUTO, static_cast<cudaStream_t>(stream));
+}
+
+size_t tq_paged_kv_cache_bytes(int32_t num_pages, int32_t hkv, int32_t head_dim, int32_t group_size,
+                               int32_t page_tokens) {
+    return tq_kv_cache_bytes(num_pages, hkv, head_dim, group_size, page_tokens);  // a page = one "sequence" row block
+}
+
+tq_status tq_paged_kv_cache_carve(tq_paged_kv_cache* cache, void* base, const int32_t* block_table, int32_t batch,
+                                  int32_t hkv, int32_t head_dim, int32_t group_size, int32_t page_tokens,
+                                  int32_t num_pages, int32_t max_pages_per_seq) {
+    if (cache == nullptr || base == nullptr || block_table == nullptr) return TQ_ERR_NULL;
+    if (batch < 1 || max_pages_per_seq < 1 || page_tokens % kPageTokenMultiple != 0) return TQ_ERR_SHAPE;
+    tq_kv_cache pool;
+    tq_status s = tq_kv_cache_carve(&pool, base, num_pages, hkv, head_dim, group_size, page_tokens);
+    if (s != TQ_OK) return s;
+    cache->k_codes = pool.k_codes;
+    cache->v_codes = pool.v_codes;
+    cache->k_scale = pool.k_scale;
+    cache->k_bias = pool.k_bias;
+    cache->v_scale = pool.v_scale;
+    cache->v_bias = pool.v_bias;
+    cache->block_table = block_table;
+    cache->batch = batch;
+    cache->num_kv_heads = hkv;
+    cache->head_dim = head_dim;
+    cache->group_size = group_size;
+    cache->page_tokens = page_tokens;
+    cache->num_pages = num_pages;
+    cache->max_pages_per_seq = max_pages_per_seq;
+    return TQ_OK;
+}
+
+tq_status tq_paged_quantize_kv_append(const tq_paged_kv_cache* raw, const uint16_t* k_new, const uint16_t* v_new,
+                                      int32_t n_new, const int32_t* write_pos, uint32_t flags, int32_t* status,
+                                      void* stream) {
+    Store st;
+    tq_status s = store_of(raw, &st);
+    if (s != TQ_OK) return s;
+    s = check_append_args(&st, k_new, v_new, n_new, write_pos);
+    if (s != TQ_OK) return s;
+    if (!valid_rotation(flags)) return TQ_ERR_UNSUPPORTED;
+    if (n_new == 0) return TQ_OK;
+    return cuda_status(tq::launch_quantize_append(append_params(&st, k_new, v_new, n_new, write_pos, status, flags),
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
+tq_status tq_paged_sdpa_int4_decode(const tq_paged_kv_cache* raw, const uint16_t* q, int32_t hq,
+                                    const int32_t* seq_lens, int32_t max_seq_len, float attn_scale, int32_t chunk,
+                                    uint32_t flags, void* workspace, size_t workspace_bytes, uint16_t* out,
+                                    int32_t* status, void* stream) {
+    Store st;
+    tq_status s = store_of(raw, &st);
+    if (s != TQ_OK) return s;
+    if (!valid_rotation(flags)) return TQ_ERR_UNSUPPORTED;
+    return decode_path(&st, nullptr, nullptr, 0, nullptr, q, hq, seq_lens, max_seq_len, attn_scale, chunk, flags,
+                       workspace, workspace_bytes, out, status, TQ_IMPL_MMA, static_cast<cudaStream_t>(stream));
+}
+
+tq_status tq_paged_decode_step(const tq_paged_kv_cache* raw, const uint16_t* k_new, const uint16_t* v_new,
+                               int32_t n_new, const int32_t* write_pos, const uint16_t* q, int32_t hq,
+                               const int32_t* seq_lens, int32_t max_seq_len, float attn_scale, int32_t chunk,
+                               uint32_t flags, void* workspace, size_t workspace_bytes, uint16_t* out,
+                               int32_t* status, void* stream) {
+    Store st;
+    tq_status s = store_of(raw, &st);
+    if (s != TQ_OK) return s;
+    s = check_append_args(&st, k_new, v_new, n_new, write_pos);
+    if (s != TQ_OK) return s;
+    return decode_path(&st, k_new, v_new, n_new, write_pos, q, hq, seq_lens, max_seq_len, attn_scale, chunk, flags,
+                       workspace, workspace_bytes, out, status, TQ_IMPL_MMA, static_cast<cudaStream_t>(stream));
 }
 
 tq_status tq_sdpa_int4_decode(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
@@ -520,18 +702,23 @@ tq_status tq_sdpa_plan(const tq_kv_cache* cache, int32_t hq, int32_t max_seq_len
         return TQ_ERR_SHAPE;
     if (!valid_impl(impl)) return TQ_ERR_UNSUPPORTED;
     Plan pl;
-    tq_status s = device_plan(cache, max_seq_len, chunk, impl, &pl);
+    const Store st = shape_of(cache);
+    tq_status s = device_plan(&st, max_seq_len, chunk, impl, &pl);
     if (s != TQ_OK) return s;
     *n_splits = pl.n_splits;
     *max_run_tokens = ceil_div(pl.units, pl.n_splits) * pl.unit_tokens;
     return TQ_OK;
 }
 
-tq_status tq_sdpa_int4_partial(const tq_kv_cache* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
+tq_status tq_sdpa_int4_partial(const tq_kv_cache* raw, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
                                int32_t max_seq_len, float attn_scale, int32_t chunk, int32_t chunks_per_split,
                                float* part_m, float* part_l, float* part_acc, int32_t* status, tq_impl impl,
                                void* stream) {
-    tq_status s = check_decode_args(cache, q, hq, seq_lens, max_seq_len, chunk, part_m);
+    Store st;
+    tq_status s = store_of(raw, &st);
+    if (s != TQ_OK) return s;
+    const Store* cache = &st;
+    s = check_decode_args(cache, q, hq, seq_lens, max_seq_len, chunk, part_m);
     if (s != TQ_OK) return s;
     if (part_l == nullptr || part_acc == nullptr) return TQ_ERR_NULL;
     if (!valid_impl(impl)) return TQ_ERR_UNSUPPORTED;

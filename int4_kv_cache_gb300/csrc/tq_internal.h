@@ -13,6 +13,31 @@ namespace tq {
 
 constexpr int kGroup = 64;
 
+// Where row t of (sequence b, kv head h) lives: in page P of the pool,
+// row (P * num_kv_heads + h) * page_tokens + t % page_tokens, with P =
+// block_table[b * max_pages + t / page_tokens].  A contiguous cache is the
+// special case block_table = null, P = b, page_tokens = capacity.
+struct RowMap {
+    const int32_t* block_table;
+    int32_t page_tokens, max_pages, num_pages;
+};
+
+#ifdef __CUDACC__
+__device__ __forceinline__ long long kv_row(const RowMap& m, int num_kv_heads, int b, int h, int t,
+                                            int32_t* status) {
+    int page = b, tp = t;
+    if (m.block_table != nullptr) {
+        page = __ldg(m.block_table + static_cast<long long>(b) * m.max_pages + t / m.page_tokens);
+        tp = t % m.page_tokens;
+        if (static_cast<unsigned>(page) >= static_cast<unsigned>(m.num_pages)) {
+            if (status != nullptr) atomicOr(status, TQ_DEV_PAGE);
+            page = 0;
+        }
+    }
+    return (static_cast<long long>(page) * num_kv_heads + h) * m.page_tokens + tp;
+}
+#endif
+
 struct AppendParams {
     const uint16_t* k_new;    // [B][Hkv][n_new][D]
     const uint16_t* v_new;
@@ -27,6 +52,7 @@ struct AppendParams {
     int32_t batch, num_kv_heads, head_dim, n_new, capacity;
     uint32_t flags;    // TQ_ROTATE_K / TQ_ROTATE_V: rotate the rows before quantizing them
     float rot_scale;   // fp32 value nearest 1 / sqrt(head_dim)
+    RowMap map;
 };
 
 // Geometry of one phase-1 launch: grid (n_splits, Hkv, B).  The sequence is
@@ -55,6 +81,7 @@ struct DecodeParams {
     // uses any of them waits for the append before it is loaded.
     const int32_t* dep_write_pos;
     int32_t dep_n_new;
+    RowMap map;
     // Fused append (tensor-core kernel only, app.n_new > 0): before reading
     // them, the CTA whose run owns rows [write_pos[b], write_pos[b] + n_new)
     // quantizes k_new / v_new into those rows itself.  A run owns
@@ -87,6 +114,11 @@ struct ReduceParams {
     int32_t batch, num_q_heads, head_dim, n_parts;
     int32_t rotate_out;       // nonzero: out = H (merged output), for a cache whose V rows were rotated
     float rot_scale;
+    // TQ_STEP_ADVANCE: after phase 1 has finished, seq_lens[b] and
+    // write_pos[b] grow by adv_n (written once per sequence)
+    int32_t* adv_seq_lens;
+    int32_t* adv_write_pos;
+    int32_t adv_n;
 };
 
 
@@ -99,6 +131,7 @@ cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, const CUtenso
 // decode kernel then waits only where it reads the appended rows).
 cudaError_t launch_quantize_append_primary(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl_secondary);
+cudaError_t launch_advance(int32_t* seq_lens, int32_t* write_pos, int batch, int n, cudaStream_t stream);
 cudaError_t launch_dequant(const DequantParams& p, int sm_count, cudaStream_t stream);
 // out[r] = fp16(H x[r]) for rows of `dim` fp16 values (dim 64 / 128 / 256); out may be x.
 cudaError_t launch_rotate_rows(const uint16_t* x, long long rows, int dim, uint16_t* out, float scale,

@@ -195,3 +195,44 @@ def test_rotation_argument_errors_launch_nothing(L):
              0x400000, None, None) == 6
     assert d(ctypes.byref(c), 0x100000, 8, 0x200000, 256, ctypes.c_float(0.1), 512, 1, 0x300000, 16, 0x400000,
              None, None) == 4
+
+
+def _fake_paged(B=2, Hkv=2, D=128, P=128, pages=8, maxp=4):
+    c = tq.tq_paged_kv_cache()
+    base = 1 << 20
+    for i, f in enumerate(("k_codes", "v_codes", "k_scale", "k_bias", "v_scale", "v_bias", "block_table")):
+        setattr(c, f, base + i * (1 << 20))
+    c.batch, c.num_kv_heads, c.head_dim, c.group_size = B, Hkv, D, 64
+    c.page_tokens, c.num_pages, c.max_pages_per_seq = P, pages, maxp
+    return c
+
+
+def test_paged_pool_bytes_and_carve(L):
+    # a page is one [Hkv][page_tokens] block of the six arrays
+    assert tq.lib().tq_paged_kv_cache_bytes(10, 8, 128, 64, 256) == tq.tq_kv_cache_bytes(10, 8, 128, 64, 256)
+    c = tq.tq_paged_kv_cache()
+    assert L.tq_paged_kv_cache_carve(ctypes.byref(c), 0x100000, 0x2000, 3, 8, 128, 64, 256, 10, 5) == 0
+    rows = 10 * 8 * 256
+    assert c.v_codes - c.k_codes == rows * 64 and c.block_table == 0x2000
+    assert (c.batch, c.page_tokens, c.num_pages, c.max_pages_per_seq) == (3, 256, 10, 5)
+    assert L.tq_paged_kv_cache_carve(ctypes.byref(c), 0x100000, 0x2000, 3, 8, 128, 64, 200, 10, 5) == 2
+    assert L.tq_paged_kv_cache_carve(ctypes.byref(c), 0x100000, None, 3, 8, 128, 64, 256, 10, 5) == 1
+
+
+def test_paged_argument_errors_launch_nothing(L):
+    d = L.tq_paged_sdpa_int4_decode
+    args = lambda c, max_len=256, flags=0: (ctypes.byref(c), 0x100000, 8, 0x200000, max_len, ctypes.c_float(0.1),
+                                            512, flags, 0x300000, 1 << 30, 0x400000, None, None)
+    bad = _fake_paged()
+    bad.block_table = 0
+    assert d(*args(bad)) == 1
+    assert d(*args(_fake_paged(P=192))) == 2                 # pages hold whole 128-token tiles
+    assert d(*args(_fake_paged(), max_len=513)) == 3         # beyond max_pages * page_tokens
+    assert d(*args(_fake_paged(), flags=0x100)) == 6         # no advance on a decode without append
+    s = L.tq_paged_decode_step
+    c = _fake_paged()
+    assert s(ctypes.byref(c), 0x1000, 0x1000, 1, 0x200000, 0x100000, 8, 0x200000, 256, ctypes.c_float(0.1), 512,
+             0x100, 0x300000, 1 << 30, 0x400000, None, None) == 2   # advance with write_pos == seq_lens
+    a = L.tq_paged_quantize_kv_append
+    assert a(ctypes.byref(c), 0x1000, 0x1000, 513, 0x2000, 0, None, None) == 3
+    assert a(ctypes.byref(c), 0x1000, 0x1000, 1, 0x2000, 8, None, None) == 6
