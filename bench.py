@@ -300,6 +300,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_extras:
         extras["full_model_80l"] = run_full_model(args, tq, synth, torch, dev, peak)
+        extras["ragged32_step"] = run_ragged(args, tq, synth, torch, dev, peak)
     st = int(status.item())
 
     # ---- reduce over ranks: max time, summed work
@@ -422,6 +423,71 @@ def run_extras(args, tq, synth, torch, dev, caches, qs, ws, out, peak):
                                                                "frac": round(gbs / peak, 4)}
     res["dequant_sdpa_baseline_128k"] = run_dequant_baseline(args, tq, torch, dev, caches, qs, peak)
     res["hadamard_rotated_128k"] = run_rotation(args, tq, synth, torch, dev, caches, qs, ws, out, peak)
+    return res
+
+
+def run_ragged(args, tq, synth, torch, dev, peak):
+    """32 sequences with lengths uniform in [1K, 32K] (Llama head shape): one
+    decode step = append one token per sequence + decode, K steps replayed
+    from one CUDA graph with the lengths advancing on the device
+    (TQ_STEP_ADVANCE); contiguous cache vs paged cache (256-token pages,
+    shuffled pool, unused logical pages pointing at one scratch page)."""
+    Bt, steps = 32, max(10, args.steps // 2)
+    lens = synth.ragged_lengths(4, Bt, 1024, 32768)
+    cap = 32768 + 256
+    q, k, v, chans = synth.torch_decode_inputs(4, Bt, HQ, HKV, D, 32768, outliers=True, device=dev)
+    kn, vn = [torch.from_numpy(a).to(dev) for a in synth.append_tokens(4, 0, Bt, HKV, D, 1, outliers=chans)]
+    zero = torch.zeros((Bt,), dtype=torch.int32, device=dev)
+    cont = tq.KVCache(Bt, HKV, D, cap, device=dev)
+    tq.tq_quantize_kv_append(cont, k, v, zero)
+    P = 256
+    per = [-(-(int(n) + steps + 1) // P) for n in lens]
+    pages = sum(per) + 1
+    paged = tq.PagedKVCache(Bt, HKV, D, P, pages, cap // P, device=dev)
+    bt = np.full((Bt, cap // P), pages - 1, np.int32)  # scratch page for logical pages past a sequence
+    perm = np.random.default_rng(4).permutation(pages - 1)
+    nxt = 0
+    for b in range(Bt):
+        bt[b, :per[b]] = perm[nxt:nxt + per[b]]
+        nxt += per[b]
+    paged.block_table.copy_(torch.from_numpy(bt))
+    tq.tq_quantize_kv_append(paged, k, v, zero)
+    del k, v
+    max_len = int(lens.max()) + steps + 1
+    ws = torch.empty(tq.tq_sdpa_workspace_bytes(Bt, HQ, HKV, D, max_len, CHUNK), dtype=torch.uint8, device=dev)
+    out = torch.empty((Bt, HQ, D), dtype=torch.float16, device=dev)
+    wp = torch.empty((Bt,), dtype=torch.int32, device=dev)
+    lt = torch.empty_like(wp)
+    h_wp, h_lt = torch.from_numpy(lens.copy()), torch.from_numpy(lens + 1)
+    res = {"sequences": Bt, "tokens": int(lens.sum()), "steps_per_graph": steps, "page_tokens": P,
+           "pages": pages, "contiguous_cache_bytes": cont.nbytes, "paged_pool_bytes": paged.buffer.numel()}
+    for name, c in (("contiguous", cont), ("paged", paged)):
+        wp.copy_(h_wp)
+        lt.copy_(h_lt)
+        step = lambda i: tq.tq_decode_step(c, kn, vn, wp, q, lt, max_len, ATTN, ws, out=out, chunk=CHUNK,
+                                           flags=tq.TQ_STEP_ADVANCE)
+        for i in range(3):
+            step(i)
+        torch.cuda.synchronize()
+        g = capture_graph(torch, step, steps)
+        times = []
+        for rep in range(3):
+            wp.copy_(h_wp)
+            lt.copy_(h_lt)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3 / steps)
+        us = min(times)
+        tok = int(lens.sum()) + Bt * (steps + 1) // 2  # mean length over the replayed steps
+        nbytes = tok * HKV * 2 * (D // 2 + 4 * D // 64) + 2 * Bt * HQ * D * 2 + append_bytes(batch=Bt)
+        res[name] = {"us_per_step": round(us, 2), "GB_per_s": round(nbytes / (us * 1e-6) / 1e9, 1),
+                     "frac": round(nbytes / (us * 1e-6) / 1e9 / peak, 4)}
+    del cont, paged
+    torch.cuda.empty_cache()
     return res
 
 

@@ -162,6 +162,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
     __shared__ uint64_t full_bar[C::STAGES];
     __shared__ unsigned int done_cnt[C::STAGES];  // warps finished with the stage, cumulative
     __shared__ float mrg_m[C::NWC][8], mrg_l[C::NWC][8], mrg_t[C::NWC][8];
+    // paged: the block-table entries of this run's pages, loaded once
+    constexpr int kPageWindow = PAGED ? 256 : 1;
+    __shared__ int32_t page_s[kPageWindow];
     extern __shared__ uint8_t dyn_smem[];
     const uint32_t dyn_base = smem_u32(dyn_smem);
     uint8_t* smem = dyn_smem + ((1024u - (dyn_base & 1023u)) & 1023u);
@@ -174,6 +177,21 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
     const int t_end = min(run_begin(split + 1, p.units, p.n_splits, p.unit_tokens), len);
     const int n_tiles = t_end > t_begin ? (t_end - t_begin + C::T - 1) / C::T : 0;
     const long long row_base = (static_cast<long long>(b) * p.num_kv_heads + kvh) * p.capacity;  // contiguous
+
+    int first_page = 0, n_win = 0;
+    if constexpr (PAGED) {
+        first_page = t_begin / p.map.page_tokens;
+        n_win = t_end > t_begin ? (t_end - 1) / p.map.page_tokens - first_page + 1 : 0;
+        n_win = min(n_win, kPageWindow);
+        for (int i = threadIdx.x; i < n_win; i += C::THREADS) {
+            int pg = __ldg(p.map.block_table + static_cast<long long>(b) * p.map.max_pages + first_page + i);
+            if (static_cast<unsigned>(pg) >= static_cast<unsigned>(p.map.num_pages)) {
+                if (p.status != nullptr) atomicOr(p.status, TQ_DEV_PAGE);
+                pg = 0;
+            }
+            page_s[i] = pg;
+        }
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -224,7 +242,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
         long long row;
         int avail;
         if constexpr (PAGED) {
-            row = kv_row(p.map, p.num_kv_heads, b, kvh, t0, p.status);
+            const int w = t0 / p.map.page_tokens - first_page;
+            row = w < n_win ? (static_cast<long long>(page_s[w]) * p.num_kv_heads + kvh) * p.map.page_tokens +
+                                  t0 % p.map.page_tokens
+                            : kv_row(p.map, p.num_kv_heads, b, kvh, t0, p.status);
             avail = C::T;
         } else {
             row = row_base + t0;

@@ -207,13 +207,21 @@ int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b
 
 // Balanced runs of whole units, about one CTA per resident slot: the unit is
 // the kernel's pipeline tile, or the chunk if that is smaller, so that runs
-// cover the sequence evenly whatever its length in chunks.
+// cover the sequence evenly whatever its length in chunks.  At least
+// kMinRuns runs per (sequence, kv head) when there are enough units: with
+// many sequences the grid then spans several waves, and sequences of
+// different lengths (known only on the device) balance over them -- a batch of
+// 32 sequences of 1K-32K tokens decodes in 133 us instead of 257 us with one
+// run per sequence.
+constexpr long long kMinRuns = 4;
+
 Plan make_plan(int batch, int hkv, int max_seq_len, int chunk, int tile_tokens, int resident) {
     Plan pl;
     pl.unit_tokens = chunk < tile_tokens ? chunk : tile_tokens;
     pl.units = ceil_div(max_seq_len, pl.unit_tokens);
     const long long heads = static_cast<long long>(batch) * hkv;
     long long ns = resident / heads;
+    if (ns < kMinRuns) ns = kMinRuns;
     const long long cap = tq::kMaxDecodeCtas / heads;
     if (ns > cap) ns = cap;
     if (ns > pl.units) ns = pl.units;
