@@ -38,6 +38,10 @@ def lib() -> ctypes.CDLL:
         L.tqo_dequantize_rows.argtypes = [P, P, P, i64, i32, i32, P]
         L.tqo_dequantize_rows_f16.argtypes = [P, P, P, i64, i32, i32, P]
         L.tqo_hadamard_f64.argtypes = [P, i32]
+        L.tqo_quantize_group_b.argtypes = [P, i32, i32, P, P, P]
+        L.tqo_quantize_rows_b.argtypes = [P, i64, i32, i32, i32, P, P, P]
+        L.tqo_dequantize_rows_b.argtypes = [P, P, P, i64, i32, i32, i32, P]
+        L.tqo_attention_b.argtypes = [P, i32, i32, i32, i32, i32, i64, P, P, P, P, P, P, P, f64, P, i64, i32, P]
         L.tqo_hadamard_f32.argtypes = [P, i32]
         L.tqo_rotate_rows_f16.argtypes = [P, i64, i32, P]
         L.tqo_attention.argtypes = [P, i32, i32, i32, i32, i32, i64, P, P, P, P, P, P, P, f64,
@@ -83,36 +87,36 @@ def f16_to_f64(h: np.ndarray) -> np.ndarray:
     return out
 
 
-def quantize_group(x: np.ndarray) -> Tuple[np.ndarray, int, int]:
-    """One group -> (unpacked codes uint8[n], scale bits, bias bits)."""
+def quantize_group(x: np.ndarray, bits: int = 4) -> Tuple[np.ndarray, int, int]:
+    """One group -> (unpacked codes uint8[n], scale bits, bias bits); bits 4 or 8."""
     x = _bits16(x).ravel()
     codes = np.empty(x.size, dtype=np.uint8)
     s = np.zeros(1, dtype=np.uint16)
     b = np.zeros(1, dtype=np.uint16)
-    lib().tqo_quantize_group(_ptr(x), x.size, _ptr(codes), _ptr(s), _ptr(b))
+    lib().tqo_quantize_group_b(_ptr(x), x.size, int(bits), _ptr(codes), _ptr(s), _ptr(b))
     return codes, int(s[0]), int(b[0])
 
 
-def quantize_rows(x: np.ndarray, group: int = 64):
-    """x[..., D] fp16 -> (codes uint8[..., D/2], scale u16[..., D/g], bias u16[..., D/g])."""
+def quantize_rows(x: np.ndarray, group: int = 64, bits: int = 4):
+    """x[..., D] fp16 -> (codes uint8[..., D*bits/8], scale u16[..., D/g], bias u16[..., D/g])."""
     x = _bits16(x)
     D = x.shape[-1]
-    assert D % group == 0 and D % 2 == 0 and D <= 1024
+    assert D % group == 0 and D % 2 == 0 and D <= 1024 and bits in (4, 8)
     rows = x.size // D
-    codes = np.empty(x.shape[:-1] + (D // 2,), dtype=np.uint8)
+    codes = np.empty(x.shape[:-1] + (D * bits // 8,), dtype=np.uint8)
     scale = np.empty(x.shape[:-1] + (D // group,), dtype=np.uint16)
     bias = np.empty_like(scale)
-    lib().tqo_quantize_rows(_ptr(x), rows, D, group, _ptr(codes), _ptr(scale), _ptr(bias))
+    lib().tqo_quantize_rows_b(_ptr(x), rows, D, group, int(bits), _ptr(codes), _ptr(scale), _ptr(bias))
     return codes, scale, bias
 
 
-def dequantize_rows(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray, group: int = 64):
+def dequantize_rows(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray, group: int = 64, bits: int = 4):
     codes = np.ascontiguousarray(codes, dtype=np.uint8)
     scale, bias = _bits16(scale), _bits16(bias)
-    D = codes.shape[-1] * 2
-    rows = codes.size // (D // 2)
+    D = codes.shape[-1] * 8 // bits
+    rows = codes.size // (D * bits // 8)
     out = np.empty(codes.shape[:-1] + (D,), dtype=np.float64)
-    lib().tqo_dequantize_rows(_ptr(codes), _ptr(scale), _ptr(bias), rows, D, group, _ptr(out))
+    lib().tqo_dequantize_rows_b(_ptr(codes), _ptr(scale), _ptr(bias), rows, D, group, int(bits), _ptr(out))
     return out
 
 
@@ -154,23 +158,24 @@ def rotate_rows_f16(x: np.ndarray) -> np.ndarray:
 class Cache:
     """A quantised cache as plain host arrays (oracle side).
 
-    codes: [B, Hkv, cap, D/2] uint8; scale/bias: [B, Hkv, cap, D/group] u16.
+    codes: [B, Hkv, cap, D * bits / 8] uint8 (bits 4: two codes per byte; 8: one);
+    scale/bias: [B, Hkv, cap, D/group] u16.
     """
 
-    def __init__(self, kc, ks, kb, vc, vs, vb, group: int = 64):
+    def __init__(self, kc, ks, kb, vc, vs, vb, group: int = 64, bits: int = 4):
         self.kc = np.ascontiguousarray(kc, dtype=np.uint8)
         self.vc = np.ascontiguousarray(vc, dtype=np.uint8)
         self.ks, self.kb = _bits16(ks), _bits16(kb)
         self.vs, self.vb = _bits16(vs), _bits16(vb)
-        self.group = group
+        self.group, self.bits = group, bits
         self.B, self.Hkv, self.cap = self.kc.shape[:3]
-        self.D = self.kc.shape[3] * 2
+        self.D = self.kc.shape[3] * 8 // bits
 
     @classmethod
-    def from_fp16(cls, k: np.ndarray, v: np.ndarray, group: int = 64) -> "Cache":
-        kc, ks, kb = quantize_rows(k, group)
-        vc, vs, vb = quantize_rows(v, group)
-        return cls(kc, ks, kb, vc, vs, vb, group)
+    def from_fp16(cls, k: np.ndarray, v: np.ndarray, group: int = 64, bits: int = 4) -> "Cache":
+        kc, ks, kb = quantize_rows(k, group, bits)
+        vc, vs, vb = quantize_rows(v, group, bits)
+        return cls(kc, ks, kb, vc, vs, vb, group, bits)
 
     def _args(self):
         return (_ptr(self.kc), _ptr(self.ks), _ptr(self.kb), _ptr(self.vc), _ptr(self.vs),
@@ -191,8 +196,8 @@ def attention(q: np.ndarray, cache: Cache, lens: np.ndarray, attn_scale: float,
     else:
         arr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int32).reshape(-1, 2))
         pp, n = _ptr(arr), arr.shape[0]
-    lib().tqo_attention(_ptr(q), B, Hq, cache.Hkv, D, cache.group, cache.cap, *cache._args(),
-                        _ptr(lens), float(attn_scale), pp, n, _ptr(out))
+    lib().tqo_attention_b(_ptr(q), B, Hq, cache.Hkv, D, cache.group, cache.cap, *cache._args(),
+                          _ptr(lens), float(attn_scale), pp, n, int(cache.bits), _ptr(out))
     return out
 
 
@@ -207,6 +212,7 @@ def attention_partials(q: np.ndarray, cache: Cache, lens: np.ndarray, attn_scale
     m = np.empty((B, Hq, n_chunks))
     l = np.empty((B, Hq, n_chunks))
     acc = np.empty((B, Hq, n_chunks, D))
+    assert cache.bits == 4, "per-chunk partials are kept for the int4 cache"
     a = cache._args()
     lib().tqo_attention_partials(_ptr(q), B, Hq, cache.Hkv, D, cache.group, cache.cap, *a,
                                  _ptr(lens), float(attn_scale), chunk, n_chunks, _ptr(m),

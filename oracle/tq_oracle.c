@@ -82,8 +82,11 @@ void tqo_f16_to_f64_array(const uint16_t* h, int64_t n, double* out) {
 /* bias; [TQ] group 64).  Steps in the order fixed by the header.             */
 /* ------------------------------------------------------------------------ */
 
-void tqo_quantize_group(const uint16_t* x, int n, uint8_t* codes,
-                        uint16_t* scale, uint16_t* bias) {
+/* levels = 2^bits - 1 codes above zero: 15 for int4 ([G4] Background), 255
+ * for int8 ([TQ] driver flag --kv-bits {4,8}); the same affine rule. */
+void tqo_quantize_group_b(const uint16_t* x, int n, int bits, uint8_t* codes,
+                          uint16_t* scale, uint16_t* bias) {
+    const float levels = (float)((1 << bits) - 1);
     float mn = INFINITY, mx = -INFINITY;
     for (int i = 0; i < n; ++i) {
         float xi = (float)tqo_f16_to_f64(x[i]); /* exact: every fp16 is a float */
@@ -92,7 +95,7 @@ void tqo_quantize_group(const uint16_t* x, int n, uint8_t* codes,
     }
     if (mn == 0.0f) mn = 0.0f;               /* a zero minimum is stored as +0 */
     volatile float range = mx - mn;          /* one binary32 subtraction */
-    volatile float s32 = range / 15.0f;      /* one binary32 division */
+    volatile float s32 = range / levels;     /* one binary32 division */
     uint16_t sh = tqo_f32_to_f16(s32);
     uint16_t bh = tqo_f32_to_f16(mn);        /* exact: mn is an fp16 value */
     float s = (float)tqo_f16_to_f64(sh);
@@ -109,13 +112,20 @@ void tqo_quantize_group(const uint16_t* x, int n, uint8_t* codes,
         volatile float t = d / s;            /* binary32 division */
         float r = rintf(t);                  /* default rounding mode: nearest-even */
         if (r < 0.0f) r = 0.0f;
-        if (r > 15.0f) r = 15.0f;
+        if (r > levels) r = levels;
         codes[i] = (uint8_t)r;
     }
 }
 
-void tqo_quantize_rows(const uint16_t* x, int64_t rows, int D, int group,
-                       uint8_t* codes_packed, uint16_t* scale, uint16_t* bias) {
+void tqo_quantize_group(const uint16_t* x, int n, uint8_t* codes,
+                        uint16_t* scale, uint16_t* bias) {
+    tqo_quantize_group_b(x, n, 4, codes, scale, bias);
+}
+
+/* int4: two codes per byte (element 2i in the low nibble of byte i); int8:
+ * one code per byte. */
+void tqo_quantize_rows_b(const uint16_t* x, int64_t rows, int D, int group, int bits,
+                         uint8_t* codes_packed, uint16_t* scale, uint16_t* bias) {
     int ng = D / group;
 #ifdef _OPENMP
 #pragma omp parallel for schedule(static)
@@ -123,8 +133,12 @@ void tqo_quantize_rows(const uint16_t* x, int64_t rows, int D, int group,
     for (int64_t r = 0; r < rows; ++r) {
         uint8_t codes[1024];
         for (int g = 0; g < ng; ++g) {
-            tqo_quantize_group(x + r * D + (int64_t)g * group, group, codes + g * group,
-                               scale + r * ng + g, bias + r * ng + g);
+            tqo_quantize_group_b(x + r * D + (int64_t)g * group, group, bits, codes + g * group,
+                                 scale + r * ng + g, bias + r * ng + g);
+        }
+        if (bits == 8) {
+            for (int i = 0; i < D; ++i) codes_packed[r * D + i] = codes[i];
+            continue;
         }
         for (int i = 0; i < D / 2; ++i) {
             /* [G4] masks 0xF then 0xF0: the earlier element sits in the low nibble */
@@ -133,22 +147,44 @@ void tqo_quantize_rows(const uint16_t* x, int64_t rows, int D, int group,
     }
 }
 
-static double dequant_one(const uint8_t* row_codes, const uint16_t* row_scale,
-                          const uint16_t* row_bias, int d, int group) {
-    uint8_t byte = row_codes[d / 2];
-    int code = (d & 1) ? (byte >> 4) : (byte & 0xf);
+void tqo_quantize_rows(const uint16_t* x, int64_t rows, int D, int group,
+                       uint8_t* codes_packed, uint16_t* scale, uint16_t* bias) {
+    tqo_quantize_rows_b(x, rows, D, group, 4, codes_packed, scale, bias);
+}
+
+static double dequant_one_b(const uint8_t* row_codes, const uint16_t* row_scale,
+                            const uint16_t* row_bias, int d, int group, int bits) {
+    int code;
+    if (bits == 8) {
+        code = row_codes[d];
+    } else {
+        uint8_t byte = row_codes[d / 2];
+        code = (d & 1) ? (byte >> 4) : (byte & 0xf);
+    }
     int g = d / group;
     return tqo_f16_to_f64(row_scale[g]) * (double)code + tqo_f16_to_f64(row_bias[g]);
+}
+
+static double dequant_one(const uint8_t* row_codes, const uint16_t* row_scale,
+                          const uint16_t* row_bias, int d, int group) {
+    return dequant_one_b(row_codes, row_scale, row_bias, d, group, 4);
+}
+
+void tqo_dequantize_rows_b(const uint8_t* codes_packed, const uint16_t* scale,
+                           const uint16_t* bias, int64_t rows, int D, int group, int bits,
+                           double* out) {
+    int ng = D / group;
+    int64_t row_bytes = (int64_t)D * bits / 8;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int d = 0; d < D; ++d)
+            out[r * D + d] = dequant_one_b(codes_packed + r * row_bytes, scale + r * ng,
+                                           bias + r * ng, d, group, bits);
 }
 
 void tqo_dequantize_rows(const uint8_t* codes_packed, const uint16_t* scale,
                          const uint16_t* bias, int64_t rows, int D, int group,
                          double* out) {
-    int ng = D / group;
-    for (int64_t r = 0; r < rows; ++r)
-        for (int d = 0; d < D; ++d)
-            out[r * D + d] = dequant_one(codes_packed + r * (D / 2), scale + r * ng,
-                                         bias + r * ng, d, group);
+    tqo_dequantize_rows_b(codes_packed, scale, bias, rows, D, group, 4, out);
 }
 
 /* fp16 dequantisation: the float K/V a dequantize-then-SDPA baseline builds
@@ -237,13 +273,14 @@ typedef struct {
     int64_t cap;
     const uint8_t *kc, *vc;
     const uint16_t *ks, *kb, *vs, *vb;
+    int bits; /* 4: two codes per byte; 8: one */
 } cache_view;
 
 static void row_ptrs(const cache_view* c, int b, int kvh, int64_t t,
                      const uint8_t** codes, const uint16_t** s, const uint16_t** bi, int is_v) {
     int ng = c->D / c->group;
     int64_t row = ((int64_t)b * c->Hkv + kvh) * c->cap + t;
-    *codes = (is_v ? c->vc : c->kc) + row * (c->D / 2);
+    *codes = (is_v ? c->vc : c->kc) + row * ((int64_t)c->D * c->bits / 8);
     *s = (is_v ? c->vs : c->ks) + row * ng;
     *bi = (is_v ? c->vb : c->kb) + row * ng;
 }
@@ -255,7 +292,7 @@ static double score(const cache_view* c, const double* qd, int b, int kvh, int64
     const uint16_t *s, *bi;
     row_ptrs(c, b, kvh, t, &codes, &s, &bi, 0);
     double acc = 0.0;
-    for (int d = 0; d < c->D; ++d) acc += qd[d] * dequant_one(codes, s, bi, d, c->group);
+    for (int d = 0; d < c->D; ++d) acc += qd[d] * dequant_one_b(codes, s, bi, d, c->group, c->bits);
     return attn_scale * acc;
 }
 
@@ -264,7 +301,7 @@ static void add_weighted_v(const cache_view* c, int b, int kvh, int64_t t, doubl
     const uint8_t* codes;
     const uint16_t *s, *bi;
     row_ptrs(c, b, kvh, t, &codes, &s, &bi, 1);
-    for (int d = 0; d < c->D; ++d) acc[d] += w * dequant_one(codes, s, bi, d, c->group);
+    for (int d = 0; d < c->D; ++d) acc[d] += w * dequant_one_b(codes, s, bi, d, c->group, c->bits);
 }
 
 static void attend_one(const cache_view* c, const uint16_t* q, int b, int h, int64_t len,
@@ -296,12 +333,12 @@ static void attend_one(const cache_view* c, const uint16_t* q, int b, int h, int
     free(qd);
 }
 
-void tqo_attention(const uint16_t* q, int B, int Hq, int Hkv, int D, int group,
-                   int64_t cap, const uint8_t* kc, const uint16_t* ks,
-                   const uint16_t* kb, const uint8_t* vc, const uint16_t* vs,
-                   const uint16_t* vb, const int32_t* lens, double attn_scale,
-                   const int32_t* pairs, int64_t n_pairs, double* out) {
-    cache_view c = {B, Hq, Hkv, D, group, cap, kc, vc, ks, kb, vs, vb};
+void tqo_attention_b(const uint16_t* q, int B, int Hq, int Hkv, int D, int group,
+                     int64_t cap, const uint8_t* kc, const uint16_t* ks,
+                     const uint16_t* kb, const uint8_t* vc, const uint16_t* vs,
+                     const uint16_t* vb, const int32_t* lens, double attn_scale,
+                     const int32_t* pairs, int64_t n_pairs, int bits, double* out) {
+    cache_view c = {B, Hq, Hkv, D, group, cap, kc, vc, ks, kb, vs, vb, bits};
     int64_t n = pairs ? n_pairs : (int64_t)B * Hq;
 #ifdef _OPENMP
 #pragma omp parallel for schedule(dynamic, 1)
@@ -311,6 +348,15 @@ void tqo_attention(const uint16_t* q, int B, int Hq, int Hkv, int D, int group,
         int h = pairs ? pairs[2 * i + 1] : (int)(i % Hq);
         attend_one(&c, q, b, h, lens[b], attn_scale, out + ((int64_t)b * Hq + h) * D);
     }
+}
+
+void tqo_attention(const uint16_t* q, int B, int Hq, int Hkv, int D, int group,
+                   int64_t cap, const uint8_t* kc, const uint16_t* ks,
+                   const uint16_t* kb, const uint8_t* vc, const uint16_t* vs,
+                   const uint16_t* vb, const int32_t* lens, double attn_scale,
+                   const int32_t* pairs, int64_t n_pairs, double* out) {
+    tqo_attention_b(q, B, Hq, Hkv, D, group, cap, kc, ks, kb, vc, vs, vb, lens, attn_scale, pairs,
+                    n_pairs, 4, out);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -326,7 +372,7 @@ void tqo_attention_partials(const uint16_t* q, int B, int Hq, int Hkv, int D,
                             const uint16_t* vb, const int32_t* lens,
                             double attn_scale, int chunk, int n_chunks,
                             double* part_m, double* part_l, double* part_acc) {
-    cache_view c = {B, Hq, Hkv, D, group, cap, kc, vc, ks, kb, vs, vb};
+    cache_view c = {B, Hq, Hkv, D, group, cap, kc, vc, ks, kb, vs, vb, 4};
     int G = Hq / Hkv;
 #ifdef _OPENMP
 #pragma omp parallel for schedule(dynamic, 1)

@@ -74,6 +74,21 @@ void tqo_dequantize_rows_f16(const uint8_t* codes_packed, const uint16_t* scale,
                              const uint16_t* bias, int64_t rows, int D, int group,
                              uint16_t* out);
 
+/* The same with a code width: bits = 4 (levels 15, two codes per byte) or 8
+ * (levels 255, one code per byte); the functions above are bits = 4. */
+void tqo_quantize_group_b(const uint16_t* x, int n, int bits, uint8_t* codes,
+                          uint16_t* scale, uint16_t* bias);
+void tqo_quantize_rows_b(const uint16_t* x, int64_t rows, int D, int group, int bits,
+                         uint8_t* codes_packed, uint16_t* scale, uint16_t* bias);
+void tqo_dequantize_rows_b(const uint8_t* codes_packed, const uint16_t* scale,
+                           const uint16_t* bias, int64_t rows, int D, int group, int bits,
+                           double* out);
+void tqo_attention_b(const uint16_t* q, int B, int Hq, int Hkv, int D, int group,
+                     int64_t cap, const uint8_t* kc, const uint16_t* ks,
+                     const uint16_t* kb, const uint8_t* vc, const uint16_t* vs,
+                     const uint16_t* vb, const int32_t* lens, double attn_scale,
+                     const int32_t* pairs, int64_t n_pairs, int bits, double* out);
+
 /* Normalised Sylvester Hadamard transform in place, n a power of two:
  * x <- (1/sqrt(n)) H_n x by the fast transform (stages h = 1, 2, ..., n/2).
  * The f64 form is the reference; the f32 form performs the same operations in

@@ -439,3 +439,69 @@ def test_rotate_rows_f16_is_rounded_fp32_transform():
     e = np.zeros((1, 64), np.float16)
     e[0, 5] = 8.0                                                    # 8 / sqrt(64) = 1
     assert np.array_equal(np.abs(oracle.rotate_rows_f16(e).astype(np.float64)), np.ones((1, 64)))
+
+
+# --------------------------------------------------------------------------
+# int8 codes ("Running and Evaluating TurboQuant optimized Gemma 4", driver
+# flags --kv-bits {4,8}): the same affine rule with 255 levels
+# --------------------------------------------------------------------------
+
+def test_int8_grid_values_and_ties():
+    # four groups of 64 cover codes 0..255 on the grid -1 + k/128 (exact in fp16),
+    # each holding both ends so that scale = (max - min)/255 = 1/128 exactly
+    ks = np.arange(256)
+    for part in range(4):
+        k = np.concatenate([[0, 255], ks[part * 62:(part + 1) * 62]])[:64]
+        if k.size < 64:
+            k = np.concatenate([k, np.full(64 - k.size, 7)])
+        x = (-1.0 + k / 128.0).astype(np.float16)
+        assert np.array_equal(x.astype(np.float64), -1.0 + k / 128.0)
+        codes, s, b = oracle.quantize_group(x, bits=8)
+        assert np.uint16(s).view(np.float16) == np.float16(1 / 128) and np.uint16(b).view(np.float16) == -1
+        assert np.array_equal(codes, k)
+    # exact midpoints k + 0.5 round to the even neighbour
+    half = np.array([0.5, 1.5, 2.5, 100.5, 101.5, 253.5, 254.5])
+    k = np.concatenate([[0, 255], half, np.full(64 - 2 - half.size, 9)])
+    x = (-1.0 + k / 128.0).astype(np.float16)
+    assert np.array_equal(x.astype(np.float64), -1.0 + k / 128.0)
+    codes, _, _ = oracle.quantize_group(x, bits=8)
+    assert list(codes[2:2 + half.size]) == [0, 2, 2, 100, 102, 254, 254]
+
+
+def test_int8_round_trip_bound_and_ends():
+    rng = np.random.default_rng(31)
+    xs = _random_groups(rng, 2000)
+    codes, sc, bi = oracle.quantize_rows(xs, bits=8)
+    assert codes.shape == xs.shape                                   # one byte per code
+    xh = oracle.dequantize_rows(codes, sc, bi, bits=8)
+    x = xs.astype(np.float64)
+    s = sc.view(np.float16).astype(np.float64)[:, 0]
+    mn, mx = x.min(axis=1), x.max(axis=1)
+    exact = (mx - mn) / 255.0
+    assert np.all(np.abs(s - exact) <= np.maximum(exact * 2.0**-11, 2.0**-25) * (1 + 1e-9))
+    # half a step, plus what the scale's own rounding costs the top codes
+    # (255 |s - (max - min)/255|: large only for subnormal fp16 scales, where
+    # codes past 255 clamp)
+    assert np.all(np.abs(x - xh) <= (s * (0.5 + 1e-5) + 255 * np.abs(s - exact))[:, None] * (1 + 1e-9))
+    assert np.all(np.abs(x - xh)[s >= 2.0**-14] <= s[s >= 2.0**-14, None] * 0.63)
+    rows = np.arange(xs.shape[0])
+    assert np.all(codes[rows, x.argmin(axis=1)] == 0)
+    normal = s >= 2.0**-14                                            # subnormal scales may clamp below 255
+    assert np.all(codes[rows, x.argmax(axis=1)][normal] == 255)
+    # int8 error is about 17x below int4 on the same groups
+    c4, s4, b4 = oracle.quantize_rows(xs)
+    e4 = np.abs(x - oracle.dequantize_rows(c4, s4, b4)).mean()
+    assert np.abs(x - xh).mean() < e4 / 10
+
+
+def test_int8_attention_closed_forms():
+    rng = np.random.default_rng(32)
+    q = rng.standard_normal((1, 4, 64)).astype(np.float16)
+    k = rng.standard_normal((1, 2, 5, 64)).astype(np.float16)
+    v = rng.standard_normal((1, 2, 5, 64)).astype(np.float16)
+    c = oracle.Cache.from_fp16(k, v, bits=8)
+    vh = oracle.dequantize_rows(c.vc, c.vs, c.vb, bits=8)
+    out = oracle.attention(q, c, np.array([1], np.int32), 0.3)      # one token: the value itself
+    assert np.allclose(out[0, :2], vh[0, 0, 0], atol=1e-12) and np.allclose(out[0, 2:], vh[0, 1, 0], atol=1e-12)
+    out0 = oracle.attention(q, c, np.array([5], np.int32), 0.0)     # attn_scale 0: the mean value
+    assert np.allclose(out0[0, 0], vh[0, 0].mean(axis=0), atol=1e-12)
