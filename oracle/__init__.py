@@ -41,6 +41,7 @@ def lib() -> ctypes.CDLL:
         L.tqo_quantize_group_b.argtypes = [P, i32, i32, P, P, P]
         L.tqo_quantize_rows_b.argtypes = [P, i64, i32, i32, i32, P, P, P]
         L.tqo_dequantize_rows_b.argtypes = [P, P, P, i64, i32, i32, i32, P]
+        L.tqo_dequantize_rows_f16_b.argtypes = [P, P, P, i64, i32, i32, i32, P]
         L.tqo_attention_b.argtypes = [P, i32, i32, i32, i32, i32, i64, P, P, P, P, P, P, P, f64, P, i64, i32, P]
         L.tqo_hadamard_f32.argtypes = [P, i32]
         L.tqo_rotate_rows_f16.argtypes = [P, i64, i32, P]
@@ -120,14 +121,14 @@ def dequantize_rows(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray, grou
     return out
 
 
-def dequantize_rows_f16(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray, group: int = 64):
+def dequantize_rows_f16(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray, group: int = 64, bits: int = 4):
     """fp16 bits [.., D] of fp16_rne(fp32(scale * code + bias)) per element."""
     codes = np.ascontiguousarray(codes, dtype=np.uint8)
     scale, bias = _bits16(scale), _bits16(bias)
-    D = codes.shape[-1] * 2
-    rows = codes.size // (D // 2)
+    D = codes.shape[-1] * 8 // bits
+    rows = codes.size // (D * bits // 8)
     out = np.empty(codes.shape[:-1] + (D,), dtype=np.uint16)
-    lib().tqo_dequantize_rows_f16(_ptr(codes), _ptr(scale), _ptr(bias), rows, D, group, _ptr(out))
+    lib().tqo_dequantize_rows_f16_b(_ptr(codes), _ptr(scale), _ptr(bias), rows, D, group, int(bits), _ptr(out))
     return out
 
 

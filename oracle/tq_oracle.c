@@ -192,21 +192,32 @@ void tqo_dequantize_rows(const uint8_t* codes_packed, const uint16_t* scale,
  * cache to float K/V and runs ordinary SDPA).  Reading: one fp32 rounding of
  * scale * code + bias (the product is exact in fp32: 11 x 4 significant bits),
  * then RNE to binary16. */
-void tqo_dequantize_rows_f16(const uint8_t* codes_packed, const uint16_t* scale,
-                             const uint16_t* bias, int64_t rows, int D, int group,
-                             uint16_t* out) {
+void tqo_dequantize_rows_f16_b(const uint8_t* codes_packed, const uint16_t* scale,
+                               const uint16_t* bias, int64_t rows, int D, int group, int bits,
+                               uint16_t* out) {
     int ng = D / group;
     for (int64_t r = 0; r < rows; ++r) {
-        const uint8_t* rc = codes_packed + r * (D / 2);
+        const uint8_t* rc = codes_packed + r * ((int64_t)D * bits / 8);
         for (int d = 0; d < D; ++d) {
-            uint8_t byte = rc[d / 2];
-            int code = (d & 1) ? (byte >> 4) : (byte & 0xf);
+            int code;
+            if (bits == 8) {
+                code = rc[d];
+            } else {
+                uint8_t byte = rc[d / 2];
+                code = (d & 1) ? (byte >> 4) : (byte & 0xf);
+            }
             int g = d / group;
             float sc = (float)tqo_f16_to_f64(scale[r * ng + g]);
             float bi = (float)tqo_f16_to_f64(bias[r * ng + g]);
             out[r * D + d] = tqo_f32_to_f16(fmaf(sc, (float)code, bi));
         }
     }
+}
+
+void tqo_dequantize_rows_f16(const uint8_t* codes_packed, const uint16_t* scale,
+                             const uint16_t* bias, int64_t rows, int D, int group,
+                             uint16_t* out) {
+    tqo_dequantize_rows_f16_b(codes_packed, scale, bias, rows, D, group, 4, out);
 }
 
 /* ------------------------------------------------------------------------ */

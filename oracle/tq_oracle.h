@@ -80,6 +80,9 @@ void tqo_quantize_group_b(const uint16_t* x, int n, int bits, uint8_t* codes,
                           uint16_t* scale, uint16_t* bias);
 void tqo_quantize_rows_b(const uint16_t* x, int64_t rows, int D, int group, int bits,
                          uint8_t* codes_packed, uint16_t* scale, uint16_t* bias);
+void tqo_dequantize_rows_f16_b(const uint8_t* codes_packed, const uint16_t* scale,
+                               const uint16_t* bias, int64_t rows, int D, int group, int bits,
+                               uint16_t* out);
 void tqo_dequantize_rows_b(const uint8_t* codes_packed, const uint16_t* scale,
                            const uint16_t* bias, int64_t rows, int D, int group, int bits,
                            double* out);

@@ -505,3 +505,19 @@ def test_int8_attention_closed_forms():
     assert np.allclose(out[0, :2], vh[0, 0, 0], atol=1e-12) and np.allclose(out[0, 2:], vh[0, 1, 0], atol=1e-12)
     out0 = oracle.attention(q, c, np.array([5], np.int32), 0.0)     # attn_scale 0: the mean value
     assert np.allclose(out0[0, 0], vh[0, 0].mean(axis=0), atol=1e-12)
+
+
+def test_dequantize_f16_int8_pins():
+    """The fp16 expansion of int8 codes: grid values exact, half an fp16 ulp of
+    the exact value otherwise."""
+    k = np.concatenate([[0, 255], np.arange(1, 63)])
+    x = (-1.0 + k / 128.0).astype(np.float16)
+    c, sc, bi = oracle.quantize_rows(x.reshape(1, 64), bits=8)
+    assert np.array_equal(oracle.dequantize_rows_f16(c, sc, bi, bits=8).view(np.float16).ravel(), x)
+    rng = np.random.default_rng(33)
+    xs = _random_groups(rng, 500)
+    c, sc, bi = oracle.quantize_rows(xs, bits=8)
+    got = oracle.dequantize_rows_f16(c, sc, bi, bits=8).view(np.float16).astype(np.float64)
+    exact = oracle.dequantize_rows(c, sc, bi, bits=8)
+    assert np.all(np.abs(got - exact) <= 0.5 * _ulp16(np.maximum(np.abs(got), np.abs(exact))) +
+                  np.abs(exact) * 2.0**-24)
