@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define TQ_ABI_VERSION 1
+#define TQ_ABI_VERSION 2
 #define TQ_GROUP_SIZE 64
 #define TQ_DEFAULT_CHUNK 512
 
@@ -104,8 +104,8 @@ typedef enum tq_impl {
 } tq_impl;
 
 typedef struct tq_kv_cache {
-    uint8_t* k_codes;  /* [B][Hkv][cap][D/2] */
-    uint8_t* v_codes;  /* [B][Hkv][cap][D/2] */
+    uint8_t* k_codes;  /* [B][Hkv][cap][D * bits / 8] */
+    uint8_t* v_codes;  /* [B][Hkv][cap][D * bits / 8] */
     uint16_t* k_scale; /* [B][Hkv][cap][D/64] fp16 */
     uint16_t* k_bias;
     uint16_t* v_scale;
@@ -115,6 +115,10 @@ typedef struct tq_kv_cache {
     int32_t head_dim;
     int32_t group_size; /* must be 64 */
     int32_t capacity;   /* tokens per (sequence, kv head) */
+    int32_t bits;       /* code width: 4 (two codes per byte, element 2i in the low
+                           nibble of byte i) or 8 (one code per byte; the
+                           TurboQuant Gemma 4 page's --kv-bits 8); head_dim 256
+                           takes 4 only */
 } tq_kv_cache;
 
 /* Paged cache: a pool of pages, each holding page_tokens consecutive tokens of
@@ -127,7 +131,7 @@ typedef struct tq_kv_cache {
  * pages before appending into them; a table entry outside [0, num_pages) sets
  * TQ_DEV_PAGE and page 0 is used instead (no fault). */
 typedef struct tq_paged_kv_cache {
-    uint8_t* k_codes;  /* [num_pages][Hkv][page_tokens][D/2] */
+    uint8_t* k_codes;  /* [num_pages][Hkv][page_tokens][D * bits / 8] */
     uint8_t* v_codes;
     uint16_t* k_scale; /* [num_pages][Hkv][page_tokens][D/64] fp16 */
     uint16_t* k_bias;
@@ -141,6 +145,7 @@ typedef struct tq_paged_kv_cache {
     int32_t page_tokens; /* a multiple of 128 */
     int32_t num_pages;
     int32_t max_pages_per_seq; /* logical capacity = max_pages_per_seq * page_tokens */
+    int32_t bits;              /* code width, as in tq_kv_cache */
 } tq_paged_kv_cache;
 
 /* ABI version of the loaded library (TQ_ABI_VERSION it was built with). */
@@ -164,6 +169,14 @@ size_t tq_kv_cache_bytes(int32_t batch, int32_t num_kv_heads, int32_t head_dim,
 tq_status tq_kv_cache_carve(tq_kv_cache* cache, void* base, int32_t batch,
                             int32_t num_kv_heads, int32_t head_dim,
                             int32_t group_size, int32_t capacity);
+
+/* The same for a code width of `bits` (4 or 8); the two functions above are
+ * bits = 4 (and tq_kv_cache_carve sets cache->bits = 4). */
+size_t tq_kv_cache_bytes_ex(int32_t batch, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t group_size, int32_t bits, int32_t capacity);
+tq_status tq_kv_cache_carve_ex(tq_kv_cache* cache, void* base, int32_t batch,
+                               int32_t num_kv_heads, int32_t head_dim,
+                               int32_t group_size, int32_t bits, int32_t capacity);
 
 /* Quantize-on-store.
  * k_new, v_new: fp16 [batch][num_kv_heads][n_new][head_dim], contiguous.
@@ -200,14 +213,14 @@ tq_status tq_hadamard_rotate(const uint16_t* x, int64_t rows, int32_t dim,
  * Bytes of a page pool for these sizes (the six arrays, each 256-aligned),
  * 0 for invalid sizes.  Host-only. */
 size_t tq_paged_kv_cache_bytes(int32_t num_pages, int32_t num_kv_heads, int32_t head_dim,
-                               int32_t group_size, int32_t page_tokens);
+                               int32_t group_size, int32_t bits, int32_t page_tokens);
 
 /* Fill *cache with the arrays carved from `base` (device, 256-byte aligned,
  * tq_paged_kv_cache_bytes long) and the given block table.  Host-only. */
 tq_status tq_paged_kv_cache_carve(tq_paged_kv_cache* cache, void* base, const int32_t* block_table,
                                   int32_t batch, int32_t num_kv_heads, int32_t head_dim,
-                                  int32_t group_size, int32_t page_tokens, int32_t num_pages,
-                                  int32_t max_pages_per_seq);
+                                  int32_t group_size, int32_t bits, int32_t page_tokens,
+                                  int32_t num_pages, int32_t max_pages_per_seq);
 
 /* tq_quantize_kv_append_ex into a paged cache (rows through the block table). */
 tq_status tq_paged_quantize_kv_append(const tq_paged_kv_cache* cache, const uint16_t* k_new,

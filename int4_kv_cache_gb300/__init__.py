@@ -57,7 +57,7 @@ class tq_kv_cache(ctypes.Structure):
         ("v_scale", ctypes.c_void_p), ("v_bias", ctypes.c_void_p),
         ("batch", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
         ("head_dim", ctypes.c_int32), ("group_size", ctypes.c_int32),
-        ("capacity", ctypes.c_int32),
+        ("capacity", ctypes.c_int32), ("bits", ctypes.c_int32),
     ]
 
 
@@ -70,7 +70,7 @@ class tq_paged_kv_cache(ctypes.Structure):
         ("batch", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
         ("head_dim", ctypes.c_int32), ("group_size", ctypes.c_int32),
         ("page_tokens", ctypes.c_int32), ("num_pages", ctypes.c_int32),
-        ("max_pages_per_seq", ctypes.c_int32),
+        ("max_pages_per_seq", ctypes.c_int32), ("bits", ctypes.c_int32),
     ]
 
 
@@ -108,8 +108,10 @@ def lib() -> ctypes.CDLL:
             "tq_hadamard_rotate": ([P, ctypes.c_int64, i32, P, P], i32),
             "tq_sdpa_int4_decode_ex": ([C, P, i32, P, i32, f32, i32, u32, P, sz, P, P, P], i32),
             "tq_decode_step_ex": ([C, P, P, i32, P, P, i32, P, i32, f32, i32, u32, P, sz, P, P, P], i32),
-            "tq_paged_kv_cache_bytes": ([i32] * 5, sz),
-            "tq_paged_kv_cache_carve": ([PC, P, P] + [i32] * 7, i32),
+            "tq_paged_kv_cache_bytes": ([i32] * 6, sz),
+            "tq_paged_kv_cache_carve": ([PC, P, P] + [i32] * 8, i32),
+            "tq_kv_cache_bytes_ex": ([i32] * 6, sz),
+            "tq_kv_cache_carve_ex": ([C, P] + [i32] * 6, i32),
             "tq_paged_quantize_kv_append": ([PC, P, P, i32, P, u32, P, P], i32),
             "tq_paged_sdpa_int4_decode": ([PC, P, i32, P, i32, f32, i32, u32, P, sz, P, P, P], i32),
             "tq_paged_decode_step": ([PC, P, P, i32, P, P, i32, P, i32, f32, i32, u32, P, sz, P, P, P], i32),
@@ -118,7 +120,7 @@ def lib() -> ctypes.CDLL:
             fn = getattr(L, name)
             fn.argtypes = args
             fn.restype = res
-        if L.tq_abi_version() != 1:
+        if L.tq_abi_version() != 2:
             raise ImportError("libtq.so ABI version mismatch")
         _lib = L
     return _lib
@@ -172,16 +174,17 @@ class KVCache:
     """
 
     def __init__(self, batch: int, num_kv_heads: int, head_dim: int, capacity: int,
-                 device=None, group_size: int = GROUP_SIZE):
-        nbytes = tq_kv_cache_bytes(batch, num_kv_heads, head_dim, group_size, capacity)
+                 device=None, group_size: int = GROUP_SIZE, bits: int = 4):
+        nbytes = int(lib().tq_kv_cache_bytes_ex(batch, num_kv_heads, head_dim, group_size, bits, capacity))
         if nbytes == 0:
             raise ValueError("invalid cache sizes")
         self.buffer = torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
         self.struct = tq_kv_cache()
-        _check("tq_kv_cache_carve", lib().tq_kv_cache_carve(ctypes.byref(self.struct), _ptr(self.buffer), batch,
-                                                             num_kv_heads, head_dim, group_size, capacity))
+        _check("tq_kv_cache_carve_ex", lib().tq_kv_cache_carve_ex(ctypes.byref(self.struct), _ptr(self.buffer),
+                                                                   batch, num_kv_heads, head_dim, group_size, bits,
+                                                                   capacity))
         self.batch, self.num_kv_heads, self.head_dim, self.capacity = batch, num_kv_heads, head_dim, capacity
-        self.group_size = group_size
+        self.group_size, self.bits = group_size, bits
         base = self.buffer.data_ptr()
         rows = batch * num_kv_heads * capacity
         ng = head_dim // group_size
@@ -191,11 +194,12 @@ class KVCache:
             nb = n * torch.empty((), dtype=dtype).element_size()
             return self.buffer[off: off + nb].view(dtype).view(shape)
 
-        cs = (batch, num_kv_heads, capacity, head_dim // 2)
+        cw = head_dim * bits // 8
+        cs = (batch, num_kv_heads, capacity, cw)
         ss = (batch, num_kv_heads, capacity, ng)
         s = self.struct
-        self.k_codes = view(s.k_codes, rows * head_dim // 2, torch.uint8, cs)
-        self.v_codes = view(s.v_codes, rows * head_dim // 2, torch.uint8, cs)
+        self.k_codes = view(s.k_codes, rows * cw, torch.uint8, cs)
+        self.v_codes = view(s.v_codes, rows * cw, torch.uint8, cs)
         self.k_scale = view(s.k_scale, rows * ng, torch.float16, ss)
         self.k_bias = view(s.k_bias, rows * ng, torch.float16, ss)
         self.v_scale = view(s.v_scale, rows * ng, torch.float16, ss)
@@ -222,8 +226,8 @@ class PagedKVCache:
     paged = True
 
     def __init__(self, batch: int, num_kv_heads: int, head_dim: int, page_tokens: int, num_pages: int,
-                 max_pages_per_seq: int, device=None, group_size: int = GROUP_SIZE):
-        nbytes = int(lib().tq_paged_kv_cache_bytes(num_pages, num_kv_heads, head_dim, group_size, page_tokens))
+                 max_pages_per_seq: int, device=None, group_size: int = GROUP_SIZE, bits: int = 4):
+        nbytes = int(lib().tq_paged_kv_cache_bytes(num_pages, num_kv_heads, head_dim, group_size, bits, page_tokens))
         if nbytes == 0:
             raise ValueError("invalid page pool sizes")
         dev = device or "cuda"
@@ -232,11 +236,11 @@ class PagedKVCache:
         self.struct = tq_paged_kv_cache()
         _check("tq_paged_kv_cache_carve", lib().tq_paged_kv_cache_carve(
             ctypes.byref(self.struct), _ptr(self.buffer), _ptr(self.block_table), batch, num_kv_heads, head_dim,
-            group_size, page_tokens, num_pages, max_pages_per_seq))
+            group_size, bits, page_tokens, num_pages, max_pages_per_seq))
         self.batch, self.num_kv_heads, self.head_dim = batch, num_kv_heads, head_dim
         self.page_tokens, self.num_pages, self.max_pages_per_seq = page_tokens, num_pages, max_pages_per_seq
         self.capacity = page_tokens * max_pages_per_seq
-        self.group_size = group_size
+        self.group_size, self.bits = group_size, bits
         base = self.buffer.data_ptr()
         rows = num_pages * num_kv_heads * page_tokens
         ng = head_dim // group_size
@@ -246,11 +250,12 @@ class PagedKVCache:
             nb = n * torch.empty((), dtype=dtype).element_size()
             return self.buffer[off: off + nb].view(dtype).view(shape)
 
-        cs = (num_pages, num_kv_heads, page_tokens, head_dim // 2)
+        cw = head_dim * bits // 8
+        cs = (num_pages, num_kv_heads, page_tokens, cw)
         ss = (num_pages, num_kv_heads, page_tokens, ng)
         st = self.struct
-        self.k_codes = view(st.k_codes, rows * head_dim // 2, torch.uint8, cs)
-        self.v_codes = view(st.v_codes, rows * head_dim // 2, torch.uint8, cs)
+        self.k_codes = view(st.k_codes, rows * cw, torch.uint8, cs)
+        self.v_codes = view(st.v_codes, rows * cw, torch.uint8, cs)
         self.k_scale = view(st.k_scale, rows * ng, torch.float16, ss)
         self.k_bias = view(st.k_bias, rows * ng, torch.float16, ss)
         self.v_scale = view(st.v_scale, rows * ng, torch.float16, ss)

@@ -53,16 +53,18 @@ namespace {
 constexpr uint32_t kLoNib = 0x000F000Fu;  // nibbles at bits 0..3 / 16..19 -> n * 2^-24
 constexpr uint32_t kHiNib = 0x00F000F0u;  // nibbles at bits 4..7 / 20..23 -> 16 n * 2^-24
 constexpr float kLazyMax = 8.0f;          // slack of the running softmax max (log2 units)
-constexpr float kCodeMean = 7.5f;         // mean of a code uniform on 0..15
+constexpr uint32_t kByte = 0x00FF00FFu;   // int8: bytes 0 and 2 of a register -> n * 2^-24
 
-template <int D>
+template <int D, int BITS = 4>
 struct Cfg {
     static constexpr int NG = D / kGroup;          // scale/bias groups per row
-    static constexpr int BPT = D / 2;              // code bytes per token
+    static constexpr int BPT = D * BITS / 8;       // code bytes per token
     static constexpr int SPT = BPT / 16;           // 16-byte segments per token
-    static constexpr int TPR = 128 / BPT;          // tokens per 128-byte swizzle row (D=256: 1)
+    static constexpr int EPS = 128 / BITS;         // elements per 16-byte segment
+    static constexpr int TPR = 128 / BPT;          // tokens per 128-byte swizzle row (1 for 128-byte tokens)
     static constexpr int NWC = 4;                  // warps (all consume; the last to finish a stage refills it)
-    static constexpr int MT = (D == 256) ? 1 : 2;  // 16-token m-tiles per warp per stage
+    static constexpr int MT = (BPT >= 128) ? 1 : 2;  // 16-token m-tiles per warp per stage
+    static constexpr float CODE_MEAN = ((1 << BITS) - 1) * 0.5f;  // mean of a code uniform on 0..L
     static constexpr int T = NWC * MT * 16;        // tokens per stage
     static constexpr int STAGES = 4;
     static constexpr int CODE_BYTES = T * BPT;     // one code tile (K or V)
@@ -71,10 +73,12 @@ struct Cfg {
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // +1024 for base alignment
     static constexpr int THREADS = NWC * 32;
     static constexpr int NKS = D / 16;             // k-steps of the score MMA = m-tiles of P.V
-    static constexpr bool EVEN_ODD = D <= 128;     // token order inside a 16-token tile
-    // Resident CTAs per SM: 3 for D = 128 (shared memory: 4 stages of 18 KB
-    // each), 4 for D = 64 (whose stages are half as large), 2 for D = 256.
-    static constexpr int MIN_CTAS = (D == 256) ? 2 : (D == 128 ? 3 : 4);
+    static constexpr bool EVEN_ODD = TPR >= 2;     // token order inside a 16-token tile
+    // Resident CTAs per SM: 3 for int4 D = 128 (shared memory: 4 stages of 18
+    // KB each) and for int8, 4 for int4 D = 64 (whose stages are half as
+    // large), 2 for D = 256.
+    static constexpr int MIN_CTAS = (D == 256) ? 2 : ((D == 128 || BITS == 8) ? 3 : 4);
+    static_assert(BPT <= 128, "a token's codes fit one 128-byte swizzle row");
     static_assert(CODE_BYTES % 1024 == 0, "code tiles must keep the 1024-byte swizzle period");
     static_assert(STAGES * STAGE_BYTES >= NWC * 8 * D * 4, "merge buffer must fit in the stages");
 };
@@ -83,17 +87,26 @@ struct Cfg {
 // 0..7 take the even tokens and rows 8..15 the odd ones, so that the eight
 // rows of every ldmatrix fall into eight different 16-byte bank groups of the
 // swizzled tile and a C-fragment row pair (m, m+8) is two adjacent tokens.
-template <int D>
+// Merge-buffer layout: element d of head h = 2 tig + hh is stored at h * D +
+// (d ^ merge_xor(tig)), which spreads the four tig lanes of each store over
+// different banks (int4 rows d = 32s + 4gid + 2j: flip bits 0-1; int8 rows
+// d = 16i + 2gid: flip bit 0 and bit 4).
+template <int BITS>
+__device__ __forceinline__ int merge_xor(int tig) {
+    if constexpr (BITS == 8) return (tig & 1) | ((tig >> 1) << 4);
+    else return tig;
+}
+
+template <class C>
 __device__ __forceinline__ int tok_of_row(int m) {
-    if constexpr (Cfg<D>::EVEN_ODD) return m < 8 ? 2 * m : 2 * (m - 8) + 1;
+    if constexpr (C::EVEN_ODD) return m < 8 ? 2 * m : 2 * (m - 8) + 1;
     else return m;
 }
 
 // Shared address of 16-byte segment `seg` of token `tok` in a code tile laid
 // out by a TMA box of 128-byte rows with CU_TENSOR_MAP_SWIZZLE_128B.
-template <int D>
+template <class C>
 __device__ __forceinline__ uint32_t code_addr(uint32_t tile, int tok, int seg) {
-    using C = Cfg<D>;
     const int row = tok / C::TPR;
     const int chunk = (tok % C::TPR) * C::SPT + seg;
     return tile + row * 128 + ((chunk ^ (row & 7)) << 4);
@@ -124,16 +137,16 @@ __device__ __forceinline__ void load_row_sb(const uint16_t* base, int tok, float
 
 // NG fp16 values of two token rows; for D <= 128 the rows are adjacent and one
 // load brings both.
-template <int D, int NG>
+template <class C, int NG>
 __device__ __forceinline__ void load_pair_sb(const uint16_t* base, int tok_a, int tok_b, float (&a)[NG],
                                              float (&bb)[NG]) {
-    if constexpr (Cfg<D>::EVEN_ODD && NG == 2) {  // tok_b == tok_a + 1
+    if constexpr (C::EVEN_ODD && NG == 2) {  // tok_b == tok_a + 1
         const Half4 h = *reinterpret_cast<const Half4*>(base + tok_a * 2);
         a[0] = __low2float(h.a);
         a[1] = __high2float(h.a);
         bb[0] = __low2float(h.b);
         bb[1] = __high2float(h.b);
-    } else if constexpr (Cfg<D>::EVEN_ODD && NG == 1) {
+    } else if constexpr (C::EVEN_ODD && NG == 1) {
         const __half2 h = *reinterpret_cast<const __half2*>(base + tok_a);
         a[0] = __low2float(h);
         bb[0] = __high2float(h);
@@ -153,11 +166,11 @@ __device__ __forceinline__ int clamp_len(const DecodeParams& p, int b) {
     return len;
 }
 
-template <int D, bool PAGED>
-__global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
+template <int D, bool PAGED, int BITS>
+__global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const DecodeParams p) {
-    using C = Cfg<D>;
+    using C = Cfg<D, BITS>;
     constexpr int NG = C::NG;
     __shared__ uint64_t full_bar[C::STAGES];
     __shared__ unsigned int done_cnt[C::STAGES];  // warps finished with the stage, cumulative
@@ -298,6 +311,19 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
         const __half sixteenth = __float2half_rn(0.0625f);
 #pragma unroll
         for (int g = 0; g < NG; ++g) qsum_own[g] = 0.0f;
+        if constexpr (BITS == 8) {
+            // segment s = dims 16s .. 16s+15; k-step s: k=2tig,2tig+1 <- dims +4tig, +4tig+2;
+            // k=2tig+8,+9 <- dims +4tig+1, +4tig+3 (bytes 0, 2 and 1, 3 of a register)
+#pragma unroll
+            for (int s = 0; s < C::SPT; ++s) {
+                uint2 raw = hv ? *reinterpret_cast<const uint2*>(qrow + 16 * s + 4 * tig) : make_uint2(0, 0);
+                const __half* h = reinterpret_cast<const __half*>(&raw);
+                qb[s][0] = pack_half2_bits(h[0], h[2]);
+                qb[s][1] = pack_half2_bits(h[1], h[3]);
+                qsum_own[(16 * s) / kGroup] +=
+                    (__half2float(h[0]) + __half2float(h[1])) + (__half2float(h[2]) + __half2float(h[3]));
+            }
+        } else {
 #pragma unroll
         for (int s = 0; s < C::SPT; ++s) {
             uint4 raw = hv ? *reinterpret_cast<const uint4*>(qrow + 32 * s + 8 * tig) : make_uint4(0, 0, 0, 0);
@@ -313,6 +339,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
             for (int j = 0; j < 8; ++j) part += __half2float(h[j]);
             qsum_own[(32 * s) / kGroup] += part;
         }
+        }
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
             qsum_own[g] += __shfl_xor_sync(0xffffffffu, qsum_own[g], 1);
@@ -327,7 +354,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
         qs_l2[g][1] = __shfl_sync(0xffffffffu, qsum_own[g], (2 * tig + 1) * 4) * sl2;
     }
     const float k_coef = sl2 * 16777216.0f;  // undo the 2^-24 of the subnormal operands
-    const int r0 = tok_of_row<D>(gid), r1 = tok_of_row<D>(gid + 8);
+    const int r0 = tok_of_row<C>(gid), r1 = tok_of_row<C>(gid + 8);
 
     float m_run[2] = {-INFINITY, -INFINITY};  // reference max of l, acc (lazy)
     float m_true[2] = {-INFINITY, -INFINITY}; // this thread's largest score so far
@@ -347,14 +374,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
             const bool valid = task < app_tasks;
             uint4 raw = app_raw;
             if (t0 > 0 && valid) raw = __ldcs(reinterpret_cast<const uint4*>(app_src(task)));
-            const GroupQ gq = quantize_lane8(raw);
+            const GroupQ<BITS> gq = quantize_lane8<BITS>(raw);
             if (valid) {
                 const int kv = task & 1, g = (task >> 1) % NG, r = app_lo + (task >> 1) / NG;
                 long long row;
                 if constexpr (PAGED) row = kv_row(p.map, p.num_kv_heads, b, kvh, r, p.status);
                 else row = row_base + r;
-                *reinterpret_cast<uint32_t*>((kv ? p.app.v_codes : p.app.k_codes) + row * (D / 2) +
-                                             g * (kGroup / 2) + app_part * 4) = gq.codes;
+                uint8_t* dst = (kv ? p.app.v_codes : p.app.k_codes) + row * C::BPT + g * (kGroup * BITS / 8) +
+                               app_part * BITS;  // this lane's 8 codes: BITS bytes
+                if constexpr (BITS == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(gq.codes[0], gq.codes[1]);
+                else *reinterpret_cast<uint32_t*>(dst) = gq.codes[0];
                 if (app_part == 0) {
                     (kv ? p.app.v_scale : p.app.k_scale)[row * NG + g] = __half_as_ushort(gq.scale);
                     (kv ? p.app.v_bias : p.app.k_bias)[row * NG + g] = __half_as_ushort(gq.bias);
@@ -381,7 +410,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
 
     // ldmatrix row address pattern: lane -> (matrix, row)
     const int lm_mat = lane >> 3, lm_row = lane & 7;
-    const int lm_tok = tok_of_row<D>((lm_mat & 1) * 8 + lm_row);  // token within the 16-token tile
+    const int lm_tok = tok_of_row<C>((lm_mat & 1) * 8 + lm_row);  // token within the 16-token tile
     const int lm_seg = lm_mat >> 1;                                // first or second segment
     // per-lane ldmatrix offset inside a 16-token tile for each segment pair.
     // A tile starting at token tb begins at swizzle row tb / TPR; its phase
@@ -389,7 +418,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
     // for D >= 128, where a tile covers a multiple of 8 rows).
     uint32_t lm_off[C::SPT / 2];
 #pragma unroll
-    for (int sp = 0; sp < C::SPT / 2; ++sp) lm_off[sp] = code_addr<D>(0u, lm_tok, 2 * sp + lm_seg);
+    for (int sp = 0; sp < C::SPT / 2; ++sp) lm_off[sp] = code_addr<C>(0u, lm_tok, 2 * sp + lm_seg);
 
     for (int it = 0; it < n_tiles; ++it) {
         const int stage = it % C::STAGES;
@@ -428,18 +457,25 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
     #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int s = 2 * sp + e;
-                        const int g = (32 * s) / kGroup;
+                        const int g = (C::EPS * s) / kGroup;
                         const uint32_t xa = e ? x2 : x0;  // rows 0..7
                         const uint32_t xb = e ? x3 : x1;  // rows 8..15
-                        mma_16816(cg[g], xa & kLoNib, xb & kLoNib, xa & kHiNib, xb & kHiNib, qb[2 * s][0], qb[2 * s][1]);
-                        const uint32_t ya = xa >> 8, yb = xb >> 8;
-                        mma_16816(cg[g], ya & kLoNib, yb & kLoNib, ya & kHiNib, yb & kHiNib, qb[2 * s + 1][0],
-                                  qb[2 * s + 1][1]);
+                        if constexpr (BITS == 8) {
+                            // bytes 0, 2 -> k 2tig, 2tig+1; bytes 1, 3 -> k 2tig+8, 2tig+9
+                            mma_16816(cg[g], xa & kByte, xb & kByte, (xa >> 8) & kByte, (xb >> 8) & kByte, qb[s][0],
+                                      qb[s][1]);
+                        } else {
+                            mma_16816(cg[g], xa & kLoNib, xb & kLoNib, xa & kHiNib, xb & kHiNib, qb[2 * s][0],
+                                      qb[2 * s][1]);
+                            const uint32_t ya = xa >> 8, yb = xb >> 8;
+                            mma_16816(cg[g], ya & kLoNib, yb & kLoNib, ya & kHiNib, yb & kHiNib, qb[2 * s + 1][0],
+                                      qb[2 * s + 1][1]);
+                        }
                     }
                 }
                 float ksa[NG], kba[NG], ksb[NG], kbb[NG];
-                load_pair_sb<D, NG>(ks_s, tb + r0, tb + r1, ksa, ksb);
-                load_pair_sb<D, NG>(kb_s, tb + r0, tb + r1, kba, kbb);
+                load_pair_sb<C, NG>(ks_s, tb + r0, tb + r1, ksa, ksb);
+                load_pair_sb<C, NG>(kb_s, tb + r0, tb + r1, kba, kbb);
                 const bool va = !kTail || t0 + tb + r0 < t_end, vb = !kTail || t0 + tb + r1 < t_end;
     #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
@@ -513,8 +549,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
                 l_run[0] += pr[0] + pr[2];
                 l_run[1] += pr[1] + pr[3];
                 float vsa[NG], vba[NG], vsb[NG], vbb[NG];
-                load_pair_sb<D, NG>(vs_s, tb + r0, tb + r1, vsa, vsb);
-                load_pair_sb<D, NG>(vb_s, tb + r0, tb + r1, vba, vbb);
+                load_pair_sb<C, NG>(vs_s, tb + r0, tb + r1, vsa, vsb);
+                load_pair_sb<C, NG>(vb_s, tb + r0, tb + r1, vba, vbb);
     #pragma unroll
                 for (int g = 0; g < NG; ++g) {
                     // masked rows may hold stale scale/bias bits: select, never multiply
@@ -525,8 +561,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
                     const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
                     e_run[g][0] = fmaf(pr[0], ba, fmaf(pr[2], bb, e_run[g][0]));
                     e_run[g][1] = fmaf(pr[1], ba, fmaf(pr[3], bb, e_run[g][1]));
-                    e_run[g][0] = fmaf(kCodeMean, (q0 - f01.x) + (q2 - f23.x), e_run[g][0]);
-                    e_run[g][1] = fmaf(kCodeMean, (q1 - f01.y) + (q3 - f23.y), e_run[g][1]);
+                    e_run[g][0] = fmaf(C::CODE_MEAN, (q0 - f01.x) + (q2 - f23.x), e_run[g][0]);
+                    e_run[g][1] = fmaf(C::CODE_MEAN, (q1 - f01.y) + (q3 - f23.y), e_run[g][1]);
                     bhi[mt][g][0] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h01));
                     bhi[mt][g][1] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h23));
                 }
@@ -550,7 +586,21 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
     #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int s = 2 * sp + e;
-                    const int g = (32 * s) / kGroup;
+                    const int g = (C::EPS * s) / kGroup;
+                    if constexpr (BITS == 8) {
+                        // A = V^T: low bytes -> dims 16s + 2gid (rows 0..7), high bytes ->
+                        // dims 16s + 2gid + 1 (rows 8..15); tokens in k
+                        float t[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    #pragma unroll
+                        for (int mt = 0; mt < C::MT; ++mt) {
+                            const uint32_t xa = e ? x[mt][2] : x[mt][0];  // tokens of rows 0..7  (k 0..7)
+                            const uint32_t xb = e ? x[mt][3] : x[mt][1];  // tokens of rows 8..15 (k 8..15)
+                            mma_16816(t, xa & kByte, (xa >> 8) & kByte, xb & kByte, (xb >> 8) & kByte,
+                                      bhi[mt][g][0], bhi[mt][g][1]);
+                        }
+    #pragma unroll
+                        for (int c = 0; c < 4; ++c) acc[s][c] = __fadd_rn(acc[s][c], t[c]);
+                    } else {
     #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         float t[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -564,6 +614,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
                         }
     #pragma unroll
                         for (int c = 0; c < 4; ++c) acc[2 * s + j][c] = __fadd_rn(acc[2 * s + j][c], t[c]);
+                    }
                     }
                 }
             }
@@ -609,6 +660,20 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
     float* mrg_acc = reinterpret_cast<float*>(smem);  // [NWC][8][D]
     {
         float* wacc = mrg_acc + warp * 8 * D;
+        if constexpr (BITS == 8) {
+#pragma unroll
+            for (int i = 0; i < C::NKS; ++i) {
+                const int d_lo = 16 * i + 2 * gid;  // fragment row gid (low bytes)
+                const int d_hi = d_lo + 1;          // fragment row gid + 8 (high bytes)
+                const int g = d_lo / kGroup;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int h = 2 * tig + hh, x = merge_xor<BITS>(tig);
+                    wacc[h * D + (d_lo ^ x)] = fmaf(acc[i][hh], 16777216.0f, e_run[g][hh]);
+                    wacc[h * D + (d_hi ^ x)] = fmaf(acc[i][2 + hh], 16777216.0f, e_run[g][hh]);
+                }
+            }
+        } else {
 #pragma unroll
         for (int i = 0; i < C::NKS; ++i) {
             const int s = i >> 1, j = i & 1;
@@ -623,6 +688,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
                 wacc[h * D + (d_lo ^ tig)] = fmaf(acc[i][hh], 16777216.0f, e_run[g][hh]);
                 wacc[h * D + (d_hi ^ tig)] = fmaf(acc[i][2 + hh], 1048576.0f, e_run[g][hh]);
             }
+        }
         }
         if (gid == 0) {
             mrg_m[warp][2 * tig] = m_run[0];
@@ -646,7 +712,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
             for (int w = 0; w < C::NWC; ++w) {
                 const float wt = mrg_m[w][h] == -INFINITY ? 0.0f : ex2_approx(mrg_m[w][h] - M);
                 L = fmaf(wt, mrg_l[w][h], L);
-                A = fmaf(wt, mrg_acc[(w * 8 + h) * D + (d ^ (h >> 1 & 3))], A);
+                A = fmaf(wt, mrg_acc[(w * 8 + h) * D + (d ^ merge_xor<BITS>(h >> 1 & 3))], A);
             }
         }
         const long long ph = (static_cast<long long>(b) * p.num_q_heads + kvh * G + h) * p.n_splits + split;
@@ -658,25 +724,24 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, Cfg<D>::MIN_CTAS)
     }
 }
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, int BITS>
 cudaError_t set_smem_attr() {
     static bool done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-    cudaError_t e =
-        cudaFuncSetAttribute(decode_mma_kernel<D, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<D>::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, PAGED, BITS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, BITS>::SMEM_BYTES);
     if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
     return e;
 }
 
-template <int D>
+template <int D, int BITS>
 cudaError_t launch_d(const DecodeParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v, cudaStream_t stream,
                      bool pdl_secondary) {
-    using C = Cfg<D>;
+    using C = Cfg<D, BITS>;
     const bool paged = p.map.block_table != nullptr;
-    cudaError_t e = paged ? set_smem_attr<D, true>() : set_smem_attr<D, false>();
+    cudaError_t e = paged ? set_smem_attr<D, true, BITS>() : set_smem_attr<D, false, BITS>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_splits, p.num_kv_heads, p.batch);
@@ -688,56 +753,63 @@ cudaError_t launch_d(const DecodeParams& p, const CUtensorMap& tm_k, const CUten
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_secondary ? 1 : 0;
-    if (paged) return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, true>, tm_k, tm_v, p);
-    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, false>, tm_k, tm_v, p);
+    if (paged) return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, true, BITS>, tm_k, tm_v, p);
+    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, false, BITS>, tm_k, tm_v, p);
 }
 
-template <int D>
+template <int D, int BITS>
 int ctas_per_sm_d() {
-    if (set_smem_attr<D, false>() != cudaSuccess) return 1;
+    if (set_smem_attr<D, false, BITS>() != cudaSuccess) return 1;
     int n = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D, false>, Cfg<D>::THREADS,
-                                                  Cfg<D>::SMEM_BYTES);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D, false, BITS>, Cfg<D, BITS>::THREADS,
+                                                  Cfg<D, BITS>::SMEM_BYTES);
     return n > 0 ? n : 1;
 }
 
 }  // namespace
 
-int mma_tile_tokens(int head_dim) {
-    switch (head_dim) {
-        case 64: return Cfg<64>::T;
-        case 128: return Cfg<128>::T;
-        case 256: return Cfg<256>::T;
-        default: return 0;
-    }
+// (head_dim, bits) pairs with a kernel: int4 at 64 / 128 / 256, int8 at 64 / 128
+// (an int8 row of 256 would not fit one 128-byte swizzle row).
+bool mma_supported(int head_dim, int bits) {
+    return (bits == 4 && (head_dim == 64 || head_dim == 128 || head_dim == 256)) ||
+           (bits == 8 && (head_dim == 64 || head_dim == 128));
 }
 
-int mma_smem_bytes(int head_dim) {
-    switch (head_dim) {
-        case 64: return Cfg<64>::SMEM_BYTES;
-        case 128: return Cfg<128>::SMEM_BYTES;
-        case 256: return Cfg<256>::SMEM_BYTES;
-        default: return 0;
-    }
+#define TQ_DISPATCH(EXPR64_4, EXPR128_4, EXPR256_4, EXPR64_8, EXPR128_8, FALLBACK) \
+    if (bits == 8) {                                                              \
+        if (head_dim == 64) return EXPR64_8;                                      \
+        if (head_dim == 128) return EXPR128_8;                                    \
+    } else {                                                                      \
+        if (head_dim == 64) return EXPR64_4;                                      \
+        if (head_dim == 128) return EXPR128_4;                                    \
+        if (head_dim == 256) return EXPR256_4;                                    \
+    }                                                                             \
+    return FALLBACK;
+
+int mma_tile_tokens(int head_dim, int bits) {
+    TQ_DISPATCH(Cfg<64>::T, Cfg<128>::T, Cfg<256>::T, (Cfg<64, 8>::T), (Cfg<128, 8>::T), 0)
 }
 
-int mma_ctas_per_sm(int head_dim) {
-    switch (head_dim) {
-        case 64: return ctas_per_sm_d<64>();
-        case 128: return ctas_per_sm_d<128>();
-        case 256: return ctas_per_sm_d<256>();
-        default: return 1;
-    }
+int mma_smem_bytes(int head_dim, int bits) {
+    TQ_DISPATCH(Cfg<64>::SMEM_BYTES, Cfg<128>::SMEM_BYTES, Cfg<256>::SMEM_BYTES, (Cfg<64, 8>::SMEM_BYTES),
+                (Cfg<128, 8>::SMEM_BYTES), 0)
+}
+
+int mma_ctas_per_sm(int head_dim, int bits) {
+    TQ_DISPATCH((ctas_per_sm_d<64, 4>()), (ctas_per_sm_d<128, 4>()), (ctas_per_sm_d<256, 4>()),
+                (ctas_per_sm_d<64, 8>()), (ctas_per_sm_d<128, 8>()), 1)
 }
 
 cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                               cudaStream_t stream, bool pdl_secondary) {
-    switch (head_dim) {
-        case 64: return launch_d<64>(p, tm_k, tm_v, stream, pdl_secondary);
-        case 128: return launch_d<128>(p, tm_k, tm_v, stream, pdl_secondary);
-        case 256: return launch_d<256>(p, tm_k, tm_v, stream, pdl_secondary);
-        default: return cudaErrorInvalidValue;
-    }
+    const int bits = p.bits;
+    TQ_DISPATCH((launch_d<64, 4>(p, tm_k, tm_v, stream, pdl_secondary)),
+                (launch_d<128, 4>(p, tm_k, tm_v, stream, pdl_secondary)),
+                (launch_d<256, 4>(p, tm_k, tm_v, stream, pdl_secondary)),
+                (launch_d<64, 8>(p, tm_k, tm_v, stream, pdl_secondary)),
+                (launch_d<128, 8>(p, tm_k, tm_v, stream, pdl_secondary)), cudaErrorInvalidValue)
 }
+
+#undef TQ_DISPATCH
 
 }  // namespace tq

@@ -40,6 +40,7 @@ __device__ __forceinline__ void rotate_staged(uint4 (&tile)[32][8], int lane, in
     }
 }
 
+template <int BITS>
 __global__ void __launch_bounds__(kQuantThreads) quantize_append_kernel(const AppendParams p) {
     // staging: per warp and tensor, 32 groups x 8 words of 16 bytes; word w of
     // group r sits at slot w ^ (r & 7), so that the eight lanes of each phase of
@@ -98,19 +99,19 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_append_kernel(const Ap
     const long long dst_row =
         kv_row(p.map, p.num_kv_heads, b, static_cast<int>(bh - static_cast<long long>(b) * p.num_kv_heads), wp + i,
                p.status);
-    const long long code_off = dst_row * (p.head_dim / 2) + g * (kGroup / 2);  // 32-byte aligned
+    const long long code_off = dst_row * (p.head_dim * BITS / 8) + g * (kGroup * BITS / 8);  // 32-byte aligned
     const long long sb = dst_row * ng + g;
 #pragma unroll 1
     for (int t = 0; t < 2; ++t) {
         uint4 x[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) x[j] = stage[warp][t][lane][j ^ (lane & 7)];
-        uint32_t c[8];
+        uint32_t c[2 * BITS];
         __half sc, bi;
-        quantize_group64(x, c, sc, bi);
+        quantize_group64<BITS>(x, c, sc, bi);
         uint4* dst = reinterpret_cast<uint4*>((t ? p.v_codes : p.k_codes) + code_off);
-        dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
-        dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+#pragma unroll
+        for (int w = 0; w < BITS / 2; ++w) dst[w] = make_uint4(c[4 * w], c[4 * w + 1], c[4 * w + 2], c[4 * w + 3]);
         (t ? p.v_scale : p.k_scale)[sb] = __half_as_ushort(sc);
         (t ? p.v_bias : p.k_bias)[sb] = __half_as_ushort(bi);
     }
@@ -123,7 +124,8 @@ cudaError_t launch_quantize_append(const AppendParams& p, cudaStream_t stream) {
     const int block = kQuantThreads;
     const long long blocks = (groups + block - 1) / block;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    quantize_append_kernel<<<static_cast<unsigned>(blocks), block, 0, stream>>>(p);
+    if (p.bits == 8) quantize_append_kernel<8><<<static_cast<unsigned>(blocks), block, 0, stream>>>(p);
+    else quantize_append_kernel<4><<<static_cast<unsigned>(blocks), block, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

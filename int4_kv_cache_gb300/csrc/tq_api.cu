@@ -34,12 +34,13 @@ tq_status check_cache(const tq_kv_cache* c) {
     if (!c->k_codes || !c->v_codes || !c->k_scale || !c->k_bias || !c->v_scale || !c->v_bias) return TQ_ERR_NULL;
     if (c->batch < 1 || c->num_kv_heads < 1 || c->capacity < 16 || c->capacity % 16 != 0) return TQ_ERR_SHAPE;
     if (c->group_size != TQ_GROUP_SIZE || !supported_dim(c->head_dim)) return TQ_ERR_UNSUPPORTED;
+    if (!tq::mma_supported(c->head_dim, c->bits)) return TQ_ERR_UNSUPPORTED;
     if (!aligned16(c->k_codes) || !aligned16(c->v_codes) || !aligned16(c->k_scale) || !aligned16(c->k_bias) ||
         !aligned16(c->v_scale) || !aligned16(c->v_bias))
         return TQ_ERR_ALIGN;
     // index arithmetic is 64-bit, but TMA row coordinates are int32
     const long long rows128 =
-        static_cast<long long>(c->batch) * c->num_kv_heads * c->capacity * (c->head_dim / 2) / 128;
+        static_cast<long long>(c->batch) * c->num_kv_heads * c->capacity * (c->head_dim * c->bits / 8) / 128;
     if (rows128 >= (1LL << 31)) return TQ_ERR_SHAPE;
     return TQ_OK;
 }
@@ -56,7 +57,7 @@ struct Store {
     uint16_t* k_bias;
     uint16_t* v_scale;
     uint16_t* v_bias;
-    int32_t batch, num_kv_heads, head_dim, group_size, capacity;
+    int32_t batch, num_kv_heads, head_dim, group_size, capacity, bits;
     tq::RowMap map;
     bool paged;
 };
@@ -75,6 +76,7 @@ Store shape_of(const tq_kv_cache* c) {
     st.head_dim = c->head_dim;
     st.group_size = c->group_size;
     st.capacity = c->capacity;
+    st.bits = c->bits;
     st.map = {nullptr, c->capacity, 1, c->batch};
     st.paged = false;
     return st;
@@ -98,13 +100,14 @@ tq_status store_of(const tq_paged_kv_cache* c, Store* st) {
     if (c->batch < 1 || c->num_kv_heads < 1 || c->num_pages < 1 || c->max_pages_per_seq < 1) return TQ_ERR_SHAPE;
     if (c->page_tokens < kPageTokenMultiple || c->page_tokens % kPageTokenMultiple != 0) return TQ_ERR_SHAPE;
     if (c->group_size != TQ_GROUP_SIZE || !supported_dim(c->head_dim)) return TQ_ERR_UNSUPPORTED;
+    if (!tq::mma_supported(c->head_dim, c->bits)) return TQ_ERR_UNSUPPORTED;
     if (!aligned16(c->k_codes) || !aligned16(c->v_codes) || !aligned16(c->k_scale) || !aligned16(c->k_bias) ||
         !aligned16(c->v_scale) || !aligned16(c->v_bias))
         return TQ_ERR_ALIGN;
     const long long cap = static_cast<long long>(c->max_pages_per_seq) * c->page_tokens;
     if (cap >= (1LL << 31)) return TQ_ERR_SHAPE;
     const long long rows128 =
-        static_cast<long long>(c->num_pages) * c->num_kv_heads * c->page_tokens * (c->head_dim / 2) / 128;
+        static_cast<long long>(c->num_pages) * c->num_kv_heads * c->page_tokens * (c->head_dim * c->bits / 8) / 128;
     if (rows128 >= (1LL << 31)) return TQ_ERR_SHAPE;
     Store& t = *st;
     t = Store{};
@@ -119,6 +122,7 @@ tq_status store_of(const tq_paged_kv_cache* c, Store* st) {
     t.head_dim = c->head_dim;
     t.group_size = c->group_size;
     t.capacity = static_cast<int32_t>(cap);
+    t.bits = c->bits;
     t.map = {c->block_table, c->page_tokens, c->max_pages_per_seq, c->num_pages};
     t.paged = true;
     return TQ_OK;
@@ -149,7 +153,8 @@ tq_status make_code_map(CUtensorMap* map, const uint8_t* codes, const Store* c, 
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return cuda_status(cudaErrorNotSupported);
     const cuuint64_t rows =
-        static_cast<cuuint64_t>(c->map.num_pages) * c->num_kv_heads * c->map.page_tokens * (c->head_dim / 2) / 128;
+        static_cast<cuuint64_t>(c->map.num_pages) * c->num_kv_heads * c->map.page_tokens * (c->head_dim * c->bits / 8) /
+        128;
     cuuint64_t dims[2] = {128, rows};
     cuuint64_t strides[1] = {128};
     cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
@@ -164,7 +169,7 @@ tq_status make_code_map(CUtensorMap* map, const uint8_t* codes, const Store* c, 
 // ------------------------------------------------------------ device facts --
 struct DeviceFacts {
     int sms = 0;
-    int mma_ctas[3] = {0, 0, 0};  // per head_dim 64 / 128 / 256
+    int mma_ctas[2][3] = {{0, 0, 0}, {0, 0, 0}};  // per code width (4, 8) and head_dim 64 / 128 / 256
     int simt_ctas[3] = {0, 0, 0};
 };
 
@@ -186,7 +191,8 @@ tq_status device_facts(DeviceFacts** out) {
             if (e != cudaSuccess) return cuda_status(e);
             const int dims[3] = {64, 128, 256};
             for (int i = 0; i < 3; ++i) {
-                f.mma_ctas[i] = tq::mma_ctas_per_sm(dims[i]);
+                f.mma_ctas[0][i] = tq::mma_ctas_per_sm(dims[i], 4);
+                if (tq::mma_supported(dims[i], 8)) f.mma_ctas[1][i] = tq::mma_ctas_per_sm(dims[i], 8);
                 f.simt_ctas[i] = tq::simt_ctas_per_sm(dims[i]);
             }
             cudaGetLastError();  // occupancy queries must leave no pending error
@@ -245,8 +251,8 @@ tq_status device_plan(const Store* cache, int max_seq_len, int chunk, tq_impl im
     if (s != TQ_OK) return s;
     const int di = dim_index(cache->head_dim);
     const bool simt = impl == TQ_IMPL_SIMT;
-    const int per_sm = simt ? f->simt_ctas[di] : f->mma_ctas[di];
-    const int tile = simt ? tq::kSimtTileTokens : tq::mma_tile_tokens(cache->head_dim);
+    const int per_sm = simt ? f->simt_ctas[di] : f->mma_ctas[cache->bits == 8 ? 1 : 0][di];
+    const int tile = simt ? tq::kSimtTileTokens : tq::mma_tile_tokens(cache->head_dim, cache->bits);
     if (cache->paged && chunk < tile) chunk = tile;  // runs start on tile (hence page-aligned) boundaries
     *pl = make_plan(cache->batch, cache->num_kv_heads, max_seq_len, chunk, tile, f->sms * per_sm);
     return TQ_OK;
@@ -295,17 +301,19 @@ tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const in
     p.dep_write_pos = dep_write_pos;
     p.dep_n_new = dep_n_new;
     p.map = cache->map;
+    p.bits = cache->bits;
     p.app = {};
     if (fused_append != nullptr) {
         if (impl == TQ_IMPL_SIMT) return TQ_ERR_UNSUPPORTED;
         p.app = *fused_append;
     }
     if (impl == TQ_IMPL_SIMT) {
-        if (cache->paged) return TQ_ERR_UNSUPPORTED;  // the CUDA-core comparison path reads contiguous caches
+        // the CUDA-core comparison path reads contiguous int4 caches
+        if (cache->paged || cache->bits != 4) return TQ_ERR_UNSUPPORTED;
         return cuda_status(tq::launch_decode_simt(p, cache->head_dim, stream));
     }
     CUtensorMap tm_k, tm_v;
-    const int box_rows = tq::mma_tile_tokens(cache->head_dim) * (cache->head_dim / 2) / 128;
+    const int box_rows = tq::mma_tile_tokens(cache->head_dim, cache->bits) * (cache->head_dim * cache->bits / 8) / 128;
     tq_status s = make_code_map(&tm_k, cache->k_codes, cache, box_rows);
     if (s != TQ_OK) return s;
     s = make_code_map(&tm_v, cache->v_codes, cache, box_rows);
@@ -379,23 +387,28 @@ const char* tq_status_string(tq_status s) {
 
 int32_t tq_last_cuda_error(void) { return g_last_cuda_error; }
 
-size_t tq_kv_cache_bytes(int32_t batch, int32_t hkv, int32_t head_dim, int32_t group_size, int32_t capacity) {
+size_t tq_kv_cache_bytes_ex(int32_t batch, int32_t hkv, int32_t head_dim, int32_t group_size, int32_t bits,
+                            int32_t capacity) {
     if (batch < 1 || hkv < 1 || capacity < 1 || head_dim < 2 || head_dim % 2 != 0 || group_size < 1 ||
-        head_dim % group_size != 0)
+        head_dim % group_size != 0 || (bits != 4 && bits != 8))
         return 0;
     const size_t rows = static_cast<size_t>(batch) * hkv * capacity;
-    const size_t codes = align256(rows * (head_dim / 2));
+    const size_t codes = align256(rows * (static_cast<size_t>(head_dim) * bits / 8));
     const size_t sb = align256(rows * (head_dim / group_size) * 2);
     return 2 * codes + 4 * sb;
 }
 
-tq_status tq_kv_cache_carve(tq_kv_cache* cache, void* base, int32_t batch, int32_t hkv, int32_t head_dim,
-                            int32_t group_size, int32_t capacity) {
+size_t tq_kv_cache_bytes(int32_t batch, int32_t hkv, int32_t head_dim, int32_t group_size, int32_t capacity) {
+    return tq_kv_cache_bytes_ex(batch, hkv, head_dim, group_size, 4, capacity);
+}
+
+tq_status tq_kv_cache_carve_ex(tq_kv_cache* cache, void* base, int32_t batch, int32_t hkv, int32_t head_dim,
+                               int32_t group_size, int32_t bits, int32_t capacity) {
     if (cache == nullptr || base == nullptr) return TQ_ERR_NULL;
-    if (tq_kv_cache_bytes(batch, hkv, head_dim, group_size, capacity) == 0) return TQ_ERR_SHAPE;
+    if (tq_kv_cache_bytes_ex(batch, hkv, head_dim, group_size, bits, capacity) == 0) return TQ_ERR_SHAPE;
     if ((reinterpret_cast<uintptr_t>(base) & 255u) != 0) return TQ_ERR_ALIGN;
     const size_t rows = static_cast<size_t>(batch) * hkv * capacity;
-    const size_t codes = align256(rows * (head_dim / 2));
+    const size_t codes = align256(rows * (static_cast<size_t>(head_dim) * bits / 8));
     const size_t sb = align256(rows * (head_dim / group_size) * 2);
     uint8_t* p = static_cast<uint8_t*>(base);
     cache->k_codes = p;
@@ -409,7 +422,13 @@ tq_status tq_kv_cache_carve(tq_kv_cache* cache, void* base, int32_t batch, int32
     cache->head_dim = head_dim;
     cache->group_size = group_size;
     cache->capacity = capacity;
+    cache->bits = bits;
     return TQ_OK;
+}
+
+tq_status tq_kv_cache_carve(tq_kv_cache* cache, void* base, int32_t batch, int32_t hkv, int32_t head_dim,
+                            int32_t group_size, int32_t capacity) {
+    return tq_kv_cache_carve_ex(cache, base, batch, hkv, head_dim, group_size, 4, capacity);
 }
 
 }  // extern "C"
@@ -446,6 +465,7 @@ tq::AppendParams append_params(const Store* cache, const uint16_t* k_new, const 
     p.n_new = n_new;
     p.capacity = cache->capacity;
     p.map = cache->map;
+    p.bits = cache->bits;
     return p;
 }
 
@@ -625,18 +645,18 @@ tq_status tq_sdpa_int4_decode_ex(const tq_kv_cache* raw, const uint16_t* q, int3
                        workspace, workspace_bytes, out, status, TQ_IMPL_AUTO, static_cast<cudaStream_t>(stream));
 }
 
-size_t tq_paged_kv_cache_bytes(int32_t num_pages, int32_t hkv, int32_t head_dim, int32_t group_size,
+size_t tq_paged_kv_cache_bytes(int32_t num_pages, int32_t hkv, int32_t head_dim, int32_t group_size, int32_t bits,
                                int32_t page_tokens) {
-    return tq_kv_cache_bytes(num_pages, hkv, head_dim, group_size, page_tokens);  // a page = one "sequence" row block
+    return tq_kv_cache_bytes_ex(num_pages, hkv, head_dim, group_size, bits, page_tokens);  // a page = one row block
 }
 
 tq_status tq_paged_kv_cache_carve(tq_paged_kv_cache* cache, void* base, const int32_t* block_table, int32_t batch,
-                                  int32_t hkv, int32_t head_dim, int32_t group_size, int32_t page_tokens,
-                                  int32_t num_pages, int32_t max_pages_per_seq) {
+                                  int32_t hkv, int32_t head_dim, int32_t group_size, int32_t bits,
+                                  int32_t page_tokens, int32_t num_pages, int32_t max_pages_per_seq) {
     if (cache == nullptr || base == nullptr || block_table == nullptr) return TQ_ERR_NULL;
     if (batch < 1 || max_pages_per_seq < 1 || page_tokens % kPageTokenMultiple != 0) return TQ_ERR_SHAPE;
     tq_kv_cache pool;
-    tq_status s = tq_kv_cache_carve(&pool, base, num_pages, hkv, head_dim, group_size, page_tokens);
+    tq_status s = tq_kv_cache_carve_ex(&pool, base, num_pages, hkv, head_dim, group_size, bits, page_tokens);
     if (s != TQ_OK) return s;
     cache->k_codes = pool.k_codes;
     cache->v_codes = pool.v_codes;
@@ -652,6 +672,7 @@ tq_status tq_paged_kv_cache_carve(tq_paged_kv_cache* cache, void* base, const in
     cache->page_tokens = page_tokens;
     cache->num_pages = num_pages;
     cache->max_pages_per_seq = max_pages_per_seq;
+    cache->bits = bits;
     return TQ_OK;
 }
 
@@ -785,6 +806,7 @@ tq_status tq_dequantize_kv(const tq_kv_cache* cache, int32_t n_rows, uint16_t* k
     p.head_dim = cache->head_dim;
     p.capacity = cache->capacity;
     p.n_rows = n_rows;
+    p.bits = cache->bits;
     return cuda_status(tq::launch_dequant(p, f->sms, static_cast<cudaStream_t>(stream)));
 }
 

@@ -50,6 +50,7 @@ struct AppendParams {
     uint16_t* v_bias;
     int32_t* status;
     int32_t batch, num_kv_heads, head_dim, n_new, capacity;
+    int32_t bits;      // code width: 4 or 8
     uint32_t flags;    // TQ_ROTATE_K / TQ_ROTATE_V: rotate the rows before quantizing them
     float rot_scale;   // fp32 value nearest 1 / sqrt(head_dim)
     RowMap map;
@@ -88,6 +89,7 @@ struct DecodeParams {
     // [run_begin(s), run_begin(s + 1)); the last run also owns the rows up to
     // the capacity.
     AppendParams app;
+    int32_t bits;             // code width of the cache: 4 or 8
 };
 // Most rows per sequence the decode kernel appends itself; longer appends
 // run the append kernel first.
@@ -103,7 +105,7 @@ struct DequantParams {
     const uint16_t* v_bias;
     uint16_t* k_out;
     uint16_t* v_out;
-    int32_t batch, num_kv_heads, head_dim, capacity, n_rows;
+    int32_t batch, num_kv_heads, head_dim, capacity, n_rows, bits;
 };
 
 struct ReduceParams {
@@ -139,11 +141,13 @@ cudaError_t launch_rotate_rows(const uint16_t* x, long long rows, int dim, uint1
 // fp32 value nearest 1 / sqrt(dim), the rotation's normalisation.
 inline float rotation_scale(int dim) { return static_cast<float>(1.0 / std::sqrt(static_cast<double>(dim))); }
 
-// Tokens per pipeline stage of the tensor-core kernel (tiles are TMA boxes).
-int mma_tile_tokens(int head_dim);
-int mma_smem_bytes(int head_dim);
+// Tokens per pipeline stage of the tensor-core kernel (tiles are TMA boxes),
+// for a code width of `bits` (4 or 8).
+int mma_tile_tokens(int head_dim, int bits);
+int mma_smem_bytes(int head_dim, int bits);
+bool mma_supported(int head_dim, int bits);
 // Resident CTAs per SM of the phase-1 kernels (occupancy API).
-int mma_ctas_per_sm(int head_dim);
+int mma_ctas_per_sm(int head_dim, int bits);
 int simt_ctas_per_sm(int head_dim);
 // Largest n_parts the reduce kernel takes.
 constexpr int kMaxReduceParts = 8192;

@@ -41,7 +41,7 @@ def test_header_declares_the_boundary():
 def test_library_exports_every_declared_symbol(L):
     missing = [n for n in declared_functions() if not hasattr(L, n)]
     assert not missing, missing
-    assert tq.tq_abi_version() == 1
+    assert tq.tq_abi_version() == 2
 
 
 def test_status_strings(L):
@@ -94,6 +94,7 @@ def _fake_cache(B=1, Hkv=2, D=128, cap=256):
     for i, f in enumerate(("k_codes", "v_codes", "k_scale", "k_bias", "v_scale", "v_bias")):
         setattr(c, f, base + i * (1 << 20))
     c.batch, c.num_kv_heads, c.head_dim, c.group_size, c.capacity = B, Hkv, D, 64, cap
+    c.bits = 4
     return c
 
 
@@ -204,19 +205,20 @@ def _fake_paged(B=2, Hkv=2, D=128, P=128, pages=8, maxp=4):
         setattr(c, f, base + i * (1 << 20))
     c.batch, c.num_kv_heads, c.head_dim, c.group_size = B, Hkv, D, 64
     c.page_tokens, c.num_pages, c.max_pages_per_seq = P, pages, maxp
+    c.bits = 4
     return c
 
 
 def test_paged_pool_bytes_and_carve(L):
     # a page is one [Hkv][page_tokens] block of the six arrays
-    assert tq.lib().tq_paged_kv_cache_bytes(10, 8, 128, 64, 256) == tq.tq_kv_cache_bytes(10, 8, 128, 64, 256)
+    assert tq.lib().tq_paged_kv_cache_bytes(10, 8, 128, 64, 4, 256) == tq.tq_kv_cache_bytes(10, 8, 128, 64, 256)
     c = tq.tq_paged_kv_cache()
-    assert L.tq_paged_kv_cache_carve(ctypes.byref(c), 0x100000, 0x2000, 3, 8, 128, 64, 256, 10, 5) == 0
+    assert L.tq_paged_kv_cache_carve(ctypes.byref(c), 0x100000, 0x2000, 3, 8, 128, 64, 4, 256, 10, 5) == 0
     rows = 10 * 8 * 256
     assert c.v_codes - c.k_codes == rows * 64 and c.block_table == 0x2000
     assert (c.batch, c.page_tokens, c.num_pages, c.max_pages_per_seq) == (3, 256, 10, 5)
-    assert L.tq_paged_kv_cache_carve(ctypes.byref(c), 0x100000, 0x2000, 3, 8, 128, 64, 200, 10, 5) == 2
-    assert L.tq_paged_kv_cache_carve(ctypes.byref(c), 0x100000, None, 3, 8, 128, 64, 256, 10, 5) == 1
+    assert L.tq_paged_kv_cache_carve(ctypes.byref(c), 0x100000, 0x2000, 3, 8, 128, 64, 4, 200, 10, 5) == 2
+    assert L.tq_paged_kv_cache_carve(ctypes.byref(c), 0x100000, None, 3, 8, 128, 64, 4, 256, 10, 5) == 1
 
 
 def test_paged_argument_errors_launch_nothing(L):
@@ -236,3 +238,22 @@ def test_paged_argument_errors_launch_nothing(L):
     a = L.tq_paged_quantize_kv_append
     assert a(ctypes.byref(c), 0x1000, 0x1000, 513, 0x2000, 0, None, None) == 3
     assert a(ctypes.byref(c), 0x1000, 0x1000, 1, 0x2000, 8, None, None) == 6
+
+
+def test_int8_sizes_and_validation(L):
+    # int8: D bytes of codes per row instead of D/2
+    B, Hkv, D, cap = 1, 8, 128, 4096
+    rows = B * Hkv * cap
+    assert L.tq_kv_cache_bytes_ex(B, Hkv, D, 64, 8, cap) == 2 * rows * D + 4 * rows * (D // 64) * 2
+    assert L.tq_kv_cache_bytes_ex(B, Hkv, D, 64, 4, cap) == tq.tq_kv_cache_bytes(B, Hkv, D, 64, cap)
+    assert L.tq_kv_cache_bytes_ex(B, Hkv, D, 64, 5, cap) == 0
+    c = tq.tq_kv_cache()
+    assert L.tq_kv_cache_carve_ex(ctypes.byref(c), 0x100000, 2, 8, 128, 64, 8, 64) == 0
+    assert c.bits == 8 and c.v_codes - c.k_codes == 2 * 8 * 64 * 128
+    assert _decode(L, _fake_cache()) != 6
+    bad = _fake_cache(D=256)
+    bad.bits = 8  # an int8 row of 256 bytes: no kernel
+    assert _decode(L, bad) == 6
+    bad = _fake_cache()
+    bad.bits = 0
+    assert _decode(L, bad) == 6
