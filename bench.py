@@ -423,7 +423,48 @@ def run_extras(args, tq, synth, torch, dev, caches, qs, ws, out, peak):
                                                                "frac": round(gbs / peak, 4)}
     res["dequant_sdpa_baseline_128k"] = run_dequant_baseline(args, tq, torch, dev, caches, qs, peak)
     res["hadamard_rotated_128k"] = run_rotation(args, tq, synth, torch, dev, caches, qs, ws, out, peak)
+    res["int8_128k"] = run_int8(args, tq, synth, torch, dev, qs, peak)
     return res
+
+
+def run_int8(args, tq, synth, torch, dev, qs, peak):
+    """The int8 cache (one code per byte) at the same shape: the 128K prefill
+    quantize and the decode step (1-row fused append + decode), K steps from one
+    CUDA graph over 4 rotated layers (4 x 285 MB > L2)."""
+    nl = 4
+    caches, pre_ms = [], []
+    zero = torch.zeros((B,), dtype=torch.int32, device=dev)
+    for layer in range(nl):
+        _, k, v, _ = synth.torch_decode_inputs(SEED + 90 + layer, B, HQ, HKV, D, S, outliers=True, device=dev)
+        c = tq.KVCache(B, HKV, D, S, device=dev, bits=8)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        tq.tq_quantize_kv_append(c, k, v, zero)
+        e1.record()
+        torch.cuda.synchronize()
+        pre_ms.append(e0.elapsed_time(e1))
+        caches.append(c)
+        del k, v
+    k_new = torch.randn((B, HKV, 1, D), device=dev).half()
+    v_new = torch.randn((B, HKV, 1, D), device=dev).half()
+    write_pos = torch.full((B,), S - 1, dtype=torch.int32, device=dev)
+    seq_lens = torch.full((B,), S, dtype=torch.int32, device=dev)
+    ws = torch.empty(tq.tq_sdpa_workspace_bytes(B, HQ, HKV, D, S, CHUNK), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, HQ, D), dtype=torch.float16, device=dev)
+    step_us = time_graph(torch, lambda i: tq.tq_decode_step(caches[i % nl], k_new, v_new, write_pos, qs[i % len(qs)],
+                                                            seq_lens, S, ATTN, ws, out=out, chunk=CHUNK),
+                         max(20, args.steps))
+    cache8 = B * HKV * S * 2 * (D + 4 * (D // 64))
+    step8 = cache8 + 2 * B * HQ * D * 2 + B * HKV * (2 * D * 2 + 2 * (D + 4 * (D // 64)))
+    pre_bytes = B * HKV * S * D * 2 * 2 + cache8
+    pre = statistics.median(pre_ms[1:])
+    del caches
+    torch.cuda.empty_cache()
+    return {"decode_step_us": round(step_us, 3), "bytes_per_step": step8,
+            "decode_step_GB_per_s": round(step8 / (step_us * 1e-6) / 1e9, 1),
+            "decode_step_frac": round(step8 / (step_us * 1e-6) / 1e9 / peak, 4),
+            "prefill_quantize_ms_per_layer": round(pre, 4),
+            "prefill_GB_per_s": round(pre_bytes / (pre * 1e-3) / 1e9, 1)}
 
 
 def run_ragged(args, tq, synth, torch, dev, peak):
