@@ -358,13 +358,16 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
 
     float m_run[2] = {-INFINITY, -INFINITY};  // reference max of l, acc (lazy)
     float m_true[2] = {-INFINITY, -INFINITY}; // this thread's largest score so far
-    float l_run[2] = {0.0f, 0.0f};
-    float e_run[NG][2];
-    float acc[C::NKS][4];
+    // Per-lane state for its two heads (2tig, 2tig+1) as pairs, so that the
+    // fp32 work runs on Blackwell's paired operations (__fadd2_rn and friends:
+    // two independent round-to-nearest results, the same as two scalar ops).
+    float2 l2 = make_float2(0.0f, 0.0f);       // sum of p
+    float2 e2[NG];                             // sum of p * vbias (+ mean-code term) per group
+    float2 acc2[C::NKS][2];                    // P.V code sums: [i][0] = C rows gid, [i][1] = rows gid + 8
 #pragma unroll
-    for (int g = 0; g < NG; ++g) e_run[g][0] = e_run[g][1] = 0.0f;
+    for (int g = 0; g < NG; ++g) e2[g] = make_float2(0.0f, 0.0f);
 #pragma unroll
-    for (int i = 0; i < C::NKS; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+    for (int i = 0; i < C::NKS; ++i) acc2[i][0] = acc2[i][1] = make_float2(0.0f, 0.0f);
 
     // The fused append, part 2: quantize the rows this run owns, publish them
     // to the async proxy, then load the first tiles that use them.
@@ -477,18 +480,21 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
                 load_pair_sb<C, NG>(ks_s, tb + r0, tb + r1, ksa, ksb);
                 load_pair_sb<C, NG>(kb_s, tb + r0, tb + r1, kba, kbb);
                 const bool va = !kTail || t0 + tb + r0 < t_end, vb = !kTail || t0 + tb + r1 < t_end;
+                float2 sa = make_float2(0.0f, 0.0f), sb = make_float2(0.0f, 0.0f);  // (head 2tig, 2tig+1)
     #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float sa = 0.0f, sb = 0.0f;
-    #pragma unroll
-                    for (int g = 0; g < NG; ++g) {
-                        sa = fmaf(ksa[g] * k_coef, cg[g][hh], fmaf(kba[g], qs_l2[g][hh], sa));
-                        sb = fmaf(ksb[g] * k_coef, cg[g][2 + hh], fmaf(kbb[g], qs_l2[g][hh], sb));
-                    }
-                    // masked rows may hold stale bits: select, never compute with them
-                    sc[mt][hh] = va ? sa : -INFINITY;
-                    sc[mt][2 + hh] = vb ? sb : -INFINITY;
+                for (int g = 0; g < NG; ++g) {
+                    const float2 qs = make_float2(qs_l2[g][0], qs_l2[g][1]);
+                    const float ka = ksa[g] * k_coef, kb = ksb[g] * k_coef;
+                    sa = __ffma2_rn(make_float2(ka, ka), make_float2(cg[g][0], cg[g][1]),
+                                    __ffma2_rn(make_float2(kba[g], kba[g]), qs, sa));
+                    sb = __ffma2_rn(make_float2(kb, kb), make_float2(cg[g][2], cg[g][3]),
+                                    __ffma2_rn(make_float2(kbb[g], kbb[g]), qs, sb));
                 }
+                // masked rows may hold stale bits: select, never compute with them
+                sc[mt][0] = va ? sa.x : -INFINITY;
+                sc[mt][1] = va ? sa.y : -INFINITY;
+                sc[mt][2] = vb ? sb.x : -INFINITY;
+                sc[mt][3] = vb ? sb.y : -INFINITY;
             }
 
             // ---- online softmax update over this warp's tokens of the stage.
@@ -515,13 +521,24 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
                     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
                     if (m > m_run[hh]) {
                         const float alpha = m_run[hh] == -INFINITY ? 0.0f : ex2_approx(m_run[hh] - m);
-                        l_run[hh] *= alpha;
+                        if (hh == 0) {
+                            l2.x *= alpha;
     #pragma unroll
-                        for (int g = 0; g < NG; ++g) e_run[g][hh] *= alpha;
+                            for (int g = 0; g < NG; ++g) e2[g].x *= alpha;
     #pragma unroll
-                        for (int i = 0; i < C::NKS; ++i) {
-                            acc[i][hh] *= alpha;
-                            acc[i][2 + hh] *= alpha;
+                            for (int i = 0; i < C::NKS; ++i) {
+                                acc2[i][0].x *= alpha;
+                                acc2[i][1].x *= alpha;
+                            }
+                        } else {
+                            l2.y *= alpha;
+    #pragma unroll
+                            for (int g = 0; g < NG; ++g) e2[g].y *= alpha;
+    #pragma unroll
+                            for (int i = 0; i < C::NKS; ++i) {
+                                acc2[i][0].y *= alpha;
+                                acc2[i][1].y *= alpha;
+                            }
                         }
                         m_run[hh] = m;
                     }
@@ -543,11 +560,12 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
             for (int mt = 0; mt < C::MT; ++mt) {
                 const int tb = (warp * C::MT + mt) * 16;
                 const bool va = !kTail || t0 + tb + r0 < t_end, vb = !kTail || t0 + tb + r1 < t_end;
-                float pr[4];
-    #pragma unroll
-                for (int c = 0; c < 4; ++c) pr[c] = ex2_approx(sc[mt][c] - m_use[c & 1]);
-                l_run[0] += pr[0] + pr[2];
-                l_run[1] += pr[1] + pr[3];
+                const float2 nm = make_float2(-m_use[0], -m_use[1]);
+                const float2 da = __fadd2_rn(make_float2(sc[mt][0], sc[mt][1]), nm);
+                const float2 db = __fadd2_rn(make_float2(sc[mt][2], sc[mt][3]), nm);
+                const float2 pa = make_float2(ex2_approx(da.x), ex2_approx(da.y));  // rows a, heads (2tig, 2tig+1)
+                const float2 pb = make_float2(ex2_approx(db.x), ex2_approx(db.y));  // rows b
+                l2 = __fadd2_rn(l2, __fadd2_rn(pa, pb));
                 float vsa[NG], vba[NG], vsb[NG], vbb[NG];
                 load_pair_sb<C, NG>(vs_s, tb + r0, tb + r1, vsa, vsb);
                 load_pair_sb<C, NG>(vb_s, tb + r0, tb + r1, vba, vbb);
@@ -556,13 +574,13 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
                     // masked rows may hold stale scale/bias bits: select, never multiply
                     const float sa = va ? vsa[g] : 0.0f, sb = vb ? vsb[g] : 0.0f;
                     const float ba = va ? vba[g] : 0.0f, bb = vb ? vbb[g] : 0.0f;
-                    const float q0 = pr[0] * sa, q1 = pr[1] * sa, q2 = pr[2] * sb, q3 = pr[3] * sb;
-                    const __half2 h01 = __floats2half2_rn(q0, q1), h23 = __floats2half2_rn(q2, q3);
+                    const float2 q01 = __fmul2_rn(pa, make_float2(sa, sa)), q23 = __fmul2_rn(pb, make_float2(sb, sb));
+                    const __half2 h01 = __float22half2_rn(q01), h23 = __float22half2_rn(q23);
                     const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-                    e_run[g][0] = fmaf(pr[0], ba, fmaf(pr[2], bb, e_run[g][0]));
-                    e_run[g][1] = fmaf(pr[1], ba, fmaf(pr[3], bb, e_run[g][1]));
-                    e_run[g][0] = fmaf(C::CODE_MEAN, (q0 - f01.x) + (q2 - f23.x), e_run[g][0]);
-                    e_run[g][1] = fmaf(C::CODE_MEAN, (q1 - f01.y) + (q3 - f23.y), e_run[g][1]);
+                    const float2 m1 = make_float2(-1.0f, -1.0f);
+                    e2[g] = __ffma2_rn(pa, make_float2(ba, ba), __ffma2_rn(pb, make_float2(bb, bb), e2[g]));
+                    const float2 r = __fadd2_rn(__ffma2_rn(f01, m1, q01), __ffma2_rn(f23, m1, q23));  // q - fp16(q)
+                    e2[g] = __ffma2_rn(make_float2(C::CODE_MEAN, C::CODE_MEAN), r, e2[g]);
                     bhi[mt][g][0] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h01));
                     bhi[mt][g][1] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h23));
                 }
@@ -599,7 +617,8 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
                                       bhi[mt][g][0], bhi[mt][g][1]);
                         }
     #pragma unroll
-                        for (int c = 0; c < 4; ++c) acc[s][c] = __fadd_rn(acc[s][c], t[c]);
+                        acc2[s][0] = __fadd2_rn(acc2[s][0], make_float2(t[0], t[1]));
+                        acc2[s][1] = __fadd2_rn(acc2[s][1], make_float2(t[2], t[3]));
                     } else {
     #pragma unroll
                     for (int j = 0; j < 2; ++j) {
@@ -613,7 +632,8 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
                             mma_16816(t, a0, a1, a2, a3, bhi[mt][g][0], bhi[mt][g][1]);
                         }
     #pragma unroll
-                        for (int c = 0; c < 4; ++c) acc[2 * s + j][c] = __fadd_rn(acc[2 * s + j][c], t[c]);
+                        acc2[2 * s + j][0] = __fadd2_rn(acc2[2 * s + j][0], make_float2(t[0], t[1]));
+                        acc2[2 * s + j][1] = __fadd2_rn(acc2[2 * s + j][1], make_float2(t[2], t[3]));
                     }
                     }
                 }
@@ -636,6 +656,23 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
                 issue_tile(it + C::STAGES, policy_evict_first());
             }
         }
+    }
+
+    // back to per-head scalars for the epilogue
+    float l_run[2] = {l2.x, l2.y};
+    float e_run[NG][2];
+    float acc[C::NKS][4];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+        e_run[g][0] = e2[g].x;
+        e_run[g][1] = e2[g].y;
+    }
+#pragma unroll
+    for (int i = 0; i < C::NKS; ++i) {
+        acc[i][0] = acc2[i][0].x;
+        acc[i][1] = acc2[i][0].y;
+        acc[i][2] = acc2[i][1].x;
+        acc[i][3] = acc2[i][1].y;
     }
 
     // ---- reduce per-thread sums and maxima over the 8 token rows (lanes differing in gid)
