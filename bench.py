@@ -51,14 +51,18 @@ FULL_MODEL_LAYERS = 80
 PAGES_128K_MS = 9.9
 
 
+# code width of the headline caches (--bits; 4 unless profiling the int8 path)
+CODE_BITS = 4
+
+
 def cache_bytes(seq_len: int, batch: int = B, hkv: int = HKV, d: int = D) -> int:
-    """Algorithmic bytes of the int4 cache rows one decode reads (K and V)."""
-    return batch * seq_len * hkv * 2 * (d // 2 + 4 * (d // 64))
+    """Algorithmic bytes of the cache rows one decode reads (K and V)."""
+    return batch * seq_len * hkv * 2 * (d * CODE_BITS // 8 + 4 * (d // 64))
 
 
 def append_bytes(batch: int = B, hkv: int = HKV, d: int = D, n_new: int = 1) -> int:
     """fp16 K/V of the new tokens in, codes + scale/bias out."""
-    return batch * n_new * hkv * (2 * d * 2 + 2 * (d // 2 + 4 * (d // 64)))
+    return batch * n_new * hkv * (2 * d * 2 + 2 * (d * CODE_BITS // 8 + 4 * (d // 64)))
 
 
 def step_bytes(seq_len: int, batch: int = B, hq: int = HQ, hkv: int = HKV, d: int = D) -> int:
@@ -174,7 +178,7 @@ def make_layer_caches(tq, synth, torch, dev, n_layers, seed0):
     caches, qs, chans_all, prefill_ms = [], [], [], []
     for layer in range(n_layers):
         q, k, v, chans = synth.torch_decode_inputs(seed0 + layer, B, HQ, HKV, D, S, outliers=True, device=dev)
-        c = tq.KVCache(B, HKV, D, S, device=dev)
+        c = tq.KVCache(B, HKV, D, S, device=dev, bits=CODE_BITS)
         wp = torch.zeros(B, dtype=torch.int32, device=dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
@@ -261,23 +265,20 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     del g_steps
     clocks = clk.summary()
 
-    # ---- e2e: through the C ABI from pinned host buffers, result read back every step
+    # ---- e2e: through the C ABI from pinned host buffers, result read back every
+    # step: one tq_decode_step_host call queues the H2D copies of q, k_new,
+    # v_new, the step and the D2H copy of the output
     h_q = [torch.empty((B, HQ, D), dtype=torch.float16).pin_memory() for _ in range(nl)]
     for i in range(nl):
         h_q[i].copy_(qs[i])
     h_k = k_new.cpu().pin_memory()
     h_v = v_new.cpu().pin_memory()
     h_out = torch.empty((B, HQ, D), dtype=torch.float16).pin_memory()
-    d_q = torch.empty((B, HQ, D), dtype=torch.float16, device=dev)
-    d_k, d_v = torch.empty_like(k_new), torch.empty_like(v_new)
+    staging = torch.empty(tq.tq_host_staging_bytes(B, HQ, HKV, D, 1), dtype=torch.uint8, device=dev)
 
     def e2e_step(i):
-        d_q.copy_(h_q[i % nl], non_blocking=True)
-        d_k.copy_(h_k, non_blocking=True)
-        d_v.copy_(h_v, non_blocking=True)
-        tq.tq_decode_step(caches[i % nl], d_k, d_v, write_pos, d_q, seq_lens, S, ATTN, ws, out=out, chunk=CHUNK,
-                          status=status)
-        h_out.copy_(out, non_blocking=True)
+        tq.tq_decode_step_host(caches[i % nl], h_k, h_v, write_pos, h_q[i % nl], seq_lens, S, ATTN, ws, staging,
+                               h_out, chunk=CHUNK, status=status)
 
     for i in range(args.warmup):
         e2e_step(i)
@@ -289,8 +290,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     e1.record()
     barrier()
     e2e_ms = e0.elapsed_time(e1)
-    h2d = (d_q.numel() + d_k.numel() + d_v.numel()) * 2
-    d2h = out.numel() * 2
+    h2d = (h_q[0].numel() + h_k.numel() + h_v.numel()) * 2
+    d2h = h_out.numel() * 2
 
     peak, peak_kind = load_peaks()
     extras = {}
@@ -330,7 +331,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "config": {
             "workload": "llama70b_128k_decode_step",
             "batch": B, "num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": D, "seq_len": S,
-            "group_size": 64, "chunk": CHUNK, "attn_scale": ATTN, "n_new_per_step": 1,
+            "group_size": 64, "code_bits": CODE_BITS, "chunk": CHUNK, "attn_scale": ATTN, "n_new_per_step": 1,
             "parallelism": f"{world} independent replicas" if world > 1 else "single GPU",
             "l2": f"inputs larger than L2: {nl} rotated layer cache(s) "
                   f"({nl * cache_bytes(S) / 1e9:.2f} GB > 129 MB L2)",
@@ -354,10 +355,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                             if peak_kind == "measured" else "fallback 6.8 TB/s"),
             "frac_of_nominal_8TBs": round(p1_gbs / 8000.0, 4),
             "algorithmic_bytes_per_launch": phase1_bytes(S),
-            "traffic": load_traffic(),
+            "traffic": load_traffic() if CODE_BITS == 4 else None,
         },
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_per_step, 6)},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_per_step, 6),
+                "call": "one tq_decode_step_host per step (pinned host q/k_new/v_new in, out back), eager"},
         "gpu_launches": 2 * args.steps,  # per step: phase 1 (with the 1-row append fused in) + reduce
         "device_status": st,
         "clocks": clocks,
@@ -699,9 +701,15 @@ def main():
     ap.add_argument("--layers", type=int, default=N_LAYERS_ROTATED, help="layer caches rotated over (>= 1)")
     ap.add_argument("--no-extras", action="store_true", help="skip the length sweep and the 80-layer step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bits", type=int, choices=[4, 8], default=4,
+                    help="code width of the headline caches (8: profile the int8 path; implies --no-extras)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    global CODE_BITS
+    CODE_BITS = args.bits
+    if args.bits != 4:
+        args.no_extras = True
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

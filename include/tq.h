@@ -245,6 +245,28 @@ tq_status tq_paged_decode_step(const tq_paged_kv_cache* cache, const uint16_t* k
                                void* workspace, size_t workspace_bytes, uint16_t* out,
                                int32_t* status, void* stream);
 
+/* ------------------------------------------------------------ host buffers --
+ * tq_decode_step_ex with the step's inputs and output in host memory: copies
+ * q [batch][num_q_heads][head_dim] and k_new / v_new [batch][Hkv][n_new][D]
+ * (fp16, host; page-locked for the copies to be asynchronous) into `staging`
+ * (device, 256-byte aligned, tq_host_staging_bytes long), runs the step, and
+ * copies the fp16 output back to h_out (host).  Everything is queued on
+ * `stream` in one call (no host synchronisation): h_out holds the result once
+ * the stream has reached it.  write_pos, seq_lens, workspace and status stay
+ * device-side, as for tq_decode_step_ex.  The call a serving loop makes once
+ * per step when its activations live on the host.  When all four host buffers
+ * are page-locked and mapped (cudaHostAlloc, torch pin_memory) the kernels
+ * read and write them in place (GPU-addressable host memory, NVLink-C2C on
+ * Grace-Blackwell) and `staging` is not touched. */
+size_t tq_host_staging_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                             int32_t head_dim, int32_t n_new);
+tq_status tq_decode_step_host(const tq_kv_cache* cache, const uint16_t* h_k_new,
+                              const uint16_t* h_v_new, int32_t n_new, const int32_t* write_pos,
+                              const uint16_t* h_q, int32_t num_q_heads, const int32_t* seq_lens,
+                              int32_t max_seq_len, float attn_scale, int32_t chunk, uint32_t flags,
+                              void* workspace, size_t workspace_bytes, void* staging,
+                              size_t staging_bytes, uint16_t* h_out, int32_t* status, void* stream);
+
 /* Workspace bytes tq_sdpa_int4_decode needs for these sizes (an upper bound
  * that does not depend on the device).  Host-only. */
 size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t num_q_heads,

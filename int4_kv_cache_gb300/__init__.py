@@ -21,7 +21,7 @@ __all__ = [
     "tq_quantize_kv_append", "tq_sdpa_int4_decode", "tq_sdpa_int4_partial", "tq_sdpa_int4_reduce",
     "tq_sdpa_plan", "tq_sdpa_int4_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "tq_decode_step",
     "tq_dequantize_kv", "tq_hadamard_rotate", "TQ_ROTATE_K", "TQ_ROTATE_V", "TQ_STEP_ADVANCE", "TQ_DEV_PAGE",
-    "tq_paged_kv_cache", "PagedKVCache",
+    "tq_paged_kv_cache", "PagedKVCache", "tq_decode_step_host", "tq_host_staging_bytes",
 ]
 
 TQ_OK = 0
@@ -111,6 +111,8 @@ def lib() -> ctypes.CDLL:
             "tq_paged_kv_cache_bytes": ([i32] * 6, sz),
             "tq_paged_kv_cache_carve": ([PC, P, P] + [i32] * 8, i32),
             "tq_kv_cache_bytes_ex": ([i32] * 6, sz),
+            "tq_host_staging_bytes": ([i32] * 5, sz),
+            "tq_decode_step_host": ([C, P, P, i32, P, P, i32, P, i32, f32, i32, u32, P, sz, P, sz, P, P, P], i32),
             "tq_kv_cache_carve_ex": ([C, P] + [i32] * 6, i32),
             "tq_paged_quantize_kv_append": ([PC, P, P, i32, P, u32, P, P], i32),
             "tq_paged_sdpa_int4_decode": ([PC, P, i32, P, i32, f32, i32, u32, P, sz, P, P, P], i32),
@@ -468,3 +470,33 @@ def tq_hadamard_rotate(x: torch.Tensor, out: Optional[torch.Tensor] = None, stre
     _check("tq_hadamard_rotate", lib().tq_hadamard_rotate(_ptr(x), x.numel() // dim, dim, _ptr(out),
                                                           _stream(stream)))
     return out
+
+
+def tq_host_staging_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, n_new: int) -> int:
+    return int(lib().tq_host_staging_bytes(batch, num_q_heads, num_kv_heads, head_dim, n_new))
+
+
+def _need_host(t: torch.Tensor, name: str) -> None:
+    if t.is_cuda or t.dtype != torch.float16 or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous host float16 tensor (pinned for asynchronous copies)")
+
+
+def tq_decode_step_host(cache: KVCache, h_k_new: torch.Tensor, h_v_new: torch.Tensor, write_pos: torch.Tensor,
+                        h_q: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int, attn_scale: float,
+                        workspace: torch.Tensor, staging: torch.Tensor, h_out: torch.Tensor,
+                        chunk: int = DEFAULT_CHUNK, flags: int = 0, status: Optional[torch.Tensor] = None,
+                        stream=None) -> torch.Tensor:
+    """tq_decode_step with q / k_new / v_new / out in host memory: the copies and
+    the step are queued by one library call; h_out is valid once the stream
+    has reached it."""
+    for t, n in ((h_k_new, "h_k_new"), (h_v_new, "h_v_new"), (h_q, "h_q"), (h_out, "h_out")):
+        _need_host(t, n)
+    for t, n, dt in ((write_pos, "write_pos", torch.int32), (seq_lens, "seq_lens", torch.int32),
+                     (workspace, "workspace", torch.uint8), (staging, "staging", torch.uint8)):
+        _need(t, dt, n)
+    n_new = h_k_new.shape[2] if h_k_new.dim() == 4 else 0
+    _check("tq_decode_step_host", lib().tq_decode_step_host(
+        cache.ref(), _ptr(h_k_new), _ptr(h_v_new), n_new, _ptr(write_pos), _ptr(h_q), h_q.shape[1], _ptr(seq_lens),
+        int(max_seq_len), float(attn_scale), int(chunk), int(flags), _ptr(workspace), workspace.numel(),
+        _ptr(staging), staging.numel(), _ptr(h_out), _ptr(status), _stream(stream)))
+    return h_out

@@ -645,6 +645,68 @@ tq_status tq_sdpa_int4_decode_ex(const tq_kv_cache* raw, const uint16_t* q, int3
                        workspace, workspace_bytes, out, status, TQ_IMPL_AUTO, static_cast<cudaStream_t>(stream));
 }
 
+size_t tq_host_staging_bytes(int32_t batch, int32_t hq, int32_t hkv, int32_t head_dim, int32_t n_new) {
+    if (batch < 1 || hq < 1 || hkv < 1 || head_dim < 1 || n_new < 0) return 0;
+    const size_t qb = static_cast<size_t>(batch) * hq * head_dim * 2;
+    const size_t kb = static_cast<size_t>(batch) * hkv * n_new * head_dim * 2;
+    return 2 * align256(qb) + 2 * align256(kb);  // q, out, k_new, v_new
+}
+
+tq_status tq_decode_step_host(const tq_kv_cache* cache, const uint16_t* h_k_new, const uint16_t* h_v_new,
+                              int32_t n_new, const int32_t* write_pos, const uint16_t* h_q, int32_t hq,
+                              const int32_t* seq_lens, int32_t max_seq_len, float attn_scale, int32_t chunk,
+                              uint32_t flags, void* workspace, size_t workspace_bytes, void* staging,
+                              size_t staging_bytes, uint16_t* h_out, int32_t* status, void* stream) {
+    if (cache == nullptr || h_q == nullptr || h_out == nullptr || staging == nullptr) return TQ_ERR_NULL;
+    if (n_new > 0 && (h_k_new == nullptr || h_v_new == nullptr)) return TQ_ERR_NULL;
+    if (hq < 1 || n_new < 0) return TQ_ERR_SHAPE;
+    const size_t need = tq_host_staging_bytes(cache->batch, hq, cache->num_kv_heads, cache->head_dim, n_new);
+    if (need == 0) return TQ_ERR_SHAPE;
+    if (staging_bytes < need) return TQ_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(staging) & 255u) != 0) return TQ_ERR_ALIGN;
+    // Page-locked host buffers are addressable from the GPU (over NVLink-C2C on
+    // Grace-Blackwell): then the step reads q / k_new / v_new and writes the
+    // output in place, with no copy-engine round trips.  Other host memory
+    // goes through the staging copies.
+    auto mapped = [](const void* ptr) -> void* {
+        if (ptr == nullptr) return nullptr;
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+    };
+    {
+        void* dq = mapped(h_q);
+        void* dout = mapped(h_out);
+        void* dk = n_new > 0 ? mapped(h_k_new) : dq;
+        void* dv = n_new > 0 ? mapped(h_v_new) : dq;
+        if (dq != nullptr && dout != nullptr && dk != nullptr && dv != nullptr && aligned16(dq) && aligned16(dk) &&
+            aligned16(dv))
+            return tq_decode_step_ex(cache, static_cast<const uint16_t*>(dk), static_cast<const uint16_t*>(dv),
+                                     n_new, write_pos, static_cast<const uint16_t*>(dq), hq, seq_lens, max_seq_len,
+                                     attn_scale, chunk, flags, workspace, workspace_bytes,
+                                     static_cast<uint16_t*>(dout), status, stream);
+    }
+    const size_t qb = static_cast<size_t>(cache->batch) * hq * cache->head_dim * 2;
+    const size_t kb = static_cast<size_t>(cache->batch) * cache->num_kv_heads * n_new * cache->head_dim * 2;
+    uint8_t* st = static_cast<uint8_t*>(staging);
+    uint16_t* d_q = reinterpret_cast<uint16_t*>(st);
+    uint16_t* d_out = reinterpret_cast<uint16_t*>(st + align256(qb));
+    uint16_t* d_k = reinterpret_cast<uint16_t*>(st + 2 * align256(qb));
+    uint16_t* d_v = reinterpret_cast<uint16_t*>(st + 2 * align256(qb) + align256(kb));
+    cudaStream_t s_ = static_cast<cudaStream_t>(stream);
+    tq_status s = cuda_status(cudaMemcpyAsync(d_q, h_q, qb, cudaMemcpyHostToDevice, s_));
+    if (s == TQ_OK && kb > 0) s = cuda_status(cudaMemcpyAsync(d_k, h_k_new, kb, cudaMemcpyHostToDevice, s_));
+    if (s == TQ_OK && kb > 0) s = cuda_status(cudaMemcpyAsync(d_v, h_v_new, kb, cudaMemcpyHostToDevice, s_));
+    if (s != TQ_OK) return s;
+    s = tq_decode_step_ex(cache, d_k, d_v, n_new, write_pos, d_q, hq, seq_lens, max_seq_len, attn_scale, chunk,
+                          flags, workspace, workspace_bytes, d_out, status, stream);
+    if (s != TQ_OK) return s;
+    return cuda_status(cudaMemcpyAsync(h_out, d_out, qb, cudaMemcpyDeviceToHost, s_));
+}
+
 size_t tq_paged_kv_cache_bytes(int32_t num_pages, int32_t hkv, int32_t head_dim, int32_t group_size, int32_t bits,
                                int32_t page_tokens) {
     return tq_kv_cache_bytes_ex(num_pages, hkv, head_dim, group_size, bits, page_tokens);  // a page = one row block

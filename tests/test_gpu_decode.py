@@ -348,3 +348,31 @@ def test_fused_step_write_pos_out_of_range():
     assert torch.equal(after, ref_c2.buffer)
     oref = oracle.attention(x.q, oracle.Cache.from_fp16(kk, vv), lens, 0.088)
     assert_close(got.float().cpu().numpy(), oref, what="fused step, one row out of range")
+
+
+def test_host_buffer_step_equals_device_step():
+    """tq_decode_step_host (copies in, step, copy out, one call) gives the
+    device-buffer step's output and cache."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    B, Hq, Hkv, D, S = 2, 64, 8, 128, 4096
+    x = synth.decode_inputs(250, B, Hq, Hkv, D, S, outliers=True)
+    kn, vn = synth.append_tokens(250, 0, B, Hkv, D, 1, outliers=x.outlier_channels)
+    pos = np.array([S - 1, 1000], np.int32)
+    wp, lt = torch.from_numpy(pos).cuda(), torch.from_numpy(pos + 1).cuda()
+    ws = workspace_for(B, Hq, Hkv, D, S)
+    c1 = gpu_cache_from_fp16(x.k, x.v)
+    ref = tq.tq_decode_step(c1, torch.from_numpy(kn).cuda(), torch.from_numpy(vn).cuda(), wp,
+                            torch.from_numpy(x.q).cuda(), lt, S, 0.088, ws).cpu()
+    staging = torch.empty(tq.tq_host_staging_bytes(B, Hq, Hkv, D, 1), dtype=torch.uint8, device="cuda")
+    for pinned in (True, False):  # mapped host memory read in place; pageable memory through the staging copies
+        c2 = gpu_cache_from_fp16(x.k, x.v)
+        hq, hk, hv = (torch.from_numpy(a.copy()) for a in (x.q, kn, vn))
+        h_out = torch.empty((B, Hq, D), dtype=torch.float16)
+        if pinned:
+            hq, hk, hv, h_out = hq.pin_memory(), hk.pin_memory(), hv.pin_memory(), h_out.pin_memory()
+        tq.tq_decode_step_host(c2, hk, hv, wp.clone(), hq, lt, S, 0.088, ws, staging, h_out)
+        torch.cuda.synchronize()
+        assert torch.equal(h_out, ref), pinned
+        assert torch.equal(c1.buffer, c2.buffer), pinned
