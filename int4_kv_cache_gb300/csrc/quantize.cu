@@ -40,6 +40,44 @@ __device__ __forceinline__ void rotate_staged(uint4 (&tile)[32][8], int lane, in
     }
 }
 
+// Quantize group gi (over [B][Hkv][n_new][NG]) from its staged K and V rows
+// (eight 16-byte words each, word j at slot j ^ r7) and store the codes and
+// the scale / bias into the cache row write_pos[b] + i.
+template <int BITS>
+__device__ __forceinline__ void quantize_store(const AppendParams& p, long long gi, int ng, const uint4* rowk,
+                                               const uint4* rowv, int r7, int t_first = 0, int t_last = 1) {
+    const int g = static_cast<int>(gi % ng);
+    const long long row = gi / ng;  // over [B][Hkv][n_new]
+    const int i = static_cast<int>(row % p.n_new);
+    const long long bh = row / p.n_new;  // b * Hkv + h
+    const int b = static_cast<int>(bh / p.num_kv_heads);
+    const int wp = __ldg(p.write_pos + b);
+    if (wp < 0 || static_cast<long long>(wp) + p.n_new > p.capacity) {
+        if (p.status != nullptr && g == 0 && i == 0) atomicOr(p.status, TQ_DEV_WRITE_POS);
+        return;
+    }
+    const long long dst_row =
+        kv_row(p.map, p.num_kv_heads, b, static_cast<int>(bh - static_cast<long long>(b) * p.num_kv_heads), wp + i,
+               p.status);
+    const long long code_off = dst_row * (p.head_dim * BITS / 8) + g * (kGroup * BITS / 8);  // 32-byte aligned
+    const long long sb = dst_row * ng + g;
+#pragma unroll 1
+    for (int t = t_first; t <= t_last; ++t) {  // 0: K, 1: V
+        const uint4* src = t ? rowv : rowk;
+        uint4 x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = src[j ^ r7];
+        uint32_t c[2 * BITS];
+        __half sc, bi;
+        quantize_group64<BITS>(x, c, sc, bi);
+        uint4* dst = reinterpret_cast<uint4*>((t ? p.v_codes : p.k_codes) + code_off);
+#pragma unroll
+        for (int w = 0; w < BITS / 2; ++w) dst[w] = make_uint4(c[4 * w], c[4 * w + 1], c[4 * w + 2], c[4 * w + 3]);
+        (t ? p.v_scale : p.k_scale)[sb] = __half_as_ushort(sc);
+        (t ? p.v_bias : p.k_bias)[sb] = __half_as_ushort(bi);
+    }
+}
+
 template <int BITS>
 __global__ void __launch_bounds__(kQuantThreads) quantize_append_kernel(const AppendParams p) {
     // staging: per warp and tensor, 32 groups x 8 words of 16 bytes; word w of
@@ -86,34 +124,78 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_append_kernel(const Ap
 
     const long long gi = warp_base + lane;
     if (gi >= n_groups) return;
-    const int g = static_cast<int>(gi % ng);
-    const long long row = gi / ng;  // over [B][Hkv][n_new]
-    const int i = static_cast<int>(row % p.n_new);
-    const long long bh = row / p.n_new;  // b * Hkv + h
-    const int b = static_cast<int>(bh / p.num_kv_heads);
-    const int wp = __ldg(p.write_pos + b);
-    if (wp < 0 || static_cast<long long>(wp) + p.n_new > p.capacity) {
-        if (p.status != nullptr && g == 0 && i == 0) atomicOr(p.status, TQ_DEV_WRITE_POS);
-        return;
+    quantize_store<BITS>(p, gi, ng, stage[warp][0][lane], stage[warp][1][lane], lane & 7);
+}
+
+// Large appends (prefill): a persistent grid streams tiles of kTmaGroups
+// groups of K and of V into shared memory with 2-D TMA boxes (128-byte rows,
+// one group per row).  The 128-byte swizzle places word j of row r at slot
+// j ^ (r & 7), the layout the per-thread reads above expect.  Two stages per
+// CTA: while the threads quantize one tile, the next one is in flight.
+constexpr int kTmaGroups = 128;                     // groups (rows) per tile
+constexpr int kTmaThreads = 2 * kTmaGroups;         // one thread per (group, K or V)
+constexpr int kTmaTensorBytes = kTmaGroups * 128;   // 16 KB of K or of V
+constexpr int kTmaStageBytes = 2 * kTmaTensorBytes;
+constexpr int kTmaStages = 2;
+constexpr int kTmaSmemBytes = kTmaStages * kTmaStageBytes + 1024;
+
+template <int BITS>
+__global__ void __launch_bounds__(kTmaThreads) quantize_append_tma_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                                         const __grid_constant__ CUtensorMap tm_v,
+                                                                         const AppendParams p, long long n_groups,
+                                                                         int n_tiles) {
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ uint64_t full_bar[kTmaStages];
+    uint8_t* smem = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ng = p.head_dim / kGroup;
+    if (tid == 0) {
+        for (int s = 0; s < kTmaStages; ++s) mbar_init(&full_bar[s], 1);
+        fence_mbarrier_init();
     }
-    const long long dst_row =
-        kv_row(p.map, p.num_kv_heads, b, static_cast<int>(bh - static_cast<long long>(b) * p.num_kv_heads), wp + i,
-               p.status);
-    const long long code_off = dst_row * (p.head_dim * BITS / 8) + g * (kGroup * BITS / 8);  // 32-byte aligned
-    const long long sb = dst_row * ng + g;
-#pragma unroll 1
-    for (int t = 0; t < 2; ++t) {
-        uint4 x[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) x[j] = stage[warp][t][lane][j ^ (lane & 7)];
-        uint32_t c[2 * BITS];
-        __half sc, bi;
-        quantize_group64<BITS>(x, c, sc, bi);
-        uint4* dst = reinterpret_cast<uint4*>((t ? p.v_codes : p.k_codes) + code_off);
-#pragma unroll
-        for (int w = 0; w < BITS / 2; ++w) dst[w] = make_uint4(c[4 * w], c[4 * w + 1], c[4 * w + 2], c[4 * w + 3]);
-        (t ? p.v_scale : p.k_scale)[sb] = __half_as_ushort(sc);
-        (t ? p.v_bias : p.k_bias)[sb] = __half_as_ushort(bi);
+    __syncthreads();
+    pdl_launch_dependents();
+    auto issue = [&](int tile, int stage) {
+        const uint64_t policy = policy_evict_first();
+        uint8_t* st = smem + stage * kTmaStageBytes;
+        mbar_arrive_expect_tx(&full_bar[stage], kTmaStageBytes);
+        tma_load_2d(st, &tm_k, 0, tile * kTmaGroups, &full_bar[stage], policy);
+        tma_load_2d(st + kTmaTensorBytes, &tm_v, 0, tile * kTmaGroups, &full_bar[stage], policy);
+    };
+    if (tid == 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        for (int s = 0; s < kTmaStages; ++s)
+            if (blockIdx.x + s * gridDim.x < n_tiles) issue(blockIdx.x + s * gridDim.x, s);
+    }
+    int it = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+        const int stage = it % kTmaStages;
+        if (!mbar_wait_bounded(&full_bar[stage], (it / kTmaStages) & 1)) {
+            if (p.status != nullptr) atomicOr(p.status, TQ_DEV_TIMEOUT);
+            break;  // no further tiles are issued, so every thread gives up the same way
+        }
+        uint4 (*tk)[8] = reinterpret_cast<uint4 (*)[8]>(smem + stage * kTmaStageBytes);
+        uint4 (*tv)[8] = reinterpret_cast<uint4 (*)[8]>(smem + stage * kTmaStageBytes + kTmaTensorBytes);
+        // threads [0, 128) take the K groups, [128, 256) the V groups
+        const int t = tid >= kTmaGroups ? 1 : 0, r = tid - t * kTmaGroups;
+        if (p.flags & (t ? TQ_ROTATE_V : TQ_ROTATE_K)) {  // the same for each warp
+            uint4 (&rows)[32][8] = *reinterpret_cast<uint4 (*)[32][8]>((t ? tv : tk) + 32 * (warp & 3));
+            switch (p.head_dim) {
+                case 64: rotate_staged<2>(rows, lane, ng, p.rot_scale); break;
+                case 128: rotate_staged<4>(rows, lane, ng, p.rot_scale); break;
+                default: rotate_staged<8>(rows, lane, ng, p.rot_scale); break;
+            }
+            __syncwarp();
+        }
+        const long long gi = static_cast<long long>(tile) * kTmaGroups + r;
+        if (gi < n_groups) quantize_store<BITS>(p, gi, ng, tk[r], tv[r], r & 7, t, t);
+        // every thread is done with this stage (reads, and rotation writes)
+        // before the asynchronous copy that overwrites it is issued
+        fence_proxy_async_shared();
+        __syncthreads();
+        const int next = tile + kTmaStages * gridDim.x;
+        if (tid == 0 && next < n_tiles) issue(next, stage);
     }
 }
 
@@ -126,6 +208,33 @@ cudaError_t launch_quantize_append(const AppendParams& p, cudaStream_t stream) {
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     if (p.bits == 8) quantize_append_kernel<8><<<static_cast<unsigned>(blocks), block, 0, stream>>>(p);
     else quantize_append_kernel<4><<<static_cast<unsigned>(blocks), block, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_append_tma(const AppendParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                       int grid, cudaStream_t stream) {
+    const long long groups = static_cast<long long>(p.batch) * p.num_kv_heads * p.n_new * (p.head_dim / kGroup);
+    const long long tiles = (groups + kTmaGroups - 1) / kTmaGroups;
+    if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    const int n_tiles = static_cast<int>(tiles);
+    if (grid > n_tiles) grid = n_tiles;
+    if (grid < 1) return cudaSuccess;
+    static bool attr_done[64][2] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int bi = p.bits == 8 ? 1 : 0;
+    if (dev >= 0 && dev < 64 && !attr_done[dev][bi]) {
+        cudaError_t e = p.bits == 8 ? cudaFuncSetAttribute(quantize_append_tma_kernel<8>,
+                                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmemBytes)
+                                    : cudaFuncSetAttribute(quantize_append_tma_kernel<4>,
+                                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done[dev][bi] = true;
+    }
+    if (p.bits == 8)
+        quantize_append_tma_kernel<8><<<grid, kTmaThreads, kTmaSmemBytes, stream>>>(tm_k, tm_v, p, groups, n_tiles);
+    else
+        quantize_append_tma_kernel<4><<<grid, kTmaThreads, kTmaSmemBytes, stream>>>(tm_k, tm_v, p, groups, n_tiles);
     return cudaGetLastError();
 }
 

@@ -166,6 +166,23 @@ tq_status make_code_map(CUtensorMap* map, const uint8_t* codes, const Store* c, 
     return TQ_OK;
 }
 
+// A row-major array of `rows` rows of 128 bytes seen as uint8 [rows][128], boxes
+// of `box_rows` rows with the 128-byte swizzle (the fp16 input of an append:
+// one group of 64 halves per row).
+tq_status make_rows_map(CUtensorMap* map, const void* base, unsigned long long rows, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return cuda_status(cudaErrorNotSupported);
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_status(cudaErrorInvalidValue);
+    return TQ_OK;
+}
+
 // ------------------------------------------------------------ device facts --
 struct DeviceFacts {
     int sms = 0;
@@ -470,6 +487,23 @@ tq::AppendParams append_params(const Store* cache, const uint16_t* k_new, const 
 }
 
 bool valid_rotation(uint32_t flags) { return (flags & ~(TQ_ROTATE_K | TQ_ROTATE_V)) == 0; }
+
+// A plain (not step-fused) append: large ones take the persistent TMA kernel.
+tq_status run_append(const tq::AppendParams& ap, cudaStream_t st) {
+    const long long groups =
+        static_cast<long long>(ap.batch) * ap.num_kv_heads * ap.n_new * (ap.head_dim / tq::kGroup);
+    if (groups >= tq::kTmaAppendMinGroups && groups < (1LL << 31)) {
+        CUtensorMap tm_k, tm_v;
+        tq_status s = make_rows_map(&tm_k, ap.k_new, static_cast<unsigned long long>(groups), 128);
+        if (s == TQ_OK) s = make_rows_map(&tm_v, ap.v_new, static_cast<unsigned long long>(groups), 128);
+        if (s != TQ_OK) return s;
+        DeviceFacts* f = nullptr;
+        s = device_facts(&f);
+        if (s != TQ_OK) return s;
+        return cuda_status(tq::launch_quantize_append_tma(ap, tm_k, tm_v, f->sms * tq::kTmaAppendCtasPerSm, st));
+    }
+    return cuda_status(tq::launch_quantize_append(ap, st));
+}
 bool valid_step_flags(uint32_t flags) { return valid_rotation(flags & ~TQ_STEP_ADVANCE); }
 
 // Decode (optionally preceded by an append of n_new rows) with the workspace
@@ -594,8 +628,8 @@ tq_status tq_quantize_kv_append_ex(const tq_kv_cache* raw, const uint16_t* k_new
     if (s != TQ_OK) return s;
     if (!valid_rotation(flags)) return TQ_ERR_UNSUPPORTED;
     if (n_new == 0) return TQ_OK;
-    return cuda_status(tq::launch_quantize_append(append_params(cache, k_new, v_new, n_new, write_pos, status, flags),
-                                                  static_cast<cudaStream_t>(stream)));
+    return run_append(append_params(cache, k_new, v_new, n_new, write_pos, status, flags),
+                      static_cast<cudaStream_t>(stream));
 }
 
 tq_status tq_hadamard_rotate(const uint16_t* x, int64_t rows, int32_t dim, uint16_t* out, void* stream) {
@@ -748,8 +782,8 @@ tq_status tq_paged_quantize_kv_append(const tq_paged_kv_cache* raw, const uint16
     if (s != TQ_OK) return s;
     if (!valid_rotation(flags)) return TQ_ERR_UNSUPPORTED;
     if (n_new == 0) return TQ_OK;
-    return cuda_status(tq::launch_quantize_append(append_params(&st, k_new, v_new, n_new, write_pos, status, flags),
-                                                  static_cast<cudaStream_t>(stream)));
+    return run_append(append_params(&st, k_new, v_new, n_new, write_pos, status, flags),
+                      static_cast<cudaStream_t>(stream));
 }
 
 tq_status tq_paged_sdpa_int4_decode(const tq_paged_kv_cache* raw, const uint16_t* q, int32_t hq,

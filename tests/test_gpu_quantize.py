@@ -110,3 +110,28 @@ def test_prefill_full_128k_layer_bit_exact_sampled():
     got = [a[0][:, toks] for a in cache_arrays(cache)]
     for g, want in zip(got, (okc, oks, okb, ovc, ovs, ovb)):
         np.testing.assert_array_equal(g, want)
+
+
+@pytest.mark.parametrize("flags,bits,D", [(0, 4, 128), (3, 4, 128), (0, 8, 128), (1, 4, 64), (0, 4, 256)])
+def test_large_append_tma_path_bit_exact(flags, bits, D):
+    """Appends of >= 8192 groups stream through the persistent TMA kernel:
+    bit-exact against the oracle with a ragged last tile (the group count is
+    not a multiple of 128), with the rotation fused in, and for int8."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    B, Hkv, S = 2, 3, 2731
+    x = synth.decode_inputs(260 + D + flags, B, 2 * Hkv, Hkv, D, S, outliers=True)
+    assert (B * Hkv * S * (D // 64)) % 128 != 0 and B * Hkv * S * (D // 64) >= 8192
+    c = tq.KVCache(B, Hkv, D, 2736, bits=bits)
+    tq.tq_quantize_kv_append(c, torch.from_numpy(x.k).cuda(), torch.from_numpy(x.v).cuda(),
+                             torch.zeros(B, dtype=torch.int32, device="cuda"), flags=flags)
+    torch.cuda.synchronize()
+    kk = oracle.rotate_rows_f16(x.k) if flags & 1 else x.k
+    vv = oracle.rotate_rows_f16(x.v) if flags & 2 else x.v
+    got = cache_arrays(c)
+    for arrs, src in ((got[:3], kk), (got[3:], vv)):
+        codes, sc, bi = oracle.quantize_rows(src, bits=bits)
+        assert np.array_equal(arrs[0][:, :, :S], codes)
+        assert np.array_equal(arrs[1][:, :, :S], sc)
+        assert np.array_equal(arrs[2][:, :, :S], bi)
