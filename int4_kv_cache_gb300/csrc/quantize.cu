@@ -40,12 +40,12 @@ __device__ __forceinline__ void rotate_staged(uint4 (&tile)[32][8], int lane, in
     }
 }
 
-// Quantize group gi (over [B][Hkv][n_new][NG]) from its staged K and V rows
-// (eight 16-byte words each, word j at slot j ^ r7) and store the codes and
-// the scale / bias into the cache row write_pos[b] + i.
+// Destination of group gi (over [B][Hkv][n_new][NG]) in the cache: the code
+// and scale / bias offsets of its row write_pos[b] + i; false (and the status
+// bit) when the sequence's write position is out of range.
 template <int BITS>
-__device__ __forceinline__ void quantize_store(const AppendParams& p, long long gi, int ng, const uint4* rowk,
-                                               const uint4* rowv, int r7, int t_first = 0, int t_last = 1) {
+__device__ __forceinline__ bool group_dst(const AppendParams& p, long long gi, int ng, long long& code_off,
+                                          long long& sb) {
     const int g = static_cast<int>(gi % ng);
     const long long row = gi / ng;  // over [B][Hkv][n_new]
     const int i = static_cast<int>(row % p.n_new);
@@ -54,27 +54,45 @@ __device__ __forceinline__ void quantize_store(const AppendParams& p, long long 
     const int wp = __ldg(p.write_pos + b);
     if (wp < 0 || static_cast<long long>(wp) + p.n_new > p.capacity) {
         if (p.status != nullptr && g == 0 && i == 0) atomicOr(p.status, TQ_DEV_WRITE_POS);
-        return;
+        return false;
     }
     const long long dst_row =
         kv_row(p.map, p.num_kv_heads, b, static_cast<int>(bh - static_cast<long long>(b) * p.num_kv_heads), wp + i,
                p.status);
-    const long long code_off = dst_row * (p.head_dim * BITS / 8) + g * (kGroup * BITS / 8);  // 32-byte aligned
-    const long long sb = dst_row * ng + g;
+    code_off = dst_row * (p.head_dim * BITS / 8) + g * (kGroup * BITS / 8);  // 32-byte aligned
+    sb = dst_row * ng + g;
+    return true;
+}
+
+// Quantize one group's 64 fp16 values (eight 16-byte words) of tensor t (0: K,
+// 1: V) and store codes, scale and bias.
+template <int BITS>
+__device__ __forceinline__ void quantize_words_store(const AppendParams& p, const uint4 (&x)[8], int t,
+                                                     long long code_off, long long sb) {
+    uint32_t c[2 * BITS];
+    __half sc, bi;
+    quantize_group64<BITS>(x, c, sc, bi);
+    uint4* dst = reinterpret_cast<uint4*>((t ? p.v_codes : p.k_codes) + code_off);
+#pragma unroll
+    for (int w = 0; w < BITS / 2; ++w) dst[w] = make_uint4(c[4 * w], c[4 * w + 1], c[4 * w + 2], c[4 * w + 3]);
+    (t ? p.v_scale : p.k_scale)[sb] = __half_as_ushort(sc);
+    (t ? p.v_bias : p.k_bias)[sb] = __half_as_ushort(bi);
+}
+
+// Quantize group gi from its staged K and V rows (eight 16-byte words each,
+// word j at slot j ^ r7) and store it into the cache row write_pos[b] + i.
+template <int BITS>
+__device__ __forceinline__ void quantize_store(const AppendParams& p, long long gi, int ng, const uint4* rowk,
+                                               const uint4* rowv, int r7, int t_first = 0, int t_last = 1) {
+    long long code_off, sb;
+    if (!group_dst<BITS>(p, gi, ng, code_off, sb)) return;
 #pragma unroll 1
     for (int t = t_first; t <= t_last; ++t) {  // 0: K, 1: V
         const uint4* src = t ? rowv : rowk;
         uint4 x[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) x[j] = src[j ^ r7];
-        uint32_t c[2 * BITS];
-        __half sc, bi;
-        quantize_group64<BITS>(x, c, sc, bi);
-        uint4* dst = reinterpret_cast<uint4*>((t ? p.v_codes : p.k_codes) + code_off);
-#pragma unroll
-        for (int w = 0; w < BITS / 2; ++w) dst[w] = make_uint4(c[4 * w], c[4 * w + 1], c[4 * w + 2], c[4 * w + 3]);
-        (t ? p.v_scale : p.k_scale)[sb] = __half_as_ushort(sc);
-        (t ? p.v_bias : p.k_bias)[sb] = __half_as_ushort(bi);
+        quantize_words_store<BITS>(p, x, t, code_off, sb);
     }
 }
 
@@ -127,6 +145,84 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_append_kernel(const Ap
     quantize_store<BITS>(p, gi, ng, stage[warp][0][lane], stage[warp][1][lane], lane & 7);
 }
 
+// The Hadamard rotation of a row whose NG groups of 64 are held by NG
+// consecutive lanes, this thread holding group g in v (fp32).  The stages run
+// in the order of the fast transform (h = 1, 2, ..., 32 inside the thread,
+// then h = 64, 128 with the lanes lane ^ 1, lane ^ 2), each butterfly one
+// round-to-nearest add and one subtract, so the result equals the sequential
+// transform bit for bit; then the scale.  Every lane of the warp takes part.
+template <int NG>
+__device__ __forceinline__ void rotate_group_thread(float (&v)[64], int g, float scale) {
+#pragma unroll
+    for (int i = 0; i < 64; i += 2) {  // h = 1
+        const float u = v[i], w = v[i + 1];
+        v[i] = __fadd_rn(u, w);
+        v[i + 1] = __fsub_rn(u, w);
+    }
+    const float2 m1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+    for (int h = 2; h < 64; h <<= 1) {  // pairs (i, i+1) with bit h clear: two butterflies per paired op
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+            if ((i & h) != 0) continue;
+            const float2 a = make_float2(v[i], v[i + 1]), b = make_float2(v[i + h], v[i + h + 1]);
+            const float2 sum = __fadd2_rn(a, b), dif = __ffma2_rn(b, m1, a);
+            v[i] = sum.x;
+            v[i + 1] = sum.y;
+            v[i + h] = dif.x;
+            v[i + h + 1] = dif.y;
+        }
+    }
+#pragma unroll
+    for (int hl = 1; hl < NG; hl <<= 1) {  // h = 64 * hl: the group in lane ^ hl
+        const bool upper = (g & hl) != 0;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+            const float other = __shfl_xor_sync(0xffffffffu, v[i], hl);
+            v[i] = upper ? __fsub_rn(other, v[i]) : __fadd_rn(v[i], other);
+        }
+    }
+    const float2 sc = make_float2(scale, scale);
+#pragma unroll
+    for (int i = 0; i < 64; i += 2) {
+        const float2 r = __fmul2_rn(make_float2(v[i], v[i + 1]), sc);
+        v[i] = r.x;
+        v[i + 1] = r.y;
+    }
+}
+
+// Rotate a staged group (slots j ^ r7) in registers and quantize it.
+template <int BITS, int NG>
+__device__ __forceinline__ void rotate_quantize_store(const AppendParams& p, long long gi, int g, const uint4* row,
+                                                      int r7, int t) {
+    float v[64];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint4 w = row[j ^ r7];
+        const __half2* h = reinterpret_cast<const __half2*>(&w);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = __half22float2(h[k]);
+            v[8 * j + 2 * k] = f.x;
+            v[8 * j + 2 * k + 1] = f.y;
+        }
+    }
+    rotate_group_thread<NG>(v, g, p.rot_scale);  // all lanes, before any exit
+    uint4 x[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const __half2 h = __floats2half2_rn(v[8 * j + 2 * k], v[8 * j + 2 * k + 1]);
+            w[k] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        x[j] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    long long code_off, sb;
+    if (gi >= 0 && group_dst<BITS>(p, gi, NG, code_off, sb)) quantize_words_store<BITS>(p, x, t, code_off, sb);
+}
+
 // Large appends (prefill): a persistent grid streams tiles of kTmaGroups
 // groups of K and of V into shared memory with 2-D TMA boxes (128-byte rows,
 // one group per row).  The 128-byte swizzle places word j of row r at slot
@@ -139,8 +235,8 @@ constexpr int kTmaStageBytes = 2 * kTmaTensorBytes;
 constexpr int kTmaStages = 2;
 constexpr int kTmaSmemBytes = kTmaStages * kTmaStageBytes + 1024;
 
-template <int BITS>
-__global__ void __launch_bounds__(kTmaThreads) quantize_append_tma_kernel(const __grid_constant__ CUtensorMap tm_k,
+template <int BITS, bool ROT>
+__global__ void __launch_bounds__(kTmaThreads, ROT ? 2 : 3) quantize_append_tma_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                          const __grid_constant__ CUtensorMap tm_v,
                                                                          const AppendParams p, long long n_groups,
                                                                          int n_tiles) {
@@ -179,17 +275,19 @@ __global__ void __launch_bounds__(kTmaThreads) quantize_append_tma_kernel(const 
         uint4 (*tv)[8] = reinterpret_cast<uint4 (*)[8]>(smem + stage * kTmaStageBytes + kTmaTensorBytes);
         // threads [0, 128) take the K groups, [128, 256) the V groups
         const int t = tid >= kTmaGroups ? 1 : 0, r = tid - t * kTmaGroups;
-        if (p.flags & (t ? TQ_ROTATE_V : TQ_ROTATE_K)) {  // the same for each warp
-            uint4 (&rows)[32][8] = *reinterpret_cast<uint4 (*)[32][8]>((t ? tv : tk) + 32 * (warp & 3));
-            switch (p.head_dim) {
-                case 64: rotate_staged<2>(rows, lane, ng, p.rot_scale); break;
-                case 128: rotate_staged<4>(rows, lane, ng, p.rot_scale); break;
-                default: rotate_staged<8>(rows, lane, ng, p.rot_scale); break;
-            }
-            __syncwarp();
-        }
         const long long gi = static_cast<long long>(tile) * kTmaGroups + r;
-        if (gi < n_groups) quantize_store<BITS>(p, gi, ng, tk[r], tv[r], r & 7, t, t);
+        if (ROT && (p.flags & (t ? TQ_ROTATE_V : TQ_ROTATE_K))) {  // the same for each warp
+            // every lane rotates (the shuffles need the whole warp); lanes past
+            // the last group hold zero-filled rows and store nothing
+            const long long gq = gi < n_groups ? gi : -1;
+            switch (ng) {
+                case 1: rotate_quantize_store<BITS, 1>(p, gq, r % 1, (t ? tv : tk)[r], r & 7, t); break;
+                case 2: rotate_quantize_store<BITS, 2>(p, gq, r % 2, (t ? tv : tk)[r], r & 7, t); break;
+                default: rotate_quantize_store<BITS, 4>(p, gq, r % 4, (t ? tv : tk)[r], r & 7, t); break;
+            }
+        } else if (gi < n_groups) {
+            quantize_store<BITS>(p, gi, ng, tk[r], tv[r], r & 7, t, t);
+        }
         // every thread is done with this stage (reads, and rotation writes)
         // before the asynchronous copy that overwrites it is issued
         fence_proxy_async_shared();
@@ -219,22 +317,23 @@ cudaError_t launch_quantize_append_tma(const AppendParams& p, const CUtensorMap&
     const int n_tiles = static_cast<int>(tiles);
     if (grid > n_tiles) grid = n_tiles;
     if (grid < 1) return cudaSuccess;
-    static bool attr_done[64][2] = {};
+    const bool rot = (p.flags & (TQ_ROTATE_K | TQ_ROTATE_V)) != 0;
+    if (rot) grid = grid * 2 / 3;  // the rotating instantiation runs 2 CTAs per SM (registers)
+    if (grid < 1) grid = 1;
+    static bool attr_done[64][4] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    const int bi = p.bits == 8 ? 1 : 0;
-    if (dev >= 0 && dev < 64 && !attr_done[dev][bi]) {
-        cudaError_t e = p.bits == 8 ? cudaFuncSetAttribute(quantize_append_tma_kernel<8>,
-                                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmemBytes)
-                                    : cudaFuncSetAttribute(quantize_append_tma_kernel<4>,
-                                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmemBytes);
+    const int vi = (p.bits == 8 ? 1 : 0) + (rot ? 2 : 0);
+    auto kern = [&]() {
+        if (p.bits == 8) return rot ? quantize_append_tma_kernel<8, true> : quantize_append_tma_kernel<8, false>;
+        return rot ? quantize_append_tma_kernel<4, true> : quantize_append_tma_kernel<4, false>;
+    }();
+    if (dev >= 0 && dev < 64 && !attr_done[dev][vi]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_done[dev][bi] = true;
+        attr_done[dev][vi] = true;
     }
-    if (p.bits == 8)
-        quantize_append_tma_kernel<8><<<grid, kTmaThreads, kTmaSmemBytes, stream>>>(tm_k, tm_v, p, groups, n_tiles);
-    else
-        quantize_append_tma_kernel<4><<<grid, kTmaThreads, kTmaSmemBytes, stream>>>(tm_k, tm_v, p, groups, n_tiles);
+    kern<<<grid, kTmaThreads, kTmaSmemBytes, stream>>>(tm_k, tm_v, p, groups, n_tiles);
     return cudaGetLastError();
 }
 
