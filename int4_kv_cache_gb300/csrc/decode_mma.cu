@@ -616,7 +616,6 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
                             mma_16816(t, xa & kByte, (xa >> 8) & kByte, xb & kByte, (xb >> 8) & kByte,
                                       bhi[mt][g][0], bhi[mt][g][1]);
                         }
-    #pragma unroll
                         acc2[s][0] = __fadd2_rn(acc2[s][0], make_float2(t[0], t[1]));
                         acc2[s][1] = __fadd2_rn(acc2[s][1], make_float2(t[2], t[3]));
                     } else {
@@ -631,7 +630,6 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
                             const uint32_t a0 = ua & kLoNib, a1 = ua & kHiNib, a2 = ub & kLoNib, a3 = ub & kHiNib;
                             mma_16816(t, a0, a1, a2, a3, bhi[mt][g][0], bhi[mt][g][1]);
                         }
-    #pragma unroll
                         acc2[2 * s + j][0] = __fadd2_rn(acc2[2 * s + j][0], make_float2(t[0], t[1]));
                         acc2[2 * s + j][1] = __fadd2_rn(acc2[2 * s + j][1], make_float2(t[2], t[3]));
                     }

@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROT ? 2 : 3) quantize_append_tma_
     extern __shared__ uint8_t dyn_smem[];
     __shared__ uint64_t full_bar[kTmaStages];
     uint8_t* smem = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const int ng = p.head_dim / kGroup;
     if (tid == 0) {
         for (int s = 0; s < kTmaStages; ++s) mbar_init(&full_bar[s], 1);
