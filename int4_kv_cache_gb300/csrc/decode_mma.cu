@@ -43,6 +43,7 @@
 #include <type_traits>
 
 #include "tq_device.cuh"
+#include "tq_hadamard.cuh"
 #include "tq_internal.h"
 #include "tq_quant.cuh"
 
@@ -277,15 +278,10 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
         bulk_load(sb + 2 * C::SB_BYTES, p.v_scale + sb_off, sb_bytes, &full_bar[stage], policy);
         bulk_load(sb + 3 * C::SB_BYTES, p.v_bias + sb_off, sb_bytes, &full_bar[stage], policy);
     };
-    if (threadIdx.x == 0 && n_tiles > 0) {
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
-        const uint64_t policy = policy_evict_first();
-        for (int it = 0; it < min(n_tiles, C::STAGES); ++it)
-            if (!tile_uses(it, app_lo, app_hi)) issue_tile(it, policy);
-    }
-    // The fused append, part 1: the first pass of new-row loads is issued now
-    // so that its latency overlaps the Q loads below.
+    // The fused append, part 1: the first pass of new-row loads is issued
+    // before the tile loads, so that it does not queue behind them in the
+    // memory system (issued after them it made the owning CTA the last to
+    // finish); its latency overlaps the tile and Q loads.
     const int app_tasks = (app_hi - app_lo) * NG * 2;  // eight lanes per (row, group, K|V)
     const int app_part = threadIdx.x & 7;
     auto app_src = [&](int task) {
@@ -297,6 +293,13 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
     uint4 app_raw = make_uint4(0, 0, 0, 0);
     if (static_cast<int>(threadIdx.x >> 3) < app_tasks)
         app_raw = __ldcs(reinterpret_cast<const uint4*>(app_src(threadIdx.x >> 3)));
+    if (threadIdx.x == 0 && n_tiles > 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        const uint64_t policy = policy_evict_first();
+        for (int it = 0; it < min(n_tiles, C::STAGES); ++it)
+            if (!tile_uses(it, app_lo, app_hi)) issue_tile(it, policy);
+    }
 
     // ------------------------------------------------------------ all warps
     const int gid = lane >> 2, tig = lane & 3;
@@ -311,13 +314,62 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
         const __half sixteenth = __float2half_rn(0.0625f);
 #pragma unroll
         for (int g = 0; g < NG; ++g) qsum_own[g] = 0.0f;
+        // This lane's dims of head gid: E consecutive ones at E * tig in each
+        // segment (int4: 32 dims, E = 8; int8: 16 dims, E = 4).
+        constexpr int E = BITS == 8 ? 4 : 8;
+        struct alignas(2 * E) QVec {
+            __half h[E];
+        };
+        QVec qv[C::SPT];
+#pragma unroll
+        for (int s = 0; s < C::SPT; ++s) {
+            if (hv) {
+                qv[s] = *reinterpret_cast<const QVec*>(qrow + C::EPS * s + E * tig);
+            } else {
+#pragma unroll
+                for (int j = 0; j < E; ++j) qv[s].h[j] = __ushort_as_half(0);
+            }
+        }
+        if (p.rotate_q) {  // the same for the whole CTA
+            // dim = 4E s + E tig + j: stages h < E in the lane, h = E, 2E across
+            // the lanes of tig, then h = 4E, 8E, ... across the segments
+            float v[C::SPT][E];
+#pragma unroll
+            for (int s = 0; s < C::SPT; ++s) {
+#pragma unroll
+                for (int j = 0; j < E; ++j) v[s][j] = __half2float(qv[s].h[j]);
+                hadamard_in_lane<E>(v[s]);
+            }
+#pragma unroll
+            for (int hl = 1; hl < 4; hl <<= 1) {
+#pragma unroll
+                for (int s = 0; s < C::SPT; ++s) hadamard_across_lanes<E>(v[s], lane, hl);
+            }
+#pragma unroll
+            for (int hs = 1; hs < C::SPT; hs <<= 1) {
+#pragma unroll
+                for (int s = 0; s < C::SPT; ++s) {
+                    if ((s & hs) != 0) continue;
+#pragma unroll
+                    for (int j = 0; j < E; ++j) {
+                        const float u = v[s][j], w = v[s + hs][j];
+                        v[s][j] = __fadd_rn(u, w);
+                        v[s + hs][j] = __fsub_rn(u, w);
+                    }
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < C::SPT; ++s) {
+#pragma unroll
+                for (int j = 0; j < E; ++j) qv[s].h[j] = __float2half_rn(__fmul_rn(v[s][j], p.rot_scale));
+            }
+        }
         if constexpr (BITS == 8) {
             // segment s = dims 16s .. 16s+15; k-step s: k=2tig,2tig+1 <- dims +4tig, +4tig+2;
             // k=2tig+8,+9 <- dims +4tig+1, +4tig+3 (bytes 0, 2 and 1, 3 of a register)
 #pragma unroll
             for (int s = 0; s < C::SPT; ++s) {
-                uint2 raw = hv ? *reinterpret_cast<const uint2*>(qrow + 16 * s + 4 * tig) : make_uint2(0, 0);
-                const __half* h = reinterpret_cast<const __half*>(&raw);
+                const __half* h = qv[s].h;
                 qb[s][0] = pack_half2_bits(h[0], h[2]);
                 qb[s][1] = pack_half2_bits(h[1], h[3]);
                 qsum_own[(16 * s) / kGroup] +=
@@ -326,8 +378,7 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
         } else {
 #pragma unroll
         for (int s = 0; s < C::SPT; ++s) {
-            uint4 raw = hv ? *reinterpret_cast<const uint4*>(qrow + 32 * s + 8 * tig) : make_uint4(0, 0, 0, 0);
-            const __half* h = reinterpret_cast<const __half*>(&raw);
+            const __half* h = qv[s].h;
             // k-step (s,0): k=2tig,2tig+1 <- dims +0,+4 ; k=2tig+8,+9 <- dims +1,+5 (x 1/16)
             qb[2 * s][0] = pack_half2_bits(h[0], h[4]);
             qb[2 * s][1] = pack_half2_bits(__hmul(h[1], sixteenth), __hmul(h[5], sixteenth));
@@ -377,6 +428,26 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
             const bool valid = task < app_tasks;
             uint4 raw = app_raw;
             if (t0 > 0 && valid) raw = __ldcs(reinterpret_cast<const uint4*>(app_src(task)));
+            if constexpr (NG <= 2) {
+                if (p.app.flags != 0) {  // the same for the whole CTA: rows are stored rotated
+                    // A row's K (or V) sits in 8 NG lanes: element 64 g + 8 part + j.
+                    // Stages h = 1, 2, 4 in the lane, h = 8, 16, 32 across lane bits
+                    // 0-2 (part), h = 64 across lane bit 4 (g).  (Head dims above
+                    // 128 span two warps; their rotated appends run the append kernel.)
+                    float v[8];
+                    halves_to_floats<8>(&raw, v);
+                    hadamard_in_lane<8>(v);
+#pragma unroll
+                    for (int hl = 1; hl < 8; hl <<= 1) hadamard_across_lanes<8>(v, lane, hl);
+                    if constexpr (NG == 2) hadamard_across_lanes<8>(v, lane, 16);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], p.app.rot_scale);
+                    uint4 rot;
+                    floats_to_halves<8>(v, &rot);
+                    const bool v_lane = ((threadIdx.x >> 3) & 1) != 0;  // task & 1
+                    if ((p.app.flags & (v_lane ? TQ_ROTATE_V : TQ_ROTATE_K)) != 0) raw = rot;
+                }
+            }
             const GroupQ<BITS> gq = quantize_lane8<BITS>(raw);
             if (valid) {
                 const int kv = task & 1, g = (task >> 1) % NG, r = app_lo + (task >> 1) / NG;

@@ -290,7 +290,7 @@ tq_status check_decode_args(const Store* cache, const uint16_t* q, int32_t hq, c
 tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
                      int32_t max_seq_len, float attn_scale, const Plan& pl, float* pm, float* plv, float* pa,
                      int32_t* status, tq_impl impl, cudaStream_t stream, const int32_t* dep_write_pos = nullptr,
-                     int32_t dep_n_new = 0, const tq::AppendParams* fused_append = nullptr) {
+                     int32_t dep_n_new = 0, const tq::AppendParams* fused_append = nullptr, bool rotate_q = false) {
     if (pl.n_splits > 65535 || cache->num_kv_heads > 65535 || cache->batch > 65535) return TQ_ERR_SHAPE;
     tq::DecodeParams p{};
     p.q = q;
@@ -319,12 +319,15 @@ tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const in
     p.dep_n_new = dep_n_new;
     p.map = cache->map;
     p.bits = cache->bits;
+    p.rotate_q = rotate_q ? 1 : 0;
+    p.rot_scale = tq::rotation_scale(cache->head_dim);
     p.app = {};
     if (fused_append != nullptr) {
         if (impl == TQ_IMPL_SIMT) return TQ_ERR_UNSUPPORTED;
         p.app = *fused_append;
     }
     if (impl == TQ_IMPL_SIMT) {
+        if (rotate_q) return TQ_ERR_UNSUPPORTED;  // its callers rotate the query first
         // the CUDA-core comparison path reads contiguous int4 caches
         if (cache->paged || cache->bits != 4) return TQ_ERR_UNSUPPORTED;
         return cuda_status(tq::launch_decode_simt(p, cache->head_dim, stream));
@@ -539,27 +542,31 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
     uint16_t* q_rot = reinterpret_cast<uint16_t*>(ws + 2 * align256(parts * sizeof(float)) +
                                                   align256(parts * cache->head_dim * sizeof(float)));
     const float rs = tq::rotation_scale(cache->head_dim);
-    // keys stored rotated: attend with the rotated query, (H q).(H k) = q.k
-    if (flags & TQ_ROTATE_K) {
+    const tq_impl ph1 = impl == TQ_IMPL_SIMT ? TQ_IMPL_SIMT : TQ_IMPL_MMA;
+    // keys stored rotated: attend with the rotated query, (H q).(H k) = q.k;
+    // the tensor-core kernel rotates each query head as it loads it
+    const bool rotate_q = (flags & TQ_ROTATE_K) != 0 && ph1 == TQ_IMPL_MMA;
+    if ((flags & TQ_ROTATE_K) && !rotate_q) {
         s = cuda_status(tq::launch_rotate_rows(q, static_cast<long long>(cache->batch) * hq, cache->head_dim, q_rot,
                                                rs, st));
         if (s != TQ_OK) return s;
         q = q_rot;
     }
-    // A few new rows per sequence are quantized by the decode kernel itself
-    // (the CTA that reads them writes them first); longer or rotated appends
-    // run the append kernel, and the decode starts early and waits only for
-    // the tiles that hold the new rows.
+    // A few new rows per sequence are quantized (and rotated, for head dims
+    // up to 128, whose rows fit one warp) by the decode kernel itself: the CTA
+    // that reads them writes them first.  Longer appends, and rotated ones of
+    // wider heads, run the append kernel; the decode starts early and waits
+    // only for the tiles that hold the new rows.
     const tq::AppendParams ap = append_params(cache, k_new, v_new, n_new, write_pos, status, flags);
-    const bool fused = n_new > 0 && n_new <= tq::kFusedAppendMaxRows && flags == 0 && impl != TQ_IMPL_SIMT;
+    const bool fused = n_new > 0 && n_new <= tq::kFusedAppendMaxRows && ph1 == TQ_IMPL_MMA &&
+                       (flags == 0 || cache->head_dim <= 128);
     if (n_new > 0 && !fused) {
         s = cuda_status(tq::launch_quantize_append_primary(ap, st));
         if (s != TQ_OK) return s;
     }
-    const tq_impl ph1 = impl == TQ_IMPL_SIMT ? TQ_IMPL_SIMT : TQ_IMPL_MMA;
     const bool dep = n_new > 0 && !fused && ph1 == TQ_IMPL_MMA;
     s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, ph1, st,
-                   dep ? write_pos : nullptr, dep ? n_new : 0, fused ? &ap : nullptr);
+                   dep ? write_pos : nullptr, dep ? n_new : 0, fused ? &ap : nullptr, rotate_q);
     if (s != TQ_OK) return s;
     tq::ReduceParams r{};
     r.part_m = pm;

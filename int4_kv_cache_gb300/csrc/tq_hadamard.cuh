@@ -43,6 +43,37 @@ __device__ __forceinline__ void hadamard_warp(float (&v)[E], int lane, float sca
     for (int i = 0; i < E; ++i) v[i] = __fmul_rn(v[i], scale);
 }
 
+// Building blocks for rows spread over a few lanes in other layouts (the
+// decode kernel's query fragments and fused append): the stages h < E inside
+// a lane's E consecutive elements, and one stage whose pairs sit in lanes
+// lane and lane ^ hl (the lane with bit hl set holds the upper element).
+// Called in increasing h, they perform the butterflies of the sequential
+// transform with the same round-to-nearest operations.
+template <int E>
+__device__ __forceinline__ void hadamard_in_lane(float (&v)[E]) {
+#pragma unroll
+    for (int h = 1; h < E; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            if ((i & h) == 0) {
+                const float u = v[i], w = v[i + h];
+                v[i] = __fadd_rn(u, w);
+                v[i + h] = __fsub_rn(u, w);
+            }
+        }
+    }
+}
+
+template <int E>
+__device__ __forceinline__ void hadamard_across_lanes(float (&v)[E], int lane, int hl) {
+    const bool upper = (lane & hl) != 0;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+        const float other = __shfl_xor_sync(0xffffffffu, v[i], hl);
+        v[i] = upper ? __fsub_rn(other, v[i]) : __fadd_rn(v[i], other);
+    }
+}
+
 // E consecutive fp16 values <-> floats (E = 2, 4, 8: 4, 8 or 16 bytes).
 template <int E>
 __device__ __forceinline__ void halves_to_floats(const void* src, float (&v)[E]) {

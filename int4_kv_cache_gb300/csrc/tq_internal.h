@@ -90,6 +90,10 @@ struct DecodeParams {
     // the capacity.
     AppendParams app;
     int32_t bits;             // code width of the cache: 4 or 8
+    // Keys stored rotated (tensor-core kernel only): the kernel attends with
+    // fp16(rot_scale * H q), rotating each query head as it loads it.
+    int32_t rotate_q;
+    float rot_scale;
 };
 // Most rows per sequence the decode kernel appends itself; longer appends
 // run the append kernel first.

@@ -2,6 +2,7 @@
 Gemma 4", TurboQuant section) against the oracle: the rotation kernel and the
 rotated append bit for bit, the rotated decode within the output tolerance."""
 import math
+import types
 
 import numpy as np
 import pytest
@@ -47,31 +48,33 @@ def test_rotated_append_bit_exact(D, flags):
         assert np.array_equal(got[:, :, :S], want)
 
 
-def _rotated_reference(x, lens, scale, flags):
+def _rotated_reference(x, lens, scale, flags, bits=4):
     kk = oracle.rotate_rows_f16(x.k) if flags & 1 else x.k
     vv = oracle.rotate_rows_f16(x.v) if flags & 2 else x.v
     qq = oracle.rotate_rows_f16(x.q) if flags & 1 else x.q
-    out = oracle.attention(qq, oracle.Cache.from_fp16(kk, vv), lens, scale)
+    out = oracle.attention(qq, oracle.Cache.from_fp16(kk, vv, bits=bits), lens, scale)
     return oracle.hadamard(out) if flags & 2 else out
 
 
-@pytest.mark.parametrize("flags", [1, 2, 3])
-def test_rotated_decode_matches_oracle(flags):
+@pytest.mark.parametrize("flags,D,bits", [(1, 128, 4), (2, 128, 4), (3, 128, 4), (3, 64, 4), (1, 256, 4),
+                                          (3, 128, 8)])
+def test_rotated_decode_matches_oracle(flags, D, bits):
+    # the tensor-core kernel rotates each query head as it loads it
     torch = need_gpu()
     import int4_kv_cache_gb300 as tq
 
-    B, Hq, Hkv, D, S = 3, 16, 2, 128, 3000
+    B, Hq, Hkv, S = 3, 16, 2, 3000
     lens = np.array([3000, 1, 1377], np.int32)
-    x = synth.decode_inputs(120 + flags, B, Hq, Hkv, D, S, lens=lens, outliers=True)
-    cache = tq.KVCache(B, Hkv, D, S + 8)
+    x = synth.decode_inputs(120 + flags + D + bits, B, Hq, Hkv, D, S, lens=lens, outliers=True)
+    cache = tq.KVCache(B, Hkv, D, S + 8, bits=bits)
     wp = torch.zeros(B, dtype=torch.int32, device="cuda")
     tq.tq_quantize_kv_append(cache, torch.from_numpy(x.k).cuda(), torch.from_numpy(x.v).cuda(), wp, flags=flags)
     ws = workspace_for(B, Hq, Hkv, D, S)
     out = tq.tq_sdpa_int4_decode(cache, torch.from_numpy(x.q).cuda(), torch.from_numpy(lens).cuda(), S,
                                  1 / math.sqrt(D), ws, flags=flags)
     torch.cuda.synchronize()
-    assert_close(out.float().cpu().numpy(), _rotated_reference(x, lens, 1 / math.sqrt(D), flags),
-                 what=f"rotated decode flags={flags}")
+    assert_close(out.float().cpu().numpy(), _rotated_reference(x, lens, 1 / math.sqrt(D), flags, bits),
+                 what=f"rotated decode flags={flags} D={D} bits={bits}")
 
 
 def test_rotated_step_equals_append_then_decode():
@@ -97,3 +100,60 @@ def test_rotated_step_equals_append_then_decode():
     got = tq.tq_decode_step(caches[1], knt, vnt, wp, q, lt, S, 0.088, ws, flags=flags).float().cpu().numpy()
     assert torch.equal(caches[0].buffer, caches[1].buffer)
     assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("D,bits,flags,n_new,paged", [
+    (128, 4, 3, 1, False), (128, 4, 1, 3, False), (128, 4, 2, 1, False), (64, 4, 3, 2, False),
+    (128, 8, 3, 1, False), (64, 8, 1, 1, False), (256, 4, 3, 1, False), (128, 4, 3, 2, True)])
+def test_rotated_step_stores_oracle_rows(D, bits, flags, n_new, paged):
+    # A rotated step appends its rows inside the decode kernel for head dims
+    # up to 128 (rotation across the lanes that hold a row) and through the
+    # append kernel above: either way the stored rows are the oracle's
+    # quantised fp16(H x / sqrt(D)) bit for bit, and the output is the
+    # rotated attention within the output tolerance.
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    B, Hq, Hkv, S = 2, 16, 2, 1504
+    x = synth.decode_inputs(140 + D + bits + flags + n_new, B, Hq, Hkv, D, S, outliers=True)
+    kn, vn = synth.append_tokens(141 + D, 0, B, Hkv, D, n_new, outliers=x.outlier_channels)
+    pos = np.array([S - n_new, 767 - n_new // 2], np.int32)  # the last run; a run boundary (768)
+    lens = pos + n_new
+    if paged:
+        per = -(-S // 256)
+        cache = tq.PagedKVCache(B, Hkv, D, 256, B * per + 1, per, bits=bits)
+        perm = np.random.default_rng(7).permutation(B * per + 1)[:B * per].astype(np.int32).reshape(B, per)
+        cache.block_table.copy_(torch.from_numpy(perm))
+    else:
+        cache = tq.KVCache(B, Hkv, D, S, bits=bits)
+    zero = torch.zeros(B, dtype=torch.int32, device="cuda")
+    # history: rows [0, pos[b]) of each sequence
+    kh, vh = x.k.copy(), x.v.copy()
+    for b in range(B):
+        kh[b, :, pos[b]:] = 0
+        vh[b, :, pos[b]:] = 0
+    tq.tq_quantize_kv_append(cache, torch.from_numpy(kh).cuda(), torch.from_numpy(vh).cuda(), zero, flags=flags)
+    ws = workspace_for(B, Hq, Hkv, D, S)
+    wp = torch.from_numpy(pos).cuda()
+    out = tq.tq_decode_step(cache, torch.from_numpy(kn).cuda(), torch.from_numpy(vn).cuda(), wp,
+                            torch.from_numpy(x.q).cuda(), torch.from_numpy(lens).cuda(), S, 1 / math.sqrt(D), ws,
+                            flags=flags)
+    torch.cuda.synchronize()
+    # the fp16 rows the cache now holds, in sequence order
+    k_all, v_all = kh.copy(), vh.copy()
+    for b in range(B):
+        k_all[b, :, pos[b]:pos[b] + n_new] = kn[b]
+        v_all[b, :, pos[b]:pos[b] + n_new] = vn[b]
+    kk = oracle.rotate_rows_f16(k_all) if flags & 1 else k_all
+    vv = oracle.rotate_rows_f16(v_all) if flags & 2 else v_all
+    want = oracle.Cache.from_fp16(kk, vv, bits=bits)
+    arrays = cache_arrays(cache)
+    if paged:  # pages back in sequence order: [pages, Hkv, P, w] -> [B, Hkv, per * P, w]
+        arrays = [a[perm].transpose(0, 2, 1, 3, 4).reshape(B, Hkv, -1, a.shape[3]) for a in arrays]
+    for b in range(B):
+        n = lens[b]
+        for g_, w_ in zip(arrays, (want.kc, want.ks, want.kb, want.vc, want.vs, want.vb)):
+            assert np.array_equal(g_[b, :, :n], w_[b, :, :n])
+    full = types.SimpleNamespace(q=x.q, k=k_all, v=v_all)
+    assert_close(out.float().cpu().numpy(), _rotated_reference(full, lens, 1 / math.sqrt(D), flags, bits),
+                 what=f"rotated step D={D} bits={bits} flags={flags} n_new={n_new} paged={paged}")
