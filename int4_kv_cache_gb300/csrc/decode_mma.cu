@@ -185,6 +185,7 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    if (p.wait_at_start) pdl_wait_primary();
     const int G = p.group_q;
     const int len = clamp_len(p, b);
     const int t_begin = run_begin(split, p.units, p.n_splits, p.unit_tokens);

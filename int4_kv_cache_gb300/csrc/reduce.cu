@@ -49,6 +49,9 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReducePara
     __shared__ float red[kReduceWarps];
     __shared__ float part_sum[kReduceWarps][D];
     pdl_wait_primary();
+    // phase 1 is complete: an eager next step's phase 1 may launch now (it
+    // waits for this grid before its first read)
+    pdl_launch_dependents();
     const long long bh = blockIdx.x;
     if (p.adv_n != 0 && threadIdx.x == 0 && bh % p.num_q_heads == 0) {  // phase 1 has read the lengths
         const long long b = bh / p.num_q_heads;

@@ -94,6 +94,9 @@ struct DecodeParams {
     // fp16(rot_scale * H q), rotating each query head as it loads it.
     int32_t rotate_q;
     float rot_scale;
+    // Launched as a programmatic dependent of whatever precedes it on the
+    // stream (eager calls): wait for that grid before the first read.
+    int32_t wait_at_start;
 };
 // Most rows per sequence the decode kernel appends itself; longer appends
 // run the append kernel first.
