@@ -338,21 +338,14 @@ tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const in
     if (s != TQ_OK) return s;
     s = make_code_map(&tm_v, cache->v_codes, cache, box_rows);
     if (s != TQ_OK) return s;
-    // Eager calls launch phase 1 as a programmatic dependent of the previous
-    // kernel on the stream (typically the last step's reduce), so that its
-    // launch overlaps that kernel; it waits for it before any read.  Inside
-    // a graph capture the plain launch measured faster.
-    bool pdl = dep_write_pos != nullptr;
-    if (!pdl) {
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusActive;
-        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
-            cudaGetLastError();  // not an error of this call: launch plainly
-        } else if (cs == cudaStreamCaptureStatusNone) {
-            pdl = true;
-            p.wait_at_start = 1;
-        }
-    }
-    return cuda_status(tq::launch_decode_mma(p, cache->head_dim, tm_k, tm_v, stream, pdl));
+    // Phase 1 is always a programmatic dependent of the previous kernel on the
+    // stream (typically the last step's reduce, which lets its dependents
+    // launch once it has seen phase 1 complete), so that its launch overlaps
+    // that kernel.  Without an append before it, it waits for that kernel
+    // before any read; after an append it waits only before the tiles that
+    // hold the new rows.
+    p.wait_at_start = dep_write_pos == nullptr ? 1 : 0;
+    return cuda_status(tq::launch_decode_mma(p, cache->head_dim, tm_k, tm_v, stream, true));
 }
 
 }  // namespace

@@ -94,8 +94,9 @@ struct DecodeParams {
     // fp16(rot_scale * H q), rotating each query head as it loads it.
     int32_t rotate_q;
     float rot_scale;
-    // Launched as a programmatic dependent of whatever precedes it on the
-    // stream (eager calls): wait for that grid before the first read.
+    // Set when no append kernel precedes it: the launch is a programmatic
+    // dependent of whatever kernel precedes it on the stream, and the kernel
+    // waits for that grid before its first read.
     int32_t wait_at_start;
 };
 // Most rows per sequence the decode kernel appends itself; longer appends
