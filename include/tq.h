@@ -288,9 +288,10 @@ size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t num_q_heads,
  *           result is the same as merging one state per chunk (see
  *           tq_sdpa_int4_partial with chunks_per_split = 1).
  * workspace: device scratch (256-byte aligned) of at least
- *           tq_sdpa_workspace_bytes(...) bytes holding the fp32 partial states
- *           (and the rotated query of tq_sdpa_int4_decode_ex / tq_decode_step_ex);
- *           contents on entry are ignored.
+ *           tq_sdpa_workspace_bytes(...) bytes holding the fp32 partial states,
+ *           room for a rotated query and, for batches whose grid spans several
+ *           waves, the device-computed dispatch order of the runs (longest
+ *           first); contents on entry are ignored.
  * out:      fp16 [batch][num_q_heads][head_dim], round-to-nearest-even.
  * Accumulation is fp32; result within 2e-3 abs / 1e-3 rel-L2 of fp64 attention
  * over the dequantised cache. */

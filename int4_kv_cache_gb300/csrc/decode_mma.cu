@@ -184,8 +184,17 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
     uint8_t* smem = dyn_smem + ((1024u - (dyn_base & 1023u)) & 1023u);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     if (p.wait_at_start) pdl_wait_primary();
+    if (p.order != nullptr) {
+        // grids of several waves: the runs in the order the planning kernel
+        // wrote (longest first), each run's kv heads consecutive
+        const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+        const int item = __ldg(p.order + lin / gridDim.y);
+        kvh = lin % gridDim.y;
+        b = item / gridDim.x;
+        split = item % gridDim.x;
+    }
     const int G = p.group_q;
     const int len = clamp_len(p, b);
     const int t_begin = run_begin(split, p.units, p.n_splits, p.unit_tokens);

@@ -224,6 +224,8 @@ tq_status device_facts(DeviceFacts** out) {
 // ------------------------------------------------------------- decode plan --
 struct Plan {
     int n_splits, unit_tokens, units;
+    int tile_tokens = 0;  // the kernel's pipeline tile
+    long long resident = 0;  // CTAs the device holds at once for this kernel
 };
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
@@ -272,6 +274,8 @@ tq_status device_plan(const Store* cache, int max_seq_len, int chunk, tq_impl im
     const int tile = simt ? tq::kSimtTileTokens : tq::mma_tile_tokens(cache->head_dim, cache->bits);
     if (cache->paged && chunk < tile) chunk = tile;  // runs start on tile (hence page-aligned) boundaries
     *pl = make_plan(cache->batch, cache->num_kv_heads, max_seq_len, chunk, tile, f->sms * per_sm);
+    pl->tile_tokens = tile;
+    pl->resident = static_cast<long long>(f->sms) * per_sm;
     return TQ_OK;
 }
 
@@ -290,7 +294,8 @@ tq_status check_decode_args(const Store* cache, const uint16_t* q, int32_t hq, c
 tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
                      int32_t max_seq_len, float attn_scale, const Plan& pl, float* pm, float* plv, float* pa,
                      int32_t* status, tq_impl impl, cudaStream_t stream, const int32_t* dep_write_pos = nullptr,
-                     int32_t dep_n_new = 0, const tq::AppendParams* fused_append = nullptr, bool rotate_q = false) {
+                     int32_t dep_n_new = 0, const tq::AppendParams* fused_append = nullptr, bool rotate_q = false,
+                     int32_t* order_buf = nullptr) {
     if (pl.n_splits > 65535 || cache->num_kv_heads > 65535 || cache->batch > 65535) return TQ_ERR_SHAPE;
     tq::DecodeParams p{};
     p.q = q;
@@ -345,6 +350,24 @@ tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const in
     // before any read; after an append it waits only before the tiles that
     // hold the new rows.
     p.wait_at_start = dep_write_pos == nullptr ? 1 : 0;
+    // A batch whose grid spans several waves is dispatched longest run first
+    // (the lengths are on the device: a one-CTA kernel writes the order).
+    const long long ctas = static_cast<long long>(pl.n_splits) * cache->num_kv_heads * cache->batch;
+    if (order_buf != nullptr && cache->batch > 1 && pl.resident > 0 && ctas > pl.resident &&
+        dep_write_pos == nullptr) {
+        tq::OrderParams op{};
+        op.seq_lens = seq_lens;
+        op.order = order_buf;
+        op.batch = cache->batch;
+        op.max_seq_len = max_seq_len;
+        op.units = pl.units;
+        op.n_splits = pl.n_splits;
+        op.unit_tokens = pl.unit_tokens;
+        op.tile_tokens = pl.tile_tokens;
+        s = cuda_status(tq::launch_order_runs(op, stream));
+        if (s != TQ_OK) return s;
+        p.order = order_buf;
+    }
     return cuda_status(tq::launch_decode_mma(p, cache->head_dim, tm_k, tm_v, stream, true));
 }
 
@@ -548,6 +571,9 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
     float* pa = reinterpret_cast<float*>(ws + 2 * align256(parts * sizeof(float)));
     uint16_t* q_rot = reinterpret_cast<uint16_t*>(ws + 2 * align256(parts * sizeof(float)) +
                                                   align256(parts * cache->head_dim * sizeof(float)));
+    int32_t* order = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(q_rot) +
+                                                align256(static_cast<size_t>(cache->batch) * hq *
+                                                         cache->head_dim * sizeof(uint16_t)));
     const float rs = tq::rotation_scale(cache->head_dim);
     const tq_impl ph1 = impl == TQ_IMPL_SIMT ? TQ_IMPL_SIMT : TQ_IMPL_MMA;
     // keys stored rotated: attend with the rotated query, (H q).(H k) = q.k;
@@ -573,7 +599,7 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
     }
     const bool dep = n_new > 0 && !fused && ph1 == TQ_IMPL_MMA;
     s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, ph1, st,
-                   dep ? write_pos : nullptr, dep ? n_new : 0, fused ? &ap : nullptr, rotate_q);
+                   dep ? write_pos : nullptr, dep ? n_new : 0, fused ? &ap : nullptr, rotate_q, order);
     if (s != TQ_OK) return s;
     tq::ReduceParams r{};
     r.part_m = pm;
@@ -665,9 +691,11 @@ size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t hq, int32_t hkv, int32_t h
     if (cap < 1) cap = 1;
     if (ns > cap) ns = cap;
     const size_t parts = static_cast<size_t>(batch) * hq * static_cast<size_t>(ns);
-    // m, l, acc of every part, then the rotated query (TQ_ROTATE_K)
+    // m, l, acc of every part, the rotated query (TQ_ROTATE_K), the dispatch
+    // order of the runs
     return 2 * align256(parts * sizeof(float)) + align256(parts * head_dim * sizeof(float)) +
-           align256(static_cast<size_t>(batch) * hq * head_dim * sizeof(uint16_t));
+           align256(static_cast<size_t>(batch) * hq * head_dim * sizeof(uint16_t)) +
+           align256(static_cast<size_t>(batch) * static_cast<size_t>(ns) * sizeof(int32_t));
 }
 
 tq_status tq_sdpa_int4_decode_impl(const tq_kv_cache* raw, const uint16_t* q, int32_t hq,

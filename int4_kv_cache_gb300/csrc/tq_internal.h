@@ -98,10 +98,21 @@ struct DecodeParams {
     // dependent of whatever kernel precedes it on the stream, and the kernel
     // waits for that grid before its first read.
     int32_t wait_at_start;
+    // Optional dispatch order of the runs (grids of several waves): entry r
+    // is the run (b * n_splits + split) that CTA slots [r * Hkv, (r + 1) * Hkv)
+    // in launch order take, one per kv head.  Null: the grid's own order.
+    const int32_t* order;
 };
 // Most rows per sequence the decode kernel appends itself; longer appends
 // run the append kernel first.
 constexpr int kFusedAppendMaxRows = 16;
+
+// Longest-first dispatch order of the runs of a split decode (order.cu).
+struct OrderParams {
+    const int32_t* seq_lens;  // [B]
+    int32_t* order;           // [B * n_splits] run indices b * n_splits + s, longest first
+    int32_t batch, max_seq_len, units, n_splits, unit_tokens, tile_tokens;
+};
 
 // Expansion of the cache into fp16 K/V [B][Hkv][n_rows][D] (comparison path).
 struct DequantParams {
@@ -148,6 +159,7 @@ cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, const CUtenso
 // decode kernel then waits only where it reads the appended rows).
 cudaError_t launch_quantize_append_primary(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl_secondary);
+cudaError_t launch_order_runs(const OrderParams& p, cudaStream_t stream);
 cudaError_t launch_advance(int32_t* seq_lens, int32_t* write_pos, int batch, int n, cudaStream_t stream);
 cudaError_t launch_dequant(const DequantParams& p, int sm_count, cudaStream_t stream);
 // out[r] = fp16(H x[r]) for rows of `dim` fp16 values (dim 64 / 128 / 256); out may be x.

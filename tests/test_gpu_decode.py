@@ -61,6 +61,60 @@ def test_ragged_lengths_and_tails(D, Hq, Hkv, impl):
         assert_close(out, ref, what=f"D{D} chunk{chunk} impl{impl}")
 
 
+@pytest.mark.parametrize("B,pattern", [(2, "equal"), (64, "ties"), (128, "ties"), (129, "random"),
+                                       (200, "random"), (37, "zeros")])
+def test_batch_order_and_empty_runs(B, pattern):
+    """Batches whose grid spans several waves (here B >= 128) are dispatched
+    longest run first in an order the device computes from the lengths: every
+    run still lands in its own sequence's output, for equal lengths, many ties
+    and empty sequences; smaller batches keep the grid order."""
+    need_gpu()
+    S = 300
+    rng = np.random.default_rng(B)
+    if pattern == "equal":
+        lens = np.full(B, S, np.int32)
+    elif pattern == "ties":
+        lens = rng.choice(np.array([0, 1, 129, S], np.int32), size=B)
+    elif pattern == "zeros":
+        lens = np.where(rng.random(B) < 0.5, 0, rng.integers(1, S + 1, B)).astype(np.int32)
+    else:
+        lens = rng.integers(0, S + 1, B).astype(np.int32)
+    lens[rng.integers(0, B)] = S
+    x = synth.decode_inputs(500 + B, B, 8, 2, 64, S, lens=lens)
+    cache = gpu_cache_from_fp16(x.k, x.v)
+    a = 1 / math.sqrt(64)
+    out = decode(cache, x.q, lens, S, a, chunk=64)
+    assert np.all(out[lens == 0] == 0.0)
+    assert_close(out, oracle.attention(x.q, oracle.Cache.from_fp16(x.k, x.v), lens, a), what=f"B{B} {pattern}")
+
+
+def test_batch_order_paged_equals_contiguous():
+    """The dispatch order with a paged cache: same output as the contiguous
+    cache bit for bit, and the oracle's within the tolerance."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    B, Hq, Hkv, D, S, P = 160, 8, 2, 128, 384, 128
+    rng = np.random.default_rng(11)
+    lens = rng.integers(0, S + 1, B).astype(np.int32)
+    lens[3] = S
+    x = synth.decode_inputs(611, B, Hq, Hkv, D, S, lens=lens)
+    cont = gpu_cache_from_fp16(x.k, x.v)
+    per = S // P
+    paged = tq.PagedKVCache(B, Hkv, D, P, B * per, per)
+    perm = rng.permutation(B * per).astype(np.int32).reshape(B, per)
+    paged.block_table.copy_(torch.from_numpy(perm))
+    tq.tq_quantize_kv_append(paged, torch.from_numpy(x.k).cuda(), torch.from_numpy(x.v).cuda(),
+                             torch.zeros(B, dtype=torch.int32, device="cuda"))
+    q, lt = torch.from_numpy(x.q).cuda(), torch.from_numpy(lens).cuda()
+    ws = workspace_for(B, Hq, Hkv, D, S)
+    a = 1 / math.sqrt(D)
+    out_c = tq.tq_sdpa_int4_decode(cont, q, lt, S, a, ws).float().cpu().numpy()
+    out_p = tq.tq_sdpa_int4_decode(paged, q, lt, S, a, ws).float().cpu().numpy()
+    assert np.array_equal(out_p, out_c)
+    assert_close(out_c, oracle.attention(x.q, oracle.Cache.from_fp16(x.k, x.v), lens, a), what="ordered paged")
+
+
 @pytest.mark.parametrize("impl", IMPLS)
 def test_oracle_quantised_cache_decode(impl):
     """Decode over a cache the oracle quantized (isolates attention from the
