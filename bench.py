@@ -474,7 +474,9 @@ def run_ragged(args, tq, synth, torch, dev, peak):
     decode step = append one token per sequence + decode, K steps replayed
     from one CUDA graph with the lengths advancing on the device
     (TQ_STEP_ADVANCE); contiguous cache vs paged cache (256-token pages,
-    shuffled pool, unused logical pages pointing at one scratch page)."""
+    shuffled pool, unused logical pages pointing at one scratch page).  The
+    grid spans several waves, so each step also runs the one-CTA kernel that
+    orders the runs longest first."""
     Bt, steps = 32, max(10, args.steps // 2)
     lens = synth.ragged_lengths(4, Bt, 1024, 32768)
     cap = 32768 + 256
@@ -536,9 +538,9 @@ def run_ragged(args, tq, synth, torch, dev, peak):
 
 def run_rotation(args, tq, synth, torch, dev, caches, qs, ws, out, peak):
     """Hadamard-rotated int4 at the same shape: the decode step with K and V
-    rotated (query rotated before phase 1, output rotated back in the reduce;
-    the rotated one-row append runs the append kernel) and the 128K prefill
-    quantize with the rotation fused in."""
+    rotated (phase 1 rotates the query heads as it loads them and the one-row
+    append before quantizing it; the reduce rotates the output back) and the
+    128K prefill quantize with the rotation fused in."""
     nl = len(caches)
     flags = tq.TQ_ROTATE_K | tq.TQ_ROTATE_V
     k_new = torch.randn((B, HKV, 1, D), device=dev).half()
