@@ -40,6 +40,7 @@
 //    the swizzled tile; the permutation is undone when the state is written.
 #include <math.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "tq_device.cuh"
@@ -842,13 +843,14 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
 
 template <int D, bool PAGED, int BITS>
 cudaError_t set_smem_attr() {
-    static bool done[64] = {};
+    // per device; setting the attribute twice (two host threads) is harmless
+    static std::atomic<bool> done[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, PAGED, BITS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, BITS>::SMEM_BYTES);
-    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
     return e;
 }
 

@@ -14,6 +14,8 @@
 // writes 32 bytes of codes per tensor and the four scale / bias halves.  With
 // no cross-lane reductions the per-group work (min/max, the scale division,
 // the reciprocal) is spread over 64 elements.
+#include <atomic>
+
 #include "tq_device.cuh"
 #include "tq_hadamard.cuh"
 #include "tq_internal.h"
@@ -320,7 +322,7 @@ cudaError_t launch_quantize_append_tma(const AppendParams& p, const CUtensorMap&
     const bool rot = (p.flags & (TQ_ROTATE_K | TQ_ROTATE_V)) != 0;
     if (rot) grid = grid * 2 / 3;  // the rotating instantiation runs 2 CTAs per SM (registers)
     if (grid < 1) grid = 1;
-    static bool attr_done[64][4] = {};
+    static std::atomic<bool> attr_done[64][4];  // per device and variant; a repeated set is harmless
     int dev = 0;
     cudaGetDevice(&dev);
     const int vi = (p.bits == 8 ? 1 : 0) + (rot ? 2 : 0);
@@ -328,10 +330,10 @@ cudaError_t launch_quantize_append_tma(const AppendParams& p, const CUtensorMap&
         if (p.bits == 8) return rot ? quantize_append_tma_kernel<8, true> : quantize_append_tma_kernel<8, false>;
         return rot ? quantize_append_tma_kernel<4, true> : quantize_append_tma_kernel<4, false>;
     }();
-    if (dev >= 0 && dev < 64 && !attr_done[dev][vi]) {
+    if (dev >= 0 && dev < 64 && !attr_done[dev][vi].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmemBytes);
         if (e != cudaSuccess) return e;
-        attr_done[dev][vi] = true;
+        attr_done[dev][vi].store(true, std::memory_order_release);
     }
     kern<<<grid, kTmaThreads, kTmaSmemBytes, stream>>>(tm_k, tm_v, p, groups, n_tiles);
     return cudaGetLastError();
