@@ -14,9 +14,9 @@
 //    arrays streams into a ring of shared-memory stages: the code tiles by
 //    2-D TMA with the 128-byte swizzle, the scale/bias rows by 1-D bulk
 //    copies, completion on mbarriers.  There is no producer warp: the last
-//    warp to finish a stage issues its refill, so all four warps compute and
-//    four CTAs fit on an SM.  Every byte of the cache is read from HBM once
-//    per step, with an evict-first L2 policy.
+//    warp to finish a stage issues its refill, so all four warps compute
+//    (three CTAs per SM for int4 at head_dim 128).  Every byte of the cache
+//    is read from HBM once per step, with an evict-first L2 policy.
 //  * Consumer warps turn the nibbles into fp16 operands with one AND per
 //    register: a 4-bit code n in the low mantissa bits of a zero-exponent fp16
 //    is the subnormal n * 2^-24, and the high nibble of a byte gives
