@@ -540,7 +540,7 @@ tq_status run_append(const tq::AppendParams& ap, cudaStream_t st) {
 bool valid_step_flags(uint32_t flags) { return valid_rotation(flags & ~TQ_STEP_ADVANCE); }
 
 // Decode (optionally preceded by an append of n_new rows) with the workspace
-// laid out as [m][l][acc][rotated q]; the one path behind tq_decode_step*,
+// laid out as [m][l][acc][rotated q][run order]; the one path behind tq_decode_step*,
 // tq_sdpa_int4_decode*.
 tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t* v_new, int32_t n_new,
                       const int32_t* write_pos, const uint16_t* q, int32_t hq, const int32_t* seq_lens,
