@@ -117,8 +117,8 @@ typedef struct tq_kv_cache {
     int32_t capacity;   /* tokens per (sequence, kv head) */
     int32_t bits;       /* code width: 4 (two codes per byte, element 2i in the low
                            nibble of byte i) or 8 (one code per byte; the
-                           TurboQuant Gemma 4 page's --kv-bits 8); head_dim 256
-                           takes 4 only */
+                           TurboQuant Gemma 4 page's --kv-bits 8), every
+                           head_dim */
 } tq_kv_cache;
 
 /* Paged cache: a pool of pages, each holding page_tokens consecutive tokens of

@@ -63,13 +63,22 @@ struct Cfg {
     static constexpr int BPT = D * BITS / 8;       // code bytes per token
     static constexpr int SPT = BPT / 16;           // 16-byte segments per token
     static constexpr int EPS = 128 / BITS;         // elements per 16-byte segment
-    static constexpr int TPR = 128 / BPT;          // tokens per 128-byte swizzle row (1 for 128-byte tokens)
+    // A code tile is HALVES column blocks of T rows of ROWB bytes, each laid
+    // out by one TMA box with the 128-byte swizzle: one block (and TPR tokens
+    // per 128-byte row) when a token's codes fit 128 bytes, two 128-byte
+    // blocks for the 256-byte rows of int8 at head_dim 256.
+    static constexpr int ROWB = BPT < 128 ? BPT : 128;
+    static constexpr int HALVES = BPT / ROWB;
+    static constexpr int SPR = ROWB / 16;          // 16-byte segments of a token in one block
+    static constexpr int TPR = 128 / ROWB;         // tokens per 128-byte swizzle row (1 for 128-byte blocks)
     static constexpr int NWC = 4;                  // warps (all consume; the last to finish a stage refills it)
     static constexpr int MT = (BPT >= 128) ? 1 : 2;  // 16-token m-tiles per warp per stage
     static constexpr float CODE_MEAN = ((1 << BITS) - 1) * 0.5f;  // mean of a code uniform on 0..L
     static constexpr int T = NWC * MT * 16;        // tokens per stage
-    static constexpr int STAGES = 4;
+    // 3 stages of 34 KB for the int8 head_dim-256 tiles keep 2 CTAs per SM
+    static constexpr int STAGES = HALVES > 1 ? 3 : 4;
     static constexpr int CODE_BYTES = T * BPT;     // one code tile (K or V)
+    static constexpr int HALF_BYTES = T * ROWB;    // one column block of a code tile
     static constexpr int SB_BYTES = T * NG * 2;    // one scale or bias tile
     static constexpr int STAGE_BYTES = ((2 * CODE_BYTES + 4 * SB_BYTES + 1023) / 1024) * 1024;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;  // +1024 for base alignment
@@ -80,7 +89,7 @@ struct Cfg {
     // KB each) and for int8, 4 for int4 D = 64 (whose stages are half as
     // large), 2 for D = 256.
     static constexpr int MIN_CTAS = (D == 256) ? 2 : ((D == 128 || BITS == 8) ? 3 : 4);
-    static_assert(BPT <= 128, "a token's codes fit one 128-byte swizzle row");
+    static_assert(BPT <= 128 || BPT == 256, "a token's codes span one 128-byte swizzle row or two blocks");
     static_assert(CODE_BYTES % 1024 == 0, "code tiles must keep the 1024-byte swizzle period");
     static_assert(STAGES * STAGE_BYTES >= NWC * 8 * D * 4, "merge buffer must fit in the stages");
 };
@@ -106,12 +115,14 @@ __device__ __forceinline__ int tok_of_row(int m) {
 }
 
 // Shared address of 16-byte segment `seg` of token `tok` in a code tile laid
-// out by a TMA box of 128-byte rows with CU_TENSOR_MAP_SWIZZLE_128B.
+// out by TMA boxes of 128-byte rows with CU_TENSOR_MAP_SWIZZLE_128B (segment
+// seg of a 256-byte row sits in column block seg / 8).
 template <class C>
 __device__ __forceinline__ uint32_t code_addr(uint32_t tile, int tok, int seg) {
+    const int half = seg / C::SPR, s = seg % C::SPR;
     const int row = tok / C::TPR;
-    const int chunk = (tok % C::TPR) * C::SPT + seg;
-    return tile + row * 128 + ((chunk ^ (row & 7)) << 4);
+    const int chunk = (tok % C::TPR) * C::SPR + s;
+    return tile + half * C::HALF_BYTES + row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
 struct alignas(8) Half4 {
@@ -279,9 +290,18 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
         const uint32_t sb_bytes = static_cast<uint32_t>(avail) * NG * 2;
         uint8_t* st = smem + stage * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&full_bar[stage], 2 * C::CODE_BYTES + 4 * sb_bytes);
-        const int y = static_cast<int>((row * C::BPT) / 128);
-        tma_load_2d(st, &tm_k, 0, y, &full_bar[stage], policy);
-        tma_load_2d(st + C::CODE_BYTES, &tm_v, 0, y, &full_bar[stage], policy);
+        if constexpr (C::HALVES == 1) {  // maps of 128-byte rows
+            const int y = static_cast<int>((row * C::BPT) / 128);
+            tma_load_2d(st, &tm_k, 0, y, &full_bar[stage], policy);
+            tma_load_2d(st + C::CODE_BYTES, &tm_v, 0, y, &full_bar[stage], policy);
+        } else {  // maps of BPT-byte rows, one box per 128-byte column block
+            const int y = static_cast<int>(row);
+#pragma unroll
+            for (int h = 0; h < C::HALVES; ++h) {
+                tma_load_2d(st + h * C::HALF_BYTES, &tm_k, h * 128, y, &full_bar[stage], policy);
+                tma_load_2d(st + C::CODE_BYTES + h * C::HALF_BYTES, &tm_v, h * 128, y, &full_bar[stage], policy);
+            }
+        }
         const long long sb_off = row * NG;
         uint8_t* sb = st + 2 * C::CODE_BYTES;
         bulk_load(sb + 0 * C::SB_BYTES, p.k_scale + sb_off, sb_bytes, &full_bar[stage], policy);
@@ -538,7 +558,7 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
     #pragma unroll
                 for (int sp = 0; sp < C::SPT / 2; ++sp) {
                     uint32_t x0, x1, x2, x3;
-                    ldmatrix_x4(kc_s + tb * C::BPT + (lm_off[sp] ^ sw), x0, x1, x2, x3);
+                    ldmatrix_x4(kc_s + tb * C::ROWB + (lm_off[sp] ^ sw), x0, x1, x2, x3);
     #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int s = 2 * sp + e;
@@ -681,7 +701,7 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
                 for (int mt = 0; mt < C::MT; ++mt) {
                     const int tb = (warp * C::MT + mt) * 16;
                     const uint32_t sw = static_cast<uint32_t>((tb / C::TPR) & 7) << 4;
-                    ldmatrix_x4_trans(vc_s + tb * C::BPT + (lm_off[sp] ^ sw), x[mt][0], x[mt][1], x[mt][2], x[mt][3]);
+                    ldmatrix_x4_trans(vc_s + tb * C::ROWB + (lm_off[sp] ^ sw), x[mt][0], x[mt][1], x[mt][2], x[mt][3]);
                 }
     #pragma unroll
                 for (int e = 0; e < 2; ++e) {
@@ -889,14 +909,14 @@ int ctas_per_sm_d() {
 // (head_dim, bits) pairs with a kernel: int4 at 64 / 128 / 256, int8 at 64 / 128
 // (an int8 row of 256 would not fit one 128-byte swizzle row).
 bool mma_supported(int head_dim, int bits) {
-    return (bits == 4 && (head_dim == 64 || head_dim == 128 || head_dim == 256)) ||
-           (bits == 8 && (head_dim == 64 || head_dim == 128));
+    return (bits == 4 || bits == 8) && (head_dim == 64 || head_dim == 128 || head_dim == 256);
 }
 
-#define TQ_DISPATCH(EXPR64_4, EXPR128_4, EXPR256_4, EXPR64_8, EXPR128_8, FALLBACK) \
+#define TQ_DISPATCH(EXPR64_4, EXPR128_4, EXPR256_4, EXPR64_8, EXPR128_8, EXPR256_8, FALLBACK) \
     if (bits == 8) {                                                              \
         if (head_dim == 64) return EXPR64_8;                                      \
         if (head_dim == 128) return EXPR128_8;                                    \
+        if (head_dim == 256) return EXPR256_8;                                    \
     } else {                                                                      \
         if (head_dim == 64) return EXPR64_4;                                      \
         if (head_dim == 128) return EXPR128_4;                                    \
@@ -905,17 +925,17 @@ bool mma_supported(int head_dim, int bits) {
     return FALLBACK;
 
 int mma_tile_tokens(int head_dim, int bits) {
-    TQ_DISPATCH(Cfg<64>::T, Cfg<128>::T, Cfg<256>::T, (Cfg<64, 8>::T), (Cfg<128, 8>::T), 0)
+    TQ_DISPATCH(Cfg<64>::T, Cfg<128>::T, Cfg<256>::T, (Cfg<64, 8>::T), (Cfg<128, 8>::T), (Cfg<256, 8>::T), 0)
 }
 
 int mma_smem_bytes(int head_dim, int bits) {
     TQ_DISPATCH(Cfg<64>::SMEM_BYTES, Cfg<128>::SMEM_BYTES, Cfg<256>::SMEM_BYTES, (Cfg<64, 8>::SMEM_BYTES),
-                (Cfg<128, 8>::SMEM_BYTES), 0)
+                (Cfg<128, 8>::SMEM_BYTES), (Cfg<256, 8>::SMEM_BYTES), 0)
 }
 
 int mma_ctas_per_sm(int head_dim, int bits) {
     TQ_DISPATCH((ctas_per_sm_d<64, 4>()), (ctas_per_sm_d<128, 4>()), (ctas_per_sm_d<256, 4>()),
-                (ctas_per_sm_d<64, 8>()), (ctas_per_sm_d<128, 8>()), 1)
+                (ctas_per_sm_d<64, 8>()), (ctas_per_sm_d<128, 8>()), (ctas_per_sm_d<256, 8>()), 1)
 }
 
 cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
@@ -925,7 +945,8 @@ cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, const CUtenso
                 (launch_d<128, 4>(p, tm_k, tm_v, stream, pdl_secondary)),
                 (launch_d<256, 4>(p, tm_k, tm_v, stream, pdl_secondary)),
                 (launch_d<64, 8>(p, tm_k, tm_v, stream, pdl_secondary)),
-                (launch_d<128, 8>(p, tm_k, tm_v, stream, pdl_secondary)), cudaErrorInvalidValue)
+                (launch_d<128, 8>(p, tm_k, tm_v, stream, pdl_secondary)),
+                (launch_d<256, 8>(p, tm_k, tm_v, stream, pdl_secondary)), cudaErrorInvalidValue)
 }
 
 #undef TQ_DISPATCH

@@ -147,17 +147,21 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// The code array of a cache seen as [rows][128 bytes] (uint8), boxes of
-// `box_rows` rows with the 128-byte swizzle; reads past the end are zero-filled.
-tq_status make_code_map(CUtensorMap* map, const uint8_t* codes, const Store* c, int box_rows) {
+// The code array of a cache as a 2-D uint8 tensor map for the decode kernel's
+// tiles of `tile_tokens` tokens, with the 128-byte swizzle; reads past the end
+// are zero-filled.
+tq_status make_code_map(CUtensorMap* map, const uint8_t* codes, const Store* c, int tile_tokens) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return cuda_status(cudaErrorNotSupported);
-    const cuuint64_t rows =
-        static_cast<cuuint64_t>(c->map.num_pages) * c->num_kv_heads * c->map.page_tokens * (c->head_dim * c->bits / 8) /
-        128;
-    cuuint64_t dims[2] = {128, rows};
-    cuuint64_t strides[1] = {128};
-    cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+    const cuuint64_t bpt = static_cast<cuuint64_t>(c->head_dim) * c->bits / 8;  // code bytes per token
+    const cuuint64_t tokens = static_cast<cuuint64_t>(c->map.num_pages) * c->num_kv_heads * c->map.page_tokens;
+    // Tokens of up to 128 bytes: the codes seen as rows of 128 bytes, a tile of
+    // tile_tokens tokens one box.  256-byte tokens (int8, head_dim 256): rows of
+    // 256 bytes, a tile two boxes of 128-byte columns.
+    const bool wide = bpt > 128;
+    cuuint64_t dims[2] = {wide ? bpt : 128, wide ? tokens : tokens * bpt / 128};
+    cuuint64_t strides[1] = {wide ? bpt : 128};
+    cuuint32_t box[2] = {128, static_cast<cuuint32_t>(wide ? tile_tokens : tile_tokens * bpt / 128)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -338,10 +342,10 @@ tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const in
         return cuda_status(tq::launch_decode_simt(p, cache->head_dim, stream));
     }
     CUtensorMap tm_k, tm_v;
-    const int box_rows = tq::mma_tile_tokens(cache->head_dim, cache->bits) * (cache->head_dim * cache->bits / 8) / 128;
-    tq_status s = make_code_map(&tm_k, cache->k_codes, cache, box_rows);
+    const int tile = tq::mma_tile_tokens(cache->head_dim, cache->bits);
+    tq_status s = make_code_map(&tm_k, cache->k_codes, cache, tile);
     if (s != TQ_OK) return s;
-    s = make_code_map(&tm_v, cache->v_codes, cache, box_rows);
+    s = make_code_map(&tm_v, cache->v_codes, cache, tile);
     if (s != TQ_OK) return s;
     // Phase 1 is always a programmatic dependent of the previous kernel on the
     // stream (typically the last step's reduce, which lets its dependents

@@ -252,9 +252,9 @@ def test_int8_sizes_and_validation(L):
     assert L.tq_kv_cache_carve_ex(ctypes.byref(c), 0x100000, 2, 8, 128, 64, 8, 64) == 0
     assert c.bits == 8 and c.v_codes - c.k_codes == 2 * 8 * 64 * 128
     assert _decode(L, _fake_cache()) != 6
-    bad = _fake_cache(D=256)
-    bad.bits = 8  # an int8 row of 256 bytes: no kernel
-    assert _decode(L, bad) == 6
+    wide = _fake_cache(D=256)
+    wide.bits = 8  # int8 rows of 256 bytes: two 128-byte column blocks per tile
+    assert _decode(L, wide) != 6
     bad = _fake_cache()
     bad.bits = 0
     assert _decode(L, bad) == 6

@@ -24,7 +24,7 @@ def _cache8(tq, torch, k, v, capacity=None):
     return c
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 def test_int8_quantize_bit_exact_with_edge_groups(D):
     torch = need_gpu()
     import int4_kv_cache_gb300 as tq
@@ -67,7 +67,7 @@ def test_int8_decode_matches_oracle(name):
     assert_close(out, ref, what=f"int8 {name}")
 
 
-@pytest.mark.parametrize("D,Hq,Hkv", [(128, 8, 2), (64, 8, 8), (128, 8, 1)])
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 8, 2), (64, 8, 8), (128, 8, 1), (256, 16, 2)])
 def test_int8_ragged_lengths_and_chunks(D, Hq, Hkv):
     torch = need_gpu()
     import int4_kv_cache_gb300 as tq
@@ -149,3 +149,64 @@ def test_int8_dequantize_bit_exact():
                           oracle.dequantize_rows_f16(kc[:, :, :650], ks[:, :, :650], kb[:, :, :650], bits=8))
     assert np.array_equal(v16.cpu().numpy().view(np.uint16),
                           oracle.dequantize_rows_f16(vc[:, :, :650], vs[:, :, :650], vb[:, :, :650], bits=8))
+
+
+@pytest.mark.parametrize("name", ["gemma_33", "gemma_423", "gemma_786", "gemma_950"])
+def test_int8_gemma_shape_matches_oracle(name):
+    """int8 at head_dim 256 (two 128-byte column blocks per 256-byte row) on the
+    Gemma-style unscaled-attention configs."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    w = synth.WORKLOADS[name]
+    x = w.draw()
+    c = _cache8(tq, torch, x.k, x.v)
+    ws = workspace_for(x.q.shape[0], x.q.shape[1], x.k.shape[1], x.k.shape[3], w.seq_len)
+    out = tq.tq_sdpa_int4_decode(c, torch.from_numpy(x.q).cuda(), torch.from_numpy(x.lens).cuda(), w.seq_len,
+                                 w.attn_scale, ws).float().cpu().numpy()
+    ref = oracle.attention(x.q, oracle.Cache.from_fp16(x.k, x.v, bits=8), x.lens, w.attn_scale)
+    assert_close(out, ref, what=f"int8 {name}")
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_int8_d256_step_stores_oracle_rows(paged):
+    """The decode step with int8 head_dim 256 rows: fused append bit-exact
+    with the oracle's quantiser, output within tolerance; paged too."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    B, Hq, Hkv, D, S, P = 2, 16, 2, 256, 1024, 128
+    x = synth.decode_inputs(260 + int(paged), B, Hq, Hkv, D, S, outliers=True)
+    kn, vn = synth.append_tokens(261, 0, B, Hkv, D, 2, outliers=x.outlier_channels)
+    pos = np.array([S - 2, 500], np.int32)
+    lens = pos + 2
+    if paged:
+        per = S // P
+        c = tq.PagedKVCache(B, Hkv, D, P, B * per, per, bits=8)
+        perm = np.random.default_rng(3).permutation(B * per).astype(np.int32).reshape(B, per)
+        c.block_table.copy_(torch.from_numpy(perm))
+    else:
+        c = tq.KVCache(B, Hkv, D, S, bits=8)
+    kh, vh = x.k.copy(), x.v.copy()
+    for b in range(B):
+        kh[b, :, pos[b]:] = 0
+        vh[b, :, pos[b]:] = 0
+    tq.tq_quantize_kv_append(c, torch.from_numpy(kh).cuda(), torch.from_numpy(vh).cuda(),
+                             torch.zeros(B, dtype=torch.int32, device="cuda"))
+    ws = workspace_for(B, Hq, Hkv, D, S)
+    out = tq.tq_decode_step(c, torch.from_numpy(kn).cuda(), torch.from_numpy(vn).cuda(), torch.from_numpy(pos).cuda(),
+                            torch.from_numpy(x.q).cuda(), torch.from_numpy(lens).cuda(), S, 1.0, ws)
+    torch.cuda.synchronize()
+    for b in range(B):
+        kh[b, :, pos[b]:pos[b] + 2] = kn[b]
+        vh[b, :, pos[b]:pos[b] + 2] = vn[b]
+    want = oracle.Cache.from_fp16(kh, vh, bits=8)
+    arrays = cache_arrays(c)
+    if paged:
+        arrays = [a[perm].transpose(0, 2, 1, 3, 4).reshape(B, Hkv, -1, a.shape[3]) for a in arrays]
+    for b in range(B):
+        n = lens[b]
+        for g_, w_ in zip(arrays, (want.kc, want.ks, want.kb, want.vc, want.vs, want.vb)):
+            assert np.array_equal(g_[b, :, :n], w_[b, :, :n])
+    ref = oracle.attention(x.q, want, lens, 1.0)
+    assert_close(out.float().cpu().numpy(), ref, what=f"int8 D256 step paged={paged}")
