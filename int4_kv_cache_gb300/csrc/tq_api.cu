@@ -299,7 +299,7 @@ tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const in
                      int32_t max_seq_len, float attn_scale, const Plan& pl, float* pm, float* plv, float* pa,
                      int32_t* status, tq_impl impl, cudaStream_t stream, const int32_t* dep_write_pos = nullptr,
                      int32_t dep_n_new = 0, const tq::AppendParams* fused_append = nullptr, bool rotate_q = false,
-                     int32_t* order_buf = nullptr) {
+                     int32_t* order_buf = nullptr, uint16_t* direct_out = nullptr) {
     if (pl.n_splits > 65535 || cache->num_kv_heads > 65535 || cache->batch > 65535) return TQ_ERR_SHAPE;
     tq::DecodeParams p{};
     p.q = q;
@@ -354,6 +354,7 @@ tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const in
     // before any read; after an append it waits only before the tiles that
     // hold the new rows.
     p.wait_at_start = dep_write_pos == nullptr ? 1 : 0;
+    p.out = direct_out;
     // A batch whose grid spans several waves is dispatched longest run first
     // (the lengths are on the device: a one-CTA kernel writes the order).
     const long long ctas = static_cast<long long>(pl.n_splits) * cache->num_kv_heads * cache->batch;
@@ -602,8 +603,13 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
         if (s != TQ_OK) return s;
     }
     const bool dep = n_new > 0 && !fused && ph1 == TQ_IMPL_MMA;
+    // One run per sequence (short sequences): phase 1 writes the output
+    // itself and no reduce is launched, unless the reduce has other work (the
+    // output rotation of TQ_ROTATE_V, the length advance)
+    const bool direct = pl.n_splits == 1 && ph1 == TQ_IMPL_MMA && !(flags & TQ_ROTATE_V) && !advance;
     s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, ph1, st,
-                   dep ? write_pos : nullptr, dep ? n_new : 0, fused ? &ap : nullptr, rotate_q, order);
+                   dep ? write_pos : nullptr, dep ? n_new : 0, fused ? &ap : nullptr, rotate_q, order,
+                   direct ? out : nullptr);
     if (s != TQ_OK) return s;
     tq::ReduceParams r{};
     r.part_m = pm;
@@ -624,6 +630,7 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
         r.adv_write_pos = const_cast<int32_t*>(write_pos);
         r.adv_n = n_new;
     }
+    if (direct) return s;
     s = cuda_status(tq::launch_reduce(r, st, true));
     if (s != TQ_OK || !advance || fused || n_new == 0) return s;
     return cuda_status(tq::launch_advance(const_cast<int32_t*>(seq_lens), const_cast<int32_t*>(write_pos),

@@ -102,6 +102,9 @@ struct DecodeParams {
     // is the run (b * n_splits + split) that CTA slots [r * Hkv, (r + 1) * Hkv)
     // in launch order take, one per kv head.  Null: the grid's own order.
     const int32_t* order;
+    // One run per sequence (n_splits = 1): the merged state is the output;
+    // when set, the kernel writes fp16(acc / l) here instead of the partials.
+    uint16_t* out;
 };
 // Most rows per sequence the decode kernel appends itself; longer appends
 // run the append kernel first.

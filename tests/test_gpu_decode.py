@@ -191,12 +191,15 @@ def test_partials_match_oracle_chunks():
             assert_close(acc[ne] / l[ne][:, None], oa[ne] / ol[ne][:, None], what=f"chunk{chunk} impl{impl}")
 
 
-def test_decode_equals_partial_plan_plus_reduce():
-    """tq_sdpa_int4_decode == phase 1 with the decode's own plan + phase 2."""
+@pytest.mark.parametrize("name", ["llama70b_16k", "gemma_33", "tiny"])
+def test_decode_equals_partial_plan_plus_reduce(name):
+    """tq_sdpa_int4_decode == phase 1 with the decode's own plan + phase 2, bit
+    for bit; gemma_33 has one run per sequence, where phase 1 writes the
+    output itself (no reduce launch) with the reduce's arithmetic."""
     torch = need_gpu()
     import int4_kv_cache_gb300 as tq
 
-    w = synth.WORKLOADS["llama70b_16k"]
+    w = synth.WORKLOADS[name]
     x = w.draw()
     cache = gpu_cache_from_fp16(x.k, x.v)
     q = torch.from_numpy(x.q).cuda()
