@@ -151,17 +151,21 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_append_kernel(const Ap
 // consecutive lanes, this thread holding group g in v (fp32).  The stages run
 // in the order of the fast transform (h = 1, 2, ..., 32 inside the thread,
 // then h = 64, 128 with the lanes lane ^ 1, lane ^ 2), each butterfly one
-// round-to-nearest add and one subtract, so the result equals the sequential
-// transform bit for bit; then the scale.  Every lane of the warp takes part.
+// round-to-nearest add and one subtract (two butterflies per paired fp32
+// operation), so the result equals the sequential transform bit for bit; then
+// the scale.  Every lane of the warp takes part.
 template <int NG>
 __device__ __forceinline__ void rotate_group_thread(float (&v)[64], int g, float scale) {
-#pragma unroll
-    for (int i = 0; i < 64; i += 2) {  // h = 1
-        const float u = v[i], w = v[i + 1];
-        v[i] = __fadd_rn(u, w);
-        v[i + 1] = __fsub_rn(u, w);
-    }
     const float2 m1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+    for (int i = 0; i < 64; i += 4) {  // h = 1: butterflies (i, i+1) and (i+2, i+3) in one paired op each
+        const float2 a = make_float2(v[i], v[i + 2]), b = make_float2(v[i + 1], v[i + 3]);
+        const float2 sum = __fadd2_rn(a, b), dif = __ffma2_rn(b, m1, a);
+        v[i] = sum.x;
+        v[i + 2] = sum.y;
+        v[i + 1] = dif.x;
+        v[i + 3] = dif.y;
+    }
 #pragma unroll
     for (int h = 2; h < 64; h <<= 1) {  // pairs (i, i+1) with bit h clear: two butterflies per paired op
 #pragma unroll
@@ -177,11 +181,17 @@ __device__ __forceinline__ void rotate_group_thread(float (&v)[64], int g, float
     }
 #pragma unroll
     for (int hl = 1; hl < NG; hl <<= 1) {  // h = 64 * hl: the group in lane ^ hl
-        const bool upper = (g & hl) != 0;
+        // lower lane: v + other; upper lane: other - v; both one rounding of
+        // fma(v, c, other) with c = +1 / -1 (exact products)
+        const float c = (g & hl) != 0 ? -1.0f : 1.0f;
+        const float2 c2 = make_float2(c, c);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-            const float other = __shfl_xor_sync(0xffffffffu, v[i], hl);
-            v[i] = upper ? __fsub_rn(other, v[i]) : __fadd_rn(v[i], other);
+        for (int i = 0; i < 64; i += 2) {
+            const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, v[i], hl),
+                                         __shfl_xor_sync(0xffffffffu, v[i + 1], hl));
+            const float2 r = __ffma2_rn(make_float2(v[i], v[i + 1]), c2, o);
+            v[i] = r.x;
+            v[i + 1] = r.y;
         }
     }
     const float2 sc = make_float2(scale, scale);

@@ -112,7 +112,8 @@ def test_prefill_full_128k_layer_bit_exact_sampled():
         np.testing.assert_array_equal(g, want)
 
 
-@pytest.mark.parametrize("flags,bits,D", [(0, 4, 128), (3, 4, 128), (0, 8, 128), (1, 4, 64), (0, 4, 256)])
+@pytest.mark.parametrize("flags,bits,D", [(0, 4, 128), (3, 4, 128), (0, 8, 128), (1, 4, 64), (0, 4, 256),
+                                          (2, 4, 256), (3, 8, 256), (3, 8, 128)])
 def test_large_append_tma_path_bit_exact(flags, bits, D):
     """Appends of >= 8192 groups stream through the persistent TMA kernel:
     bit-exact against the oracle with a ragged last tile (the group count is
