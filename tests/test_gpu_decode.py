@@ -62,7 +62,7 @@ def test_ragged_lengths_and_tails(D, Hq, Hkv, impl):
 
 
 @pytest.mark.parametrize("B,pattern", [(2, "equal"), (64, "ties"), (128, "ties"), (129, "random"),
-                                       (200, "random"), (37, "zeros")])
+                                       (200, "random"), (37, "zeros"), (1500, "random")])
 def test_batch_order_and_empty_runs(B, pattern):
     """Batches whose grid spans several waves (here B >= 128) are dispatched
     longest run first in an order the device computes from the lengths: every
