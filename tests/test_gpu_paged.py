@@ -112,18 +112,22 @@ def test_bad_block_table_entry_sets_status():
 
 
 @pytest.mark.parametrize("paged", [False, True])
-def test_graph_captured_steps_advance_on_device(paged):
+@pytest.mark.parametrize("B,Hq,Hkv", [(2, 64, 8), (160, 16, 2)])
+def test_graph_captured_steps_advance_on_device(paged, B, Hq, Hkv):
     """One tq_decode_step captured in a CUDA graph with TQ_STEP_ADVANCE and
     replayed token after token (new K/V copied into the captured buffers
     between replays) gives the outputs and the cache of eager steps with
-    host-advanced lengths."""
+    host-advanced lengths.  The 160-sequence batch spans several waves, so
+    each replay also runs the kernel that orders the runs from the lengths
+    the previous replay advanced."""
     torch = need_gpu()
     import int4_kv_cache_gb300 as tq
 
-    B, Hq, Hkv, D, S0, steps, cap = 2, 64, 8, 128, 700, 6, 1024
-    x = synth.decode_inputs(170, B, Hq, Hkv, D, cap, outliers=True)
+    D, S0, steps, cap = 128, 700, 6, 1024
+    x = synth.decode_inputs(170 + B, B, Hq, Hkv, D, cap, outliers=True)
     toks = [synth.append_tokens(170, i, B, Hkv, D, 1, outliers=x.outlier_channels) for i in range(steps)]
-    start = np.array([S0, S0 - 300], np.int32)
+    start = (np.array([S0, S0 - 300], np.int32) if B == 2
+             else np.random.default_rng(B).integers(100, 1000 - steps, B).astype(np.int32))
 
     def make():
         if paged:
