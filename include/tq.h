@@ -123,9 +123,9 @@ typedef struct tq_kv_cache {
 
 /* Paged cache: a pool of pages, each holding page_tokens consecutive tokens of
  * one sequence for every kv head, and a block table mapping each sequence's
- * logical pages to pool pages (the survey's paged-cache option for ragged
- * batches; the Llama page's 18% concatenation gap is what a cache that grows
- * by reallocation costs).  Row t of (sequence b, kv head h) is row
+ * logical pages to pool pages (for ragged batches: the "turboquant-llama3.170B"
+ * README's 18% concatenation gap is what a cache that grows by reallocation
+ * costs).  Row t of (sequence b, kv head h) is row
  * t % page_tokens of head h in page block_table[b * max_pages_per_seq +
  * t / page_tokens].  The caller owns the pool and the table and allocates
  * pages before appending into them; a table entry outside [0, num_pages) sets
