@@ -8,9 +8,11 @@
 // (11 x 4 significant bits), so one fused multiply-add rounds once to fp32,
 // then the conversion rounds to binary16.
 //
-// Work split: one thread per 8 elements (one 32-bit word of codes, 16 bytes of
-// output), grid-stride over [B][Hkv][n_rows][D/8] for K (blockIdx.y = 0) and
-// V (blockIdx.y = 1); every store is a 16-byte coalesced write.
+// Work split: one thread per 8 elements (one 32-bit word of codes, 16 bytes
+// of output); a CTA of 256 threads covers 256 / (D / 8) consecutive rows of one
+// (sequence, kv head) per pass, blockIdx.z selects the (sequence, kv head) and
+// blockIdx.y K or V, so no 64-bit division is left in the loop; every store is
+// a 16-byte coalesced write.
 #include <cuda_fp16.h>
 
 #include "tq_device.cuh"
@@ -20,23 +22,21 @@ namespace tq {
 
 namespace {
 
-template <int BITS>
+template <int BITS, int D>
 __global__ void __launch_bounds__(256) dequant_kernel(const DequantParams p) {
+    constexpr int kWords = D / 8;               // threads per row: 8 codes each
+    constexpr int kRows = 256 / kWords;         // rows per CTA pass
+    constexpr int kNg = D / kGroup;
     const int kv = blockIdx.y;
-    const uint8_t* codes = kv ? p.v_codes : p.k_codes;
-    const uint16_t* scale = kv ? p.v_scale : p.k_scale;
-    const uint16_t* bias = kv ? p.v_bias : p.k_bias;
-    uint16_t* out = kv ? p.v_out : p.k_out;
-    const int words = p.head_dim / 8;  // 8 codes per thread: one 32-bit word (int4) or two (int8)
-    const int ng = p.head_dim / kGroup;
-    const long long total = static_cast<long long>(p.batch) * p.num_kv_heads * p.n_rows * words;
-    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-         i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const long long row = i / words;  // over [B][Hkv][n_rows]
-        const int w = static_cast<int>(i - row * words);
-        const long long bh = row / p.n_rows;
-        const long long src = bh * p.capacity + (row - bh * p.n_rows);
-        const uint8_t* cp = codes + src * (p.head_dim * BITS / 8) + w * BITS;  // this thread's 8 codes
+    const long long bh = blockIdx.z;            // (sequence, kv head)
+    const uint8_t* codes = (kv ? p.v_codes : p.k_codes) + bh * p.capacity * (D * BITS / 8);
+    const uint16_t* scale = (kv ? p.v_scale : p.k_scale) + bh * p.capacity * kNg;
+    const uint16_t* bias = (kv ? p.v_bias : p.k_bias) + bh * p.capacity * kNg;
+    uint16_t* out = (kv ? p.v_out : p.k_out) + bh * p.n_rows * D;
+    const int w = threadIdx.x % kWords;
+    const int g = (w * 8) / kGroup;
+    for (int r = blockIdx.x * kRows + threadIdx.x / kWords; r < p.n_rows; r += gridDim.x * kRows) {
+        const uint8_t* cp = codes + static_cast<long long>(r) * (D * BITS / 8) + w * BITS;  // this thread's 8 codes
         uint32_t c[2];
         if constexpr (BITS == 8) {
             const uint2 v = __ldcs(reinterpret_cast<const uint2*>(cp));
@@ -46,9 +46,8 @@ __global__ void __launch_bounds__(256) dequant_kernel(const DequantParams p) {
             c[0] = __ldcs(reinterpret_cast<const uint32_t*>(cp));
             c[1] = 0u;
         }
-        const int g = (w * 8) / kGroup;
-        const float s = __half2float(__ushort_as_half(__ldg(scale + src * ng + g)));
-        const float b = __half2float(__ushort_as_half(__ldg(bias + src * ng + g)));
+        const float s = __half2float(__ushort_as_half(__ldg(scale + static_cast<long long>(r) * kNg + g)));
+        const float b = __half2float(__ushort_as_half(__ldg(bias + static_cast<long long>(r) * kNg + g)));
         uint32_t h[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -65,21 +64,34 @@ __global__ void __launch_bounds__(256) dequant_kernel(const DequantParams p) {
             h[j] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
                    (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
         }
-        __stcs(reinterpret_cast<uint4*>(out + row * p.head_dim) + w, make_uint4(h[0], h[1], h[2], h[3]));
+        __stcs(reinterpret_cast<uint4*>(out + static_cast<long long>(r) * D) + w, make_uint4(h[0], h[1], h[2], h[3]));
     }
+}
+
+template <int BITS, int D>
+cudaError_t launch_dq(const DequantParams& p, int sm_count, cudaStream_t stream) {
+    constexpr int kRows = 256 / (D / 8);
+    const long long heads = static_cast<long long>(p.batch) * p.num_kv_heads;
+    if (heads > 65535) return cudaErrorInvalidConfiguration;
+    // about eight CTAs per SM in all, each (sequence, kv head) slice strided over its rows
+    const long long per_head = (static_cast<long long>(sm_count > 0 ? sm_count : 152) * 8 + 2 * heads - 1) / (2 * heads);
+    const long long need = (p.n_rows + kRows - 1) / kRows;
+    const unsigned x = static_cast<unsigned>(per_head < need ? (per_head > 0 ? per_head : 1) : need);
+    dequant_kernel<BITS, D><<<dim3(x, 2, static_cast<unsigned>(heads)), 256, 0, stream>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_dequant(const DequantParams& p, int sm_count, cudaStream_t stream) {
-    const long long total = static_cast<long long>(p.batch) * p.num_kv_heads * p.n_rows * (p.head_dim / 8);
-    if (total == 0) return cudaSuccess;
-    const long long want = (total + 255) / 256;
-    const long long cap = static_cast<long long>(sm_count > 0 ? sm_count : 152) * 8;
-    const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
-    if (p.bits == 8) dequant_kernel<8><<<dim3(blocks, 2), 256, 0, stream>>>(p);
-    else dequant_kernel<4><<<dim3(blocks, 2), 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    if (p.n_rows == 0 || p.batch == 0 || p.num_kv_heads == 0) return cudaSuccess;
+    const bool i8 = p.bits == 8;
+    switch (p.head_dim) {
+        case 64: return i8 ? launch_dq<8, 64>(p, sm_count, stream) : launch_dq<4, 64>(p, sm_count, stream);
+        case 128: return i8 ? launch_dq<8, 128>(p, sm_count, stream) : launch_dq<4, 128>(p, sm_count, stream);
+        case 256: return i8 ? launch_dq<8, 256>(p, sm_count, stream) : launch_dq<4, 256>(p, sm_count, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace tq
