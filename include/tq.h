@@ -351,6 +351,21 @@ tq_status tq_sdpa_plan(const tq_kv_cache* cache, int32_t num_q_heads,
                        int32_t max_seq_len, int32_t chunk, tq_impl impl,
                        int32_t* n_splits, int32_t* max_run_tokens);
 
+/* The split plan rule itself, without a device: the runs per (sequence, kv
+ * head) for `batch` sequences of up to `max_seq_len` tokens, `num_kv_heads`
+ * kv heads, runs made of whole units of min(chunk, tile_tokens) tokens, on a
+ * device that holds `resident_ctas` phase-1 CTAs at once (tq_sdpa_plan passes
+ * the SM count x the CTAs per SM and the kernel's tile: 128 tokens when a
+ * token's codes take under 128 bytes, 64 otherwise).  Picks the run count n <= min(units,
+ * 2048 / (batch * num_kv_heads)) that minimises
+ *   ceil(batch * num_kv_heads * n / resident_ctas) * (ceil(units / n) * unit + 2 * tile_tokens),
+ * the fewest runs on a tie.  Chunk and tile_tokens must be positive multiples
+ * of 16 and every count positive (TQ_ERR_SHAPE), the outputs non-null
+ * (TQ_ERR_NULL).  Pure host arithmetic. */
+tq_status tq_split_plan(int32_t batch, int32_t num_kv_heads, int32_t max_seq_len,
+                        int32_t chunk, int32_t tile_tokens, int32_t resident_ctas,
+                        int32_t* n_splits, int32_t* max_run_tokens);
+
 /* Split-K phase 1 alone ("turboquant-llama3.170B" README, split-K paragraph:
  * Phase 1 = partial attention over 512-token chunks processed in parallel).
  * Each part covers `chunks_per_split` consecutive chunks (1 = one state per

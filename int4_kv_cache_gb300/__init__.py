@@ -19,7 +19,7 @@ __all__ = [
     "TQ_DEV_TIMEOUT", "TQError", "lib", "lib_path", "tq_kv_cache", "KVCache",
     "tq_abi_version", "tq_status_string", "tq_kv_cache_bytes", "tq_sdpa_workspace_bytes",
     "tq_quantize_kv_append", "tq_sdpa_int4_decode", "tq_sdpa_int4_partial", "tq_sdpa_int4_reduce",
-    "tq_sdpa_plan", "tq_sdpa_int4_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "tq_decode_step",
+    "tq_sdpa_plan", "tq_split_plan", "tq_sdpa_int4_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "tq_decode_step",
     "tq_dequantize_kv", "tq_hadamard_rotate", "TQ_ROTATE_K", "TQ_ROTATE_V", "TQ_STEP_ADVANCE", "TQ_DEV_PAGE",
     "tq_paged_kv_cache", "PagedKVCache", "tq_decode_step_host", "tq_host_staging_bytes",
 ]
@@ -99,6 +99,7 @@ def lib() -> ctypes.CDLL:
             "tq_sdpa_int4_decode": ([C, P, i32, P, i32, f32, i32, P, sz, P, P, P], i32),
             "tq_sdpa_int4_decode_impl": ([C, P, i32, P, i32, f32, i32, P, sz, P, P, i32, P], i32),
             "tq_sdpa_plan": ([C, i32, i32, i32, i32, P, P], i32),
+            "tq_split_plan": ([i32, i32, i32, i32, i32, i32, P, P], i32),
             "tq_sdpa_int4_partial": ([C, P, i32, P, i32, f32, i32, i32, P, P, P, P, i32, P], i32),
             "tq_sdpa_int4_reduce": ([P, P, P, i32, i32, i32, i32, P, P], i32),
             "tq_sdpa_int4_decode_noalloc": ([C, P, i32, P, i32, f32, i32, P, P, P], i32),
@@ -379,6 +380,17 @@ def tq_sdpa_plan(cache: KVCache, num_q_heads: int, max_seq_len: int, chunk: int 
     ns, run = ctypes.c_int32(0), ctypes.c_int32(0)
     _check("tq_sdpa_plan", lib().tq_sdpa_plan(cache.ref(), num_q_heads, int(max_seq_len), int(chunk), int(impl),
                                               ctypes.byref(ns), ctypes.byref(run)))
+    return ns.value, run.value
+
+
+def tq_split_plan(batch: int, num_kv_heads: int, max_seq_len: int, chunk: int, tile_tokens: int,
+                  resident_ctas: int):
+    """(n_splits, max_run_tokens) of the split rule for a device holding
+    ``resident_ctas`` phase-1 CTAs at once (host arithmetic, no device)."""
+    ns, run = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check("tq_split_plan", lib().tq_split_plan(int(batch), int(num_kv_heads), int(max_seq_len), int(chunk),
+                                                int(tile_tokens), int(resident_ctas), ctypes.byref(ns),
+                                                ctypes.byref(run)))
     return ns.value, run.value
 
 

@@ -234,28 +234,46 @@ struct Plan {
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
-// Balanced runs of whole units, about one CTA per resident slot: the unit is
-// the kernel's pipeline tile, or the chunk if that is smaller, so that runs
-// cover the sequence evenly whatever its length in chunks.  At least
-// kMinRuns runs per (sequence, kv head) when there are enough units: with
-// many sequences the grid then spans several waves, and sequences of
-// different lengths (known only on the device) balance over them -- a batch of
-// 32 sequences of 1K-32K tokens decodes in 133 us instead of 257 us with one
-// run per sequence.
-constexpr long long kMinRuns = 4;
+// Balanced runs of whole units (the kernel's pipeline tile, or the chunk if
+// that is smaller, so that runs cover the sequence evenly whatever its length
+// in chunks), as many per (sequence, kv head) as minimise a model of the
+// grid's time: waves x (longest run + a fixed cost per CTA), waves =
+// ceil(CTAs / resident CTA slots).  The fixed cost (pipeline fill, the query
+// load, the partial-state store) is worth about two tiles of streaming.
+// Within one wave count more runs are shorter, so only the largest run count
+// of each wave count is a candidate, taken down to the fewest runs with the
+// same longest run; ties keep the fewer runs (less reduce work).  One sequence fills the resident slots once (57 runs at 128K with 8
+// kv heads and 456 slots); a batch whose grid needs several waves gets a CTA
+// count just under a whole number of waves (16 sequences of 32K: 7 runs, 896
+// CTAs for 912 slots: 110 us against 141 us with 4 runs and 512 CTAs).
+constexpr long long kRunFixedTiles = 2;
 
 Plan make_plan(int batch, int hkv, int max_seq_len, int chunk, int tile_tokens, int resident) {
     Plan pl;
     pl.unit_tokens = chunk < tile_tokens ? chunk : tile_tokens;
     pl.units = ceil_div(max_seq_len, pl.unit_tokens);
     const long long heads = static_cast<long long>(batch) * hkv;
-    long long ns = resident / heads;
-    if (ns < kMinRuns) ns = kMinRuns;
-    const long long cap = tq::kMaxDecodeCtas / heads;
-    if (ns > cap) ns = cap;
-    if (ns > pl.units) ns = pl.units;
-    if (ns < 1) ns = 1;
-    pl.n_splits = static_cast<int>(ns);
+    const long long slots = resident > 0 ? resident : 1;
+    long long cap = tq::kMaxDecodeCtas / heads;
+    if (cap > pl.units) cap = pl.units;
+    if (cap < 1) cap = 1;
+    long long best = 1, best_cost = -1;
+    for (long long w = (heads + slots - 1) / slots;; ++w) {
+        long long ns = w * slots / heads;
+        if (ns > cap) ns = cap;
+        if (ns < 1) ns = 1;
+        const long long run_units = (pl.units + ns - 1) / ns;
+        const long long n = (pl.units + run_units - 1) / run_units;  // fewest runs this long
+        const long long waves = (heads * n + slots - 1) / slots;
+        const long long run = run_units * pl.unit_tokens;
+        const long long cost = waves * (run + kRunFixedTiles * tile_tokens);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = n;
+        }
+        if (ns == cap) break;
+    }
+    pl.n_splits = static_cast<int>(best);
     return pl;
 }
 
@@ -883,6 +901,18 @@ tq_status tq_sdpa_plan(const tq_kv_cache* cache, int32_t hq, int32_t max_seq_len
     const Store st = shape_of(cache);
     tq_status s = device_plan(&st, max_seq_len, chunk, impl, &pl);
     if (s != TQ_OK) return s;
+    *n_splits = pl.n_splits;
+    *max_run_tokens = ceil_div(pl.units, pl.n_splits) * pl.unit_tokens;
+    return TQ_OK;
+}
+
+tq_status tq_split_plan(int32_t batch, int32_t num_kv_heads, int32_t max_seq_len, int32_t chunk,
+                        int32_t tile_tokens, int32_t resident_ctas, int32_t* n_splits, int32_t* max_run_tokens) {
+    if (n_splits == nullptr || max_run_tokens == nullptr) return TQ_ERR_NULL;
+    if (batch < 1 || num_kv_heads < 1 || max_seq_len < 1 || chunk < 16 || chunk % 16 || tile_tokens < 16 ||
+        tile_tokens % 16 || resident_ctas < 1)
+        return TQ_ERR_SHAPE;
+    const Plan pl = make_plan(batch, num_kv_heads, max_seq_len, chunk, tile_tokens, resident_ctas);
     *n_splits = pl.n_splits;
     *max_run_tokens = ceil_div(pl.units, pl.n_splits) * pl.unit_tokens;
     return TQ_OK;
