@@ -219,8 +219,8 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
 
     int first_page = 0, n_win = 0;
     if constexpr (PAGED) {
-        first_page = t_begin / p.map.page_tokens;
-        n_win = t_end > t_begin ? (t_end - 1) / p.map.page_tokens - first_page + 1 : 0;
+        first_page = page_index(p.map, t_begin);
+        n_win = t_end > t_begin ? page_index(p.map, t_end - 1) - first_page + 1 : 0;
         n_win = min(n_win, kPageWindow);
         for (int i = threadIdx.x; i < n_win; i += C::THREADS) {
             int pg = __ldg(p.map.block_table + static_cast<long long>(b) * p.map.max_pages + first_page + i);
@@ -281,9 +281,9 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
         long long row;
         int avail;
         if constexpr (PAGED) {
-            const int w = t0 / p.map.page_tokens - first_page;
+            const int pi = page_index(p.map, t0), w = pi - first_page;
             row = w < n_win ? (static_cast<long long>(page_s[w]) * p.num_kv_heads + kvh) * p.map.page_tokens +
-                                  t0 % p.map.page_tokens
+                                  (t0 - pi * p.map.page_tokens)
                             : kv_row(p.map, p.num_kv_heads, b, kvh, t0, p.status);
             avail = C::T;
         } else {

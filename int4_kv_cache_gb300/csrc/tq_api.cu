@@ -77,7 +77,7 @@ Store shape_of(const tq_kv_cache* c) {
     st.group_size = c->group_size;
     st.capacity = c->capacity;
     st.bits = c->bits;
-    st.map = {nullptr, c->capacity, 1, c->batch};
+    st.map = {nullptr, c->capacity, 1, c->batch, 0, 0};
     st.paged = false;
     return st;
 }
@@ -123,7 +123,7 @@ tq_status store_of(const tq_paged_kv_cache* c, Store* st) {
     t.group_size = c->group_size;
     t.capacity = static_cast<int32_t>(cap);
     t.bits = c->bits;
-    t.map = {c->block_table, c->page_tokens, c->max_pages_per_seq, c->num_pages};
+    t.map = tq::with_page_divisor({c->block_table, c->page_tokens, c->max_pages_per_seq, c->num_pages, 0, 0});
     t.paged = true;
     return TQ_OK;
 }

@@ -20,15 +20,39 @@ constexpr int kGroup = 64;
 struct RowMap {
     const int32_t* block_table;
     int32_t page_tokens, max_pages, num_pages;
+    // paged maps: floor(t / page_tokens) = umulhi(t, page_magic) >> page_shift
+    // for 0 <= t < 2^31 (set by with_page_divisor)
+    uint32_t page_magic;
+    int32_t page_shift;
 };
 
+// Division by the invariant page size as one multiply-high and a shift
+// (Granlund and Montgomery, "Division by Invariant Integers using
+// Multiplication", PLDI 1994, round-up multiplier): with l = ceil(log2 d) and
+// m = ceil(2^(31+l) / d) < 2^32, floor(t / d) = floor(t * m / 2^(31+l)) for
+// every 0 <= t < 2^31, because m * d - 2^(31+l) < d <= 2^l makes the excess
+// t * (m * d - 2^(31+l)) / (d * 2^(31+l)) smaller than 1/d.  Needs d >= 2.
+inline RowMap with_page_divisor(RowMap m) {
+    int l = 0;
+    while ((1LL << l) < m.page_tokens) ++l;
+    const unsigned long long d = static_cast<unsigned long long>(m.page_tokens);
+    m.page_magic = static_cast<uint32_t>(((1ULL << (31 + l)) + d - 1) / d);
+    m.page_shift = l - 1;
+    return m;
+}
+
 #ifdef __CUDACC__
+__device__ __forceinline__ int page_index(const RowMap& m, int t) {
+    return static_cast<int>(__umulhi(static_cast<unsigned>(t), m.page_magic) >> m.page_shift);
+}
+
 __device__ __forceinline__ long long kv_row(const RowMap& m, int num_kv_heads, int b, int h, int t,
                                             int32_t* status) {
     int page = b, tp = t;
     if (m.block_table != nullptr) {
-        page = __ldg(m.block_table + static_cast<long long>(b) * m.max_pages + t / m.page_tokens);
-        tp = t % m.page_tokens;
+        const int pi = page_index(m, t);
+        page = __ldg(m.block_table + static_cast<long long>(b) * m.max_pages + pi);
+        tp = t - pi * m.page_tokens;
         if (static_cast<unsigned>(page) >= static_cast<unsigned>(m.num_pages)) {
             if (status != nullptr) atomicOr(status, TQ_DEV_PAGE);
             page = 0;

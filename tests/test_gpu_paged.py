@@ -36,7 +36,8 @@ def _gather(paged, perm, S):
     return out
 
 
-@pytest.mark.parametrize("D,Hq,Hkv,P", [(128, 64, 8, 128), (128, 16, 2, 256), (256, 8, 2, 128), (64, 8, 4, 256)])
+@pytest.mark.parametrize("D,Hq,Hkv,P", [(128, 64, 8, 128), (128, 16, 2, 256), (256, 8, 2, 128), (64, 8, 4, 256),
+                                        (128, 16, 2, 384), (128, 64, 8, 640), (256, 32, 16, 1152)])
 def test_paged_equals_contiguous_and_oracle(D, Hq, Hkv, P):
     torch = need_gpu()
     import int4_kv_cache_gb300 as tq
