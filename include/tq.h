@@ -283,7 +283,8 @@ size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t num_q_heads,
  * chunk:    split-K chunk in tokens (multiple of 16; TQ_DEFAULT_CHUNK = 512).
  *           The sequence is split into balanced runs, one per CTA, of whole
  *           units of min(chunk, pipeline tile) tokens (the tile is 128 tokens
- *           for head_dim <= 128, 64 for 256); each run keeps one running softmax
+ *           when a token's codes take under 128 bytes, 64 otherwise); each run
+ *           keeps one running softmax
  *           state and the runs' states are merged by a log-sum-exp reduce.  The
  *           result is the same as merging one state per chunk (see
  *           tq_sdpa_int4_partial with chunks_per_split = 1).

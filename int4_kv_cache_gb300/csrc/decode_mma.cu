@@ -169,8 +169,8 @@ __device__ __forceinline__ void load_pair_sb(const uint16_t* base, int tok_a, in
     }
 }
 
-__device__ __forceinline__ int clamp_len(const DecodeParams& p, int b) {
-    int len = __ldg(p.seq_lens + b);
+__device__ __forceinline__ int clamp_len(const DecodeParams& p, const int32_t* src) {
+    int len = __ldg(src);
     if (len < 0 || len > p.max_seq_len) {
         if (p.status != nullptr && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
             atomicOr(p.status, TQ_DEV_SEQ_LEN);
@@ -200,18 +200,22 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int32_t* len_src = p.seq_lens + b;
     if (p.wait_at_start) pdl_wait_primary();
     if (p.order != nullptr) {
         // grids of several waves: the runs in the order the planning kernel
-        // wrote (longest first), each run's kv heads consecutive
+        // wrote (longest first), each run's kv heads consecutive; the entry
+        // carries the sequence's (clamped, checked) length, read in parallel
         const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
-        const int item = __ldg(p.order + lin / gridDim.y);
+        const int2* e = p.order + lin / gridDim.y;
+        const int item = __ldg(&e->x);
+        len_src = &e->y;
         kvh = lin % gridDim.y;
         b = item / gridDim.x;
         split = item % gridDim.x;
     }
     const int G = p.group_q;
-    const int len = clamp_len(p, b);
+    const int len = clamp_len(p, len_src);
     const int t_begin = run_begin(split, p.units, p.n_splits, p.unit_tokens);
     const int t_end = min(run_begin(split + 1, p.units, p.n_splits, p.unit_tokens), len);
     const int n_tiles = t_end > t_begin ? (t_end - t_begin + C::T - 1) / C::T : 0;

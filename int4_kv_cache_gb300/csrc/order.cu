@@ -7,7 +7,8 @@
 // and a long one started late decides the decode time; dispatched longest
 // first (the longest-processing-time rule), the short and empty runs fill
 // the tail instead.  One CTA counts the runs per length in tiles, takes the
-// descending prefix sum of the counts and scatters the run indices; the order
+// descending prefix sum of the counts and scatters the run indices, each with
+// its sequence's length (the decode CTA then needs no second read); the order
 // within one length is not fixed, which does not change any result (every
 // run writes its own partial state).
 #include "tq_device.cuh"
@@ -65,7 +66,12 @@ __global__ void __launch_bounds__(kOrderThreads) order_runs_kernel(const OrderPa
     count[key] = before;  // each key is owned by one thread
     __syncthreads();
     pdl_launch_dependents();
-    for (int i = tid; i < n; i += kOrderThreads) p.order[atomicAdd(&count[run_key(p, i)], 1)] = i;
+    for (int i = tid; i < n; i += kOrderThreads) {
+        const int b = i / p.n_splits, raw = __ldg(p.seq_lens + b);
+        if ((raw < 0 || raw > p.max_seq_len) && i % p.n_splits == 0 && p.status != nullptr)
+            atomicOr(p.status, TQ_DEV_SEQ_LEN);
+        p.order[atomicAdd(&count[run_key(p, i)], 1)] = make_int2(i, min(max(raw, 0), p.max_seq_len));
+    }
 }
 
 static_assert(kOrderKeys == kOrderThreads, "one key per thread in the scan");

@@ -317,7 +317,7 @@ tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const in
                      int32_t max_seq_len, float attn_scale, const Plan& pl, float* pm, float* plv, float* pa,
                      int32_t* status, tq_impl impl, cudaStream_t stream, const int32_t* dep_write_pos = nullptr,
                      int32_t dep_n_new = 0, const tq::AppendParams* fused_append = nullptr, bool rotate_q = false,
-                     int32_t* order_buf = nullptr, uint16_t* direct_out = nullptr) {
+                     int2* order_buf = nullptr, uint16_t* direct_out = nullptr) {
     if (pl.n_splits > 65535 || cache->num_kv_heads > 65535 || cache->batch > 65535) return TQ_ERR_SHAPE;
     tq::DecodeParams p{};
     p.q = q;
@@ -381,6 +381,7 @@ tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const in
         tq::OrderParams op{};
         op.seq_lens = seq_lens;
         op.order = order_buf;
+        op.status = status;
         op.batch = cache->batch;
         op.max_seq_len = max_seq_len;
         op.units = pl.units;
@@ -594,7 +595,7 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
     float* pa = reinterpret_cast<float*>(ws + 2 * align256(parts * sizeof(float)));
     uint16_t* q_rot = reinterpret_cast<uint16_t*>(ws + 2 * align256(parts * sizeof(float)) +
                                                   align256(parts * cache->head_dim * sizeof(float)));
-    int32_t* order = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(q_rot) +
+    int2* order = reinterpret_cast<int2*>(reinterpret_cast<uint8_t*>(q_rot) +
                                                 align256(static_cast<size_t>(cache->batch) * hq *
                                                          cache->head_dim * sizeof(uint16_t)));
     const float rs = tq::rotation_scale(cache->head_dim);
@@ -724,7 +725,7 @@ size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t hq, int32_t hkv, int32_t h
     // order of the runs
     return 2 * align256(parts * sizeof(float)) + align256(parts * head_dim * sizeof(float)) +
            align256(static_cast<size_t>(batch) * hq * head_dim * sizeof(uint16_t)) +
-           align256(static_cast<size_t>(batch) * static_cast<size_t>(ns) * sizeof(int32_t));
+           align256(static_cast<size_t>(batch) * static_cast<size_t>(ns) * sizeof(int2));
 }
 
 tq_status tq_sdpa_int4_decode_impl(const tq_kv_cache* raw, const uint16_t* q, int32_t hq,

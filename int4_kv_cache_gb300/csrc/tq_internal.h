@@ -123,9 +123,11 @@ struct DecodeParams {
     // waits for that grid before its first read.
     int32_t wait_at_start;
     // Optional dispatch order of the runs (grids of several waves): entry r
-    // is the run (b * n_splits + split) that CTA slots [r * Hkv, (r + 1) * Hkv)
-    // in launch order take, one per kv head.  Null: the grid's own order.
-    const int32_t* order;
+    // is {run b * n_splits + split, seq_lens[b] clamped to [0, max_seq_len]}
+    // for CTA slots [r * Hkv, (r + 1) * Hkv) in launch order, one per kv head
+    // (the length travels with the run so that a CTA makes one dependent read
+    // before its first tile, not two).  Null: the grid's own order.
+    const int2* order;
     // One run per sequence (n_splits = 1): the merged state is the output;
     // when set, the kernel writes fp16(acc / l) here instead of the partials.
     uint16_t* out;
@@ -137,7 +139,8 @@ constexpr int kFusedAppendMaxRows = 16;
 // Longest-first dispatch order of the runs of a split decode (order.cu).
 struct OrderParams {
     const int32_t* seq_lens;  // [B]
-    int32_t* order;           // [B * n_splits] run indices b * n_splits + s, longest first
+    int2* order;              // [B * n_splits] {run b * n_splits + s, clamped seq_lens[b]}, longest first
+    int32_t* status;          // optional: TQ_DEV_SEQ_LEN for a length outside [0, max_seq_len]
     int32_t batch, max_seq_len, units, n_splits, unit_tokens, tile_tokens;
 };
 

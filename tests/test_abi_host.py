@@ -81,7 +81,7 @@ def test_workspace_bytes(L):
         a256 = lambda n: -(-n // 256) * 256
         # m, l, acc per part, room for the rotated query (B * Hq * D fp16), then
         # the dispatch order of the runs (B * ns int32)
-        return 2 * a256(parts * 4) + a256(parts * D * 4) + a256(B * Hq * D * 2) + a256(B * ns * 4)
+        return 2 * a256(parts * 4) + a256(parts * D * 4) + a256(B * Hq * D * 2) + a256(B * ns * 8)
 
     assert tq.tq_sdpa_workspace_bytes(1, 64, 8, 128, 131072, 512) == want(1, 64, 8, 128, 131072)
     assert tq.tq_sdpa_workspace_bytes(32, 64, 8, 128, 32768, 512) == want(32, 64, 8, 128, 32768)
