@@ -239,13 +239,17 @@ __device__ __forceinline__ void rotate_quantize_store(const AppendParams& p, lon
 // groups of K and of V into shared memory with 2-D TMA boxes (128-byte rows,
 // one group per row).  The 128-byte swizzle places word j of row r at slot
 // j ^ (r & 7), the layout the per-thread reads above expect.  Two stages per
-// CTA: while the threads quantize one tile, the next one is in flight.
+// CTA: while the threads quantize one tile, the next one is in flight.  A
+// stage is released warp by warp (a shared count, no CTA barrier): the last
+// warp to finish with it issues its refill, and the other warps go on to the
+// next stage meanwhile.
 constexpr int kTmaGroups = 128;                     // groups (rows) per tile
 constexpr int kTmaThreads = 2 * kTmaGroups;         // one thread per (group, K or V)
 constexpr int kTmaTensorBytes = kTmaGroups * 128;   // 16 KB of K or of V
 constexpr int kTmaStageBytes = 2 * kTmaTensorBytes;
 constexpr int kTmaStages = 2;
 constexpr int kTmaSmemBytes = kTmaStages * kTmaStageBytes + 1024;
+constexpr int kTmaWarps = kTmaThreads / 32;
 
 template <int BITS, bool ROT>
 __global__ void __launch_bounds__(kTmaThreads, ROT ? 2 : 3) quantize_append_tma_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -254,11 +258,15 @@ __global__ void __launch_bounds__(kTmaThreads, ROT ? 2 : 3) quantize_append_tma_
                                                                          int n_tiles) {
     extern __shared__ uint8_t dyn_smem[];
     __shared__ uint64_t full_bar[kTmaStages];
+    __shared__ unsigned int done_cnt[kTmaStages];  // warps finished with the stage, cumulative
     uint8_t* smem = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int ng = p.head_dim / kGroup;
     if (tid == 0) {
-        for (int s = 0; s < kTmaStages; ++s) mbar_init(&full_bar[s], 1);
+        for (int s = 0; s < kTmaStages; ++s) {
+            mbar_init(&full_bar[s], 1);
+            done_cnt[s] = 0;
+        }
         fence_mbarrier_init();
     }
     __syncthreads();
@@ -300,12 +308,21 @@ __global__ void __launch_bounds__(kTmaThreads, ROT ? 2 : 3) quantize_append_tma_
         } else if (gi < n_groups) {
             quantize_store<BITS>(p, gi, ng, tk[r], tv[r], r & 7, t, t);
         }
-        // every thread is done with this stage (reads, and rotation writes)
-        // before the asynchronous copy that overwrites it is issued
-        fence_proxy_async_shared();
-        __syncthreads();
-        const int next = tile + kTmaStages * gridDim.x;
-        if (tid == 0 && next < n_tiles) issue(next, stage);
+        // Release the stage (this thread only read it).  The last warp to
+        // finish it refills it: its fences order every warp's reads (made
+        // visible by their fences before the count) before the asynchronous
+        // copy that overwrites the stage.
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            const unsigned int before = atomicAdd(&done_cnt[stage], 1u);
+            const int next = tile + kTmaStages * gridDim.x;
+            if (before % kTmaWarps == kTmaWarps - 1 && next < n_tiles) {
+                __threadfence_block();
+                fence_proxy_async_shared();
+                issue(next, stage);
+            }
+        }
     }
 }
 

@@ -152,10 +152,17 @@ __device__ __forceinline__ void quantize_group64(const uint4 (&raw)[8], uint32_t
     const float2 nb = make_float2(-b, -b), rs2 = make_float2(rs, rs);
     const float2 mg = make_float2(kMagic, kMagic), nmg = make_float2(-kMagic, -kMagic);
     const float2 m1 = make_float2(-1.0f, -1.0f);
+    // Near-tie test without per-element compares: q = e * e - c with
+    // c = (0.5 - 2 * kTieWindow)^2 is one rounding of the exact value, so its
+    // sign is exact, and q >= 0 for every |e| >= 0.5 - kTieWindow (and for a
+    // few more, which only send their word to the exact rule).  The sign bits
+    // of a word's eight q are ANDed: a clear sign bit means some q >= 0.
+    constexpr float kFar = 0.5f - 2.0f * R::kTieWindow;
+    const float2 nc = make_float2(-kFar * kFar, -kFar * kFar);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {  // input word j: elements 8j .. 8j + 7
         uint32_t w[2] = {0u, 0u};
-        bool near = false;
+        uint32_t far_bits = 0x80000000u;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {  // two elements per paired fp32 operation
             const float2 f = __half22float2(h[4 * j + k]);
@@ -163,11 +170,13 @@ __device__ __forceinline__ void quantize_group64(const uint4 (&raw)[8], uint32_t
             const float2 t = __fmul2_rn(d, rs2);                     // ~ d / s
             const float2 r = __fadd2_rn(t, mg);                      // rint(t) in the low bits
             const float2 e = __ffma2_rn(__fadd2_rn(r, nmg), m1, t);  // t - rint(t), exact
-            near |= (fabsf(e.x) > 0.5f - R::kTieWindow) | (fabsf(e.y) > 0.5f - R::kTieWindow);
+            const float2 q = __ffma2_rn(e, e, nc);                   // < 0 unless near a tie
+            far_bits &= __float_as_uint(q.x) & __float_as_uint(q.y);
             const int p = 2 * k * BITS;  // bit position of the pair within the word(s)
             w[p / 32] = bfi(__float_as_uint(r.x), w[p / 32], p % 32, BITS);
             w[(p + BITS) / 32] = bfi(__float_as_uint(r.y), w[(p + BITS) / 32], (p + BITS) % 32, BITS);
         }
+        const bool near = far_bits == 0u;
         if (near || !normal) {  // rare: redo the word with the exact scalar rule
             const uint2 x = code_word_exact<BITS>(raw[j], b, s, rs);
             w[0] = x.x;
