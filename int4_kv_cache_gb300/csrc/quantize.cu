@@ -48,11 +48,11 @@ __device__ __forceinline__ void rotate_staged(uint4 (&tile)[32][8], int lane, in
 template <int BITS>
 __device__ __forceinline__ bool group_dst(const AppendParams& p, long long gi, int ng, long long& code_off,
                                           long long& sb) {
-    const int g = static_cast<int>(gi % ng);
-    const long long row = gi / ng;  // over [B][Hkv][n_new]
-    const int i = static_cast<int>(row % p.n_new);
-    const long long bh = row / p.n_new;  // b * Hkv + h
-    const int b = static_cast<int>(bh / p.num_kv_heads);
+    const long long row = fast_div(gi, p.div_ng);  // over [B][Hkv][n_new]
+    const int g = static_cast<int>(gi - row * ng);
+    const long long bh = fast_div(row, p.div_n_new);  // b * Hkv + h
+    const int i = static_cast<int>(row - bh * p.n_new);
+    const int b = static_cast<int>(fast_div(bh, p.div_hkv));
     const int wp = __ldg(p.write_pos + b);
     if (wp < 0 || static_cast<long long>(wp) + p.n_new > p.capacity) {
         if (p.status != nullptr && g == 0 && i == 0) atomicOr(p.status, TQ_DEV_WRITE_POS);

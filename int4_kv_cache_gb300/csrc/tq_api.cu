@@ -540,6 +540,9 @@ tq::AppendParams append_params(const Store* cache, const uint16_t* k_new, const 
     p.capacity = cache->capacity;
     p.map = cache->map;
     p.bits = cache->bits;
+    p.div_ng = tq::make_fastdiv(cache->head_dim / tq::kGroup);
+    p.div_n_new = tq::make_fastdiv(n_new > 0 ? n_new : 1);
+    p.div_hkv = tq::make_fastdiv(cache->num_kv_heads);
     return p;
 }
 

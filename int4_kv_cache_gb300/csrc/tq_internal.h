@@ -41,7 +41,33 @@ inline RowMap with_page_divisor(RowMap m) {
     return m;
 }
 
+// floor(n / d) for 0 <= n < 2^63 and 1 <= d < 2^31 by a 64-bit multiply-high
+// and a shift: the same round-up multiplier with 63 in place of 31 (m =
+// ceil(2^(63+l) / d) fits 64 bits and t * (m * d - 2^(63+l)) < 2^(63+l) for
+// every n below 2^63); magic = 0 stands for d = 1.
+struct FastDiv {
+    uint64_t magic;
+    int32_t shift;
+    int32_t d;
+};
+
+inline FastDiv make_fastdiv(int32_t d) {
+    FastDiv f{0, 0, d};
+    if (d <= 1) return f;
+    int l = 0;
+    while ((1LL << l) < d) ++l;
+    const unsigned __int128 num = static_cast<unsigned __int128>(1) << (63 + l);
+    f.magic = static_cast<uint64_t>((num + static_cast<unsigned __int128>(d) - 1) / static_cast<unsigned>(d));
+    f.shift = l - 1;
+    return f;
+}
+
 #ifdef __CUDACC__
+__device__ __forceinline__ long long fast_div(long long n, const FastDiv& f) {
+    return f.magic == 0 ? n
+                        : static_cast<long long>(__umul64hi(static_cast<unsigned long long>(n), f.magic) >> f.shift);
+}
+
 __device__ __forceinline__ int page_index(const RowMap& m, int t) {
     return static_cast<int>(__umulhi(static_cast<unsigned>(t), m.page_magic) >> m.page_shift);
 }
@@ -78,6 +104,8 @@ struct AppendParams {
     uint32_t flags;    // TQ_ROTATE_K / TQ_ROTATE_V: rotate the rows before quantizing them
     float rot_scale;   // fp32 value nearest 1 / sqrt(head_dim)
     RowMap map;
+    // group index gi over [B][Hkv][n_new][NG] -> (row, g), (bh, i), (b, h)
+    FastDiv div_ng, div_n_new, div_hkv;
 };
 
 // Geometry of one phase-1 launch: grid (n_splits, Hkv, B).  The sequence is
