@@ -357,15 +357,21 @@ tq_status tq_sdpa_plan(const tq_kv_cache* cache, int32_t num_q_heads,
  * kv heads, runs made of whole units of min(chunk, tile_tokens) tokens, on a
  * device that holds `resident_ctas` phase-1 CTAs at once (tq_sdpa_plan passes
  * the SM count x the CTAs per SM and the kernel's tile: 128 tokens when a
- * token's codes take under 128 bytes, 64 otherwise).  Picks the run count n <= min(units,
- * 2048 / (batch * num_kv_heads)) that minimises
- *   ceil(batch * num_kv_heads * n / resident_ctas) * (ceil(units / n) * unit + 2 * tile_tokens),
- * the fewest runs on a tie.  Chunk and tile_tokens must be positive multiples
- * of 16 and every count positive (TQ_ERR_SHAPE), the outputs non-null
- * (TQ_ERR_NULL).  Pure host arithmetic. */
+ * token's codes take under 128 bytes, 64 otherwise).  Picks the run count
+ * n <= min(units, 2048 / (batch * num_kv_heads)) that minimises, with
+ * W = ceil(batch * num_kv_heads * n / resident_ctas) waves,
+ *   W * (ceil(units / n) * unit + 2 * tile_tokens) + R,
+ * R = tile_tokens for the reduce, or 0 when `merge` is nonzero and the
+ * decode merges the runs itself (n = 1, or n <= 8 with W = 1: one
+ * thread-block cluster per sequence and kv head); the fewest runs on a tie.
+ * tq_sdpa_plan passes merge = 1 (0 for the CUDA-core implementation); steps
+ * with TQ_ROTATE_V or TQ_STEP_ADVANCE, whose reduce has other work, plan with
+ * merge = 0.  Chunk and tile_tokens must be positive multiples of 16 and every
+ * count positive (TQ_ERR_SHAPE), the outputs non-null (TQ_ERR_NULL).  Pure
+ * host arithmetic. */
 tq_status tq_split_plan(int32_t batch, int32_t num_kv_heads, int32_t max_seq_len,
                         int32_t chunk, int32_t tile_tokens, int32_t resident_ctas,
-                        int32_t* n_splits, int32_t* max_run_tokens);
+                        int32_t merge, int32_t* n_splits, int32_t* max_run_tokens);
 
 /* Split-K phase 1 alone ("turboquant-llama3.170B" README, split-K paragraph:
  * Phase 1 = partial attention over 512-token chunks processed in parallel).

@@ -99,7 +99,7 @@ def lib() -> ctypes.CDLL:
             "tq_sdpa_int4_decode": ([C, P, i32, P, i32, f32, i32, P, sz, P, P, P], i32),
             "tq_sdpa_int4_decode_impl": ([C, P, i32, P, i32, f32, i32, P, sz, P, P, i32, P], i32),
             "tq_sdpa_plan": ([C, i32, i32, i32, i32, P, P], i32),
-            "tq_split_plan": ([i32, i32, i32, i32, i32, i32, P, P], i32),
+            "tq_split_plan": ([i32, i32, i32, i32, i32, i32, i32, P, P], i32),
             "tq_sdpa_int4_partial": ([C, P, i32, P, i32, f32, i32, i32, P, P, P, P, i32, P], i32),
             "tq_sdpa_int4_reduce": ([P, P, P, i32, i32, i32, i32, P, P], i32),
             "tq_sdpa_int4_decode_noalloc": ([C, P, i32, P, i32, f32, i32, P, P, P], i32),
@@ -384,13 +384,14 @@ def tq_sdpa_plan(cache: KVCache, num_q_heads: int, max_seq_len: int, chunk: int 
 
 
 def tq_split_plan(batch: int, num_kv_heads: int, max_seq_len: int, chunk: int, tile_tokens: int,
-                  resident_ctas: int):
+                  resident_ctas: int, merge: bool = True):
     """(n_splits, max_run_tokens) of the split rule for a device holding
-    ``resident_ctas`` phase-1 CTAs at once (host arithmetic, no device)."""
+    ``resident_ctas`` phase-1 CTAs at once (host arithmetic, no device);
+    ``merge``: the decode may merge its runs itself (no reduce)."""
     ns, run = ctypes.c_int32(0), ctypes.c_int32(0)
     _check("tq_split_plan", lib().tq_split_plan(int(batch), int(num_kv_heads), int(max_seq_len), int(chunk),
-                                                int(tile_tokens), int(resident_ctas), ctypes.byref(ns),
-                                                ctypes.byref(run)))
+                                                int(tile_tokens), int(resident_ctas), int(bool(merge)),
+                                                ctypes.byref(ns), ctypes.byref(run)))
     return ns.value, run.value
 
 

@@ -179,10 +179,16 @@ __device__ __forceinline__ int clamp_len(const DecodeParams& p, const int32_t* s
     return len;
 }
 
-// DIRECT: one run per sequence, the merged state written as the output
-// (a separate instantiation: the extra branch in the epilogue of the split
-// kernel measured 0.45 us slower per 128K decode).
-template <int D, bool PAGED, int BITS, bool DIRECT>
+// What the kernel writes (separate instantiations: an extra branch in the
+// epilogue of the split kernel measured 0.45 us slower per 128K decode):
+//  kOutParts    the run's partial state (m, l, acc), merged by the reduce;
+//  kOutDirect   one run per sequence: fp16(acc / l) is the output;
+//  kOutCluster  the runs of a (sequence, kv head) are one thread-block cluster
+//               (n_splits <= 8 CTAs): the CTAs merge their states through
+//               distributed shared memory and write the output, no reduce.
+constexpr int kOutParts = 0, kOutDirect = 1, kOutCluster = 2;
+
+template <int D, bool PAGED, int BITS, int OUT>
 __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const DecodeParams p) {
@@ -194,6 +200,10 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
     // paged: the block-table entries of this run's pages, loaded once
     constexpr int kPageWindow = PAGED ? 256 : 1;
     __shared__ int32_t page_s[kPageWindow];
+    // kOutCluster: this CTA's merged state, read by the cluster (acc after the
+    // warps' merge buffer in the dynamic shared memory)
+    constexpr int kClHeads = OUT == kOutCluster ? 8 : 1;
+    __shared__ float cl_m[kClHeads], cl_l[kClHeads];
     extern __shared__ uint8_t dyn_smem[];
     const uint32_t dyn_base = smem_u32(dyn_smem);
     uint8_t* smem = dyn_smem + ((1024u - (dyn_base & 1023u)) & 1023u);
@@ -802,6 +812,9 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
     // (every issued fill has been waited for by every warp once all pass this barrier)
     __syncthreads();
     float* mrg_acc = reinterpret_cast<float*>(smem);  // [NWC][8][D]
+    float* cl_acc = mrg_acc + C::NWC * 8 * D;          // kOutCluster: [8][D]
+    static_assert(OUT != kOutCluster || C::STAGES * C::STAGE_BYTES >= (C::NWC + 1) * 8 * D * 4,
+                  "the cluster state must fit in the stages after the merge buffer");
     {
         float* wacc = mrg_acc + warp * 8 * D;
         if constexpr (BITS == 8) {
@@ -860,8 +873,14 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
             }
         }
         const long long ph = (static_cast<long long>(b) * p.num_q_heads + kvh * G + h) * p.n_splits + split;
-        if constexpr (DIRECT) {  // one run: the same division and rounding as the reduce of one part
+        if constexpr (OUT == kOutDirect) {  // one run: the same division and rounding as the reduce of one part
             p.out[ph * D + d] = __half_as_ushort(__float2half_rn(L > 0.0f ? __fdiv_rn(A, L) : 0.0f));
+        } else if constexpr (OUT == kOutCluster) {  // the partial state, kept for the cluster merge below
+            cl_acc[h * D + d] = A;
+            if (d == 0) {
+                cl_m[h] = M == -INFINITY ? -INFINITY : M * ln2;
+                cl_l[h] = L;
+            }
         } else {
             p.part_acc[ph * D + d] = A;
             if (d == 0) {
@@ -870,52 +889,115 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
             }
         }
     }
+    if constexpr (OUT == kOutCluster) {
+        // Merge the cluster's partial states (one per run of this sequence and
+        // kv head, read from the runs' shared memory), each CTA taking a share
+        // of the (head, dim) outputs, with the reduce kernel's arithmetic for
+        // up to eight parts, operation for operation: M = max of m over parts
+        // with l > 0, w = expf(m - M), L = the reduce's shuffle-tree sum of
+        // fmaf(w, l, 0) (lanes 0..7: ((0 + 4) + (2 + 6)) + ((1 + 5) + (3 + 7))),
+        // the output sum of fmaf(w, acc, 0) in part order, fp16(acc / L).  The
+        // result is bit for bit the one of phase 1 with partials plus the reduce.
+        cluster_sync();
+        const int n_runs = static_cast<int>(gridDim.x), rank = static_cast<int>(cluster_ctarank());
+        for (int idx = rank * C::THREADS + threadIdx.x; idx < G * D; idx += n_runs * C::THREADS) {
+            const int h = idx / D, d = idx % D;
+            // all the runs' values in one round trip of remote loads
+            float m[kMaxClusterRuns], w[kMaxClusterRuns], v[kMaxClusterRuns], a[kMaxClusterRuns];
+#pragma unroll
+            for (int r = 0; r < kMaxClusterRuns; ++r) {
+                v[r] = r < n_runs ? ld_cluster_f32(&cl_l[h], r) : 0.0f;
+                m[r] = r < n_runs ? ld_cluster_f32(&cl_m[h], r) : -INFINITY;
+                a[r] = r < n_runs ? ld_cluster_f32(&cl_acc[h * D + d], r) : 0.0f;
+            }
+            float M = -INFINITY;
+#pragma unroll
+            for (int r = 0; r < kMaxClusterRuns; ++r) {
+                if (!(v[r] > 0.0f)) m[r] = -INFINITY;  // empty parts carry no weight
+                M = fmaxf(M, m[r]);
+            }
+#pragma unroll
+            for (int r = 0; r < kMaxClusterRuns; ++r) {
+                w[r] = m[r] == -INFINITY ? 0.0f : expf(m[r] - M);
+                v[r] = fmaf(w[r], v[r], 0.0f);
+            }
+            const float L = ((v[0] + v[4]) + (v[2] + v[6])) + ((v[1] + v[5]) + (v[3] + v[7]));
+            float t = 0.0f;
+#pragma unroll
+            for (int r = 0; r < kMaxClusterRuns; ++r) t += w[r] != 0.0f ? fmaf(w[r], a[r], 0.0f) : 0.0f;
+            const long long o = (static_cast<long long>(b) * p.num_q_heads + kvh * G + h) * D + d;
+            p.out[o] = __half_as_ushort(__float2half_rn(L > 0.0f ? __fdiv_rn(t, L) : 0.0f));
+        }
+        cluster_sync();  // no CTA leaves while another may still read its shared memory
+    }
 }
 
-template <int D, bool PAGED, int BITS, bool DIRECT>
+template <int D, bool PAGED, int BITS, int OUT>
 cudaError_t set_smem_attr() {
     // per device; setting the attribute twice (two host threads) is harmless
     static std::atomic<bool> done[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, PAGED, BITS, DIRECT>,
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, PAGED, BITS, OUT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, BITS>::SMEM_BYTES);
     if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
     return e;
 }
 
+template <int D, bool PAGED, int BITS, int OUT>
+cudaError_t launch_mode(cudaLaunchConfig_t& cfg, const DecodeParams& p, const CUtensorMap& tm_k,
+                        const CUtensorMap& tm_v) {
+    const cudaError_t e = set_smem_attr<D, PAGED, BITS, OUT>();
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, PAGED, BITS, OUT>, tm_k, tm_v, p);
+}
+
+// p.out set: the kernel writes the output itself, one run per sequence
+// (n_splits = 1) or the runs of each (sequence, kv head) as one cluster.
 template <int D, int BITS>
 cudaError_t launch_d(const DecodeParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v, cudaStream_t stream,
                      bool pdl_secondary) {
     using C = Cfg<D, BITS>;
-    const bool paged = p.map.block_table != nullptr, direct = p.out != nullptr;
-    cudaError_t e = paged ? (direct ? set_smem_attr<D, true, BITS, true>() : set_smem_attr<D, true, BITS, false>())
-                          : (direct ? set_smem_attr<D, false, BITS, true>() : set_smem_attr<D, false, BITS, false>());
-    if (e != cudaSuccess) return e;
+    const bool paged = p.map.block_table != nullptr;
+    const int out = p.out == nullptr ? kOutParts : (p.n_splits == 1 ? kOutDirect : kOutCluster);
+    if (out == kOutCluster && p.n_splits > kMaxClusterRuns) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_splits, p.num_kv_heads, p.batch);
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl_secondary ? 1 : 0;
-    if (paged) {
-        if (direct) return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, true, BITS, true>, tm_k, tm_v, p);
-        return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, true, BITS, false>, tm_k, tm_v, p);
+    cudaLaunchAttribute attr[2];
+    unsigned int n = 0;
+    if (pdl_secondary) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
     }
-    if (direct) return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, false, BITS, true>, tm_k, tm_v, p);
-    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, false, BITS, false>, tm_k, tm_v, p);
+    if (out == kOutCluster) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned int>(p.n_splits);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    if (paged) {
+        if (out == kOutDirect) return launch_mode<D, true, BITS, kOutDirect>(cfg, p, tm_k, tm_v);
+        if (out == kOutCluster) return launch_mode<D, true, BITS, kOutCluster>(cfg, p, tm_k, tm_v);
+        return launch_mode<D, true, BITS, kOutParts>(cfg, p, tm_k, tm_v);
+    }
+    if (out == kOutDirect) return launch_mode<D, false, BITS, kOutDirect>(cfg, p, tm_k, tm_v);
+    if (out == kOutCluster) return launch_mode<D, false, BITS, kOutCluster>(cfg, p, tm_k, tm_v);
+    return launch_mode<D, false, BITS, kOutParts>(cfg, p, tm_k, tm_v);
 }
 
 template <int D, int BITS>
 int ctas_per_sm_d() {
-    if (set_smem_attr<D, false, BITS, false>() != cudaSuccess) return 1;
+    if (set_smem_attr<D, false, BITS, kOutParts>() != cudaSuccess) return 1;
     int n = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D, false, BITS, false>, Cfg<D, BITS>::THREADS,
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D, false, BITS, kOutParts>, Cfg<D, BITS>::THREADS,
                                                   Cfg<D, BITS>::SMEM_BYTES);
     return n > 0 ? n : 1;
 }

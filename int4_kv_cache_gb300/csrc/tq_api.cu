@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -237,18 +238,28 @@ int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b
 // Balanced runs of whole units (the kernel's pipeline tile, or the chunk if
 // that is smaller, so that runs cover the sequence evenly whatever its length
 // in chunks), as many per (sequence, kv head) as minimise a model of the
-// grid's time: waves x (longest run + a fixed cost per CTA), waves =
-// ceil(CTAs / resident CTA slots).  The fixed cost (pipeline fill, the query
-// load, the partial-state store) is worth about two tiles of streaming.
-// Within one wave count more runs are shorter, so only the largest run count
-// of each wave count is a candidate, taken down to the fewest runs with the
-// same longest run; ties keep the fewer runs (less reduce work).  One sequence fills the resident slots once (57 runs at 128K with 8
-// kv heads and 456 slots); a batch whose grid needs several waves gets a CTA
-// count just under a whole number of waves (16 sequences of 32K: 7 runs, 896
-// CTAs for 912 slots: 110 us against 141 us with 4 runs and 512 CTAs).
+// decode's time: waves x (longest run + a fixed cost per CTA), waves =
+// ceil(CTAs / resident CTA slots), plus the reduce when one runs.  The fixed
+// cost (pipeline fill, the query load, the partial-state store) is worth
+// about two tiles of streaming, the reduce (the tail of the partial states'
+// round trip; its launch overlaps phase 1) about one: on a GB300 the Gemma
+// shape at 950 tokens decodes in 7.3 us as 8 merged runs of two tiles and in
+// 7.5 us as 15 runs of one tile + the reduce, and at 2,048 tokens in 8.8 us
+// as 16 runs of two tiles + the reduce against 9.6 us as 8 merged runs.  With `merge` (the decode may merge the runs
+// itself), one run per sequence, or up to kMaxClusterRuns runs in a grid of
+// one wave (one thread-block cluster per sequence and kv head), needs no
+// reduce.  Within one wave count more runs are shorter, so the candidates are
+// the largest run count of each wave count, the largest that phase 1 can
+// merge, and one run, each taken down to the fewest runs with the same
+// longest run; ties keep the fewer runs.  One sequence of 128K fills the
+// resident slots once (57 runs with 8 kv heads and 456 slots); a batch whose
+// grid needs several waves gets a CTA count just under a whole number of
+// waves (16 sequences of 32K: 7 runs, 896 CTAs for 912 slots: 110 us against
+// 141 us with 4 runs and 512 CTAs).
 constexpr long long kRunFixedTiles = 2;
+constexpr long long kReduceTiles = 1;
 
-Plan make_plan(int batch, int hkv, int max_seq_len, int chunk, int tile_tokens, int resident) {
+Plan make_plan(int batch, int hkv, int max_seq_len, int chunk, int tile_tokens, int resident, bool merge) {
     Plan pl;
     pl.unit_tokens = chunk < tile_tokens ? chunk : tile_tokens;
     pl.units = ceil_div(max_seq_len, pl.unit_tokens);
@@ -258,20 +269,25 @@ Plan make_plan(int batch, int hkv, int max_seq_len, int chunk, int tile_tokens, 
     if (cap > pl.units) cap = pl.units;
     if (cap < 1) cap = 1;
     long long best = 1, best_cost = -1;
-    for (long long w = (heads + slots - 1) / slots;; ++w) {
-        long long ns = w * slots / heads;
+    auto consider = [&](long long ns) {
         if (ns > cap) ns = cap;
         if (ns < 1) ns = 1;
         const long long run_units = (pl.units + ns - 1) / ns;
         const long long n = (pl.units + run_units - 1) / run_units;  // fewest runs this long
         const long long waves = (heads * n + slots - 1) / slots;
-        const long long run = run_units * pl.unit_tokens;
-        const long long cost = waves * (run + kRunFixedTiles * tile_tokens);
-        if (best_cost < 0 || cost < best_cost) {
+        long long cost = waves * (run_units * pl.unit_tokens + kRunFixedTiles * tile_tokens);
+        if (!(merge && (n == 1 || (n <= tq::kMaxClusterRuns && waves == 1)))) cost += kReduceTiles * tile_tokens;
+        if (best_cost < 0 || cost < best_cost || (cost == best_cost && n < best)) {
             best_cost = cost;
             best = n;
         }
-        if (ns == cap) break;
+        return ns;
+    };
+    for (long long w = (heads + slots - 1) / slots;; ++w)
+        if (consider(w * slots / heads) >= cap) break;
+    if (merge) {
+        consider(1);
+        if (heads <= slots) consider(std::min<long long>(tq::kMaxClusterRuns, slots / heads));
     }
     pl.n_splits = static_cast<int>(best);
     return pl;
@@ -286,7 +302,8 @@ Plan chunk_plan(int max_seq_len, int chunk, int cps) {
     return pl;
 }
 
-tq_status device_plan(const Store* cache, int max_seq_len, int chunk, tq_impl impl, Plan* pl) {
+tq_status device_plan(const Store* cache, int max_seq_len, int chunk, tq_impl impl, Plan* pl,
+                      bool merge = true) {
     DeviceFacts* f = nullptr;
     tq_status s = device_facts(&f);
     if (s != TQ_OK) return s;
@@ -295,7 +312,7 @@ tq_status device_plan(const Store* cache, int max_seq_len, int chunk, tq_impl im
     const int per_sm = simt ? f->simt_ctas[di] : f->mma_ctas[cache->bits == 8 ? 1 : 0][di];
     const int tile = simt ? tq::kSimtTileTokens : tq::mma_tile_tokens(cache->head_dim, cache->bits);
     if (cache->paged && chunk < tile) chunk = tile;  // runs start on tile (hence page-aligned) boundaries
-    *pl = make_plan(cache->batch, cache->num_kv_heads, max_seq_len, chunk, tile, f->sms * per_sm);
+    *pl = make_plan(cache->batch, cache->num_kv_heads, max_seq_len, chunk, tile, f->sms * per_sm, merge && !simt);
     pl->tile_tokens = tile;
     pl->resident = static_cast<long long>(f->sms) * per_sm;
     return TQ_OK;
@@ -588,7 +605,9 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
     if (workspace == nullptr || workspace_bytes < need) return TQ_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TQ_ERR_ALIGN;
     Plan pl;
-    s = device_plan(cache, max_seq_len, chunk, impl, &pl);
+    // the runs may merge in phase 1 unless the reduce has other work (the
+    // output rotation of TQ_ROTATE_V, the length advance)
+    s = device_plan(cache, max_seq_len, chunk, impl, &pl, !(flags & TQ_ROTATE_V) && !advance);
     if (s != TQ_OK) return s;
     if (pl.n_splits > tq::kMaxReduceParts) return TQ_ERR_SHAPE;
     const size_t parts = static_cast<size_t>(cache->batch) * hq * pl.n_splits;
@@ -625,10 +644,14 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
         if (s != TQ_OK) return s;
     }
     const bool dep = n_new > 0 && !fused && ph1 == TQ_IMPL_MMA;
-    // One run per sequence (short sequences): phase 1 writes the output
-    // itself and no reduce is launched, unless the reduce has other work (the
-    // output rotation of TQ_ROTATE_V, the length advance)
-    const bool direct = pl.n_splits == 1 && ph1 == TQ_IMPL_MMA && !(flags & TQ_ROTATE_V) && !advance;
+    // Phase 1 writes the output itself and no reduce is launched, unless the
+    // reduce has other work (the output rotation of TQ_ROTATE_V, the length
+    // advance): with one run per sequence, or with up to kMaxClusterRuns runs
+    // in a grid of one wave, whose runs of each (sequence, kv head) form a
+    // thread-block cluster that merges its states in shared memory.
+    const long long ctas = static_cast<long long>(pl.n_splits) * cache->num_kv_heads * cache->batch;
+    const bool direct = ph1 == TQ_IMPL_MMA && !(flags & TQ_ROTATE_V) && !advance &&
+                        (pl.n_splits == 1 || (pl.n_splits <= tq::kMaxClusterRuns && ctas <= pl.resident));
     s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, ph1, st,
                    dep ? write_pos : nullptr, dep ? n_new : 0, fused ? &ap : nullptr, rotate_q, order,
                    direct ? out : nullptr);
@@ -911,12 +934,13 @@ tq_status tq_sdpa_plan(const tq_kv_cache* cache, int32_t hq, int32_t max_seq_len
 }
 
 tq_status tq_split_plan(int32_t batch, int32_t num_kv_heads, int32_t max_seq_len, int32_t chunk,
-                        int32_t tile_tokens, int32_t resident_ctas, int32_t* n_splits, int32_t* max_run_tokens) {
+                        int32_t tile_tokens, int32_t resident_ctas, int32_t merge, int32_t* n_splits,
+                        int32_t* max_run_tokens) {
     if (n_splits == nullptr || max_run_tokens == nullptr) return TQ_ERR_NULL;
     if (batch < 1 || num_kv_heads < 1 || max_seq_len < 1 || chunk < 16 || chunk % 16 || tile_tokens < 16 ||
         tile_tokens % 16 || resident_ctas < 1)
         return TQ_ERR_SHAPE;
-    const Plan pl = make_plan(batch, num_kv_heads, max_seq_len, chunk, tile_tokens, resident_ctas);
+    const Plan pl = make_plan(batch, num_kv_heads, max_seq_len, chunk, tile_tokens, resident_ctas, merge != 0);
     *n_splits = pl.n_splits;
     *max_run_tokens = ceil_div(pl.units, pl.n_splits) * pl.unit_tokens;
     return TQ_OK;

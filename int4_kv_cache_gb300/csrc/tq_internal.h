@@ -236,6 +236,10 @@ int mma_ctas_per_sm(int head_dim, int bits);
 int simt_ctas_per_sm(int head_dim);
 // Largest n_parts the reduce kernel takes.
 constexpr int kMaxReduceParts = 8192;
+// Most runs per (sequence, kv head) merged inside phase 1 by a thread-block
+// cluster (the portable cluster size); such launches write the output and
+// need no reduce.
+constexpr int kMaxClusterRuns = 8;
 // Most CTAs a decode plan launches (bounds the workspace independently of the device).
 constexpr int kMaxDecodeCtas = 2048;
 // Tokens per work unit of the SIMT phase-1 kernel.

@@ -193,9 +193,11 @@ def test_partials_match_oracle_chunks():
 
 @pytest.mark.parametrize("name", ["llama70b_16k", "gemma_33", "tiny"])
 def test_decode_equals_partial_plan_plus_reduce(name):
-    """tq_sdpa_int4_decode == phase 1 with the decode's own plan + phase 2, bit
-    for bit; gemma_33 has one run per sequence, where phase 1 writes the
-    output itself (no reduce launch) with the reduce's arithmetic."""
+    """tq_sdpa_int4_decode == phase 1 with the decode's own plan + phase 2,
+    bit for bit: with the reduce (llama70b_16k: 43 runs), with one run per
+    sequence (gemma_33: phase 1 writes the output itself with the reduce's
+    arithmetic), and with runs merged inside a thread-block cluster (tiny: 2
+    runs, the reduce's operations in the reduce's order)."""
     torch = need_gpu()
     import int4_kv_cache_gb300 as tq
 
@@ -208,6 +210,38 @@ def test_decode_equals_partial_plan_plus_reduce(name):
     m, l, acc = tq.tq_sdpa_int4_partial(cache, q, lens, w.seq_len, w.attn_scale, chunks_per_split=0)
     two = tq.tq_sdpa_int4_reduce(m, l, acc).float().cpu().numpy()
     assert np.array_equal(full, two.astype(np.float64))
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,S,bits", [(128, 64, 8, 1024, 4), (128, 16, 2, 700, 4), (256, 32, 16, 423, 4),
+                                             (64, 8, 4, 900, 4), (128, 64, 8, 500, 8), (256, 32, 16, 786, 8)])
+def test_cluster_merged_decode_matches_oracle(D, Hq, Hkv, S, bits):
+    """Two to eight runs per (sequence, kv head) in a grid of one wave: the
+    runs form one thread-block cluster and merge their states in shared
+    memory, with no reduce launch.  Against the oracle, with ragged lengths
+    (runs past a sequence's end are empty) and a sequence of length 0."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    B = 3
+    lens = np.array([S, S // 3 + 5, 0], np.int32)
+    x = synth.decode_inputs(400 + D + bits, B, Hq, Hkv, D, S, lens=lens, outliers=True)
+    k, v = torch.from_numpy(x.k).cuda(), torch.from_numpy(x.v).cuda()
+    cap = -(-S // 16) * 16
+    cache = tq.KVCache(B, Hkv, D, cap, bits=bits)
+    tq.tq_quantize_kv_append(cache, k, v, torch.zeros(B, dtype=torch.int32, device="cuda"))
+    n_splits = tq.tq_sdpa_plan(cache, Hq, S)[0]
+    assert 2 <= n_splits <= 8, n_splits
+    a = 1 / math.sqrt(D)
+    got = decode(cache, x.q, lens, S, a)
+    oc = oracle.Cache.from_fp16(x.k, x.v, bits=bits)
+    ref = oracle.attention(x.q, oc, lens, a)
+    assert np.all(got[2] == 0)
+    assert_close(got, ref, what=f"cluster D{D} bits{bits}")
+    # the same bits as phase 1 with partial states plus the reduce
+    lt = torch.from_numpy(lens).cuda()
+    m, l, acc = tq.tq_sdpa_int4_partial(cache, torch.from_numpy(x.q).cuda(), lt, S, a, chunks_per_split=0)
+    two = tq.tq_sdpa_int4_reduce(m, l, acc).float().cpu().numpy().astype(np.float64)
+    assert np.array_equal(got, two)
 
 
 def test_reduce_matches_oracle_merge():
