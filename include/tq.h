@@ -285,9 +285,12 @@ size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t num_q_heads,
  *           units of min(chunk, pipeline tile) tokens (the tile is 128 tokens
  *           when a token's codes take under 128 bytes, 64 otherwise); each run
  *           keeps one running softmax
- *           state and the runs' states are merged by a log-sum-exp reduce.  The
- *           result is the same as merging one state per chunk (see
- *           tq_sdpa_int4_partial with chunks_per_split = 1).
+ *           state and the runs' states are merged by a log-sum-exp reduce
+ *           (tq_sdpa_int4_reduce; with at most 8 runs in a grid of one wave the
+ *           runs of each (sequence, kv head) form one thread-block cluster and
+ *           merge in phase 1 with the reduce's operations, bit for bit the same
+ *           output).  The result is the same as merging one state per chunk
+ *           (see tq_sdpa_int4_partial with chunks_per_split = 1).
  * workspace: device scratch (256-byte aligned) of at least
  *           tq_sdpa_workspace_bytes(...) bytes holding the fp32 partial states,
  *           room for a rotated query and, for batches whose grid spans several
