@@ -652,9 +652,19 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
     const long long ctas = static_cast<long long>(pl.n_splits) * cache->num_kv_heads * cache->batch;
     const bool direct = ph1 == TQ_IMPL_MMA && !(flags & TQ_ROTATE_V) && !advance &&
                         (pl.n_splits == 1 || (pl.n_splits <= tq::kMaxClusterRuns && ctas <= pl.resident));
+    bool own_out = direct;
     s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, ph1, st,
                    dep ? write_pos : nullptr, dep ? n_new : 0, fused ? &ap : nullptr, rotate_q, order,
-                   direct ? out : nullptr);
+                   own_out ? out : nullptr);
+    if (s != TQ_OK && own_out && pl.n_splits > 1) {
+        // a cluster launch the device refused (nothing was queued; e.g. a GPU
+        // partition too small to place the cluster): the same runs with
+        // partial states and the reduce, the same output
+        cudaGetLastError();
+        own_out = false;
+        s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, ph1, st,
+                       dep ? write_pos : nullptr, dep ? n_new : 0, fused ? &ap : nullptr, rotate_q, order, nullptr);
+    }
     if (s != TQ_OK) return s;
     tq::ReduceParams r{};
     r.part_m = pm;
@@ -675,7 +685,7 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
         r.adv_write_pos = const_cast<int32_t*>(write_pos);
         r.adv_n = n_new;
     }
-    if (direct) return s;
+    if (own_out) return s;
     s = cuda_status(tq::launch_reduce(r, st, true));
     if (s != TQ_OK || !advance || fused || n_new == 0) return s;
     return cuda_status(tq::launch_advance(const_cast<int32_t*>(seq_lens), const_cast<int32_t*>(write_pos),
