@@ -993,6 +993,32 @@ cudaError_t launch_d(const DecodeParams& p, const CUtensorMap& tm_k, const CUten
     return launch_mode<D, false, BITS, kOutParts>(cfg, p, tm_k, tm_v);
 }
 
+// Clusters of n CTAs of the cluster-merging instantiation the device holds at
+// once (0 if it cannot place one).
+template <int D, bool PAGED, int BITS>
+int max_clusters_d(int n) {
+    using C = Cfg<D, BITS>;
+    if (set_smem_attr<D, PAGED, BITS, kOutCluster>() != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned int>(n), 1, 1);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = static_cast<unsigned int>(n);
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, decode_mma_kernel<D, PAGED, BITS, kOutCluster>, &cfg) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return clusters;
+}
+
 template <int D, int BITS>
 int ctas_per_sm_d() {
     if (set_smem_attr<D, false, BITS, kOutParts>() != cudaSuccess) return 1;
@@ -1029,6 +1055,18 @@ int mma_tile_tokens(int head_dim, int bits) {
 int mma_smem_bytes(int head_dim, int bits) {
     TQ_DISPATCH(Cfg<64>::SMEM_BYTES, Cfg<128>::SMEM_BYTES, Cfg<256>::SMEM_BYTES, (Cfg<64, 8>::SMEM_BYTES),
                 (Cfg<128, 8>::SMEM_BYTES), (Cfg<256, 8>::SMEM_BYTES), 0)
+}
+
+int mma_max_active_clusters(int head_dim, int bits, bool paged, int n) {
+    if (n < 2 || n > kMaxClusterRuns) return 0;
+    if (paged) {
+        TQ_DISPATCH((max_clusters_d<64, true, 4>(n)), (max_clusters_d<128, true, 4>(n)),
+                    (max_clusters_d<256, true, 4>(n)), (max_clusters_d<64, true, 8>(n)),
+                    (max_clusters_d<128, true, 8>(n)), (max_clusters_d<256, true, 8>(n)), 0)
+    }
+    TQ_DISPATCH((max_clusters_d<64, false, 4>(n)), (max_clusters_d<128, false, 4>(n)),
+                (max_clusters_d<256, false, 4>(n)), (max_clusters_d<64, false, 8>(n)),
+                (max_clusters_d<128, false, 8>(n)), (max_clusters_d<256, false, 8>(n)), 0)
 }
 
 int mma_ctas_per_sm(int head_dim, int bits) {

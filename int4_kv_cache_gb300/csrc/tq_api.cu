@@ -193,6 +193,9 @@ struct DeviceFacts {
     int sms = 0;
     int mma_ctas[2][3] = {{0, 0, 0}, {0, 0, 0}};  // per code width (4, 8) and head_dim 64 / 128 / 256
     int simt_ctas[3] = {0, 0, 0};
+    // clusters of n CTAs of the cluster-merging kernel held at once, per code
+    // width, head_dim, layout (contiguous, paged) and n
+    int clusters[2][3][2][tq::kMaxClusterRuns + 1] = {};
 };
 
 int dim_index(int d) { return d == 64 ? 0 : (d == 128 ? 1 : 2); }
@@ -216,6 +219,12 @@ tq_status device_facts(DeviceFacts** out) {
                 f.mma_ctas[0][i] = tq::mma_ctas_per_sm(dims[i], 4);
                 if (tq::mma_supported(dims[i], 8)) f.mma_ctas[1][i] = tq::mma_ctas_per_sm(dims[i], 8);
                 f.simt_ctas[i] = tq::simt_ctas_per_sm(dims[i]);
+                for (int bi = 0; bi < 2; ++bi) {
+                    if (!tq::mma_supported(dims[i], bi ? 8 : 4)) continue;
+                    for (int pg = 0; pg < 2; ++pg)
+                        for (int n = 2; n <= tq::kMaxClusterRuns; ++n)
+                            f.clusters[bi][i][pg][n] = tq::mma_max_active_clusters(dims[i], bi ? 8 : 4, pg != 0, n);
+                }
             }
             cudaGetLastError();  // occupancy queries must leave no pending error
             facts[dev] = f;
@@ -229,6 +238,7 @@ tq_status device_facts(DeviceFacts** out) {
 // ------------------------------------------------------------- decode plan --
 struct Plan {
     int n_splits, unit_tokens, units;
+    bool merged = false;  // the decode merges the runs itself (one run, or one cluster per sequence and kv head)
     int tile_tokens = 0;  // the kernel's pipeline tile
     long long resident = 0;  // CTAs the device holds at once for this kernel
 };
@@ -259,7 +269,10 @@ int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b
 constexpr long long kRunFixedTiles = 2;
 constexpr long long kReduceTiles = 1;
 
-Plan make_plan(int batch, int hkv, int max_seq_len, int chunk, int tile_tokens, int resident, bool merge) {
+// cluster_cap[n]: clusters of n CTAs the device holds at once (null: every
+// grid of one wave, the host rule).
+Plan make_plan(int batch, int hkv, int max_seq_len, int chunk, int tile_tokens, int resident, bool merge,
+               const int* cluster_cap = nullptr) {
     Plan pl;
     pl.unit_tokens = chunk < tile_tokens ? chunk : tile_tokens;
     pl.units = ceil_div(max_seq_len, pl.unit_tokens);
@@ -268,7 +281,14 @@ Plan make_plan(int batch, int hkv, int max_seq_len, int chunk, int tile_tokens, 
     long long cap = tq::kMaxDecodeCtas / heads;
     if (cap > pl.units) cap = pl.units;
     if (cap < 1) cap = 1;
+    auto mergeable = [&](long long n, long long waves) {
+        if (!merge) return false;
+        if (n == 1) return true;
+        if (n > tq::kMaxClusterRuns) return false;
+        return cluster_cap != nullptr ? heads <= cluster_cap[n] : waves == 1;
+    };
     long long best = 1, best_cost = -1;
+    bool best_merged = false;
     auto consider = [&](long long ns) {
         if (ns > cap) ns = cap;
         if (ns < 1) ns = 1;
@@ -276,20 +296,21 @@ Plan make_plan(int batch, int hkv, int max_seq_len, int chunk, int tile_tokens, 
         const long long n = (pl.units + run_units - 1) / run_units;  // fewest runs this long
         const long long waves = (heads * n + slots - 1) / slots;
         long long cost = waves * (run_units * pl.unit_tokens + kRunFixedTiles * tile_tokens);
-        if (!(merge && (n == 1 || (n <= tq::kMaxClusterRuns && waves == 1)))) cost += kReduceTiles * tile_tokens;
+        const bool merged = mergeable(n, waves);
+        if (!merged) cost += kReduceTiles * tile_tokens;
         if (best_cost < 0 || cost < best_cost || (cost == best_cost && n < best)) {
             best_cost = cost;
             best = n;
+            best_merged = merged;
         }
         return ns;
     };
     for (long long w = (heads + slots - 1) / slots;; ++w)
         if (consider(w * slots / heads) >= cap) break;
-    if (merge) {
-        consider(1);
-        if (heads <= slots) consider(std::min<long long>(tq::kMaxClusterRuns, slots / heads));
-    }
+    if (merge)
+        for (long long n = 1; n <= tq::kMaxClusterRuns; ++n) consider(n);
     pl.n_splits = static_cast<int>(best);
+    pl.merged = best_merged;
     return pl;
 }
 
@@ -312,7 +333,8 @@ tq_status device_plan(const Store* cache, int max_seq_len, int chunk, tq_impl im
     const int per_sm = simt ? f->simt_ctas[di] : f->mma_ctas[cache->bits == 8 ? 1 : 0][di];
     const int tile = simt ? tq::kSimtTileTokens : tq::mma_tile_tokens(cache->head_dim, cache->bits);
     if (cache->paged && chunk < tile) chunk = tile;  // runs start on tile (hence page-aligned) boundaries
-    *pl = make_plan(cache->batch, cache->num_kv_heads, max_seq_len, chunk, tile, f->sms * per_sm, merge && !simt);
+    *pl = make_plan(cache->batch, cache->num_kv_heads, max_seq_len, chunk, tile, f->sms * per_sm, merge && !simt,
+                    f->clusters[cache->bits == 8 ? 1 : 0][di][cache->paged ? 1 : 0]);
     pl->tile_tokens = tile;
     pl->resident = static_cast<long long>(f->sms) * per_sm;
     return TQ_OK;
@@ -644,14 +666,12 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
         if (s != TQ_OK) return s;
     }
     const bool dep = n_new > 0 && !fused && ph1 == TQ_IMPL_MMA;
-    // Phase 1 writes the output itself and no reduce is launched, unless the
-    // reduce has other work (the output rotation of TQ_ROTATE_V, the length
-    // advance): with one run per sequence, or with up to kMaxClusterRuns runs
-    // in a grid of one wave, whose runs of each (sequence, kv head) form a
-    // thread-block cluster that merges its states in shared memory.
-    const long long ctas = static_cast<long long>(pl.n_splits) * cache->num_kv_heads * cache->batch;
-    const bool direct = ph1 == TQ_IMPL_MMA && !(flags & TQ_ROTATE_V) && !advance &&
-                        (pl.n_splits == 1 || (pl.n_splits <= tq::kMaxClusterRuns && ctas <= pl.resident));
+    // Phase 1 writes the output itself and no reduce is launched when the plan
+    // says so (never when the reduce has other work: the output rotation of
+    // TQ_ROTATE_V, the length advance): one run per sequence, or up to
+    // kMaxClusterRuns runs whose clusters (one per sequence and kv head, merging
+    // their states in shared memory) the device holds all at once.
+    const bool direct = ph1 == TQ_IMPL_MMA && !(flags & TQ_ROTATE_V) && !advance && pl.merged;
     bool own_out = direct;
     s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, ph1, st,
                    dep ? write_pos : nullptr, dep ? n_new : 0, fused ? &ap : nullptr, rotate_q, order,

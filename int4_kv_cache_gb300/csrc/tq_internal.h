@@ -233,6 +233,9 @@ int mma_smem_bytes(int head_dim, int bits);
 bool mma_supported(int head_dim, int bits);
 // Resident CTAs per SM of the phase-1 kernels (occupancy API).
 int mma_ctas_per_sm(int head_dim, int bits);
+// Clusters of n (2..kMaxClusterRuns) CTAs of the cluster-merging phase-1
+// kernel the device holds at once (occupancy API; 0: none).
+int mma_max_active_clusters(int head_dim, int bits, bool paged, int n);
 int simt_ctas_per_sm(int head_dim);
 // Largest n_parts the reduce kernel takes.
 constexpr int kMaxReduceParts = 8192;
