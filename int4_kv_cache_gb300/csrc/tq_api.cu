@@ -462,6 +462,12 @@ tq_status decode_into_partials(const tq_kv_cache* raw, const uint16_t* q, int32_
     float* pm = reinterpret_cast<float*>(partials);
     float* plv = reinterpret_cast<float*>(partials + align256(parts * sizeof(float)));
     float* pa = reinterpret_cast<float*>(partials + 2 * align256(parts * sizeof(float)));
+    if (pl.merged) {  // phase 1 writes the output (one run, or clusters); else as below
+        s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, TQ_IMPL_MMA,
+                       stream, nullptr, 0, nullptr, false, nullptr, out);
+        if (s == TQ_OK || pl.n_splits == 1) return s;
+        cudaGetLastError();  // a refused cluster launch: the partial states and the reduce
+    }
     s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, TQ_IMPL_MMA, stream);
     if (s != TQ_OK) return s;
     ReduceParams r{};
