@@ -1,7 +1,7 @@
 /*
  * abi_example.c -- the C ABI used from plain C (no Python, no PyTorch): quantize
  * a cache, decode, run one fused step, and check everything against the CPU
- * oracle.  Test infrastructure (it links the oracle); tests/test_gpu_c_abi.py
+ * oracle.  Test infrastructure (it links the oracle); tests/test_c_abi.py
  * compiles and runs it.
  *
  * Exit status 0 and a line "OK ..." when the codes, scales and biases equal the
