@@ -96,6 +96,19 @@ typedef enum tq_status {
  * advancing lengths. */
 #define TQ_STEP_ADVANCE 0x100u
 
+/* tq_decode_step_ex, tq_sdpa_int4_decode_ex and the paged forms: the caller
+ * promises that no work queued ahead of this call on the stream, and still
+ * running when it starts, writes the cache rows the decode reads (other than
+ * the rows this call appends) or seq_lens / write_pos.  The decode kernel may
+ * then start streaming the cache before the kernel ahead of it has finished
+ * and waits for that kernel only before reading the query and the new K/V
+ * rows, which it may produce.  Typical use: the attention of layer l + 1,
+ * queued behind layer l's work, which never writes layer l + 1's cache.
+ * Breaking the promise is a data race (stale rows may be read).  Not with
+ * TQ_STEP_ADVANCE (TQ_ERR_UNSUPPORTED): a step that advances the lengths for
+ * the next one writes what that one reads.  Results are unchanged. */
+#define TQ_CACHE_READY 0x200u
+
 /* Decode implementations (tq_sdpa_int4_decode_impl and friends). */
 typedef enum tq_impl {
     TQ_IMPL_AUTO = 0, /* the tensor-core path */
@@ -282,8 +295,9 @@ size_t tq_sdpa_workspace_bytes(int32_t batch, int32_t num_q_heads,
  * attn_scale: multiplies q.k (1/sqrt(head_dim) for Llama, 1.0 for Gemma)
  * chunk:    split-K chunk in tokens (multiple of 16; TQ_DEFAULT_CHUNK = 512).
  *           The sequence is split into balanced runs, one per CTA, of whole
- *           units of min(chunk, pipeline tile) tokens (the tile is 128 tokens
- *           when a token's codes take under 128 bytes, 64 otherwise); each run
+ *           units of min(chunk, pipeline tile) tokens (the tile is 384 tokens
+ *           for contiguous int4 caches at head_dim 128, else 128 tokens when a
+ *           token's codes take under 128 bytes, 64 otherwise); each run
  *           keeps one running softmax
  *           state and the runs' states are merged by a log-sum-exp reduce
  *           (tq_sdpa_int4_reduce; with at most 8 runs in a grid of one wave the
@@ -359,7 +373,8 @@ tq_status tq_sdpa_plan(const tq_kv_cache* cache, int32_t num_q_heads,
  * head) for `batch` sequences of up to `max_seq_len` tokens, `num_kv_heads`
  * kv heads, runs made of whole units of min(chunk, tile_tokens) tokens, on a
  * device that holds `resident_ctas` phase-1 CTAs at once (tq_sdpa_plan passes
- * the SM count x the CTAs per SM and the kernel's tile: 128 tokens when a
+ * the SM count x the CTAs per SM and the kernel's tile: 384 tokens for a
+ * contiguous int4 cache at head_dim 128, one CTA per SM; else 128 tokens when a
  * token's codes take under 128 bytes, 64 otherwise).  Picks the run count
  * n <= min(units, 2048 / (batch * num_kv_heads)) that minimises, with
  * W = ceil(batch * num_kv_heads * n / resident_ctas) waves,

@@ -14,9 +14,10 @@
 //    arrays streams into a ring of shared-memory stages: the code tiles by
 //    2-D TMA with the 128-byte swizzle, the scale/bias rows by 1-D bulk
 //    copies, completion on mbarriers.  There is no producer warp: the last
-//    warp to finish a stage issues its refill, so all four warps compute
-//    (three CTAs per SM for int4 at head_dim 128).  Every byte of the cache
-//    is read from HBM once per step, with an evict-first L2 policy.
+//    warp to finish a stage issues its refill, so every warp computes (one
+//    CTA of twelve warps per SM for contiguous int4 caches at head_dim 128,
+//    else several CTAs of four warps).  Every byte of the cache is read from
+//    HBM once per step, with an evict-first L2 policy.
 //  * Consumer warps turn the nibbles into fp16 operands with one AND per
 //    register: a 4-bit code n in the low mantissa bits of a zero-exponent fp16
 //    is the subnormal n * 2^-24, and the high nibble of a byte gives
@@ -57,7 +58,21 @@ constexpr uint32_t kHiNib = 0x00F000F0u;  // nibbles at bits 4..7 / 20..23 -> 16
 constexpr float kLazyMax = 8.0f;          // slack of the running softmax max (log2 units)
 constexpr uint32_t kByte = 0x00FF00FFu;   // int8: bytes 0 and 2 of a register -> n * 2^-24
 
-template <int D, int BITS = 4>
+// The SM layouts of phase 1.  WIDE: one CTA of 12 warps per SM sharing one
+// ring of 384-token stages, for contiguous int4 caches at head_dim 128 when
+// the plan's grid is one wave over (nearly) every SM.  Three independent
+// 4-warp CTAs on an SM finish at staggered times (the scheduler favours the
+// first placed) and the SM runs its last stretch on one CTA; twelve warps
+// releasing the same stages stay within a stage of each other, and a
+// (sequence, kv head) needs a third as many runs.  At 128K: 152 CTAs of
+// 6,912 tokens instead of 456 of 2,304, the step 33.4 -> 31.9 us; 2 CTAs of 6
+// warps per SM measured 33.4 us, one of 8 warps with 6 stages 34.7 us.  In a
+// grid of several waves an SM idles while its next CTA fills its ring, which
+// three CTAs per SM hide (ragged batch of 32: 123 us wide against 109 us), and
+// paged caches keep 128-token tiles (their pages hold whole tiles).
+__host__ __device__ constexpr bool wide_ok(int D, int BITS, bool PAGED) { return D == 128 && BITS == 4 && !PAGED; }
+
+template <int D, int BITS = 4, bool WIDE = false>
 struct Cfg {
     static constexpr int NG = D / kGroup;          // scale/bias groups per row
     static constexpr int BPT = D * BITS / 8;       // code bytes per token
@@ -71,7 +86,7 @@ struct Cfg {
     static constexpr int HALVES = BPT / ROWB;
     static constexpr int SPR = ROWB / 16;          // 16-byte segments of a token in one block
     static constexpr int TPR = 128 / ROWB;         // tokens per 128-byte swizzle row (1 for 128-byte blocks)
-    static constexpr int NWC = 4;                  // warps (all consume; the last to finish a stage refills it)
+    static constexpr int NWC = WIDE ? 12 : 4;      // warps (all consume; the last to finish a stage refills it)
     static constexpr int MT = (BPT >= 128) ? 1 : 2;  // 16-token m-tiles per warp per stage
     static constexpr float CODE_MEAN = ((1 << BITS) - 1) * 0.5f;  // mean of a code uniform on 0..L
     static constexpr int T = NWC * MT * 16;        // tokens per stage
@@ -85,10 +100,10 @@ struct Cfg {
     static constexpr int THREADS = NWC * 32;
     static constexpr int NKS = D / 16;             // k-steps of the score MMA = m-tiles of P.V
     static constexpr bool EVEN_ODD = TPR >= 2;     // token order inside a 16-token tile
-    // Resident CTAs per SM: 3 for int4 D = 128 (shared memory: 4 stages of 18
-    // KB each) and for int8, 4 for int4 D = 64 (whose stages are half as
-    // large), 2 for D = 256.
-    static constexpr int MIN_CTAS = (D == 256) ? 2 : ((D == 128 || BITS == 8) ? 3 : 4);
+    // Resident CTAs per SM: 1 for the wide layout (4 stages of 54 KB), 3 for
+    // int4 D = 128 (shared memory: 4 stages of 18 KB each) and for int8, 4 for
+    // int4 D = 64 (whose stages are half as large), 2 for D = 256.
+    static constexpr int MIN_CTAS = WIDE ? 1 : ((D == 256) ? 2 : ((D == 128 || BITS == 8) ? 3 : 4));
     static_assert(BPT <= 128 || BPT == 256, "a token's codes span one 128-byte swizzle row or two blocks");
     static_assert(CODE_BYTES % 1024 == 0, "code tiles must keep the 1024-byte swizzle period");
     static_assert(STAGES * STAGE_BYTES >= NWC * 8 * D * 4, "merge buffer must fit in the stages");
@@ -188,11 +203,12 @@ __device__ __forceinline__ int clamp_len(const DecodeParams& p, const int32_t* s
 //               distributed shared memory and write the output, no reduce.
 constexpr int kOutParts = 0, kOutDirect = 1, kOutCluster = 2;
 
-template <int D, bool PAGED, int BITS, int OUT>
-__global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
+template <int D, bool PAGED, int BITS, int OUT, bool WIDE>
+__global__ void __launch_bounds__(Cfg<D, BITS, WIDE>::THREADS, Cfg<D, BITS, WIDE>::MIN_CTAS)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const DecodeParams p) {
-    using C = Cfg<D, BITS>;
+    using C = Cfg<D, BITS, WIDE>;
+    static_assert(!WIDE || wide_ok(D, BITS, PAGED), "the wide layout is for contiguous int4 head_dim 128");
     constexpr int NG = C::NG;
     __shared__ uint64_t full_bar[C::STAGES];
     __shared__ unsigned int done_cnt[C::STAGES];  // warps finished with the stage, cumulative
@@ -211,7 +227,7 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int32_t* len_src = p.seq_lens + b;
-    if (p.wait_at_start) pdl_wait_primary();
+    if (p.wait_at_start == kWaitAtStart) pdl_wait_primary();
     if (p.order != nullptr) {
         // grids of several waves: the runs in the order the planning kernel
         // wrote (longest first), each run's kv heads consecutive; the entry
@@ -338,8 +354,13 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
                (((static_cast<long long>(b) * p.num_kv_heads + kvh) * p.app.n_new + (r - app_wp)) * D + g * kGroup +
                 app_part * 8);
     };
+    // kWaitAfterRing: the rows, lengths and write positions are not written
+    // by the kernels ahead of this one (the caller's promise), so the first
+    // ring of tiles streams in while those kernels finish; the query and the
+    // new rows, which they may produce, are read only after the wait.
+    const bool ring_first = p.wait_at_start == kWaitAfterRing;
     uint4 app_raw = make_uint4(0, 0, 0, 0);
-    if (static_cast<int>(threadIdx.x >> 3) < app_tasks)
+    if (!ring_first && static_cast<int>(threadIdx.x >> 3) < app_tasks)
         app_raw = __ldcs(reinterpret_cast<const uint4*>(app_src(threadIdx.x >> 3)));
     if (threadIdx.x == 0 && n_tiles > 0) {
         prefetch_tensormap(&tm_k);
@@ -347,6 +368,11 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
         const uint64_t policy = policy_evict_first();
         for (int it = 0; it < min(n_tiles, C::STAGES); ++it)
             if (!tile_uses(it, app_lo, app_hi)) issue_tile(it, policy);
+    }
+    if (ring_first) {
+        pdl_wait_primary();
+        if (static_cast<int>(threadIdx.x >> 3) < app_tasks)
+            app_raw = __ldcs(reinterpret_cast<const uint4*>(app_src(threadIdx.x >> 3)));
     }
 
     // ------------------------------------------------------------ all warps
@@ -932,25 +958,35 @@ __global__ void __launch_bounds__(Cfg<D, BITS>::THREADS, Cfg<D, BITS>::MIN_CTAS)
     }
 }
 
-template <int D, bool PAGED, int BITS, int OUT>
+template <int D, bool PAGED, int BITS, int OUT, bool WIDE>
 cudaError_t set_smem_attr() {
     // per device; setting the attribute twice (two host threads) is harmless
     static std::atomic<bool> done[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, PAGED, BITS, OUT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, BITS>::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, PAGED, BITS, OUT, WIDE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, BITS, WIDE>::SMEM_BYTES);
     if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
     return e;
 }
 
-template <int D, bool PAGED, int BITS, int OUT>
+template <int D, bool PAGED, int BITS, int OUT, bool WIDE>
 cudaError_t launch_mode(cudaLaunchConfig_t& cfg, const DecodeParams& p, const CUtensorMap& tm_k,
                         const CUtensorMap& tm_v) {
-    const cudaError_t e = set_smem_attr<D, PAGED, BITS, OUT>();
+    const cudaError_t e = set_smem_attr<D, PAGED, BITS, OUT, WIDE>();
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, PAGED, BITS, OUT>, tm_k, tm_v, p);
+    cfg.blockDim = dim3(Cfg<D, BITS, WIDE>::THREADS);
+    cfg.dynamicSmemBytes = Cfg<D, BITS, WIDE>::SMEM_BYTES;
+    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, PAGED, BITS, OUT, WIDE>, tm_k, tm_v, p);
+}
+
+template <int D, bool PAGED, int BITS, bool WIDE>
+cudaError_t launch_out(cudaLaunchConfig_t& cfg, const DecodeParams& p, const CUtensorMap& tm_k,
+                       const CUtensorMap& tm_v, int out) {
+    if (out == kOutDirect) return launch_mode<D, PAGED, BITS, kOutDirect, WIDE>(cfg, p, tm_k, tm_v);
+    if (out == kOutCluster) return launch_mode<D, PAGED, BITS, kOutCluster, WIDE>(cfg, p, tm_k, tm_v);
+    return launch_mode<D, PAGED, BITS, kOutParts, WIDE>(cfg, p, tm_k, tm_v);
 }
 
 // p.out set: the kernel writes the output itself, one run per sequence
@@ -958,14 +994,12 @@ cudaError_t launch_mode(cudaLaunchConfig_t& cfg, const DecodeParams& p, const CU
 template <int D, int BITS>
 cudaError_t launch_d(const DecodeParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v, cudaStream_t stream,
                      bool pdl_secondary) {
-    using C = Cfg<D, BITS>;
     const bool paged = p.map.block_table != nullptr;
     const int out = p.out == nullptr ? kOutParts : (p.n_splits == 1 ? kOutDirect : kOutCluster);
     if (out == kOutCluster && p.n_splits > kMaxClusterRuns) return cudaErrorInvalidValue;
+    if (p.wide && !wide_ok(D, BITS, paged)) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_splits, p.num_kv_heads, p.batch);
-    cfg.blockDim = dim3(C::THREADS);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     unsigned int n = 0;
@@ -983,22 +1017,19 @@ cudaError_t launch_d(const DecodeParams& p, const CUtensorMap& tm_k, const CUten
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    if (paged) {
-        if (out == kOutDirect) return launch_mode<D, true, BITS, kOutDirect>(cfg, p, tm_k, tm_v);
-        if (out == kOutCluster) return launch_mode<D, true, BITS, kOutCluster>(cfg, p, tm_k, tm_v);
-        return launch_mode<D, true, BITS, kOutParts>(cfg, p, tm_k, tm_v);
+    if (paged) return launch_out<D, true, BITS, false>(cfg, p, tm_k, tm_v, out);
+    if constexpr (wide_ok(D, BITS, false)) {
+        if (p.wide) return launch_out<D, false, BITS, true>(cfg, p, tm_k, tm_v, out);
     }
-    if (out == kOutDirect) return launch_mode<D, false, BITS, kOutDirect>(cfg, p, tm_k, tm_v);
-    if (out == kOutCluster) return launch_mode<D, false, BITS, kOutCluster>(cfg, p, tm_k, tm_v);
-    return launch_mode<D, false, BITS, kOutParts>(cfg, p, tm_k, tm_v);
+    return launch_out<D, false, BITS, false>(cfg, p, tm_k, tm_v, out);
 }
 
 // Clusters of n CTAs of the cluster-merging instantiation the device holds at
 // once (0 if it cannot place one).
-template <int D, bool PAGED, int BITS>
+template <int D, bool PAGED, int BITS, bool WIDE>
 int max_clusters_d(int n) {
-    using C = Cfg<D, BITS>;
-    if (set_smem_attr<D, PAGED, BITS, kOutCluster>() != cudaSuccess) return 0;
+    using C = Cfg<D, BITS, WIDE>;
+    if (set_smem_attr<D, PAGED, BITS, kOutCluster, WIDE>() != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned int>(n), 1, 1);
     cfg.blockDim = dim3(C::THREADS);
@@ -1011,7 +1042,7 @@ int max_clusters_d(int n) {
     cfg.attrs = a;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, decode_mma_kernel<D, PAGED, BITS, kOutCluster>, &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&clusters, decode_mma_kernel<D, PAGED, BITS, kOutCluster, WIDE>, &cfg) !=
         cudaSuccess) {
         cudaGetLastError();
         return 0;
@@ -1019,12 +1050,13 @@ int max_clusters_d(int n) {
     return clusters;
 }
 
-template <int D, int BITS>
+template <int D, bool PAGED, int BITS, bool WIDE>
 int ctas_per_sm_d() {
-    if (set_smem_attr<D, false, BITS, kOutParts>() != cudaSuccess) return 1;
+    using C = Cfg<D, BITS, WIDE>;
+    if (set_smem_attr<D, PAGED, BITS, kOutParts, WIDE>() != cudaSuccess) return 1;
     int n = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D, false, BITS, kOutParts>, Cfg<D, BITS>::THREADS,
-                                                  Cfg<D, BITS>::SMEM_BYTES);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_mma_kernel<D, PAGED, BITS, kOutParts, WIDE>, C::THREADS,
+                                                  C::SMEM_BYTES);
     return n > 0 ? n : 1;
 }
 
@@ -1048,30 +1080,37 @@ bool mma_supported(int head_dim, int bits) {
     }                                                                             \
     return FALLBACK;
 
-int mma_tile_tokens(int head_dim, int bits) {
+int mma_tile_tokens(int head_dim, int bits, bool wide) {
+    if (wide) return head_dim == 128 && bits == 4 ? Cfg<128, 4, true>::T : 0;
     TQ_DISPATCH(Cfg<64>::T, Cfg<128>::T, Cfg<256>::T, (Cfg<64, 8>::T), (Cfg<128, 8>::T), (Cfg<256, 8>::T), 0)
 }
 
-int mma_smem_bytes(int head_dim, int bits) {
+int mma_smem_bytes(int head_dim, int bits, bool wide) {
+    if (wide) return head_dim == 128 && bits == 4 ? Cfg<128, 4, true>::SMEM_BYTES : 0;
     TQ_DISPATCH(Cfg<64>::SMEM_BYTES, Cfg<128>::SMEM_BYTES, Cfg<256>::SMEM_BYTES, (Cfg<64, 8>::SMEM_BYTES),
                 (Cfg<128, 8>::SMEM_BYTES), (Cfg<256, 8>::SMEM_BYTES), 0)
 }
 
-int mma_max_active_clusters(int head_dim, int bits, bool paged, int n) {
+bool mma_wide_supported(int head_dim, int bits, bool paged) { return wide_ok(head_dim, bits, paged); }
+
+int mma_max_active_clusters(int head_dim, int bits, bool paged, bool wide, int n) {
     if (n < 2 || n > kMaxClusterRuns) return 0;
+    if (wide) return wide_ok(head_dim, bits, paged) ? max_clusters_d<128, false, 4, true>(n) : 0;
     if (paged) {
-        TQ_DISPATCH((max_clusters_d<64, true, 4>(n)), (max_clusters_d<128, true, 4>(n)),
-                    (max_clusters_d<256, true, 4>(n)), (max_clusters_d<64, true, 8>(n)),
-                    (max_clusters_d<128, true, 8>(n)), (max_clusters_d<256, true, 8>(n)), 0)
+        TQ_DISPATCH((max_clusters_d<64, true, 4, false>(n)), (max_clusters_d<128, true, 4, false>(n)),
+                    (max_clusters_d<256, true, 4, false>(n)), (max_clusters_d<64, true, 8, false>(n)),
+                    (max_clusters_d<128, true, 8, false>(n)), (max_clusters_d<256, true, 8, false>(n)), 0)
     }
-    TQ_DISPATCH((max_clusters_d<64, false, 4>(n)), (max_clusters_d<128, false, 4>(n)),
-                (max_clusters_d<256, false, 4>(n)), (max_clusters_d<64, false, 8>(n)),
-                (max_clusters_d<128, false, 8>(n)), (max_clusters_d<256, false, 8>(n)), 0)
+    TQ_DISPATCH((max_clusters_d<64, false, 4, false>(n)), (max_clusters_d<128, false, 4, false>(n)),
+                (max_clusters_d<256, false, 4, false>(n)), (max_clusters_d<64, false, 8, false>(n)),
+                (max_clusters_d<128, false, 8, false>(n)), (max_clusters_d<256, false, 8, false>(n)), 0)
 }
 
-int mma_ctas_per_sm(int head_dim, int bits) {
-    TQ_DISPATCH((ctas_per_sm_d<64, 4>()), (ctas_per_sm_d<128, 4>()), (ctas_per_sm_d<256, 4>()),
-                (ctas_per_sm_d<64, 8>()), (ctas_per_sm_d<128, 8>()), (ctas_per_sm_d<256, 8>()), 1)
+int mma_ctas_per_sm(int head_dim, int bits, bool wide) {
+    if (wide) return head_dim == 128 && bits == 4 ? ctas_per_sm_d<128, false, 4, true>() : 1;
+    TQ_DISPATCH((ctas_per_sm_d<64, false, 4, false>()), (ctas_per_sm_d<128, false, 4, false>()),
+                (ctas_per_sm_d<256, false, 4, false>()), (ctas_per_sm_d<64, false, 8, false>()),
+                (ctas_per_sm_d<128, false, 8, false>()), (ctas_per_sm_d<256, false, 8, false>()), 1)
 }
 
 cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, const CUtensorMap& tm_k, const CUtensorMap& tm_v,

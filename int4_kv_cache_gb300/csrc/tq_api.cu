@@ -192,10 +192,12 @@ tq_status make_rows_map(CUtensorMap* map, const void* base, unsigned long long r
 struct DeviceFacts {
     int sms = 0;
     int mma_ctas[2][3] = {{0, 0, 0}, {0, 0, 0}};  // per code width (4, 8) and head_dim 64 / 128 / 256
+    int wide_ctas = 0;  // the one-CTA-per-SM layout (contiguous int4, head_dim 128)
     int simt_ctas[3] = {0, 0, 0};
     // clusters of n CTAs of the cluster-merging kernel held at once, per code
     // width, head_dim, layout (contiguous, paged) and n
     int clusters[2][3][2][tq::kMaxClusterRuns + 1] = {};
+    int wide_clusters[tq::kMaxClusterRuns + 1] = {};
 };
 
 int dim_index(int d) { return d == 64 ? 0 : (d == 128 ? 1 : 2); }
@@ -216,16 +218,20 @@ tq_status device_facts(DeviceFacts** out) {
             if (e != cudaSuccess) return cuda_status(e);
             const int dims[3] = {64, 128, 256};
             for (int i = 0; i < 3; ++i) {
-                f.mma_ctas[0][i] = tq::mma_ctas_per_sm(dims[i], 4);
-                if (tq::mma_supported(dims[i], 8)) f.mma_ctas[1][i] = tq::mma_ctas_per_sm(dims[i], 8);
+                f.mma_ctas[0][i] = tq::mma_ctas_per_sm(dims[i], 4, false);
+                if (tq::mma_supported(dims[i], 8)) f.mma_ctas[1][i] = tq::mma_ctas_per_sm(dims[i], 8, false);
                 f.simt_ctas[i] = tq::simt_ctas_per_sm(dims[i]);
                 for (int bi = 0; bi < 2; ++bi) {
                     if (!tq::mma_supported(dims[i], bi ? 8 : 4)) continue;
                     for (int pg = 0; pg < 2; ++pg)
                         for (int n = 2; n <= tq::kMaxClusterRuns; ++n)
-                            f.clusters[bi][i][pg][n] = tq::mma_max_active_clusters(dims[i], bi ? 8 : 4, pg != 0, n);
+                            f.clusters[bi][i][pg][n] =
+                                tq::mma_max_active_clusters(dims[i], bi ? 8 : 4, pg != 0, false, n);
                 }
             }
+            f.wide_ctas = tq::mma_ctas_per_sm(128, 4, true);
+            for (int n = 2; n <= tq::kMaxClusterRuns; ++n)
+                f.wide_clusters[n] = tq::mma_max_active_clusters(128, 4, false, true, n);
             cudaGetLastError();  // occupancy queries must leave no pending error
             facts[dev] = f;
             ready[dev].store(true, std::memory_order_release);
@@ -241,6 +247,8 @@ struct Plan {
     bool merged = false;  // the decode merges the runs itself (one run, or one cluster per sequence and kv head)
     int tile_tokens = 0;  // the kernel's pipeline tile
     long long resident = 0;  // CTAs the device holds at once for this kernel
+    bool wide = false;    // one 12-warp CTA per SM (else several 4-warp CTAs)
+    long long waves = 1;  // ceil(CTAs / resident)
 };
 
 int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
@@ -311,6 +319,7 @@ Plan make_plan(int batch, int hkv, int max_seq_len, int chunk, int tile_tokens, 
         for (long long n = 1; n <= tq::kMaxClusterRuns; ++n) consider(n);
     pl.n_splits = static_cast<int>(best);
     pl.merged = best_merged;
+    pl.waves = (heads * best + slots - 1) / slots;
     return pl;
 }
 
@@ -331,12 +340,28 @@ tq_status device_plan(const Store* cache, int max_seq_len, int chunk, tq_impl im
     const int di = dim_index(cache->head_dim);
     const bool simt = impl == TQ_IMPL_SIMT;
     const int per_sm = simt ? f->simt_ctas[di] : f->mma_ctas[cache->bits == 8 ? 1 : 0][di];
-    const int tile = simt ? tq::kSimtTileTokens : tq::mma_tile_tokens(cache->head_dim, cache->bits);
+    const int tile = simt ? tq::kSimtTileTokens : tq::mma_tile_tokens(cache->head_dim, cache->bits, false);
     if (cache->paged && chunk < tile) chunk = tile;  // runs start on tile (hence page-aligned) boundaries
     *pl = make_plan(cache->batch, cache->num_kv_heads, max_seq_len, chunk, tile, f->sms * per_sm, merge && !simt,
                     f->clusters[cache->bits == 8 ? 1 : 0][di][cache->paged ? 1 : 0]);
     pl->tile_tokens = tile;
     pl->resident = static_cast<long long>(f->sms) * per_sm;
+    // The one-CTA-per-SM layout where its plan is one wave over at least 90 %
+    // of the SMs (long single sequences, small batches); grids of several
+    // waves, and thin ones, keep several CTAs per SM.
+    if (!simt && f->wide_ctas > 0 && tq::mma_wide_supported(cache->head_dim, cache->bits, cache->paged)) {
+        const int wtile = tq::mma_tile_tokens(cache->head_dim, cache->bits, true);
+        const long long wres = static_cast<long long>(f->sms) * f->wide_ctas;
+        const Plan w = make_plan(cache->batch, cache->num_kv_heads, max_seq_len, chunk, wtile, static_cast<int>(wres),
+                                 merge, f->wide_clusters);
+        const long long ctas = static_cast<long long>(w.n_splits) * cache->num_kv_heads * cache->batch;
+        if (w.waves == 1 && ctas * 10 >= wres * 9) {
+            *pl = w;
+            pl->tile_tokens = wtile;
+            pl->resident = wres;
+            pl->wide = true;
+        }
+    }
     return TQ_OK;
 }
 
@@ -356,7 +381,7 @@ tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const in
                      int32_t max_seq_len, float attn_scale, const Plan& pl, float* pm, float* plv, float* pa,
                      int32_t* status, tq_impl impl, cudaStream_t stream, const int32_t* dep_write_pos = nullptr,
                      int32_t dep_n_new = 0, const tq::AppendParams* fused_append = nullptr, bool rotate_q = false,
-                     int2* order_buf = nullptr, uint16_t* direct_out = nullptr) {
+                     int2* order_buf = nullptr, uint16_t* direct_out = nullptr, bool ring_first = false) {
     if (pl.n_splits > 65535 || cache->num_kv_heads > 65535 || cache->batch > 65535) return TQ_ERR_SHAPE;
     tq::DecodeParams p{};
     p.q = q;
@@ -399,18 +424,20 @@ tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const in
         return cuda_status(tq::launch_decode_simt(p, cache->head_dim, stream));
     }
     CUtensorMap tm_k, tm_v;
-    const int tile = tq::mma_tile_tokens(cache->head_dim, cache->bits);
+    const int tile = tq::mma_tile_tokens(cache->head_dim, cache->bits, pl.wide);
+    p.wide = pl.wide ? 1 : 0;
     tq_status s = make_code_map(&tm_k, cache->k_codes, cache, tile);
     if (s != TQ_OK) return s;
     s = make_code_map(&tm_v, cache->v_codes, cache, tile);
     if (s != TQ_OK) return s;
     // Phase 1 is always a programmatic dependent of the previous kernel on the
     // stream (typically the last step's reduce, which lets its dependents
-    // launch once it has seen phase 1 complete), so that its launch overlaps
-    // that kernel.  Without an append before it, it waits for that kernel
-    // before any read; after an append it waits only before the tiles that
-    // hold the new rows.
-    p.wait_at_start = dep_write_pos == nullptr ? 1 : 0;
+    // launch as soon as it starts), so that its launch overlaps that kernel.
+    // Without an append before it, it waits for that kernel before any read,
+    // or, with TQ_CACHE_READY, once its first ring of tile loads is issued;
+    // after an append it waits only before the tiles that hold the new rows.
+    p.wait_at_start = dep_write_pos != nullptr ? tq::kWaitForAppend
+                                               : (ring_first ? tq::kWaitAfterRing : tq::kWaitAtStart);
     p.out = direct_out;
     // A batch whose grid spans several waves is dispatched longest run first
     // (the lengths are on the device: a one-CTA kernel writes the order).
@@ -430,6 +457,7 @@ tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const in
         s = cuda_status(tq::launch_order_runs(op, stream));
         if (s != TQ_OK) return s;
         p.order = order_buf;
+        p.wait_at_start = tq::kWaitAtStart;  // the order is the previous kernel's output
     }
     return cuda_status(tq::launch_decode_mma(p, cache->head_dim, tm_k, tm_v, stream, true));
 }
@@ -609,7 +637,13 @@ tq_status run_append(const tq::AppendParams& ap, cudaStream_t st) {
     }
     return cuda_status(tq::launch_quantize_append(ap, st));
 }
-bool valid_step_flags(uint32_t flags) { return valid_rotation(flags & ~TQ_STEP_ADVANCE); }
+bool valid_step_flags(uint32_t flags) {
+    // TQ_CACHE_READY promises that no earlier work still writes the rows or the
+    // lengths, which a step that advances them for the next one contradicts
+    if ((flags & TQ_CACHE_READY) && (flags & TQ_STEP_ADVANCE)) return false;
+    return valid_rotation(flags & ~(TQ_STEP_ADVANCE | TQ_CACHE_READY));
+}
+bool valid_decode_flags(uint32_t flags) { return valid_rotation(flags & ~TQ_CACHE_READY); }
 
 // Decode (optionally preceded by an append of n_new rows) with the workspace
 // laid out as [m][l][acc][rotated q][run order]; the one path behind tq_decode_step*,
@@ -626,7 +660,8 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
     }
     if (!valid_impl(impl) || !valid_step_flags(flags)) return TQ_ERR_UNSUPPORTED;
     const bool advance = (flags & TQ_STEP_ADVANCE) != 0;
-    flags &= ~TQ_STEP_ADVANCE;
+    const bool ring_first = (flags & TQ_CACHE_READY) != 0;
+    flags &= ~(TQ_STEP_ADVANCE | TQ_CACHE_READY);
     if (advance && (write_pos == nullptr || write_pos == seq_lens)) return TQ_ERR_SHAPE;
     const size_t need =
         tq_sdpa_workspace_bytes(cache->batch, hq, cache->num_kv_heads, cache->head_dim, max_seq_len, chunk);
@@ -681,7 +716,7 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
     bool own_out = direct;
     s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, ph1, st,
                    dep ? write_pos : nullptr, dep ? n_new : 0, fused ? &ap : nullptr, rotate_q, order,
-                   own_out ? out : nullptr);
+                   own_out ? out : nullptr, ring_first && !((flags & TQ_ROTATE_K) && !rotate_q));
     if (s != TQ_OK && own_out && pl.n_splits > 1) {
         // a cluster launch the device refused (nothing was queued; e.g. a GPU
         // partition too small to place the cluster): the same runs with
@@ -689,7 +724,8 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
         cudaGetLastError();
         own_out = false;
         s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, ph1, st,
-                       dep ? write_pos : nullptr, dep ? n_new : 0, fused ? &ap : nullptr, rotate_q, order, nullptr);
+                       dep ? write_pos : nullptr, dep ? n_new : 0, fused ? &ap : nullptr, rotate_q, order, nullptr,
+                       ring_first && !((flags & TQ_ROTATE_K) && !rotate_q));
     }
     if (s != TQ_OK) return s;
     tq::ReduceParams r{};
@@ -808,7 +844,7 @@ tq_status tq_sdpa_int4_decode_ex(const tq_kv_cache* raw, const uint16_t* q, int3
     Store st;
     tq_status s = store_of(raw, &st);
     if (s != TQ_OK) return s;
-    if (!valid_rotation(flags)) return TQ_ERR_UNSUPPORTED;
+    if (!valid_decode_flags(flags)) return TQ_ERR_UNSUPPORTED;
     return decode_path(&st, nullptr, nullptr, 0, nullptr, q, hq, seq_lens, max_seq_len, attn_scale, chunk, flags,
                        workspace, workspace_bytes, out, status, TQ_IMPL_AUTO, static_cast<cudaStream_t>(stream));
 }
@@ -927,7 +963,7 @@ tq_status tq_paged_sdpa_int4_decode(const tq_paged_kv_cache* raw, const uint16_t
     Store st;
     tq_status s = store_of(raw, &st);
     if (s != TQ_OK) return s;
-    if (!valid_rotation(flags)) return TQ_ERR_UNSUPPORTED;
+    if (!valid_decode_flags(flags)) return TQ_ERR_UNSUPPORTED;
     return decode_path(&st, nullptr, nullptr, 0, nullptr, q, hq, seq_lens, max_seq_len, attn_scale, chunk, flags,
                        workspace, workspace_bytes, out, status, TQ_IMPL_MMA, static_cast<cudaStream_t>(stream));
 }

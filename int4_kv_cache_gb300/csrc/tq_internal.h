@@ -146,9 +146,15 @@ struct DecodeParams {
     // fp16(rot_scale * H q), rotating each query head as it loads it.
     int32_t rotate_q;
     float rot_scale;
-    // Set when no append kernel precedes it: the launch is a programmatic
-    // dependent of whatever kernel precedes it on the stream, and the kernel
-    // waits for that grid before its first read.
+    // Where the kernel waits for the grid ahead of it on the stream (the
+    // launch is always a programmatic dependent of that grid):
+    //  kWaitAtStart    before its first read;
+    //  kWaitAfterRing  after issuing the first ring of tile loads (caller's
+    //                  TQ_CACHE_READY: nothing ahead writes the rows it reads
+    //                  other than those it appends, nor the lengths), before
+    //                  reading the query and the new rows;
+    //  kWaitForAppend  an append kernel is the grid ahead: only before the
+    //                  tiles holding its rows (dep_write_pos).
     int32_t wait_at_start;
     // Optional dispatch order of the runs (grids of several waves): entry r
     // is {run b * n_splits + split, seq_lens[b] clamped to [0, max_seq_len]}
@@ -159,7 +165,10 @@ struct DecodeParams {
     // One run per sequence (n_splits = 1): the merged state is the output;
     // when set, the kernel writes fp16(acc / l) here instead of the partials.
     uint16_t* out;
+    // The plan's SM layout: one 12-warp CTA per SM (mma_wide_supported only).
+    int32_t wide;
 };
+constexpr int32_t kWaitForAppend = 0, kWaitAtStart = 1, kWaitAfterRing = 2;
 // Most rows per sequence the decode kernel appends itself; longer appends
 // run the append kernel first.
 constexpr int kFusedAppendMaxRows = 16;
@@ -228,14 +237,16 @@ inline float rotation_scale(int dim) { return static_cast<float>(1.0 / std::sqrt
 
 // Tokens per pipeline stage of the tensor-core kernel (tiles are TMA boxes),
 // for a code width of `bits` (4 or 8).
-int mma_tile_tokens(int head_dim, int bits);
-int mma_smem_bytes(int head_dim, int bits);
+// wide: the layout of one 12-warp CTA per SM (contiguous int4 head_dim 128)
+int mma_tile_tokens(int head_dim, int bits, bool wide);
+int mma_smem_bytes(int head_dim, int bits, bool wide);
+bool mma_wide_supported(int head_dim, int bits, bool paged);
 bool mma_supported(int head_dim, int bits);
 // Resident CTAs per SM of the phase-1 kernels (occupancy API).
-int mma_ctas_per_sm(int head_dim, int bits);
+int mma_ctas_per_sm(int head_dim, int bits, bool wide);
 // Clusters of n (2..kMaxClusterRuns) CTAs of the cluster-merging phase-1
 // kernel the device holds at once (occupancy API; 0: none).
-int mma_max_active_clusters(int head_dim, int bits, bool paged, int n);
+int mma_max_active_clusters(int head_dim, int bits, bool paged, bool wide, int n);
 int simt_ctas_per_sm(int head_dim);
 // Largest n_parts the reduce kernel takes.
 constexpr int kMaxReduceParts = 8192;

@@ -52,12 +52,34 @@ def gpu_cache_from_oracle(oc, capacity=None):
     return cache
 
 
+def same_layout(head_dim, bits=4):
+    """Whether contiguous and paged caches of this width decode with the same
+    kernel layout (then their outputs agree bit for bit; the contiguous int4
+    cache at head_dim 128 runs twelve warps per CTA, the paged one four, so
+    there the two sum in different orders and agree within the tolerance)."""
+    return not (head_dim == 128 and bits == 4)
+
+
+def identity_paged(tq, torch, src, page_tokens):
+    """A paged cache holding the rows of the paged cache `src` with each
+    sequence's pages in order (block_table[b, i] = b * per + i): decoding it
+    runs the same kernel over the same rows as `src`, so any difference from
+    `src`'s output is the block-table translation."""
+    B, per = src.block_table.shape
+    ident = tq.PagedKVCache(B, src.num_kv_heads, src.head_dim, page_tokens, B * per, per, bits=src.bits)
+    ident.block_table.copy_(torch.arange(B * per, dtype=torch.int32, device="cuda").reshape(B, per))
+    tab = src.block_table.long()
+    for f in ("k_codes", "v_codes", "k_scale", "k_bias", "v_scale", "v_bias"):
+        getattr(ident, f).copy_(getattr(src, f)[tab.reshape(-1)])
+    return ident
+
+
 def workspace_for(B, Hq, Hkv, D, max_len, chunk=512):
     import torch
 
     import int4_kv_cache_gb300 as tq
 
-    return torch.empty(tq.tq_sdpa_workspace_bytes(B, Hq, Hkv, D, max_len, chunk), dtype=torch.uint8, device="cuda")
+    return tq.workspace(B, Hq, Hkv, D, max_len, chunk)
 
 
 def decode(cache, q, lens, max_len, attn_scale, chunk=512, impl=0, status=None):

@@ -12,8 +12,8 @@ import pytest
 
 import oracle
 from int4_kv_cache_gb300 import synth
-from tests.gpu_helpers import (ATOL, assert_close, decode, gpu_cache_from_fp16, gpu_cache_from_oracle, need_gpu,
-                               workspace_for)
+from tests.gpu_helpers import (ATOL, assert_close, decode, gpu_cache_from_fp16, gpu_cache_from_oracle, identity_paged,
+                               need_gpu, workspace_for)
 
 pytestmark = pytest.mark.gpu
 
@@ -89,8 +89,9 @@ def test_batch_order_and_empty_runs(B, pattern):
 
 
 def test_batch_order_paged_equals_contiguous():
-    """The dispatch order with a paged cache: same output as the contiguous
-    cache bit for bit, and the oracle's within the tolerance."""
+    """The dispatch order with a paged cache: the same output as the same rows
+    with the pages in order bit for bit, the contiguous cache's and the
+    oracle's within the tolerance."""
     torch = need_gpu()
     import int4_kv_cache_gb300 as tq
 
@@ -111,7 +112,9 @@ def test_batch_order_paged_equals_contiguous():
     a = 1 / math.sqrt(D)
     out_c = tq.tq_sdpa_int4_decode(cont, q, lt, S, a, ws).float().cpu().numpy()
     out_p = tq.tq_sdpa_int4_decode(paged, q, lt, S, a, ws).float().cpu().numpy()
-    assert np.array_equal(out_p, out_c)
+    out_i = tq.tq_sdpa_int4_decode(identity_paged(tq, torch, paged, P), q, lt, S, a, ws).float().cpu().numpy()
+    assert np.array_equal(out_p, out_i)
+    assert_close(out_p, out_c, what="ordered paged vs contiguous")
     assert_close(out_c, oracle.attention(x.q, oracle.Cache.from_fp16(x.k, x.v), lens, a), what="ordered paged")
 
 
@@ -375,6 +378,17 @@ def _run_begins(n_splits, max_len, unit=128):
     return [(s * units // n_splits) * unit for s in range(n_splits + 1)]
 
 
+def _plan_runs(n_splits, max_run, max_len):
+    """Run boundaries of a plan: its unit is the kernel's tile (384 tokens in
+    the one-CTA-per-SM layout, 128 otherwise), the one whose longest run is the
+    plan's."""
+    for unit in (384, 128, 64):
+        rb = _run_begins(n_splits, max_len, unit)
+        if max(b - a for a, b in zip(rb, rb[1:])) == max_run:
+            return rb
+    raise AssertionError("no tile size reproduces the plan's runs")
+
+
 @pytest.mark.parametrize("n_new", [1, 16, 17, 40])
 def test_fused_step_rows_across_run_boundaries(n_new):
     """Up to 16 new rows per sequence are quantized by the decode kernel (each
@@ -389,8 +403,7 @@ def test_fused_step_rows_across_run_boundaries(n_new):
     x = synth.decode_inputs(71, B, Hq, Hkv, D, S, outliers=True)
     c1 = gpu_cache_from_fp16(x.k, x.v)
     ns, run = tq.tq_sdpa_plan(c1, Hq, S)
-    rb = _run_begins(ns, S)
-    assert max(b - a for a, b in zip(rb, rb[1:])) == run  # the boundaries the kernel uses
+    rb = _plan_runs(ns, run, S)  # the boundaries the kernel uses
     pos = np.array([0, rb[ns // 2] - n_new // 2, S - n_new], np.int32)
     kn, vn = synth.append_tokens(71, n_new, B, Hkv, D, n_new, outliers=x.outlier_channels)
     lens = pos + n_new

@@ -1,7 +1,8 @@
 """GPU paged int4 cache (block table over a page pool) against the contiguous
-cache and the oracle: same bytes in the pages, bit-identical decode, fused and
-separate appends, a bad block-table entry, and a CUDA-graph decode loop whose
-lengths advance on the device."""
+cache and the oracle: same bytes in the pages, a decode bit-identical to the
+same rows with the pages in order (and to the contiguous cache wherever both
+run the same kernel layout), fused and separate appends, a bad block-table
+entry, and a CUDA-graph decode loop whose lengths advance on the device."""
 import math
 
 import numpy as np
@@ -9,7 +10,8 @@ import pytest
 
 import oracle
 from int4_kv_cache_gb300 import synth
-from tests.gpu_helpers import assert_close, gpu_cache_from_fp16, need_gpu, workspace_for
+from tests.gpu_helpers import (assert_close, gpu_cache_from_fp16, identity_paged, need_gpu, same_layout,
+                               workspace_for)
 
 pytestmark = pytest.mark.gpu
 
@@ -57,7 +59,12 @@ def test_paged_equals_contiguous_and_oracle(D, Hq, Hkv, P):
     a = 1 / math.sqrt(D)
     out_c = tq.tq_sdpa_int4_decode(cont, q, lt, S, a, ws).float().cpu().numpy()
     out_p = tq.tq_sdpa_int4_decode(paged, q, lt, S, a, ws).float().cpu().numpy()
-    assert np.array_equal(out_p, out_c)
+    out_i = tq.tq_sdpa_int4_decode(identity_paged(tq, torch, paged, P), q, lt, S, a, ws).float().cpu().numpy()
+    assert np.array_equal(out_p, out_i)
+    if same_layout(D):
+        assert np.array_equal(out_p, out_c)
+    else:
+        assert_close(out_p, out_c, what="paged vs contiguous")
     assert_close(out_p, oracle.attention(x.q, oracle.Cache.from_fp16(x.k, x.v), lens, a), what="paged decode")
 
 
@@ -81,7 +88,10 @@ def test_paged_step_equals_contiguous_step(n_new):
     ws = workspace_for(B, Hq, Hkv, D, S)
     o_c = tq.tq_decode_step(cont, knt, vnt, wp, q, lt, S, 0.088, ws).float().cpu().numpy()
     o_p = tq.tq_decode_step(paged, knt, vnt, wp, q, lt, S, 0.088, ws).float().cpu().numpy()
-    assert np.array_equal(o_p, o_c)
+    # the rows now in the pool, pages in order: the same decode bit for bit
+    o_i = tq.tq_sdpa_int4_decode(identity_paged(tq, torch, paged, P), q, lt, S, 0.088, ws).float().cpu().numpy()
+    assert np.array_equal(o_p, o_i)
+    assert_close(o_p, o_c, what="paged step vs contiguous step")
     for got, want in zip(_gather(paged, perm, S), (cont.k_codes, cont.k_scale, cont.k_bias, cont.v_codes,
                                                    cont.v_scale, cont.v_bias)):
         assert np.array_equal(got.view(np.uint8), want[:, :, :S].cpu().numpy().view(np.uint8))
