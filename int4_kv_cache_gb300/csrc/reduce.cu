@@ -4,10 +4,13 @@
 //
 // Per (b, h):  M = max_c m_c over parts with l_c > 0,  w_c = e^{m_c - M},
 //              out = sum_c w_c acc_c / sum_c w_c l_c   (fp16, RNE; 0 if empty)
-// One CTA per (b, h); the weights go through shared memory once, then the
-// warps split the parts between them.  Launched as a programmatic dependent
-// of phase 1, it waits for phase 1's memory before the first read.
+// One CTA per (b, h): reduce_fast_kernel for up to 32 parts (one round trip,
+// no barriers), reduce_kernel otherwise and for the output rotation.
+// Launched as a programmatic dependent of phase 1, each waits for phase 1's
+// memory before the first read.
 #include <math.h>
+
+#include <atomic>
 
 #include "tq_device.cuh"
 #include "tq_hadamard.cuh"
@@ -146,6 +149,76 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReducePara
     }
 }
 
+// Up to 32 parts (the plans of one wave; 19 at 128K in the one-CTA-per-SM
+// layout): one thread per head_dim element loads its element of every part
+// and each warp the parts' m and l at once, one round trip to L2, then
+//   M = warp max over lanes (lane c holds part c),  w_c = expf(m_c - M),
+//   L = xor-tree warp sum of fmaf(w_c, l_c, 0),
+//   t = sum over parts in order of fmaf(w_c, acc_c, 0) (w_c = 0 skipped),
+// no shared memory and no CTA barrier.  M, w and L are reduce_kernel's for
+// any such part count (its block reduction sees the same 32 values, the other
+// warps' zeros added exactly), and t its too up to 8 parts (one part per warp
+// there), so the two give the same bits up to 8 parts, as does the cluster
+// merge in phase 1.  (reduce_kernel: 2.2 us after its release for 19 parts,
+// five barriers and dependent loads.)
+//   Its CTAs are launched while phase 1 runs and take SMs as phase-1 CTAs
+// leave; small as they are, the first SMs to free up would take seven each,
+// and their loads queue there (128K step 32.8 us, against 31.0 us spread).
+// Each CTA therefore reserves kFastSmemPad bytes of shared memory it does not
+// use, so that at most two share an SM.
+constexpr int kFastParts = 32;
+constexpr int kFastSmemPad = 100 * 1024;
+
+template <int D>
+__global__ void __launch_bounds__(D < 128 ? D : 128) reduce_fast_kernel(const ReduceParams p) {
+    constexpr int TH = D < 128 ? D : 128;
+    constexpr int DPT = D / TH;  // head_dim elements per thread
+    pdl_wait_primary();
+    // phase 1 is complete: an eager next step's phase 1 may launch now (it
+    // waits for this grid before its first read)
+    pdl_launch_dependents();
+    const long long bh = blockIdx.x;
+    if (p.adv_n != 0 && threadIdx.x == 0 && bh % p.num_q_heads == 0) {  // phase 1 has read the lengths
+        const long long b = bh / p.num_q_heads;
+        p.adv_seq_lens[b] += p.adv_n;
+        p.adv_write_pos[b] += p.adv_n;
+    }
+    const int n = p.n_parts;
+    const int lane = threadIdx.x & 31;
+    const float* pa = p.part_acc + bh * n * D + threadIdx.x;
+    float a[kFastParts][DPT];
+#pragma unroll
+    for (int c = 0; c < kFastParts; ++c) {
+#pragma unroll
+        for (int j = 0; j < DPT; ++j) a[c][j] = c < n ? __ldcg(pa + c * D + j * TH) : 0.0f;
+    }
+    const float l = lane < n ? __ldcg(p.part_l + bh * n + lane) : 0.0f;
+    const float mv = lane < n ? __ldcg(p.part_m + bh * n + lane) : -INFINITY;
+    const float m = l > 0.0f ? mv : -INFINITY;  // empty parts carry no weight
+    float M = m;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float w = m == -INFINITY ? 0.0f : expf(m - M);
+    float L = fmaf(w, l, 0.0f);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    float t[DPT];
+#pragma unroll
+    for (int j = 0; j < DPT; ++j) t[j] = 0.0f;
+#pragma unroll
+    for (int c = 0; c < kFastParts; ++c) {
+        const float wc = __shfl_sync(0xffffffffu, w, c);
+        if (c < n && wc != 0.0f) {
+#pragma unroll
+            for (int j = 0; j < DPT; ++j) t[j] += fmaf(wc, a[c][j], 0.0f);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < DPT; ++j)
+        p.out[bh * D + threadIdx.x + j * TH] =
+            __half_as_ushort(__float2half_rn(L > 0.0f ? __fdiv_rn(t[j], L) : 0.0f));
+}
+
 // TQ_STEP_ADVANCE after a step whose append ran as its own kernel: a plain
 // launch after the reduce, so stream order covers the append as well.
 __global__ void advance_lengths_kernel(int32_t* seq_lens, int32_t* write_pos, int batch, int n) {
@@ -163,6 +236,24 @@ cudaError_t launch_advance(int32_t* seq_lens, int32_t* write_pos, int batch, int
     return cudaGetLastError();
 }
 
+// The fast reduce's shared-memory reservation, once per device.
+cudaError_t fast_attrs() {
+    static std::atomic<bool> done[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const bool cache = dev >= 0 && dev < 64;
+    if (cache && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(reduce_fast_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFastSmemPad);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(reduce_fast_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFastSmemPad);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(reduce_fast_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFastSmemPad);
+    if (e == cudaSuccess && cache) done[dev].store(true, std::memory_order_release);
+    return e;
+}
+
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl_secondary) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.batch) * p.num_q_heads);
@@ -174,6 +265,18 @@ cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl_s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_secondary ? 1 : 0;
+    if (!p.rotate_out && p.n_parts <= kFastParts) {
+        cfg.blockDim = dim3(p.head_dim < 128 ? p.head_dim : 128);
+        cfg.dynamicSmemBytes = kFastSmemPad;
+        const cudaError_t e = fast_attrs();
+        if (e != cudaSuccess) return e;
+        switch (p.head_dim) {
+            case 64: return cudaLaunchKernelEx(&cfg, reduce_fast_kernel<64>, p);
+            case 128: return cudaLaunchKernelEx(&cfg, reduce_fast_kernel<128>, p);
+            case 256: return cudaLaunchKernelEx(&cfg, reduce_fast_kernel<256>, p);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (p.head_dim) {
         case 64: return cudaLaunchKernelEx(&cfg, reduce_kernel<64>, p);
         case 128: return cudaLaunchKernelEx(&cfg, reduce_kernel<128>, p);
