@@ -45,7 +45,6 @@ CHUNK = 512
 ATTN = 1.0 / math.sqrt(128.0)
 SEED = 2
 N_LAYERS_ROTATED = 8
-FULL_MODEL_LAYERS = 80
 # The Llama page's fused-kernel latency at 128K (Apple M-series GPU, Metal):
 # 9.9 ms for the same single-layer shape -- another machine, context only.
 PAGES_128K_MS = 9.9
@@ -609,8 +608,10 @@ def run_dequant_baseline(args, tq, torch, dev, caches, qs, peak):
 def run_full_model(args, tq, synth, torch, dev, peak):
     """80 layers x Llama-70B attention shape at 128K: one decode step = 80 x
     (append + decode), timed end to end; also the 128K prefill quantize GB/s."""
-    caches, qs, chans, prefill_ms = make_layer_caches(tq, synth, torch, dev, FULL_MODEL_LAYERS, 50000)
-    k_new, v_new = [torch.from_numpy(a).to(dev) for a in synth.append_tokens(SEED, 1, B, HKV, D, 1, outliers=chans[0])]
+    caches, qs, chans, prefill_ms = make_layer_caches(tq, synth, torch, dev, synth.FULL_MODEL_LAYERS,
+                                                      synth.FULL_MODEL_SEED0)
+    k_new, v_new = [torch.from_numpy(a).to(dev)
+                    for a in synth.append_tokens(synth.FULL_MODEL_SEED0, 0, B, HKV, D, 1, outliers=chans[0])]
     write_pos = torch.full((B,), S - 1, dtype=torch.int32, device=dev)
     seq_lens = torch.full((B,), S, dtype=torch.int32, device=dev)
     ws = tq.workspace(B, HQ, HKV, D, S, CHUNK, device=dev)
@@ -621,10 +622,10 @@ def run_full_model(args, tq, synth, torch, dev, peak):
             tq.tq_decode_step(c, k_new, v_new, write_pos, q, seq_lens, S, ATTN, ws, out=out, chunk=CHUNK)
 
     us = time_graph(torch, model_step, max(5, args.steps // 5))
-    nbytes = FULL_MODEL_LAYERS * step_bytes(S)
+    nbytes = synth.FULL_MODEL_LAYERS * step_bytes(S)
     gbs = nbytes / (us * 1e-6) / 1e9
     res = {"ms_per_step": round(us / 1e3, 4), "GB_per_s": round(gbs, 1), "frac": round(gbs / peak, 4),
-           "layers": FULL_MODEL_LAYERS, "cache_bytes_resident": FULL_MODEL_LAYERS * cache_bytes(S),
+           "layers": synth.FULL_MODEL_LAYERS, "cache_bytes_resident": synth.FULL_MODEL_LAYERS * cache_bytes(S),
            "prefill_quantize_128k_80l": prefill_summary(prefill_ms, peak)}
     del caches
     torch.cuda.empty_cache()

@@ -170,6 +170,20 @@ const char* tq_status_string(tq_status s);
 /* The cudaError_t of the most recent TQ_ERR_CUDA on the calling host thread. */
 int32_t tq_last_cuda_error(void);
 
+/* Diagnostic of the device-side failure path (no counterpart on the pages):
+ * the decode kernels wait on their pipeline stages with a time limit and,
+ * when a wait runs out, OR TQ_DEV_TIMEOUT into the status word and leave.
+ * This call runs that wait on one CTA: it copies 1,024 bytes from `src`
+ * (device, 16-byte aligned) into shared memory and waits for the copy, then
+ * waits on a barrier that nothing arrives at, giving up after `limit_us`
+ * microseconds (1..100000).  It then ORs TQ_DEV_TIMEOUT into *status and
+ * writes to *copied the sum (mod 2^32) of the 256 32-bit words it copied
+ * (0xFFFFFFFF if even the copy had not landed).  Nothing is in flight when
+ * the kernel ends.  Null pointers: TQ_ERR_NULL; misaligned src:
+ * TQ_ERR_ALIGN; limit out of range: TQ_ERR_SHAPE. */
+tq_status tq_wait_timeout_selftest(const void* src, int32_t* status, uint32_t limit_us,
+                                   uint32_t* copied, void* stream);
+
 /* Bytes of the six cache arrays together, each rounded up to 256 bytes, as
  * laid out by tq_kv_cache_carve.  0 for invalid sizes.  Host-only. */
 size_t tq_kv_cache_bytes(int32_t batch, int32_t num_kv_heads, int32_t head_dim,

@@ -93,6 +93,7 @@ def lib() -> ctypes.CDLL:
             "tq_abi_version": ([], i32),
             "tq_status_string": ([i32], ctypes.c_char_p),
             "tq_last_cuda_error": ([], i32),
+            "tq_wait_timeout_selftest": ([P, P, u32, P, P], i32),
             "tq_kv_cache_bytes": ([i32] * 5, sz),
             "tq_kv_cache_carve": ([C, P, i32, i32, i32, i32, i32], i32),
             "tq_quantize_kv_append": ([C, P, P, i32, P, P, P], i32),
@@ -160,6 +161,19 @@ def _need(t: torch.Tensor, dtype, name: str) -> None:
 # ------------------------------------------------------------------ host-only
 def tq_abi_version() -> int:
     return int(lib().tq_abi_version())
+
+
+def tq_wait_timeout_selftest(src: torch.Tensor, status: torch.Tensor, limit_us: int, copied: torch.Tensor,
+                             stream=None) -> None:
+    """The bounded-wait diagnostic: a 1 KB copy from ``src`` (uint8, >= 1024
+    bytes), then a wait nothing ends, given up after ``limit_us``."""
+    _need(src, torch.uint8, "src")
+    _need(status, torch.int32, "status")
+    _need(copied, torch.int32, "copied")
+    if src.numel() < 1024:
+        raise ValueError("src must hold at least 1024 bytes")
+    _check("tq_wait_timeout_selftest", lib().tq_wait_timeout_selftest(_ptr(src), _ptr(status), int(limit_us),
+                                                                      _ptr(copied), _stream(stream)))
 
 
 def tq_status_string(status: int) -> str:

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libtq.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["tq_api.cu", "quantize.cu", "decode_mma.cu", "decode_simt.cu", "reduce.cu", "decode_noalloc.cu", "dequant.cu", "rotate.cu", "order.cu"]
+SOURCES = ["tq_api.cu", "quantize.cu", "decode_mma.cu", "decode_simt.cu", "reduce.cu", "decode_noalloc.cu", "dequant.cu", "rotate.cu", "order.cu", "selftest.cu"]
 
 
 def nvcc() -> str:

@@ -534,6 +534,15 @@ const char* tq_status_string(tq_status s) {
 
 int32_t tq_last_cuda_error(void) { return g_last_cuda_error; }
 
+tq_status tq_wait_timeout_selftest(const void* src, int32_t* status, uint32_t limit_us, uint32_t* copied,
+                                   void* stream) {
+    if (src == nullptr || status == nullptr || copied == nullptr) return TQ_ERR_NULL;
+    if (!aligned16(src)) return TQ_ERR_ALIGN;
+    if (limit_us < 1 || limit_us > 100000) return TQ_ERR_SHAPE;
+    return cuda_status(tq::launch_wait_timeout_selftest(src, status, static_cast<uint64_t>(limit_us) * 1000ull,
+                                                        copied, static_cast<cudaStream_t>(stream)));
+}
+
 size_t tq_kv_cache_bytes_ex(int32_t batch, int32_t hkv, int32_t head_dim, int32_t group_size, int32_t bits,
                             int32_t capacity) {
     if (batch < 1 || hkv < 1 || capacity < 1 || head_dim < 2 || head_dim % 2 != 0 || group_size < 1 ||

@@ -228,6 +228,10 @@ cudaError_t launch_quantize_append_primary(const AppendParams& p, cudaStream_t s
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl_secondary);
 cudaError_t launch_order_runs(const OrderParams& p, cudaStream_t stream);
 cudaError_t launch_advance(int32_t* seq_lens, int32_t* write_pos, int batch, int n, cudaStream_t stream);
+// The bounded-wait diagnostic (selftest.cu): *copied = sum of the 32-bit words
+// of the 1 KB copied from src (0xFFFFFFFF if the copy did not land in time).
+cudaError_t launch_wait_timeout_selftest(const void* src, int32_t* status, uint64_t limit_ns, uint32_t* copied,
+                                         cudaStream_t stream);
 cudaError_t launch_dequant(const DequantParams& p, int sm_count, cudaStream_t stream);
 // out[r] = fp16(H x[r]) for rows of `dim` fp16 values (dim 64 / 128 / 256); out may be x.
 cudaError_t launch_rotate_rows(const uint16_t* x, long long rows, int dim, uint16_t* out, float scale,

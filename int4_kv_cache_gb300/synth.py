@@ -38,6 +38,9 @@ __all__ = [
     "append_tokens",
     "WORKLOADS",
     "Workload",
+    "FULL_MODEL_LAYERS",
+    "FULL_MODEL_SEED0",
+    "full_model_layer",
 ]
 
 
@@ -164,6 +167,20 @@ WORKLOADS = {
     # ragged batch of 32 sequences, lengths uniform in [1K, 32K]
     "ragged32": Workload("ragged32", 4, 32, 64, 8, 128, 32768, _LLAMA_SCALE, outliers=True),
 }
+
+# The full model at 128K: FULL_MODEL_LAYERS caches of the Llama-70B layer,
+# layer l drawn by torch_decode_inputs with seed FULL_MODEL_SEED0 + l; one
+# decode step appends the same new token (append_tokens(FULL_MODEL_SEED0, 0),
+# outlier channels of layer 0) at row 131071 of every layer, then decodes it.
+FULL_MODEL_LAYERS = 80
+FULL_MODEL_SEED0 = 5
+
+
+def full_model_layer(layer: int, device="cuda"):
+    """(q, k, v, outlier_channels) of one layer of the full-model workload."""
+    w = WORKLOADS["llama70b_128k"]
+    return torch_decode_inputs(FULL_MODEL_SEED0 + layer, w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                               w.seq_len, outliers=True, device=device)
 
 
 def torch_decode_inputs(seed: int, batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,

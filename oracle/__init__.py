@@ -49,6 +49,8 @@ def lib() -> ctypes.CDLL:
                                     P, i64, P]
         L.tqo_attention_partials.argtypes = [P, i32, i32, i32, i32, i32, i64, P, P, P, P, P, P,
                                              P, f64, i32, i32, P, P, P]
+        L.tqo_attention_partials_b.argtypes = [P, i32, i32, i32, i32, i32, i64, P, P, P, P, P, P,
+                                               P, f64, i32, i32, i32, P, P, P]
         L.tqo_merge_partials.argtypes = [P, P, P, i32, i32, i32, i32, P]
         L.tqo_num_threads.restype = i32
         _lib = L
@@ -213,11 +215,10 @@ def attention_partials(q: np.ndarray, cache: Cache, lens: np.ndarray, attn_scale
     m = np.empty((B, Hq, n_chunks))
     l = np.empty((B, Hq, n_chunks))
     acc = np.empty((B, Hq, n_chunks, D))
-    assert cache.bits == 4, "per-chunk partials are kept for the int4 cache"
     a = cache._args()
-    lib().tqo_attention_partials(_ptr(q), B, Hq, cache.Hkv, D, cache.group, cache.cap, *a,
-                                 _ptr(lens), float(attn_scale), chunk, n_chunks, _ptr(m),
-                                 _ptr(l), _ptr(acc))
+    lib().tqo_attention_partials_b(_ptr(q), B, Hq, cache.Hkv, D, cache.group, cache.cap, *a,
+                                   _ptr(lens), float(attn_scale), chunk, n_chunks, int(cache.bits), _ptr(m),
+                                   _ptr(l), _ptr(acc))
     return m, l, acc
 
 

@@ -376,14 +376,14 @@ void tqo_attention(const uint16_t* q, int B, int Hq, int Hkv, int D, int group,
 /* phase 2 reduces the partials with a log-sum-exp merge.                     */
 /* ------------------------------------------------------------------------ */
 
-void tqo_attention_partials(const uint16_t* q, int B, int Hq, int Hkv, int D,
-                            int group, int64_t cap, const uint8_t* kc,
-                            const uint16_t* ks, const uint16_t* kb,
-                            const uint8_t* vc, const uint16_t* vs,
-                            const uint16_t* vb, const int32_t* lens,
-                            double attn_scale, int chunk, int n_chunks,
-                            double* part_m, double* part_l, double* part_acc) {
-    cache_view c = {B, Hq, Hkv, D, group, cap, kc, vc, ks, kb, vs, vb, 4};
+void tqo_attention_partials_b(const uint16_t* q, int B, int Hq, int Hkv, int D,
+                              int group, int64_t cap, const uint8_t* kc,
+                              const uint16_t* ks, const uint16_t* kb,
+                              const uint8_t* vc, const uint16_t* vs,
+                              const uint16_t* vb, const int32_t* lens,
+                              double attn_scale, int chunk, int n_chunks, int bits,
+                              double* part_m, double* part_l, double* part_acc) {
+    cache_view c = {B, Hq, Hkv, D, group, cap, kc, vc, ks, kb, vs, vb, bits};
     int G = Hq / Hkv;
 #ifdef _OPENMP
 #pragma omp parallel for schedule(dynamic, 1)
@@ -412,6 +412,17 @@ void tqo_attention_partials(const uint16_t* q, int B, int Hq, int Hkv, int D,
         }
         free(qd);
     }
+}
+
+void tqo_attention_partials(const uint16_t* q, int B, int Hq, int Hkv, int D,
+                            int group, int64_t cap, const uint8_t* kc,
+                            const uint16_t* ks, const uint16_t* kb,
+                            const uint8_t* vc, const uint16_t* vs,
+                            const uint16_t* vb, const int32_t* lens,
+                            double attn_scale, int chunk, int n_chunks,
+                            double* part_m, double* part_l, double* part_acc) {
+    tqo_attention_partials_b(q, B, Hq, Hkv, D, group, cap, kc, ks, kb, vc, vs, vb, lens, attn_scale, chunk,
+                             n_chunks, 4, part_m, part_l, part_acc);
 }
 
 void tqo_merge_partials(const double* part_m, const double* part_l,

@@ -128,6 +128,15 @@ void tqo_attention_partials(const uint16_t* q, int B, int Hq, int Hkv, int D,
                             const uint16_t* vb, const int32_t* lens,
                             double attn_scale, int chunk, int n_chunks,
                             double* part_m, double* part_l, double* part_acc);
+/* The same for a cache of `bits`-bit codes (4 or 8: "Running and Evaluating
+ * TurboQuant optimized Gemma 4", driver flags --kv-bits {4,8}). */
+void tqo_attention_partials_b(const uint16_t* q, int B, int Hq, int Hkv, int D,
+                              int group, int64_t cap, const uint8_t* kc,
+                              const uint16_t* ks, const uint16_t* kb,
+                              const uint8_t* vc, const uint16_t* vs,
+                              const uint16_t* vb, const int32_t* lens,
+                              double attn_scale, int chunk, int n_chunks, int bits,
+                              double* part_m, double* part_l, double* part_acc);
 
 /* Split-K phase 2: log-sum-exp merge of n_chunks partials per (b, h).
  * out[B][Hq][D] = sum_c e^{m_c - M} acc_c / sum_c e^{m_c - M} l_c,

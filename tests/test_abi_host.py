@@ -277,3 +277,13 @@ def test_cache_ready_flag_is_accepted_and_excludes_advance(L):
     assert s(*args(0x300, 1 << 30)) == 6
     assert s(*args(0x400, 1 << 30)) == 6   # unknown flag bit
     assert tq.TQ_CACHE_READY == 0x200
+
+
+def test_wait_timeout_selftest_argument_errors(L):
+    f = L.tq_wait_timeout_selftest
+    assert f(None, 0x1000, 100, 0x2000, None) == 1
+    assert f(0x1000, None, 100, 0x2000, None) == 1
+    assert f(0x1000, 0x2000, 100, None, None) == 1
+    assert f(0x1008, 0x2000, 100, 0x3000, None) == 7   # src not 16-byte aligned
+    assert f(0x1000, 0x2000, 0, 0x3000, None) == 2     # limit out of range
+    assert f(0x1000, 0x2000, 100001, 0x3000, None) == 2

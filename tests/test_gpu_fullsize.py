@@ -1,0 +1,159 @@
+"""Full-size parity for exactly what the benchmark times.
+
+* The decode step at the Llama-3.1-70B single-layer shape ("turboquant-
+  llama3.170B" README, kernel latency table: 64 q / 8 kv heads, head_dim 128)
+  at 64K and 128K tokens, called as the benchmark calls it: tq_decode_step
+  appending the new token at row S - 1 and decoding over S rows, eagerly and
+  replayed from a CUDA graph.  Every query head against the oracle, and the
+  appended row bit for bit.
+* The 80-layer model at 128K (the same README, memory table: 80 layers x 8
+  kv heads): the 80 caches built as the benchmark builds them and one model
+  step of 80 tq_decode_step calls.  Layers 0, 79 and one seeded layer are
+  compared in full (every code, scale and bias bit for bit, every head of the
+  output within the bar); every layer has seeded rows and its appended row
+  compared bit for bit.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from int4_kv_cache_gb300 import synth
+from tests.gpu_helpers import assert_close, cache_arrays, need_gpu, workspace_for
+
+pytestmark = pytest.mark.gpu
+
+B, HQ, HKV, D = 1, 64, 8, 128
+ATTN = 1.0 / math.sqrt(128.0)
+STEP_SEED = 2  # the benchmark's first layer cache and its new token
+
+
+def _host(t):
+    return np.ascontiguousarray(t.cpu().numpy())
+
+
+def _with_row(x, row, new):
+    """fp16 host copy of x [B, Hkv, S, D] with row `row` replaced by new [B, Hkv, 1, D]."""
+    y = x.copy()
+    y[:, :, row] = new[:, :, 0]
+    return y
+
+
+@pytest.mark.parametrize("S", [65536, 131072])
+def test_timed_step_all_heads(S):
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    q, k, v, chans = synth.torch_decode_inputs(STEP_SEED, B, HQ, HKV, D, S, outliers=True)
+    cache = tq.KVCache(B, HKV, D, S)
+    tq.tq_quantize_kv_append(cache, k, v, torch.zeros(B, dtype=torch.int32, device="cuda"))
+    kn, vn = synth.append_tokens(STEP_SEED, 0, B, HKV, D, 1, outliers=chans)
+    knt, vnt = torch.from_numpy(kn).cuda(), torch.from_numpy(vn).cuda()
+    wp = torch.full((B,), S - 1, dtype=torch.int32, device="cuda")
+    lens = torch.full((B,), S, dtype=torch.int32, device="cuda")
+    ws = workspace_for(B, HQ, HKV, D, S)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty((B, HQ, D), dtype=torch.float16, device="cuda")
+
+    def step():
+        tq.tq_decode_step(cache, knt, vnt, wp, q, lens, S, ATTN, ws, out=out, chunk=512, status=st)
+
+    step()
+    torch.cuda.synchronize()
+    eager = _host(out).copy()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.array_equal(_host(out).view(np.uint16), eager.view(np.uint16))
+    # the appended row, bit for bit
+    for new, codes, scale, bias in ((kn, cache.k_codes, cache.k_scale, cache.k_bias),
+                                    (vn, cache.v_codes, cache.v_scale, cache.v_bias)):
+        wc, ws_, wb = oracle.quantize_rows(new)
+        assert np.array_equal(_host(codes[:, :, S - 1:S]), wc)
+        assert np.array_equal(_host(scale[:, :, S - 1:S]).view(np.uint16), ws_)
+        assert np.array_equal(_host(bias[:, :, S - 1:S]).view(np.uint16), wb)
+    # every head against the oracle over the cache that now holds the new row
+    kk, vv = _with_row(_host(k), S - 1, kn), _with_row(_host(v), S - 1, vn)
+    del k, v
+    ref = oracle.attention(_host(q), oracle.Cache.from_fp16(kk, vv), np.array([S], np.int32), ATTN)
+    assert_close(eager.astype(np.float64), ref, what=f"timed step S={S}")
+
+
+def test_full_model_80_layers():
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    L, S = synth.FULL_MODEL_LAYERS, synth.WORKLOADS["llama70b_128k"].seq_len
+    check = sorted({0, L - 1, int(np.random.default_rng(80).integers(1, L - 1))})
+    rng = np.random.default_rng(81)
+    samples = {}  # layer -> (kv heads, tokens, fp16 K rows, fp16 V rows)
+    full = {}     # checked layer -> host (q, k, v)
+    caches, qs = [], []
+    zero = torch.zeros(B, dtype=torch.int32, device="cuda")
+    chans0 = None
+    for layer in range(L):
+        q, k, v, chans = synth.full_model_layer(layer)
+        if layer == 0:
+            chans0 = chans
+        c = tq.KVCache(B, HKV, D, S)
+        tq.tq_quantize_kv_append(c, k, v, zero)
+        h = rng.integers(0, HKV, 16)
+        t = rng.integers(0, S - 1, 16)
+        hi, ti = torch.from_numpy(h).cuda(), torch.from_numpy(t).cuda()
+        samples[layer] = (h, t, _host(k[0, hi, ti]), _host(v[0, hi, ti]))
+        if layer in check:
+            full[layer] = (_host(q), _host(k), _host(v))
+        caches.append(c)
+        qs.append(q)
+        del k, v
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    kn, vn = synth.append_tokens(synth.FULL_MODEL_SEED0, 0, B, HKV, D, 1, outliers=chans0)
+    knt, vnt = torch.from_numpy(kn).cuda(), torch.from_numpy(vn).cuda()
+    wp = torch.full((B,), S - 1, dtype=torch.int32, device="cuda")
+    lens = torch.full((B,), S, dtype=torch.int32, device="cuda")
+    ws = workspace_for(B, HQ, HKV, D, S)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = [torch.empty((B, HQ, D), dtype=torch.float16, device="cuda") for _ in range(L)]
+
+    def model_step():
+        for layer in range(L):
+            tq.tq_decode_step(caches[layer], knt, vnt, wp, qs[layer], lens, S, ATTN, ws, out=outs[layer], chunk=512,
+                              status=st)
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        model_step()
+    g.replay()
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    # every layer: seeded rows and the appended row, bit for bit
+    new_k = oracle.quantize_rows(kn)
+    new_v = oracle.quantize_rows(vn)
+    for layer in range(L):
+        c = caches[layer]
+        h, t, kr, vr = samples[layer]
+        for rows, want_new, codes, scale, bias in ((kr, new_k, c.k_codes, c.k_scale, c.k_bias),
+                                                   (vr, new_v, c.v_codes, c.v_scale, c.v_bias)):
+            wc, wsc, wb = oracle.quantize_rows(rows)
+            idx_h, idx_t = torch.from_numpy(h).cuda(), torch.from_numpy(t).cuda()
+            assert np.array_equal(_host(codes[0, idx_h, idx_t]), wc), layer
+            assert np.array_equal(_host(scale[0, idx_h, idx_t]).view(np.uint16), wsc), layer
+            assert np.array_equal(_host(bias[0, idx_h, idx_t]).view(np.uint16), wb), layer
+            assert np.array_equal(_host(codes[:, :, S - 1:S]), want_new[0]), layer
+            assert np.array_equal(_host(scale[:, :, S - 1:S]).view(np.uint16), want_new[1]), layer
+            assert np.array_equal(_host(bias[:, :, S - 1:S]).view(np.uint16), want_new[2]), layer
+    # the checked layers in full
+    for layer in check:
+        qh, kh, vh = full[layer]
+        oc = oracle.Cache.from_fp16(_with_row(kh, S - 1, kn), _with_row(vh, S - 1, vn))
+        got = cache_arrays(caches[layer])
+        for g_, w_ in zip(got, (oc.kc, oc.ks, oc.kb, oc.vc, oc.vs, oc.vb)):
+            assert np.array_equal(g_, w_), layer
+        ref = oracle.attention(qh, oc, np.array([S], np.int32), ATTN)
+        assert_close(_host(outs[layer]).astype(np.float64), ref, what=f"80-layer model, layer {layer}")

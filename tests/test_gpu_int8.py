@@ -210,3 +210,35 @@ def test_int8_d256_step_stores_oracle_rows(paged):
             assert np.array_equal(g_[b, :, :n], w_[b, :, :n])
     ref = oracle.attention(x.q, want, lens, 1.0)
     assert_close(out.float().cpu().numpy(), ref, what=f"int8 D256 step paged={paged}")
+
+
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 16, 2), (256, 32, 16), (64, 8, 4)])
+def test_int8_partials_match_oracle_chunks(D, Hq, Hkv):
+    """Phase 1 alone on an int8 cache, one partial state per chunk ("Running and
+    Evaluating TurboQuant optimized Gemma 4", --kv-bits 8; "turboquant-
+    llama3.170B" README, split-K paragraph), against the oracle's per-chunk
+    states (m, l, acc) with an empty chunk beyond the shorter sequence."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    lens = np.array([700, 1100], dtype=np.int32)
+    x = synth.decode_inputs(43 + D, 2, Hq, Hkv, D, 1100, lens=lens, outliers=True)
+    cache = tq.KVCache(2, Hkv, D, 1104, bits=8)
+    tq.tq_quantize_kv_append(cache, torch.from_numpy(x.k).cuda(), torch.from_numpy(x.v).cuda(),
+                             torch.zeros(2, dtype=torch.int32, device="cuda"))
+    oc = oracle.Cache.from_fp16(x.k, x.v, bits=8)
+    a = 1 / math.sqrt(D)
+    for chunk in (64, 512):
+        om, ol, oa = oracle.attention_partials(x.q, oc, lens, a, chunk)
+        m, l, acc = tq.tq_sdpa_int4_partial(cache, torch.from_numpy(x.q).cuda(), torch.from_numpy(lens).cuda(),
+                                            1100, a, chunk=chunk, chunks_per_split=1)
+        torch.cuda.synchronize()
+        m, l, acc = m.cpu().numpy(), l.cpu().numpy(), acc.cpu().numpy()
+        empty = ol == 0
+        assert empty.any()
+        assert np.array_equal(l == 0, empty)
+        assert np.all(np.isneginf(m[empty]))
+        ne = ~empty
+        np.testing.assert_allclose(m[ne], om[ne], rtol=1e-5, atol=1e-5)
+        np.testing.assert_allclose(l[ne], ol[ne], rtol=1e-3)
+        assert_close(acc[ne] / l[ne][:, None], oa[ne] / ol[ne][:, None], what=f"int8 D{D} chunk{chunk}")

@@ -230,8 +230,8 @@ def _small_problem(seed, B=2, Hq=8, Hkv=2, D=128, S=37):
 
 
 def _dequant(cache):
-    kh = oracle.dequantize_rows(cache.kc, cache.ks, cache.kb, cache.group)
-    vh = oracle.dequantize_rows(cache.vc, cache.vs, cache.vb, cache.group)
+    kh = oracle.dequantize_rows(cache.kc, cache.ks, cache.kb, cache.group, cache.bits)
+    vh = oracle.dequantize_rows(cache.vc, cache.vs, cache.vb, cache.group, cache.bits)
     return kh, vh
 
 
@@ -346,10 +346,11 @@ def test_attention_ragged_lengths_and_empty():
     assert np.isnan(part[1, 0]).all()
 
 
+@pytest.mark.parametrize("bits", [4, 8])
 @pytest.mark.parametrize("chunk", [1, 7, 64, 512, 1000])
-def test_split_k_equals_unsplit(chunk):
+def test_split_k_equals_unsplit(chunk, bits):
     q, k, v = _small_problem(12, B=2, S=1000)
-    cache = oracle.Cache.from_fp16(k, v)
+    cache = oracle.Cache.from_fp16(k, v, bits=bits)
     lens = np.array([1000, 517], np.int32)
     ref = oracle.attention(q, cache, lens, 1 / math.sqrt(128))
     m, l, acc = oracle.attention_partials(q, cache, lens, 1 / math.sqrt(128), chunk)
@@ -362,11 +363,12 @@ def test_split_k_equals_unsplit(chunk):
         assert np.all(l[1, :, first_empty:] == 0) and np.all(np.isneginf(m[1, :, first_empty:]))
 
 
-def test_partial_state_definition():
+@pytest.mark.parametrize("bits", [4, 8])
+def test_partial_state_definition(bits):
     # one chunk covering the sequence: m = max score, l = sum exp(s - m),
-    # acc / l = attention output
+    # acc / l = attention output (int4 and int8 caches)
     q, k, v = _small_problem(13, B=1, S=20)
-    cache = oracle.Cache.from_fp16(k, v)
+    cache = oracle.Cache.from_fp16(k, v, bits=bits)
     a = 0.25
     m, l, acc = oracle.attention_partials(q, cache, np.array([20]), a, chunk=64)
     kh, vh = _dequant(cache)
