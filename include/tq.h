@@ -459,13 +459,20 @@ tq_status tq_sdpa_int4_reduce(const float* part_m, const float* part_l,
  * have no allocator at hand or may not use one: code in host callbacks or
  * other paths where cudaMalloc is forbidden, plugins of frameworks that own
  * all device memory, plain C programs that link only this library.
- *   - Same arguments, layouts and results as tq_sdpa_int4_decode.
- *   - Requests whose partial states do not fit the array
- *     (batch * num_q_heads * n_splits * (head_dim + 2) * 4 bytes, n_splits as
- *     tq_sdpa_plan reports) return TQ_ERR_WORKSPACE before any launch.
+ *   - Same arguments, layouts and results as tq_sdpa_int4_decode, bit for
+ *     bit (the same plan and kernels).  One difference in speed: batches
+ *     whose grid spans several waves run in grid order, without the
+ *     longest-run-first dispatch pass of the workspace decode.
+ *   - Requests whose partial states do not fit the array return
+ *     TQ_ERR_WORKSPACE before any launch.  They need, with P = batch *
+ *     num_q_heads * n_splits (n_splits as tq_sdpa_plan reports) and A(n) = n
+ *     rounded up to a multiple of 256,  2 * A(4 P) + 4 P * head_dim  bytes
+ *     (m and l, each 256-byte aligned, then acc).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept per device and looked
+ *     up again when the device has a new context (after cudaDeviceReset);
+ *     make that next call before any capture too.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents; nothing in it needs clearing (each call writes every element
  *     it reads), but calls that overlap on the GPU (other streams, other host
