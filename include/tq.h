@@ -96,19 +96,6 @@ typedef enum tq_status {
  * advancing lengths. */
 #define TQ_STEP_ADVANCE 0x100u
 
-/* tq_decode_step_ex, tq_sdpa_int4_decode_ex and the paged forms: the caller
- * promises that no work queued ahead of this call on the stream, and still
- * running when it starts, writes the cache rows the decode reads (other than
- * the rows this call appends) or seq_lens / write_pos.  The decode kernel may
- * then start streaming the cache before the kernel ahead of it has finished
- * and waits for that kernel only before reading the query and the new K/V
- * rows, which it may produce.  Typical use: the attention of layer l + 1,
- * queued behind layer l's work, which never writes layer l + 1's cache.
- * Breaking the promise is a data race (stale rows may be read).  Not with
- * TQ_STEP_ADVANCE (TQ_ERR_UNSUPPORTED): a step that advances the lengths for
- * the next one writes what that one reads.  Results are unchanged. */
-#define TQ_CACHE_READY 0x200u
-
 /* Decode implementations (tq_sdpa_int4_decode_impl and friends). */
 typedef enum tq_impl {
     TQ_IMPL_AUTO = 0, /* the tensor-core path */

@@ -20,7 +20,7 @@ __all__ = [
     "tq_abi_version", "tq_status_string", "tq_kv_cache_bytes", "tq_sdpa_workspace_bytes", "workspace",
     "tq_quantize_kv_append", "tq_sdpa_int4_decode", "tq_sdpa_int4_partial", "tq_sdpa_int4_reduce",
     "tq_sdpa_plan", "tq_split_plan", "tq_sdpa_int4_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "tq_decode_step",
-    "tq_dequantize_kv", "tq_hadamard_rotate", "TQ_ROTATE_K", "TQ_ROTATE_V", "TQ_STEP_ADVANCE", "TQ_CACHE_READY", "TQ_DEV_PAGE",
+    "tq_dequantize_kv", "tq_hadamard_rotate", "TQ_ROTATE_K", "TQ_ROTATE_V", "TQ_STEP_ADVANCE", "TQ_DEV_PAGE",
     "tq_paged_kv_cache", "PagedKVCache", "tq_decode_step_host", "tq_host_staging_bytes",
 ]
 
@@ -29,7 +29,6 @@ TQ_IMPL_AUTO, TQ_IMPL_MMA, TQ_IMPL_SIMT = 0, 1, 2
 TQ_DEV_WRITE_POS, TQ_DEV_SEQ_LEN, TQ_DEV_TIMEOUT = 0x1, 0x2, 0x4
 TQ_ROTATE_K, TQ_ROTATE_V = 0x1, 0x2
 TQ_STEP_ADVANCE = 0x100
-TQ_CACHE_READY = 0x200
 TQ_DEV_PAGE = 0x8
 GROUP_SIZE = 64
 DEFAULT_CHUNK = 512

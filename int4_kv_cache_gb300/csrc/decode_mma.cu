@@ -354,13 +354,8 @@ __global__ void __launch_bounds__(Cfg<D, BITS, WIDE>::THREADS, Cfg<D, BITS, WIDE
                (((static_cast<long long>(b) * p.num_kv_heads + kvh) * p.app.n_new + (r - app_wp)) * D + g * kGroup +
                 app_part * 8);
     };
-    // kWaitAfterRing: the rows, lengths and write positions are not written
-    // by the kernels ahead of this one (the caller's promise), so the first
-    // ring of tiles streams in while those kernels finish; the query and the
-    // new rows, which they may produce, are read only after the wait.
-    const bool ring_first = p.wait_at_start == kWaitAfterRing;
     uint4 app_raw = make_uint4(0, 0, 0, 0);
-    if (!ring_first && static_cast<int>(threadIdx.x >> 3) < app_tasks)
+    if (static_cast<int>(threadIdx.x >> 3) < app_tasks)
         app_raw = __ldcs(reinterpret_cast<const uint4*>(app_src(threadIdx.x >> 3)));
     if (threadIdx.x == 0 && n_tiles > 0) {
         prefetch_tensormap(&tm_k);
@@ -368,11 +363,6 @@ __global__ void __launch_bounds__(Cfg<D, BITS, WIDE>::THREADS, Cfg<D, BITS, WIDE
         const uint64_t policy = policy_evict_first();
         for (int it = 0; it < min(n_tiles, C::STAGES); ++it)
             if (!tile_uses(it, app_lo, app_hi)) issue_tile(it, policy);
-    }
-    if (ring_first) {
-        pdl_wait_primary();
-        if (static_cast<int>(threadIdx.x >> 3) < app_tasks)
-            app_raw = __ldcs(reinterpret_cast<const uint4*>(app_src(threadIdx.x >> 3)));
     }
 
     // ------------------------------------------------------------ all warps

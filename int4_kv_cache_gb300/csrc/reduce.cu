@@ -149,24 +149,25 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReducePara
     }
 }
 
-// Up to 32 parts (the plans of one wave; 19 at 128K in the one-CTA-per-SM
-// layout): one thread per head_dim element loads its element of every part
-// and each warp the parts' m and l at once, one round trip to L2, then
-//   M = warp max over lanes (lane c holds part c),  w_c = expf(m_c - M),
-//   L = xor-tree warp sum of fmaf(w_c, l_c, 0),
+// Up to 64 parts (19 at 128K in the one-CTA-per-SM layout, 43 at 16K in the
+// three-CTA one): one thread per head_dim element loads its element of every
+// part and each warp the parts' m and l at once, one round trip to L2, then
+//   M = warp max over lanes (lane c holds parts c and c + 32),
+//   w_c = expf(m_c - M),
+//   L = xor-tree warp sum of fmaf(w_c, l_c, 0) + fmaf(w_c+32, l_c+32, 0),
 //   t = sum over parts in order of fmaf(w_c, acc_c, 0) (w_c = 0 skipped),
-// no shared memory and no CTA barrier.  M, w and L are reduce_kernel's for
-// any such part count (its block reduction sees the same 32 values, the other
+// no shared memory and no CTA barrier.  Up to 32 parts M, w and L are
+// reduce_kernel's (its block reduction sees the same 32 values, the other
 // warps' zeros added exactly), and t its too up to 8 parts (one part per warp
 // there), so the two give the same bits up to 8 parts, as does the cluster
-// merge in phase 1.  (reduce_kernel: 2.2 us after its release for 19 parts,
-// five barriers and dependent loads.)
+// merge in phase 1.  (reduce_kernel: 2.0-2.2 us after its release for 19 or
+// 43 parts, five barriers and dependent loads.)
 //   Its CTAs are launched while phase 1 runs and take SMs as phase-1 CTAs
 // leave; small as they are, the first SMs to free up would take seven each,
 // and their loads queue there (128K step 32.8 us, against 31.0 us spread).
 // Each CTA therefore reserves kFastSmemPad bytes of shared memory it does not
 // use, so that at most two share an SM.
-constexpr int kFastParts = 32;
+constexpr int kFastParts = 64;
 constexpr int kFastSmemPad = 100 * 1024;
 
 template <int D>
@@ -192,14 +193,20 @@ __global__ void __launch_bounds__(D < 128 ? D : 128) reduce_fast_kernel(const Re
 #pragma unroll
         for (int j = 0; j < DPT; ++j) a[c][j] = c < n ? __ldcg(pa + c * D + j * TH) : 0.0f;
     }
-    const float l = lane < n ? __ldcg(p.part_l + bh * n + lane) : 0.0f;
-    const float mv = lane < n ? __ldcg(p.part_m + bh * n + lane) : -INFINITY;
-    const float m = l > 0.0f ? mv : -INFINITY;  // empty parts carry no weight
-    float M = m;
+    float l[2], m[2], w[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int c = lane + 32 * i;
+        l[i] = c < n ? __ldcg(p.part_l + bh * n + c) : 0.0f;
+        const float mv = c < n ? __ldcg(p.part_m + bh * n + c) : -INFINITY;
+        m[i] = l[i] > 0.0f ? mv : -INFINITY;  // empty parts carry no weight
+    }
+    float M = fmaxf(m[0], m[1]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    const float w = m == -INFINITY ? 0.0f : expf(m - M);
-    float L = fmaf(w, l, 0.0f);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) w[i] = m[i] == -INFINITY ? 0.0f : expf(m[i] - M);
+    float L = fmaf(w[0], l[0], 0.0f) + fmaf(w[1], l[1], 0.0f);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
     float t[DPT];
@@ -207,7 +214,7 @@ __global__ void __launch_bounds__(D < 128 ? D : 128) reduce_fast_kernel(const Re
     for (int j = 0; j < DPT; ++j) t[j] = 0.0f;
 #pragma unroll
     for (int c = 0; c < kFastParts; ++c) {
-        const float wc = __shfl_sync(0xffffffffu, w, c);
+        const float wc = __shfl_sync(0xffffffffu, w[c / 32], c & 31);
         if (c < n && wc != 0.0f) {
 #pragma unroll
             for (int j = 0; j < DPT; ++j) t[j] += fmaf(wc, a[c][j], 0.0f);

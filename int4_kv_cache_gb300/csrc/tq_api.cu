@@ -346,16 +346,27 @@ tq_status device_plan(const Store* cache, int max_seq_len, int chunk, tq_impl im
                     f->clusters[cache->bits == 8 ? 1 : 0][di][cache->paged ? 1 : 0]);
     pl->tile_tokens = tile;
     pl->resident = static_cast<long long>(f->sms) * per_sm;
-    // The one-CTA-per-SM layout where its plan is one wave over at least 90 %
-    // of the SMs (long single sequences, small batches); grids of several
-    // waves, and thin ones, keep several CTAs per SM.
+    // The one-CTA-per-SM layout, for a plan of one wave that either covers
+    // at least 95 % of the SMs (each SM's work the same as with three CTAs per
+    // SM, without their staggered finish), or has one run per (sequence, kv
+    // head) and so no merge at all, or covers at least 75 % with runs of at
+    // most 12 stages (the ramp of its four stages then dominates: fewer,
+    // longer streams fill sooner).  Measured (steps of 20, Llama-70B heads):
+    // 1 x 128K 31.5 us (three CTAs per SM: 32.7), 1 x 64K 20.3 (21.1),
+    // 1 x 16K 12.0 (12.5), 8 x 8K 22.0 (23.0), 16 x 8K 33.8 (38.1); with
+    // longer runs over 84 % of the SMs it lost: 4 x 32K 34.9 (33.2), 8 x 32K
+    // 61.5 (58.5).  Grids of several waves keep three CTAs per SM.
     if (!simt && f->wide_ctas > 0 && tq::mma_wide_supported(cache->head_dim, cache->bits, cache->paged)) {
         const int wtile = tq::mma_tile_tokens(cache->head_dim, cache->bits, true);
         const long long wres = static_cast<long long>(f->sms) * f->wide_ctas;
         const Plan w = make_plan(cache->batch, cache->num_kv_heads, max_seq_len, chunk, wtile, static_cast<int>(wres),
                                  merge, f->wide_clusters);
         const long long ctas = static_cast<long long>(w.n_splits) * cache->num_kv_heads * cache->batch;
-        if (w.waves == 1 && ctas * 10 >= wres * 9) {
+        const long long run = static_cast<long long>(ceil_div(w.units, w.n_splits)) * w.unit_tokens;
+        const bool full = ctas * 20 >= wres * 19;
+        const bool no_merge = w.n_splits == 1;
+        const bool short_runs = ctas * 4 >= wres * 3 && run <= 12LL * wtile;
+        if (w.waves == 1 && (full || no_merge || short_runs)) {
             *pl = w;
             pl->tile_tokens = wtile;
             pl->resident = wres;
@@ -381,7 +392,7 @@ tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const in
                      int32_t max_seq_len, float attn_scale, const Plan& pl, float* pm, float* plv, float* pa,
                      int32_t* status, tq_impl impl, cudaStream_t stream, const int32_t* dep_write_pos = nullptr,
                      int32_t dep_n_new = 0, const tq::AppendParams* fused_append = nullptr, bool rotate_q = false,
-                     int2* order_buf = nullptr, uint16_t* direct_out = nullptr, bool ring_first = false) {
+                     int2* order_buf = nullptr, uint16_t* direct_out = nullptr) {
     if (pl.n_splits > 65535 || cache->num_kv_heads > 65535 || cache->batch > 65535) return TQ_ERR_SHAPE;
     tq::DecodeParams p{};
     p.q = q;
@@ -432,12 +443,11 @@ tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const in
     if (s != TQ_OK) return s;
     // Phase 1 is always a programmatic dependent of the previous kernel on the
     // stream (typically the last step's reduce, which lets its dependents
-    // launch as soon as it starts), so that its launch overlaps that kernel.
-    // Without an append before it, it waits for that kernel before any read,
-    // or, with TQ_CACHE_READY, once its first ring of tile loads is issued;
-    // after an append it waits only before the tiles that hold the new rows.
-    p.wait_at_start = dep_write_pos != nullptr ? tq::kWaitForAppend
-                                               : (ring_first ? tq::kWaitAfterRing : tq::kWaitAtStart);
+    // launch once it has seen phase 1 complete), so that its launch overlaps
+    // that kernel.  Without an append before it, it waits for that kernel
+    // before any read; after an append it waits only before the tiles that
+    // hold the new rows.
+    p.wait_at_start = dep_write_pos != nullptr ? tq::kWaitForAppend : tq::kWaitAtStart;
     p.out = direct_out;
     // A batch whose grid spans several waves is dispatched longest run first
     // (the lengths are on the device: a one-CTA kernel writes the order).
@@ -457,7 +467,6 @@ tq_status run_phase1(const Store* cache, const uint16_t* q, int32_t hq, const in
         s = cuda_status(tq::launch_order_runs(op, stream));
         if (s != TQ_OK) return s;
         p.order = order_buf;
-        p.wait_at_start = tq::kWaitAtStart;  // the order is the previous kernel's output
     }
     return cuda_status(tq::launch_decode_mma(p, cache->head_dim, tm_k, tm_v, stream, true));
 }
@@ -646,13 +655,7 @@ tq_status run_append(const tq::AppendParams& ap, cudaStream_t st) {
     }
     return cuda_status(tq::launch_quantize_append(ap, st));
 }
-bool valid_step_flags(uint32_t flags) {
-    // TQ_CACHE_READY promises that no earlier work still writes the rows or the
-    // lengths, which a step that advances them for the next one contradicts
-    if ((flags & TQ_CACHE_READY) && (flags & TQ_STEP_ADVANCE)) return false;
-    return valid_rotation(flags & ~(TQ_STEP_ADVANCE | TQ_CACHE_READY));
-}
-bool valid_decode_flags(uint32_t flags) { return valid_rotation(flags & ~TQ_CACHE_READY); }
+bool valid_step_flags(uint32_t flags) { return valid_rotation(flags & ~TQ_STEP_ADVANCE); }
 
 // Decode (optionally preceded by an append of n_new rows) with the workspace
 // laid out as [m][l][acc][rotated q][run order]; the one path behind tq_decode_step*,
@@ -669,8 +672,7 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
     }
     if (!valid_impl(impl) || !valid_step_flags(flags)) return TQ_ERR_UNSUPPORTED;
     const bool advance = (flags & TQ_STEP_ADVANCE) != 0;
-    const bool ring_first = (flags & TQ_CACHE_READY) != 0;
-    flags &= ~(TQ_STEP_ADVANCE | TQ_CACHE_READY);
+    flags &= ~TQ_STEP_ADVANCE;
     if (advance && (write_pos == nullptr || write_pos == seq_lens)) return TQ_ERR_SHAPE;
     const size_t need =
         tq_sdpa_workspace_bytes(cache->batch, hq, cache->num_kv_heads, cache->head_dim, max_seq_len, chunk);
@@ -725,7 +727,7 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
     bool own_out = direct;
     s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, ph1, st,
                    dep ? write_pos : nullptr, dep ? n_new : 0, fused ? &ap : nullptr, rotate_q, order,
-                   own_out ? out : nullptr, ring_first && !((flags & TQ_ROTATE_K) && !rotate_q));
+                   own_out ? out : nullptr);
     if (s != TQ_OK && own_out && pl.n_splits > 1) {
         // a cluster launch the device refused (nothing was queued; e.g. a GPU
         // partition too small to place the cluster): the same runs with
@@ -733,8 +735,7 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
         cudaGetLastError();
         own_out = false;
         s = run_phase1(cache, q, hq, seq_lens, max_seq_len, attn_scale, pl, pm, plv, pa, status, ph1, st,
-                       dep ? write_pos : nullptr, dep ? n_new : 0, fused ? &ap : nullptr, rotate_q, order, nullptr,
-                       ring_first && !((flags & TQ_ROTATE_K) && !rotate_q));
+                       dep ? write_pos : nullptr, dep ? n_new : 0, fused ? &ap : nullptr, rotate_q, order, nullptr);
     }
     if (s != TQ_OK) return s;
     tq::ReduceParams r{};
@@ -853,7 +854,7 @@ tq_status tq_sdpa_int4_decode_ex(const tq_kv_cache* raw, const uint16_t* q, int3
     Store st;
     tq_status s = store_of(raw, &st);
     if (s != TQ_OK) return s;
-    if (!valid_decode_flags(flags)) return TQ_ERR_UNSUPPORTED;
+    if (!valid_rotation(flags)) return TQ_ERR_UNSUPPORTED;
     return decode_path(&st, nullptr, nullptr, 0, nullptr, q, hq, seq_lens, max_seq_len, attn_scale, chunk, flags,
                        workspace, workspace_bytes, out, status, TQ_IMPL_AUTO, static_cast<cudaStream_t>(stream));
 }
@@ -972,7 +973,7 @@ tq_status tq_paged_sdpa_int4_decode(const tq_paged_kv_cache* raw, const uint16_t
     Store st;
     tq_status s = store_of(raw, &st);
     if (s != TQ_OK) return s;
-    if (!valid_decode_flags(flags)) return TQ_ERR_UNSUPPORTED;
+    if (!valid_rotation(flags)) return TQ_ERR_UNSUPPORTED;
     return decode_path(&st, nullptr, nullptr, 0, nullptr, q, hq, seq_lens, max_seq_len, attn_scale, chunk, flags,
                        workspace, workspace_bytes, out, status, TQ_IMPL_MMA, static_cast<cudaStream_t>(stream));
 }

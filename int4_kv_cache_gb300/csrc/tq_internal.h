@@ -149,10 +149,6 @@ struct DecodeParams {
     // Where the kernel waits for the grid ahead of it on the stream (the
     // launch is always a programmatic dependent of that grid):
     //  kWaitAtStart    before its first read;
-    //  kWaitAfterRing  after issuing the first ring of tile loads (caller's
-    //                  TQ_CACHE_READY: nothing ahead writes the rows it reads
-    //                  other than those it appends, nor the lengths), before
-    //                  reading the query and the new rows;
     //  kWaitForAppend  an append kernel is the grid ahead: only before the
     //                  tiles holding its rows (dep_write_pos).
     int32_t wait_at_start;
@@ -168,7 +164,7 @@ struct DecodeParams {
     // The plan's SM layout: one 12-warp CTA per SM (mma_wide_supported only).
     int32_t wide;
 };
-constexpr int32_t kWaitForAppend = 0, kWaitAtStart = 1, kWaitAfterRing = 2;
+constexpr int32_t kWaitForAppend = 0, kWaitAtStart = 1;
 // Most rows per sequence the decode kernel appends itself; longer appends
 // run the append kernel first.
 constexpr int kFusedAppendMaxRows = 16;

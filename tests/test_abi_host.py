@@ -260,25 +260,6 @@ def test_int8_sizes_and_validation(L):
     assert _decode(L, bad) == 6
 
 
-def test_cache_ready_flag_is_accepted_and_excludes_advance(L):
-    # TQ_CACHE_READY (0x200) passes the flag checks (the call then stops at the
-    # workspace check); with TQ_STEP_ADVANCE (0x100) it is refused: a step that
-    # advances the lengths writes what the next step reads
-    c = _fake_cache()
-    d = L.tq_sdpa_int4_decode_ex
-    assert d(ctypes.byref(c), 0x100000, 8, 0x200000, 256, ctypes.c_float(0.1), 512, 0x200, 0x300000, 16,
-             0x400000, None, None) == 4
-    assert d(ctypes.byref(c), 0x100000, 8, 0x200000, 256, ctypes.c_float(0.1), 512, 0x201, 0x300000, 16,
-             0x400000, None, None) == 4
-    s = L.tq_decode_step_ex
-    args = lambda flags, ws_bytes: (ctypes.byref(c), 0x1000, 0x1000, 1, 0x500000, 0x100000, 8, 0x200000, 256,
-                                    ctypes.c_float(0.1), 512, flags, 0x300000, ws_bytes, 0x400000, None, None)
-    assert s(*args(0x200, 16)) == 4
-    assert s(*args(0x300, 1 << 30)) == 6
-    assert s(*args(0x400, 1 << 30)) == 6   # unknown flag bit
-    assert tq.TQ_CACHE_READY == 0x200
-
-
 def test_wait_timeout_selftest_argument_errors(L):
     f = L.tq_wait_timeout_selftest
     assert f(None, 0x1000, 100, 0x2000, None) == 1
