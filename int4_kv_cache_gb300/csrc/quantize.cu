@@ -147,27 +147,149 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_append_kernel(const Ap
     quantize_store<BITS>(p, gi, ng, stage[warp][0][lane], stage[warp][1][lane], lane & 7);
 }
 
-// The Hadamard rotation of a row whose NG groups of 64 are held by NG
-// consecutive lanes, this thread holding group g in v (fp32).  The stages run
-// in the order of the fast transform (h = 1, 2, ..., 32 inside the thread,
-// then h = 64, 128 with the lanes lane ^ 1, lane ^ 2), each butterfly one
-// round-to-nearest add and one subtract (two butterflies per paired fp32
-// operation), so the result equals the sequential transform bit for bit; then
-// the scale.  Every lane of the warp takes part.
+// Large appends (prefill): a persistent grid streams tiles of ROWS rows of
+// 128 bytes (one group of 64 fp16 values per row) of K and of V into shared
+// memory with 2-D TMA boxes.  The 128-byte swizzle places word j of row r at
+// slot j ^ (r & 7).  One thread per row takes the group of K, then the group
+// of V (both go to the same cache offsets, found once).  K and V have a
+// buffer each: a thread copies its group into registers and releases the
+// buffer at once; the last warp to release it issues the next tile's copy
+// into it, which then lands while the CTA works on the other tensor.  The
+// release is counted per warp (no CTA barrier).
+template <int ROWS, int WARPS>
+struct KVTiles {
+    static constexpr int kTensorBytes = ROWS * 128;
+    static constexpr int kSmemBytes = 2 * kTensorBytes + 1024;
+
+    uint8_t* smem;  // 1024-byte aligned (the swizzle pattern repeats every 1024 bytes)
+    uint64_t* full_bar;      // [2]: K, V
+    unsigned int* done_cnt;  // [2]: warps finished with the buffer, cumulative
+    const CUtensorMap* tm_k;
+    const CUtensorMap* tm_v;
+    int n_tiles;
+
+    __device__ __forceinline__ void issue(int tile, int t) const {
+        mbar_arrive_expect_tx(&full_bar[t], kTensorBytes);
+        tma_load_2d(smem + t * kTensorBytes, t ? tm_v : tm_k, 0, tile * ROWS, &full_bar[t], policy_evict_first());
+    }
+    // Barriers, then the first tile in flight; every thread of the CTA calls it.
+    __device__ __forceinline__ void start() const {
+        if (threadIdx.x == 0) {
+            for (int t = 0; t < 2; ++t) {
+                mbar_init(&full_bar[t], 1);
+                done_cnt[t] = 0;
+            }
+            fence_mbarrier_init();
+        }
+        __syncthreads();
+        pdl_launch_dependents();
+        if (threadIdx.x == 0 && blockIdx.x < n_tiles) {
+            prefetch_tensormap(tm_k);
+            prefetch_tensormap(tm_v);
+            issue(blockIdx.x, 0);
+            issue(blockIdx.x, 1);
+        }
+    }
+    // Tensor t of this CTA's it-th tile has landed (false: the bounded wait gave up).
+    __device__ __forceinline__ bool wait(int it, int t) const { return mbar_wait_bounded(&full_bar[t], it & 1); }
+    __device__ __forceinline__ const uint4 (*rows(int t) const)[8] {
+        return reinterpret_cast<const uint4(*)[8]>(smem + t * kTensorBytes);
+    }
+    // This warp is done reading buffer t.  The last warp to finish it refills
+    // it: its fences order every warp's reads (made visible by their fences
+    // before the count) before the asynchronous copy that overwrites it.
+    __device__ __forceinline__ void release(int tile, int t) const {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) {
+            __threadfence_block();
+            const unsigned int before = atomicAdd(&done_cnt[t], 1u);
+            const int next = tile + gridDim.x;
+            if (before % WARPS == WARPS - 1 && next < n_tiles) {
+                __threadfence_block();
+                fence_proxy_async_shared();
+                issue(next, t);
+            }
+        }
+    }
+};
+
+constexpr int kTmaGroups = kTmaAppendBoxRows;  // rows per tile
+constexpr int kTmaThreads = kTmaGroups;        // one thread per row: its K group, then its V group
+constexpr int kTmaWarps = kTmaThreads / 32;
+using AppendTiles = KVTiles<kTmaGroups, kTmaWarps>;
+
+template <int ROWS, int WARPS>
+__device__ __forceinline__ KVTiles<ROWS, WARPS> kv_tiles(uint8_t* dyn_smem, uint64_t* full_bar, unsigned int* done_cnt,
+                                                        const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                                        int n_tiles) {
+    KVTiles<ROWS, WARPS> r;
+    r.smem = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
+    r.full_bar = full_bar;
+    r.done_cnt = done_cnt;
+    r.tm_k = tm_k;
+    r.tm_v = tm_v;
+    r.n_tiles = n_tiles;
+    return r;
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kTmaThreads, 3)
+    quantize_append_tma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                               const AppendParams p, long long n_groups, int n_tiles) {
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ uint64_t full_bar[2];
+    __shared__ unsigned int done_cnt[2];
+    const AppendTiles tiles = kv_tiles<kTmaGroups, kTmaWarps>(dyn_smem, full_bar, done_cnt, &tm_k, &tm_v, n_tiles);
+    tiles.start();
+    const int ng = p.head_dim / kGroup, r = threadIdx.x;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+        const long long gi = static_cast<long long>(tile) * kTmaGroups + r;
+        long long code_off = 0, sb = 0;
+        const bool ok = gi < n_groups && group_dst<BITS>(p, gi, ng, code_off, sb);
+#pragma unroll 1
+        for (int t = 0; t < 2; ++t) {
+            if (!tiles.wait(it, t)) {
+                if (p.status != nullptr) atomicOr(p.status, TQ_DEV_TIMEOUT);
+                return;  // no further tiles are issued, so every thread gives up the same way
+            }
+            uint4 x[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] = tiles.rows(t)[r][j ^ (r & 7)];
+            tiles.release(tile, t);  // the group is in registers
+            if (ok) quantize_words_store<BITS>(p, x, t, code_off, sb);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------
+// Rotated: the same one thread per (group of 64, K or V); a row's NG groups
+// sit in NG consecutive lanes ("Running and Evaluating TurboQuant optimized
+// Gemma 4", TurboQuant section: x -> H x / sqrt(D) before quantisation).  The
+// fast transform runs its stages in increasing order h = 1, 2, ..., D / 2,
+// each butterfly one round-to-nearest fp32 add or subtract, then the scale
+// and the fp16 rounding: the same operations as the sequential transform, so
+// the stored rows are bit-identical to it.  Stages h < 64 run in the thread,
+// h = 64, 128 between the lanes lane and lane ^ 1, lane ^ 2.
+constexpr int kRotCtasPerSm = 2;  // registers: 64 fp32 values per thread
+
+// x: the group's 64 fp16 values (eight 16-byte words) -> v: H x / sqrt(D) of
+// this group's part of the row, fp32.
 template <int NG>
-__device__ __forceinline__ void rotate_group_thread(float (&v)[64], int g, float scale) {
+__device__ __forceinline__ void rotate_group_thread(const uint4 (&x)[8], float (&v)[64], int g, float scale) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // h = 1 straight from fp16: x0 + x1, x0 - x1 with x1 widened once
+        const __half2* hp = reinterpret_cast<const __half2*>(&x[j]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float u = __high2float(hp[e]);
+            v[8 * j + 2 * e] = add_h_f(__low2half(hp[e]), u);
+            v[8 * j + 2 * e + 1] = sub_h_f(__low2half(hp[e]), u);
+        }
+    }
     const float2 m1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
-    for (int i = 0; i < 64; i += 4) {  // h = 1: butterflies (i, i+1) and (i+2, i+3) in one paired op each
-        const float2 a = make_float2(v[i], v[i + 2]), b = make_float2(v[i + 1], v[i + 3]);
-        const float2 sum = __fadd2_rn(a, b), dif = __ffma2_rn(b, m1, a);
-        v[i] = sum.x;
-        v[i + 2] = sum.y;
-        v[i + 1] = dif.x;
-        v[i + 3] = dif.y;
-    }
-#pragma unroll
-    for (int h = 2; h < 64; h <<= 1) {  // pairs (i, i+1) with bit h clear: two butterflies per paired op
+    for (int h = 2; h < 64; h <<= 1) {  // pairs (i, i + 1) with bit h clear: two butterflies per paired op
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {
             if ((i & h) != 0) continue;
@@ -203,125 +325,40 @@ __device__ __forceinline__ void rotate_group_thread(float (&v)[64], int g, float
     }
 }
 
-// Rotate a staged group (slots j ^ r7) in registers and quantize it.
 template <int BITS, int NG>
-__device__ __forceinline__ void rotate_quantize_store(const AppendParams& p, long long gi, int g, const uint4* row,
-                                                      int r7, int t) {
-    float v[64];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint4 w = row[j ^ r7];
-        const __half2* h = reinterpret_cast<const __half2*>(&w);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float2 f = __half22float2(h[k]);
-            v[8 * j + 2 * k] = f.x;
-            v[8 * j + 2 * k + 1] = f.y;
-        }
-    }
-    rotate_group_thread<NG>(v, g, p.rot_scale);  // all lanes, before any exit
-    uint4 x[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        uint32_t w[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const __half2 h = __floats2half2_rn(v[8 * j + 2 * k], v[8 * j + 2 * k + 1]);
-            w[k] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        x[j] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    long long code_off, sb;
-    if (gi >= 0 && group_dst<BITS>(p, gi, NG, code_off, sb)) quantize_words_store<BITS>(p, x, t, code_off, sb);
-}
-
-// Large appends (prefill): a persistent grid streams tiles of kTmaGroups
-// groups of K and of V into shared memory with 2-D TMA boxes (128-byte rows,
-// one group per row).  The 128-byte swizzle places word j of row r at slot
-// j ^ (r & 7), the layout the per-thread reads above expect.  Two stages per
-// CTA: while the threads quantize one tile, the next one is in flight.  A
-// stage is released warp by warp (a shared count, no CTA barrier): the last
-// warp to finish with it issues its refill, and the other warps go on to the
-// next stage meanwhile.
-constexpr int kTmaGroups = 128;                     // groups (rows) per tile
-constexpr int kTmaThreads = 2 * kTmaGroups;         // one thread per (group, K or V)
-constexpr int kTmaTensorBytes = kTmaGroups * 128;   // 16 KB of K or of V
-constexpr int kTmaStageBytes = 2 * kTmaTensorBytes;
-constexpr int kTmaStages = 2;
-constexpr int kTmaSmemBytes = kTmaStages * kTmaStageBytes + 1024;
-constexpr int kTmaWarps = kTmaThreads / 32;
-
-template <int BITS, bool ROT>
-__global__ void __launch_bounds__(kTmaThreads, ROT ? 2 : 3) quantize_append_tma_kernel(const __grid_constant__ CUtensorMap tm_k,
-                                                                         const __grid_constant__ CUtensorMap tm_v,
-                                                                         const AppendParams p, long long n_groups,
-                                                                         int n_tiles) {
+__global__ void __launch_bounds__(kTmaThreads, kRotCtasPerSm)
+    quantize_append_rot_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                               const AppendParams p, long long n_groups, int n_tiles) {
     extern __shared__ uint8_t dyn_smem[];
-    __shared__ uint64_t full_bar[kTmaStages];
-    __shared__ unsigned int done_cnt[kTmaStages];  // warps finished with the stage, cumulative
-    uint8_t* smem = dyn_smem + ((1024u - (smem_u32(dyn_smem) & 1023u)) & 1023u);
-    const int tid = threadIdx.x, lane = tid & 31;
-    const int ng = p.head_dim / kGroup;
-    if (tid == 0) {
-        for (int s = 0; s < kTmaStages; ++s) {
-            mbar_init(&full_bar[s], 1);
-            done_cnt[s] = 0;
-        }
-        fence_mbarrier_init();
-    }
-    __syncthreads();
-    pdl_launch_dependents();
-    auto issue = [&](int tile, int stage) {
-        const uint64_t policy = policy_evict_first();
-        uint8_t* st = smem + stage * kTmaStageBytes;
-        mbar_arrive_expect_tx(&full_bar[stage], kTmaStageBytes);
-        tma_load_2d(st, &tm_k, 0, tile * kTmaGroups, &full_bar[stage], policy);
-        tma_load_2d(st + kTmaTensorBytes, &tm_v, 0, tile * kTmaGroups, &full_bar[stage], policy);
-    };
-    if (tid == 0) {
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
-        for (int s = 0; s < kTmaStages; ++s)
-            if (blockIdx.x + s * gridDim.x < n_tiles) issue(blockIdx.x + s * gridDim.x, s);
-    }
+    __shared__ uint64_t full_bar[2];
+    __shared__ unsigned int done_cnt[2];
+    const AppendTiles tiles = kv_tiles<kTmaGroups, kTmaWarps>(dyn_smem, full_bar, done_cnt, &tm_k, &tm_v, n_tiles);
+    tiles.start();
+    const int r = threadIdx.x;
     int it = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
-        const int stage = it % kTmaStages;
-        if (!mbar_wait_bounded(&full_bar[stage], (it / kTmaStages) & 1)) {
-            if (p.status != nullptr) atomicOr(p.status, TQ_DEV_TIMEOUT);
-            break;  // no further tiles are issued, so every thread gives up the same way
-        }
-        uint4 (*tk)[8] = reinterpret_cast<uint4 (*)[8]>(smem + stage * kTmaStageBytes);
-        uint4 (*tv)[8] = reinterpret_cast<uint4 (*)[8]>(smem + stage * kTmaStageBytes + kTmaTensorBytes);
-        // threads [0, 128) take the K groups, [128, 256) the V groups
-        const int t = tid >= kTmaGroups ? 1 : 0, r = tid - t * kTmaGroups;
         const long long gi = static_cast<long long>(tile) * kTmaGroups + r;
-        if (ROT && (p.flags & (t ? TQ_ROTATE_V : TQ_ROTATE_K))) {  // the same for each warp
-            // every lane rotates (the shuffles need the whole warp); lanes past
-            // the last group hold zero-filled rows and store nothing
-            const long long gq = gi < n_groups ? gi : -1;
-            switch (ng) {
-                case 1: rotate_quantize_store<BITS, 1>(p, gq, r % 1, (t ? tv : tk)[r], r & 7, t); break;
-                case 2: rotate_quantize_store<BITS, 2>(p, gq, r % 2, (t ? tv : tk)[r], r & 7, t); break;
-                default: rotate_quantize_store<BITS, 4>(p, gq, r % 4, (t ? tv : tk)[r], r & 7, t); break;
+        long long code_off = 0, sb = 0;
+        const bool ok = gi < n_groups && group_dst<BITS>(p, gi, NG, code_off, sb);
+#pragma unroll 1
+        for (int t = 0; t < 2; ++t) {
+            if (!tiles.wait(it, t)) {
+                if (p.status != nullptr) atomicOr(p.status, TQ_DEV_TIMEOUT);
+                return;  // no further tiles are issued, so every thread gives up the same way
             }
-        } else if (gi < n_groups) {
-            quantize_store<BITS>(p, gi, ng, tk[r], tv[r], r & 7, t, t);
-        }
-        // Release the stage (this thread only read it).  The last warp to
-        // finish it refills it: its fences order every warp's reads (made
-        // visible by their fences before the count) before the asynchronous
-        // copy that overwrites the stage.
-        __syncwarp();
-        if (lane == 0) {
-            __threadfence_block();
-            const unsigned int before = atomicAdd(&done_cnt[stage], 1u);
-            const int next = tile + kTmaStages * gridDim.x;
-            if (before % kTmaWarps == kTmaWarps - 1 && next < n_tiles) {
-                __threadfence_block();
-                fence_proxy_async_shared();
-                issue(next, stage);
+            uint4 x[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] = tiles.rows(t)[r][j ^ (r & 7)];
+            tiles.release(tile, t);  // the group is in registers
+            if ((p.flags & (t ? TQ_ROTATE_V : TQ_ROTATE_K)) != 0) {  // the same for the CTA
+                // every lane (shuffles); lanes past the last group hold zero-filled rows
+                float v[64];
+                rotate_group_thread<NG>(x, v, r % NG, p.rot_scale);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    floats_to_halves<8>(*reinterpret_cast<const float(*)[8]>(&v[8 * j]), &x[j]);
             }
+            if (ok) quantize_words_store<BITS>(p, x, t, code_off, sb);
         }
     }
 }
@@ -339,30 +376,42 @@ cudaError_t launch_quantize_append(const AppendParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_quantize_append_tma(const AppendParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                       int grid, cudaStream_t stream) {
+                                       int sms, cudaStream_t stream) {
     const long long groups = static_cast<long long>(p.batch) * p.num_kv_heads * p.n_new * (p.head_dim / kGroup);
+    const bool rot = (p.flags & (TQ_ROTATE_K | TQ_ROTATE_V)) != 0;
     const long long tiles = (groups + kTmaGroups - 1) / kTmaGroups;
     if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int n_tiles = static_cast<int>(tiles);
+    int grid = sms * (rot ? kRotCtasPerSm : kTmaAppendCtasPerSm);
     if (grid > n_tiles) grid = n_tiles;
     if (grid < 1) return cudaSuccess;
-    const bool rot = (p.flags & (TQ_ROTATE_K | TQ_ROTATE_V)) != 0;
-    if (rot) grid = grid * 2 / 3;  // the rotating instantiation runs 2 CTAs per SM (registers)
-    if (grid < 1) grid = 1;
-    static std::atomic<bool> attr_done[64][4];  // per device and variant; a repeated set is harmless
+    using Kern = void (*)(CUtensorMap, CUtensorMap, AppendParams, long long, int);
+    Kern kern = nullptr;
+    int vi = 0;  // variant: code width x (plain, rotated head_dim 64 / 128 / 256)
+    if (!rot) {
+        kern = p.bits == 8 ? quantize_append_tma_kernel<8> : quantize_append_tma_kernel<4>;
+        vi = 0;
+    } else if (p.head_dim == 64) {
+        kern = p.bits == 8 ? quantize_append_rot_kernel<8, 1> : quantize_append_rot_kernel<4, 1>;
+        vi = 1;
+    } else if (p.head_dim == 128) {
+        kern = p.bits == 8 ? quantize_append_rot_kernel<8, 2> : quantize_append_rot_kernel<4, 2>;
+        vi = 2;
+    } else {
+        kern = p.bits == 8 ? quantize_append_rot_kernel<8, 4> : quantize_append_rot_kernel<4, 4>;
+        vi = 3;
+    }
+    vi = 2 * vi + (p.bits == 8 ? 1 : 0);
+    const int smem = AppendTiles::kSmemBytes;
+    static std::atomic<bool> attr_done[64][8];  // per device and variant; a repeated set is harmless
     int dev = 0;
     cudaGetDevice(&dev);
-    const int vi = (p.bits == 8 ? 1 : 0) + (rot ? 2 : 0);
-    auto kern = [&]() {
-        if (p.bits == 8) return rot ? quantize_append_tma_kernel<8, true> : quantize_append_tma_kernel<8, false>;
-        return rot ? quantize_append_tma_kernel<4, true> : quantize_append_tma_kernel<4, false>;
-    }();
     if (dev >= 0 && dev < 64 && !attr_done[dev][vi].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr_done[dev][vi].store(true, std::memory_order_release);
     }
-    kern<<<grid, kTmaThreads, kTmaSmemBytes, stream>>>(tm_k, tm_v, p, groups, n_tiles);
+    kern<<<grid, kTmaThreads, smem, stream>>>(tm_k, tm_v, p, groups, n_tiles);
     return cudaGetLastError();
 }
 

@@ -645,13 +645,14 @@ tq_status run_append(const tq::AppendParams& ap, cudaStream_t st) {
         static_cast<long long>(ap.batch) * ap.num_kv_heads * ap.n_new * (ap.head_dim / tq::kGroup);
     if (groups >= tq::kTmaAppendMinGroups && groups < (1LL << 31)) {
         CUtensorMap tm_k, tm_v;
-        tq_status s = make_rows_map(&tm_k, ap.k_new, static_cast<unsigned long long>(groups), 128);
-        if (s == TQ_OK) s = make_rows_map(&tm_v, ap.v_new, static_cast<unsigned long long>(groups), 128);
+        const int box = tq::kTmaAppendBoxRows;
+        tq_status s = make_rows_map(&tm_k, ap.k_new, static_cast<unsigned long long>(groups), box);
+        if (s == TQ_OK) s = make_rows_map(&tm_v, ap.v_new, static_cast<unsigned long long>(groups), box);
         if (s != TQ_OK) return s;
         DeviceFacts* f = nullptr;
         s = device_facts(&f);
         if (s != TQ_OK) return s;
-        return cuda_status(tq::launch_quantize_append_tma(ap, tm_k, tm_v, f->sms * tq::kTmaAppendCtasPerSm, st));
+        return cuda_status(tq::launch_quantize_append_tma(ap, tm_k, tm_v, f->sms, st));
     }
     return cuda_status(tq::launch_quantize_append(ap, st));
 }

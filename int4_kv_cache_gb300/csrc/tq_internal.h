@@ -208,13 +208,14 @@ struct ReduceParams {
 
 // Launchers (return the cudaError_t of the launch).
 cudaError_t launch_quantize_append(const AppendParams& p, cudaStream_t stream);
-// The same for large appends: a persistent grid of `grid` CTAs streaming the
-// fp16 rows through TMA (tm_k / tm_v: k_new / v_new as [groups][128 bytes],
-// boxes of 128 rows, 128-byte swizzle).
+// The same for large appends: a persistent grid (a few CTAs per SM of `sms`)
+// streaming the fp16 rows through TMA.  tm_k / tm_v: k_new / v_new as
+// [groups][128 bytes], boxes of kTmaAppendBoxRows rows, 128-byte swizzle.
 constexpr long long kTmaAppendMinGroups = 8192;
 constexpr int kTmaAppendCtasPerSm = 3;
+constexpr int kTmaAppendBoxRows = 256;
 cudaError_t launch_quantize_append_tma(const AppendParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                       int grid, cudaStream_t stream);
+                                       int sms, cudaStream_t stream);
 cudaError_t launch_decode_simt(const DecodeParams& p, int head_dim, cudaStream_t stream);
 cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, const CUtensorMap& tm_k,
                               const CUtensorMap& tm_v, cudaStream_t stream, bool pdl_secondary);

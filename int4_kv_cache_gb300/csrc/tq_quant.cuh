@@ -9,11 +9,12 @@
 // the scale is 0.  Every step is one IEEE fp32 operation with
 // round-to-nearest-even, so the result is bit-identical to the CPU oracle.
 //
-// The per-element division is replaced by a multiply with fp32(1/scale):
-// d * fp32(1/s) is within 3 * 2^-24 relative of fp32(d / s), so both round to
-// the same integer unless a half-integer lies closer than that to the product
-// (6e-6 absolute for int4, t < 32; 5e-5 for int8, t < 264): within the window
-// kTieWindow of a half-integer the IEEE division decides.
+// The per-element division is replaced by multiplications with rounded
+// reciprocals, and the IEEE division decides only where they could round to
+// another code: the eight-lane quantizer tests d * fp32(1/s) (within
+// 3 * 2^-24 relative of fp32(d / s)) against the window kTieWindow around a
+// half-integer; the one-thread-per-group quantizer brackets fp32(d / s)
+// between two products (quantize_word8).
 #pragma once
 
 #include <cuda_fp16.h>
@@ -26,6 +27,21 @@ struct QuantRule {
     static constexpr float kLevels = static_cast<float>((1 << BITS) - 1);
     static constexpr float kTieWindow = BITS == 4 ? 1.0e-5f : 1.0e-4f;
 };
+
+// The scale and bias of a group from its minimum and maximum (fp32 values of
+// fp16 elements) and the sign bit of its first element: the stored scale is
+// fp16(fp32(max - min) / L) with a zero minimum taken as +0.  The rule's
+// maximum is the first element holding the largest value, so a group of
+// zeros only has the range (first element) - (+0): -0 when the group opens
+// with -0 (then the scale is -0), +0 otherwise.
+template <int BITS>
+__device__ __forceinline__ void group_scale_bias(float mn, float mx, bool first_neg, __half& scale, __half& bias) {
+    using R = QuantRule<BITS>;
+    if (mn == 0.0f) mn = 0.0f;  // a zero minimum is stored as +0
+    if (mx == 0.0f) mx = first_neg && mn == 0.0f ? -0.0f : 0.0f;
+    scale = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), R::kLevels));
+    bias = __float2half_rn(mn);  // exact: mn is an fp16 value
+}
 
 // ---------------------------------------------- eight lanes per group of 64 --
 template <int BITS>
@@ -57,11 +73,10 @@ __device__ __forceinline__ GroupQ<BITS> quantize_lane8(uint4 raw) {
         mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     }
-    if (mn == 0.0f) mn = 0.0f;  // a zero minimum is stored as +0
-    const float range = __fsub_rn(mx, mn);
+    // the group's first element sits in the lowest of its eight lanes
+    const uint32_t first = __shfl_sync(0xffffffffu, raw.x, (threadIdx.x & 31) & ~7);
     GroupQ<BITS> g;
-    g.scale = __float2half_rn(__fdiv_rn(range, R::kLevels));
-    g.bias = __float2half_rn(mn);  // exact: mn is an fp16 value
+    group_scale_bias<BITS>(mn, mx, (first & 0x8000u) != 0u, g.scale, g.bias);
     const float s = __half2float(g.scale);
     const float b = __half2float(g.bias);
 #pragma unroll
@@ -124,10 +139,75 @@ static __device__ __noinline__ uint2 code_word_exact(uint4 word, float b, float 
     return make_uint2(w[0], w[1]);
 }
 
+// fp32(x) + c and fp32(x) - c with one rounding each, x an fp16 value (widened
+// exactly).
+__device__ __forceinline__ float add_h_f(__half x, float c) {
+    float d;
+    asm("add.rn.f32.f16 %0, %1, %2;" : "=f"(d) : "h"(__half_as_ushort(x)), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float sub_h_f(__half x, float c) {
+    float d;
+    asm("sub.rn.f32.f16 %0, %1, %2;" : "=f"(d) : "h"(__half_as_ushort(x)), "f"(c));
+    return d;
+}
+
+// Multipliers bracketing 1 / s: lo <= (1 / s)(1 - 2^-23) and
+// hi >= (1 / s)(1 + 2^-23).  rs = fp32(1 / s) is within 2^-24 relative of
+// 1 / s and each product below adds at most 2^-24 more, so a relative step of
+// 2^-21 keeps both bounds.
+struct RecipBracket {
+    float lo, hi;
+};
+__device__ __forceinline__ RecipBracket recip_bracket(float rs) {
+    return {__fmul_rn(rs, 1.0f - 0x1p-21f), __fmul_rn(rs, 1.0f + 0x1p-21f)};
+}
+
+// The codes of one 16-byte word (8 elements, element 0 lowest; BITS / 4
+// words) of a group with scale s > 0, bias b, rs = fp32(1 / s) and the
+// bracket br of 1 / s.  For d = fp32(x - b) >= 0, fp32(d / s) is within
+// 2^-24 relative of d / s, so it lies in [d * br.lo, d * br.hi]; rint is
+// non-decreasing, so where rint(d * br.lo) == rint(d * br.hi) that is also
+// rint(fp32(d / s)), the code.  Each rint is one fused multiply-add with
+// 1.5 * 2^23, which leaves round-to-nearest-even of the exact product in the
+// low bits.  A normal fp16 scale is within 2^-11 of range / L, so every
+// product stays below L + 0.5 and no clamp is needed.  A word where the two
+// roundings differ for some element (a half-integer lies in its interval:
+// within about 2^-22 relative of a tie) or whose scale is subnormal takes the
+// exact scalar rule.
+template <int BITS>
+__device__ __forceinline__ uint2 quantize_word8(const uint4& raw, float b, float s, float rs, RecipBracket br) {
+    const bool normal = s >= 6.103515625e-05f;  // 2^-14
+    const float2 lo2 = make_float2(br.lo, br.lo), hi2 = make_float2(br.hi, br.hi);
+    const float2 mg = make_float2(kMagic, kMagic);
+    const __half2* h = reinterpret_cast<const __half2*>(&raw);
+    // The code bits of an element are the low bits of its fp32 result (the
+    // bits of 1.5 * 2^23 are zero below bit 22), so the word is put together
+    // by a tree of bit-field inserts: pairs, then quads, then the word.
+    uint32_t pr[4], t[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {  // two elements per paired fp32 operation
+        const float2 d = make_float2(sub_h_f(__low2half(h[k]), b), sub_h_f(__high2half(h[k]), b));  // x - b
+        const float2 ra = __ffma2_rn(d, lo2, mg), rb = __ffma2_rn(d, hi2, mg);
+        t[k] = (__float_as_uint(ra.x) ^ __float_as_uint(rb.x)) | (__float_as_uint(ra.y) ^ __float_as_uint(rb.y));
+        pr[k] = bfi(__float_as_uint(ra.y), __float_as_uint(ra.x), BITS, BITS);  // elements 2k, 2k + 1
+    }
+    const uint32_t diff = (t[0] | t[1]) | (t[2] | t[3]);
+    uint2 w;
+    if (BITS == 4) {
+        w.x = bfi(bfi(pr[3], pr[2], 8, 8), bfi(pr[1], pr[0], 8, 8), 16, 16);
+        w.y = 0u;
+    } else {
+        w.x = bfi(pr[1], pr[0], 16, 16);
+        w.y = bfi(pr[3], pr[2], 16, 16);
+    }
+    if (diff != 0u || !normal) return code_word_exact<BITS>(raw, b, s, rs);  // rare: the exact scalar rule
+    return w;
+}
+
 template <int BITS>
 __device__ __forceinline__ void quantize_group64(const uint4 (&raw)[8], uint32_t (&codes)[2 * BITS], __half& scale,
                                                  __half& bias) {
-    using R = QuantRule<BITS>;
     const __half2* h = reinterpret_cast<const __half2*>(raw);  // 32 pairs
     __half2 mn2 = h[0], mx2 = h[0];
 #pragma unroll
@@ -135,55 +215,20 @@ __device__ __forceinline__ void quantize_group64(const uint4 (&raw)[8], uint32_t
         mn2 = __hmin2(mn2, h[i]);
         mx2 = __hmax2(mx2, h[i]);
     }
-    float mn = fminf(__low2float(mn2), __high2float(mn2));
+    const float mn = fminf(__low2float(mn2), __high2float(mn2));
     const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
-    if (mn == 0.0f) mn = 0.0f;  // a zero minimum is stored as +0
-    scale = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), R::kLevels));
-    bias = __float2half_rn(mn);  // exact: mn is an fp16 value
+    group_scale_bias<BITS>(mn, mx, (raw[0].x & 0x8000u) != 0u, scale, bias);
     const float s = __half2float(scale), b = __half2float(bias);
 #pragma unroll
     for (int j = 0; j < 2 * BITS; ++j) codes[j] = 0u;
     if (s == 0.0f) return;
     const float rs = __frcp_rn(s);
-    // A normal fp16 scale is within 2^-11 of range / L, so every t stays below
-    // L + 0.5 and rounds into 0..L with no clamp; subnormal scales take the
-    // scalar path, which clamps.
-    const bool normal = s >= 6.103515625e-05f;  // 2^-14
-    const float2 nb = make_float2(-b, -b), rs2 = make_float2(rs, rs);
-    const float2 mg = make_float2(kMagic, kMagic), nmg = make_float2(-kMagic, -kMagic);
-    const float2 m1 = make_float2(-1.0f, -1.0f);
-    // Near-tie test without per-element compares: q = e * e - c with
-    // c = (0.5 - 2 * kTieWindow)^2 is one rounding of the exact value, so its
-    // sign is exact, and q >= 0 for every |e| >= 0.5 - kTieWindow (and for a
-    // few more, which only send their word to the exact rule).  The sign bits
-    // of a word's eight q are ANDed: a clear sign bit means some q >= 0.
-    constexpr float kFar = 0.5f - 2.0f * R::kTieWindow;
-    const float2 nc = make_float2(-kFar * kFar, -kFar * kFar);
+    const RecipBracket br = recip_bracket(rs);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {  // input word j: elements 8j .. 8j + 7
-        uint32_t w[2] = {0u, 0u};
-        uint32_t far_bits = 0x80000000u;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {  // two elements per paired fp32 operation
-            const float2 f = __half22float2(h[4 * j + k]);
-            const float2 d = __fadd2_rn(f, nb);                      // x - b
-            const float2 t = __fmul2_rn(d, rs2);                     // ~ d / s
-            const float2 r = __fadd2_rn(t, mg);                      // rint(t) in the low bits
-            const float2 e = __ffma2_rn(__fadd2_rn(r, nmg), m1, t);  // t - rint(t), exact
-            const float2 q = __ffma2_rn(e, e, nc);                   // < 0 unless near a tie
-            far_bits &= __float_as_uint(q.x) & __float_as_uint(q.y);
-            const int p = 2 * k * BITS;  // bit position of the pair within the word(s)
-            w[p / 32] = bfi(__float_as_uint(r.x), w[p / 32], p % 32, BITS);
-            w[(p + BITS) / 32] = bfi(__float_as_uint(r.y), w[(p + BITS) / 32], (p + BITS) % 32, BITS);
-        }
-        const bool near = far_bits == 0u;
-        if (near || !normal) {  // rare: redo the word with the exact scalar rule
-            const uint2 x = code_word_exact<BITS>(raw[j], b, s, rs);
-            w[0] = x.x;
-            w[1] = x.y;
-        }
-        codes[j * BITS / 4] = w[0];
-        if (BITS == 8) codes[j * BITS / 4 + 1] = w[1];
+        const uint2 x = quantize_word8<BITS>(raw[j], b, s, rs, br);
+        codes[j * BITS / 4] = x.x;
+        if (BITS == 8) codes[j * BITS / 4 + 1] = x.y;
     }
 }
 
