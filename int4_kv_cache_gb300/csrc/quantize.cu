@@ -6,14 +6,16 @@
 // with a per-group scale and bias).  The rounding rule is the one stated in
 // tq.h; every step is a single IEEE fp32 operation with round-to-nearest-even,
 // so codes, scales and biases are bit-identical to the CPU oracle.  The
-// per-element division is replaced by a multiply with the reciprocal wherever
-// that provably rounds to the same code (tq_quant.cuh).
+// per-element division is replaced by two fused multiply-adds with multipliers
+// bracketing 1/scale wherever they provably give the division's code
+// (tq_quant.cuh).
 //
-// Work split: one thread per (row, group of 64): it loads the group of K and
-// the group of V (eight 16-byte words each, all issued before any use), and
-// writes 32 bytes of codes per tensor and the four scale / bias halves.  With
-// no cross-lane reductions the per-group work (min/max, the scale division,
-// the reciprocal) is spread over 64 elements.
+// Work split: one thread per (row, group of 64): it takes the group of K and
+// the group of V (eight 16-byte words each) and writes 32 bytes of codes per
+// tensor and the four scale / bias halves.  With no cross-lane reductions the
+// per-group work (min/max, the scale division, the reciprocal) is spread over
+// 64 elements.  Small appends stage each warp's groups through shared memory
+// with coalesced loads; prefills stream 256-row tiles by TMA (below).
 #include <atomic>
 
 #include "tq_device.cuh"
@@ -263,9 +265,10 @@ __global__ void __launch_bounds__(kTmaThreads, 3)
 }
 
 // ------------------------------------------------------------------------
-// Rotated: the same one thread per (group of 64, K or V); a row's NG groups
-// sit in NG consecutive lanes ("Running and Evaluating TurboQuant optimized
-// Gemma 4", TurboQuant section: x -> H x / sqrt(D) before quantisation).  The
+// Rotated: the same one thread per group row (its K group, then its V group);
+// a head row's NG groups sit in NG consecutive lanes ("Running and Evaluating
+// TurboQuant optimized Gemma 4", TurboQuant section: x -> H x / sqrt(D) before
+// quantisation).  The
 // fast transform runs its stages in increasing order h = 1, 2, ..., D / 2,
 // each butterfly one round-to-nearest fp32 add or subtract, then the scale
 // and the fp16 rounding: the same operations as the sequential transform, so
