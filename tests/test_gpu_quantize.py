@@ -115,15 +115,16 @@ def test_prefill_full_128k_layer_bit_exact_sampled():
 @pytest.mark.parametrize("flags,bits,D", [(0, 4, 128), (3, 4, 128), (0, 8, 128), (1, 4, 64), (0, 4, 256),
                                           (2, 4, 256), (3, 8, 256), (3, 8, 128)])
 def test_large_append_tma_path_bit_exact(flags, bits, D):
-    """Appends of >= 8192 groups stream through the persistent TMA kernel:
+    """Appends of >= 8192 groups stream through the persistent TMA kernels:
     bit-exact against the oracle with a ragged last tile (the group count is
-    not a multiple of 128), with the rotation fused in, and for int8."""
+    not a multiple of the 256-row tile), with the rotation fused in (one or
+    both tensors), and for int8."""
     torch = need_gpu()
     import int4_kv_cache_gb300 as tq
 
     B, Hkv, S = 2, 3, 2731
     x = synth.decode_inputs(260 + D + flags, B, 2 * Hkv, Hkv, D, S, outliers=True)
-    assert (B * Hkv * S * (D // 64)) % 128 != 0 and B * Hkv * S * (D // 64) >= 8192
+    assert (B * Hkv * S * (D // 64)) % 256 != 0 and B * Hkv * S * (D // 64) >= 8192
     c = tq.KVCache(B, Hkv, D, 2736, bits=bits)
     tq.tq_quantize_kv_append(c, torch.from_numpy(x.k).cuda(), torch.from_numpy(x.v).cuda(),
                              torch.zeros(B, dtype=torch.int32, device="cuda"), flags=flags)
