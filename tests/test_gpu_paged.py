@@ -215,3 +215,33 @@ def test_advance_after_separate_append(paged):
         assert np.array_equal(wp.cpu().numpy(), pos + want * n_new)
         assert np.array_equal(lt.cpu().numpy(), pos + n_new + want * n_new)
     assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("flags,D,bits", [(3, 128, 4), (1, 64, 4), (2, 256, 8)])
+def test_paged_rotated_prefill_equals_oracle(flags, D, bits):
+    """A rotated prefill large enough for the persistent TMA kernels, into a
+    paged cache from a shuffled pool: the pages hold the oracle's codes,
+    scales and biases of the rotated rows, bit for bit."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    B, Hkv, S, P = 2, 4, 1500, 256
+    assert B * Hkv * S * (D // 64) >= 8192
+    x = synth.decode_inputs(170 + D + flags, B, 2 * Hkv, Hkv, D, S, outliers=True)
+    per = -(-S // P)
+    pages = B * per + 3
+    paged = tq.PagedKVCache(B, Hkv, D, P, pages, per, bits=bits)
+    paged.buffer.zero_()
+    perm = np.random.default_rng(D + flags).permutation(pages)[: B * per].reshape(B, per).astype(np.int32)
+    paged.block_table.copy_(torch.from_numpy(perm))
+    tq.tq_quantize_kv_append(paged, torch.from_numpy(x.k).cuda(), torch.from_numpy(x.v).cuda(),
+                             torch.zeros(B, dtype=torch.int32, device="cuda"), flags=flags)
+    torch.cuda.synchronize()
+    kk = oracle.rotate_rows_f16(x.k) if flags & 1 else x.k
+    vv = oracle.rotate_rows_f16(x.v) if flags & 2 else x.v
+    got = _gather(paged, perm, S)
+    for arrs, src in ((got[:3], kk), (got[3:], vv)):
+        codes, sc, bi = oracle.quantize_rows(src, bits=bits)
+        assert np.array_equal(arrs[0].view(np.uint8), codes)
+        assert np.array_equal(arrs[1].view(np.uint16), sc)
+        assert np.array_equal(arrs[2].view(np.uint16), bi)
