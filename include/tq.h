@@ -199,7 +199,9 @@ tq_status tq_kv_cache_carve_ex(tq_kv_cache* cache, void* base, int32_t batch,
  * Per group of 64 elements x_0..x_63 (fp32 arithmetic, round-to-nearest-even):
  *   mn, mx = min, max;  scale = fp16(fp32(mx - mn) / 15);  bias = fp16(mn)
  *   code_i = clamp(rint(fp32(x_i - bias) / float(scale)), 0, 15), or 0 when
- *   float(scale) == 0;  a zero minimum is stored as +0.
+ *   float(scale) == 0;  a zero minimum is stored as +0, and mx is the first
+ *   element holding the largest value (so a group of zeros opening with -0
+ *   stores scale -0).
  * Bit-identical to the CPU oracle.  Rows with an out-of-range write position
  * are skipped and TQ_DEV_WRITE_POS is set. */
 tq_status tq_quantize_kv_append(const tq_kv_cache* cache, const uint16_t* k_new,

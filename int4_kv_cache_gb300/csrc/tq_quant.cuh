@@ -31,9 +31,9 @@ struct QuantRule {
 // The scale and bias of a group from its minimum and maximum (fp32 values of
 // fp16 elements) and the sign bit of its first element: the stored scale is
 // fp16(fp32(max - min) / L) with a zero minimum taken as +0.  The rule's
-// maximum is the first element holding the largest value, so a group of
-// zeros only has the range (first element) - (+0): -0 when the group opens
-// with -0 (then the scale is -0), +0 otherwise.
+// maximum is the first element holding the largest value, so in a group of
+// zeros the range is (first element) - (+0): -0 when the group opens with -0
+// (the scale is then -0), +0 otherwise.
 template <int BITS>
 __device__ __forceinline__ void group_scale_bias(float mn, float mx, bool first_neg, __half& scale, __half& bias) {
     using R = QuantRule<BITS>;
