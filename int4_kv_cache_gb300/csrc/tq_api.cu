@@ -350,7 +350,7 @@ tq_status device_plan(const Store* cache, int max_seq_len, int chunk, tq_impl im
     // at least 95 % of the SMs (each SM's work the same as with three CTAs per
     // SM, without their staggered finish), or has one run per (sequence, kv
     // head) and so no merge at all, or covers at least 75 % with runs of at
-    // most 12 stages (the ramp of its four stages then dominates: fewer,
+    // most 12 stages (the ramp of its ring then dominates: fewer,
     // longer streams fill sooner).  Measured (steps of 20, Llama-70B heads):
     // 1 x 128K 31.5 us (three CTAs per SM: 32.7), 1 x 64K 20.3 (21.1),
     // 1 x 16K 12.0 (12.5), 8 x 8K 22.0 (23.0), 16 x 8K 33.8 (38.1); with
