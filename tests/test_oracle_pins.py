@@ -190,6 +190,32 @@ def test_quantize_degenerate_groups():
     assert s == 0 and np.all(codes == 0) and b == 0
 
 
+def test_quantize_group_of_zeros_scale_follows_first_element():
+    """All 64 elements are ±0: the rule's maximum is the first element holding
+    the largest value (a plain scan), so r = first - (+0) and the stored scale
+    is -0 exactly when the group opens with -0; codes 0 and bias +0 always.
+    The cases are written out by hand: which zero a scan keeps is the point."""
+    neg, pos = np.float16(-0.0), np.float16(0.0)
+    cases = [
+        (np.full(64, neg), 0x8000),                                  # all -0
+        (np.full(64, pos), 0x0000),                                  # all +0
+        (np.array([neg] + [pos] * 63, np.float16), 0x8000),          # -0 first
+        (np.array([pos] + [neg] * 63, np.float16), 0x0000),          # +0 first
+        (np.array([neg, pos] * 32, np.float16), 0x8000),
+        (np.array([pos, neg] * 32, np.float16), 0x0000),
+    ]
+    for x, want_scale in cases:
+        for bits in (4, 8):
+            codes, s, b = oracle.quantize_rows(x.reshape(1, 64), 64, bits)
+            assert int(s.reshape(-1)[0]) == want_scale, (x[:2], bits)
+            assert int(b.reshape(-1)[0]) == 0x0000
+            assert not codes.any()
+    # one nonzero element: the range is positive whatever the zeros' signs
+    x = np.array([neg] * 63 + [np.float16(-1.0)], np.float16)
+    _, s, _ = oracle.quantize_rows(x.reshape(1, 64), 64, 4)
+    assert int(s.reshape(-1)[0]) == int(np.float16(1.0 / 15).view(np.uint16))
+
+
 def test_quantize_signed_zero_minimum_is_positive_zero():
     # -0 and +0 both present at the minimum: the bias is +0 whichever comes first
     for first in (-0.0, 0.0):
