@@ -87,11 +87,11 @@ __device__ __forceinline__ void quantize_words_store(const AppendParams& p, cons
 // word j at slot j ^ r7) and store it into the cache row write_pos[b] + i.
 template <int BITS>
 __device__ __forceinline__ void quantize_store(const AppendParams& p, long long gi, int ng, const uint4* rowk,
-                                               const uint4* rowv, int r7, int t_first = 0, int t_last = 1) {
+                                               const uint4* rowv, int r7) {
     long long code_off, sb;
     if (!group_dst<BITS>(p, gi, ng, code_off, sb)) return;
 #pragma unroll 1
-    for (int t = t_first; t <= t_last; ++t) {  // 0: K, 1: V
+    for (int t = 0; t < 2; ++t) {  // 0: K, 1: V
         const uint4* src = t ? rowv : rowk;
         uint4 x[8];
 #pragma unroll
