@@ -12,6 +12,8 @@
   compared in full (every code, scale and bias bit for bit, every head of the
   output within the bar); every layer has seeded rows and its appended row
   compared bit for bit.
+* The Hadamard-rotated leg at 128K: the rotated prefill checked in full and
+  the rotated step against the oracle.
 """
 import math
 
@@ -157,3 +159,48 @@ def test_full_model_80_layers():
             assert np.array_equal(g_, w_), layer
         ref = oracle.attention(qh, oc, np.array([S], np.int32), ATTN)
         assert_close(_host(outs[layer]).astype(np.float64), ref, what=f"80-layer model, layer {layer}")
+
+
+def test_rotated_timed_step_128k():
+    """The bench's Hadamard-rotated leg at full size ("Running and Evaluating
+    TurboQuant optimized Gemma 4", TurboQuant section: K and V stored as
+    quantize(H x / sqrt(D))): the 128K prefill through the rotated TMA
+    kernel, every code, scale and bias bit for bit against the oracle's
+    rotate-then-quantize; then the step the bench times (flags K | V: the
+    query rotated in phase 1, the new row rotated before it is quantized, the
+    output rotated back by the reduce), every head against the oracle."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    S, flags = 131072, tq.TQ_ROTATE_K | tq.TQ_ROTATE_V
+    q, k, v, chans = synth.torch_decode_inputs(STEP_SEED + 77, B, HQ, HKV, D, S, outliers=True)
+    cache = tq.KVCache(B, HKV, D, S)
+    tq.tq_quantize_kv_append(cache, k, v, torch.zeros(B, dtype=torch.int32, device="cuda"), flags=flags)
+    torch.cuda.synchronize()
+    kh, vh = _host(k), _host(v)
+    del k, v
+    got = cache_arrays(cache)
+    for rows, arrs in ((kh, got[:3]), (vh, got[3:])):
+        wc, ws_, wb = oracle.quantize_rows(oracle.rotate_rows_f16(rows))
+        assert np.array_equal(arrs[0], wc)
+        assert np.array_equal(arrs[1], ws_)
+        assert np.array_equal(arrs[2], wb)
+    kn, vn = synth.append_tokens(STEP_SEED + 77, 0, B, HKV, D, 1, outliers=chans)
+    wp = torch.full((B,), S - 1, dtype=torch.int32, device="cuda")
+    lens = torch.full((B,), S, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = tq.tq_decode_step(cache, torch.from_numpy(kn).cuda(), torch.from_numpy(vn).cuda(), wp, q, lens, S, ATTN,
+                            workspace_for(B, HQ, HKV, D, S), chunk=512, status=st, flags=flags)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    kk = oracle.rotate_rows_f16(_with_row(kh, S - 1, kn))
+    vv = oracle.rotate_rows_f16(_with_row(vh, S - 1, vn))
+    for new, codes, scale, bias in ((kk, cache.k_codes, cache.k_scale, cache.k_bias),
+                                    (vv, cache.v_codes, cache.v_scale, cache.v_bias)):
+        wc, ws_, wb = oracle.quantize_rows(new[:, :, S - 1:S])
+        assert np.array_equal(_host(codes[:, :, S - 1:S]), wc)
+        assert np.array_equal(_host(scale[:, :, S - 1:S]).view(np.uint16), ws_)
+        assert np.array_equal(_host(bias[:, :, S - 1:S]).view(np.uint16), wb)
+    ref = oracle.attention(oracle.rotate_rows_f16(_host(q)), oracle.Cache.from_fp16(kk, vv), np.array([S], np.int32),
+                           ATTN)
+    assert_close(_host(out).astype(np.float64), oracle.hadamard(ref), what="rotated timed step S=131072")
