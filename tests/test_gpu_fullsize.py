@@ -12,8 +12,8 @@
   compared in full (every code, scale and bias bit for bit, every head of the
   output within the bar); every layer has seeded rows and its appended row
   compared bit for bit.
-* The Hadamard-rotated leg at 128K: the rotated prefill checked in full and
-  the rotated step against the oracle.
+* The Hadamard-rotated and the int8 legs at 128K: each prefill checked in
+  full and each timed step against the oracle.
 """
 import math
 
@@ -204,3 +204,37 @@ def test_rotated_timed_step_128k():
     ref = oracle.attention(oracle.rotate_rows_f16(_host(q)), oracle.Cache.from_fp16(kk, vv), np.array([S], np.int32),
                            ATTN)
     assert_close(_host(out).astype(np.float64), oracle.hadamard(ref), what="rotated timed step S=131072")
+
+
+def test_int8_timed_step_128k():
+    """The bench's int8 leg at full size ("Running and Evaluating TurboQuant
+    optimized Gemma 4", driver flag --kv-bits 8): the 128K int8 prefill
+    through the TMA kernel checked in full, then the timed step (the fused
+    one-row append at S - 1 and the decode) over every head."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    S = 131072
+    q, k, v, chans = synth.torch_decode_inputs(STEP_SEED + 90, B, HQ, HKV, D, S, outliers=True)
+    cache = tq.KVCache(B, HKV, D, S, bits=8)
+    tq.tq_quantize_kv_append(cache, k, v, torch.zeros(B, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    kh, vh = _host(k), _host(v)
+    del k, v
+    got = cache_arrays(cache)
+    for rows, arrs in ((kh, got[:3]), (vh, got[3:])):
+        wc, ws_, wb = oracle.quantize_rows(rows, 64, 8)
+        assert np.array_equal(arrs[0], wc)
+        assert np.array_equal(arrs[1], ws_)
+        assert np.array_equal(arrs[2], wb)
+    kn, vn = synth.append_tokens(STEP_SEED + 90, 0, B, HKV, D, 1, outliers=chans)
+    wp = torch.full((B,), S - 1, dtype=torch.int32, device="cuda")
+    lens = torch.full((B,), S, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = tq.tq_decode_step(cache, torch.from_numpy(kn).cuda(), torch.from_numpy(vn).cuda(), wp, q, lens, S, ATTN,
+                            workspace_for(B, HQ, HKV, D, S), chunk=512, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    kk, vv = _with_row(kh, S - 1, kn), _with_row(vh, S - 1, vn)
+    ref = oracle.attention(_host(q), oracle.Cache.from_fp16(kk, vv, bits=8), np.array([S], np.int32), ATTN)
+    assert_close(_host(out).astype(np.float64), ref, what="int8 timed step S=131072")
