@@ -14,6 +14,8 @@
   compared bit for bit.
 * The Hadamard-rotated and the int8 legs at 128K: each prefill checked in
   full and each timed step against the oracle.
+* The ragged batch of 32 sequences (1K-32K tokens), contiguous and paged:
+  one step as the bench's graph runs it, every head against the oracle.
 """
 import math
 
@@ -238,3 +240,52 @@ def test_int8_timed_step_128k():
     kk, vv = _with_row(kh, S - 1, kn), _with_row(vh, S - 1, vn)
     ref = oracle.attention(_host(q), oracle.Cache.from_fp16(kk, vv, bits=8), np.array([S], np.int32), ATTN)
     assert_close(_host(out).astype(np.float64), ref, what="int8 timed step S=131072")
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_ragged_batch_step_all_heads(paged):
+    """The bench's ragged leg: 32 sequences with lengths uniform in [1K, 32K]
+    (Llama heads), one step as the bench's graph runs it (append one token per
+    sequence at write_pos = len, decode over len + 1, lengths advanced on the
+    device, the longest-first run order of a multi-wave grid), on the
+    contiguous cache and on 256-token pages from a shuffled pool; every head
+    of every sequence against the oracle."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    Bt, P, smax = 32, 256, 32768
+    lens = synth.ragged_lengths(4, Bt, 1024, smax)
+    cap = smax + P
+    q, k, v, chans = synth.torch_decode_inputs(4, Bt, HQ, HKV, D, smax, outliers=True)
+    kn, vn = synth.append_tokens(4, 0, Bt, HKV, D, 1, outliers=chans)
+    zero = torch.zeros(Bt, dtype=torch.int32, device="cuda")
+    if paged:
+        per = [-(-(int(n) + 2) // P) for n in lens]
+        pages = sum(per) + 1
+        cache = tq.PagedKVCache(Bt, HKV, D, P, pages, cap // P)
+        bt = np.full((Bt, cap // P), pages - 1, np.int32)  # logical pages past a sequence: one scratch page
+        perm = np.random.default_rng(4).permutation(pages - 1)
+        nxt = 0
+        for b in range(Bt):
+            bt[b, :per[b]] = perm[nxt:nxt + per[b]]
+            nxt += per[b]
+        cache.block_table.copy_(torch.from_numpy(bt))
+    else:
+        cache = tq.KVCache(Bt, HKV, D, cap)
+    tq.tq_quantize_kv_append(cache, k, v, zero)
+    kh, vh = _host(k), _host(v)
+    del k, v
+    wp = torch.from_numpy(lens.copy()).cuda()
+    lt = torch.from_numpy(lens + 1).cuda()
+    max_len = int(lens.max()) + 2
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = tq.tq_decode_step(cache, torch.from_numpy(kn).cuda(), torch.from_numpy(vn).cuda(), wp, q, lt, max_len, ATTN,
+                            workspace_for(Bt, HQ, HKV, D, max_len), chunk=512, status=st, flags=tq.TQ_STEP_ADVANCE)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.array_equal(_host(wp), lens + 1) and np.array_equal(_host(lt), lens + 2)
+    for b in range(Bt):  # the appended token replaces row len of each sequence
+        kh[b, :, lens[b]] = kn[b, :, 0]
+        vh[b, :, lens[b]] = vn[b, :, 0]
+    ref = oracle.attention(_host(q), oracle.Cache.from_fp16(kh, vh), lens + 1, ATTN)
+    assert_close(_host(out).astype(np.float64), ref, what=f"ragged step paged={paged}")
