@@ -144,11 +144,11 @@ def test_int8_dequantize_bit_exact():
     c = _cache8(tq, torch, x.k, x.v)
     k16, v16 = tq.tq_dequantize_kv(c, 650)
     torch.cuda.synchronize()
-    kc, ks, kb, vc, vs, vb = cache_arrays(c)
+    oc = oracle.Cache.from_fp16(x.k, x.v, bits=8)  # the oracle's own codes (the GPU's are checked equal elsewhere)
     assert np.array_equal(k16.cpu().numpy().view(np.uint16),
-                          oracle.dequantize_rows_f16(kc[:, :, :650], ks[:, :, :650], kb[:, :, :650], bits=8))
+                          oracle.dequantize_rows_f16(oc.kc[:, :, :650], oc.ks[:, :, :650], oc.kb[:, :, :650], bits=8))
     assert np.array_equal(v16.cpu().numpy().view(np.uint16),
-                          oracle.dequantize_rows_f16(vc[:, :, :650], vs[:, :, :650], vb[:, :, :650], bits=8))
+                          oracle.dequantize_rows_f16(oc.vc[:, :, :650], oc.vs[:, :, :650], oc.vb[:, :, :650], bits=8))
 
 
 @pytest.mark.parametrize("name", ["gemma_33", "gemma_423", "gemma_786", "gemma_950"])
