@@ -4,7 +4,7 @@
 //
 // Per (b, h):  M = max_c m_c over parts with l_c > 0,  w_c = e^{m_c - M},
 //              out = sum_c w_c acc_c / sum_c w_c l_c   (fp16, RNE; 0 if empty)
-// One CTA per (b, h): reduce_fast_kernel for up to 32 parts (one round trip,
+// One CTA per (b, h): reduce_fast_kernel for up to 64 parts (one round trip,
 // no barriers), reduce_kernel otherwise and for the output rotation.
 // Launched as a programmatic dependent of phase 1, each waits for phase 1's
 // memory before the first read.
@@ -251,9 +251,8 @@ cudaError_t fast_attrs() {
     cudaGetDevice(&dev);
     const bool cache = dev >= 0 && dev < 64;
     if (cache && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-    cudaError_t e = cudaSuccess;
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(reduce_fast_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFastSmemPad);
+    cudaError_t e =
+        cudaFuncSetAttribute(reduce_fast_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFastSmemPad);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(reduce_fast_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFastSmemPad);
     if (e == cudaSuccess)
