@@ -4,8 +4,9 @@
 //
 // Per (b, h):  M = max_c m_c over parts with l_c > 0,  w_c = e^{m_c - M},
 //              out = sum_c w_c acc_c / sum_c w_c l_c   (fp16, RNE; 0 if empty)
-// One CTA per (b, h): reduce_fast_kernel for up to 64 parts (one round trip,
-// no barriers), reduce_kernel otherwise and for the output rotation.
+// One CTA per (b, h): reduce_fast_kernel for up to 64 parts (one round trip;
+// barriers only for the output rotation's cross-warp stages), reduce_kernel
+// beyond.
 // Launched as a programmatic dependent of phase 1, each waits for phase 1's
 // memory before the first read.
 #include <math.h>
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReducePara
 //   w_c = expf(m_c - M),
 //   L = xor-tree warp sum of fmaf(w_c, l_c, 0) + fmaf(w_c+32, l_c+32, 0),
 //   t = sum over parts in order of fmaf(w_c, acc_c, 0) (w_c = 0 skipped),
-// no shared memory and no CTA barrier.  Up to 32 parts M, w and L are
+// no CTA barrier (but for ROT below).  Up to 32 parts M, w and L are
 // reduce_kernel's (its block reduction sees the same 32 values, the other
 // warps' zeros added exactly), and t its too up to 8 parts (one part per warp
 // there), so the two give the same bits up to 8 parts, as does the cluster
@@ -168,13 +169,21 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReducePara
 // Each CTA therefore reserves kFastSmemPad bytes of shared memory it does not
 // use, so that at most two share an SM (grids of up to two CTAs per SM; a
 // batch's larger grid runs unpadded: ragged batch of 32, 110.7 -> 106.7 us).
+//   ROT (values stored rotated): the output is H applied to the merged fp32
+// output, then the scale and one fp16 rounding, with the stages in increasing
+// order h = 1, 2, ..., D / 2 and each butterfly one round-to-nearest add or
+// subtract, as in reduce_kernel: element d = thread + j * TH, so stages
+// h < 32 pair lanes (shuffles), 32 <= h < TH pair warps (shared memory) and
+// h = TH (head_dim 256) pairs a thread's two elements.  Given the same merged
+// values both rotate to the same bits.
 constexpr int kFastParts = 64;
 constexpr int kFastSmemPad = 100 * 1024;
 
-template <int D>
+template <int D, bool ROT>
 __global__ void __launch_bounds__(D < 128 ? D : 128) reduce_fast_kernel(const ReduceParams p) {
     constexpr int TH = D < 128 ? D : 128;
     constexpr int DPT = D / TH;  // head_dim elements per thread
+    __shared__ float xs[ROT ? D : 1];  // ROT: one cross-warp stage's values
     pdl_wait_primary();
     // phase 1 is complete: an eager next step's phase 1 may launch now (it
     // waits for this grid before its first read)
@@ -221,10 +230,41 @@ __global__ void __launch_bounds__(D < 128 ? D : 128) reduce_fast_kernel(const Re
             for (int j = 0; j < DPT; ++j) t[j] += fmaf(wc, a[c][j], 0.0f);
         }
     }
+    float o[DPT];
 #pragma unroll
-    for (int j = 0; j < DPT; ++j)
-        p.out[bh * D + threadIdx.x + j * TH] =
-            __half_as_ushort(__float2half_rn(L > 0.0f ? __fdiv_rn(t[j], L) : 0.0f));
+    for (int j = 0; j < DPT; ++j) o[j] = L > 0.0f ? __fdiv_rn(t[j], L) : 0.0f;
+    if constexpr (ROT) {
+        const int x = threadIdx.x;
+#pragma unroll
+        for (int h = 1; h < 32; h <<= 1) {  // the partner element in lane ^ h
+#pragma unroll
+            for (int j = 0; j < DPT; ++j) {
+                const float other = __shfl_xor_sync(0xffffffffu, o[j], h);
+                o[j] = (x & h) != 0 ? __fsub_rn(other, o[j]) : __fadd_rn(o[j], other);
+            }
+        }
+#pragma unroll
+        for (int h = 32; h < TH; h <<= 1) {  // the partner element in another warp
+#pragma unroll
+            for (int j = 0; j < DPT; ++j) xs[x + j * TH] = o[j];
+            __syncthreads();
+#pragma unroll
+            for (int j = 0; j < DPT; ++j) {
+                const float other = xs[(x ^ h) + j * TH];
+                o[j] = (x & h) != 0 ? __fsub_rn(other, o[j]) : __fadd_rn(o[j], other);
+            }
+            __syncthreads();
+        }
+        if constexpr (DPT == 2) {  // h = TH: this thread's elements x and x + TH
+            const float u = o[0], w = o[1];
+            o[0] = __fadd_rn(u, w);
+            o[1] = __fsub_rn(u, w);
+        }
+#pragma unroll
+        for (int j = 0; j < DPT; ++j) o[j] = __fmul_rn(o[j], p.rot_scale);
+    }
+#pragma unroll
+    for (int j = 0; j < DPT; ++j) p.out[bh * D + threadIdx.x + j * TH] = __half_as_ushort(__float2half_rn(o[j]));
 }
 
 // TQ_STEP_ADVANCE after a step whose append ran as its own kernel: a plain
@@ -251,12 +291,13 @@ cudaError_t fast_attrs() {
     cudaGetDevice(&dev);
     const bool cache = dev >= 0 && dev < 64;
     if (cache && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-    cudaError_t e =
-        cudaFuncSetAttribute(reduce_fast_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFastSmemPad);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(reduce_fast_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFastSmemPad);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(reduce_fast_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFastSmemPad);
+    using Kern = void (*)(ReduceParams);
+    const Kern kerns[6] = {reduce_fast_kernel<64, false>,  reduce_fast_kernel<128, false>,
+                           reduce_fast_kernel<256, false>, reduce_fast_kernel<64, true>,
+                           reduce_fast_kernel<128, true>,  reduce_fast_kernel<256, true>};
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < 6 && e == cudaSuccess; ++i)
+        e = cudaFuncSetAttribute(kerns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, kFastSmemPad);
     if (e == cudaSuccess && cache) done[dev].store(true, std::memory_order_release);
     return e;
 }
@@ -272,7 +313,7 @@ cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl_s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_secondary ? 1 : 0;
-    if (!p.rotate_out && p.n_parts <= kFastParts) {
+    if (p.n_parts <= kFastParts) {
         cfg.blockDim = dim3(p.head_dim < 128 ? p.head_dim : 128);
         // the spreading pad only while the grid fits in two CTAs per SM: a
         // larger grid (a batch) runs in waves anyway, and padded CTAs would
@@ -289,12 +330,16 @@ cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream, bool pdl_s
         cfg.dynamicSmemBytes = cfg.gridDim.x <= 2u * static_cast<unsigned>(sms) ? kFastSmemPad : 0;
         const cudaError_t e = fast_attrs();
         if (e != cudaSuccess) return e;
+        using Kern = void (*)(ReduceParams);
+        Kern k = nullptr;
+        const bool rot = p.rotate_out != 0;
         switch (p.head_dim) {
-            case 64: return cudaLaunchKernelEx(&cfg, reduce_fast_kernel<64>, p);
-            case 128: return cudaLaunchKernelEx(&cfg, reduce_fast_kernel<128>, p);
-            case 256: return cudaLaunchKernelEx(&cfg, reduce_fast_kernel<256>, p);
+            case 64: k = rot ? reduce_fast_kernel<64, true> : reduce_fast_kernel<64, false>; break;
+            case 128: k = rot ? reduce_fast_kernel<128, true> : reduce_fast_kernel<128, false>; break;
+            case 256: k = rot ? reduce_fast_kernel<256, true> : reduce_fast_kernel<256, false>; break;
             default: return cudaErrorInvalidValue;
         }
+        return cudaLaunchKernelEx(&cfg, k, p);
     }
     switch (p.head_dim) {
         case 64: return cudaLaunchKernelEx(&cfg, reduce_kernel<64>, p);

@@ -9,6 +9,7 @@ import pytest
 
 import oracle
 from int4_kv_cache_gb300 import synth
+from tests.fwht_f32 import sequential_transform_f32
 from tests.gpu_helpers import assert_close, cache_arrays, gpu_cache_from_fp16, need_gpu, workspace_for
 
 pytestmark = pytest.mark.gpu
@@ -157,3 +158,39 @@ def test_rotated_step_stores_oracle_rows(D, bits, flags, n_new, paged):
     full = types.SimpleNamespace(q=x.q, k=k_all, v=v_all)
     assert_close(out.float().cpu().numpy(), _rotated_reference(full, lens, 1 / math.sqrt(D), flags, bits),
                  what=f"rotated step D={D} bits={bits} flags={flags} n_new={n_new} paged={paged}")
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_reduce_rotates_the_merged_output_bit_for_bit(D):
+    """TQ_ROTATE_V: the decode applies H to the merged fp32 output, then the
+    scale fp32(1 / sqrt(D)) and one fp16 rounding (tq.h, rotation flags).  With
+    one run per sequence the merged output is fp32(acc / l) of phase 1's own
+    state (the weight is expf(0) = 1; the sum starts from +0), so the same
+    transform restated in numpy float32 from that state must give the decode's
+    output bit for bit, whichever threads, lanes and warps the reduce spreads
+    the stages over.  A consistency check of the rotation step; parity with
+    the oracle is test_rotated_decode_matches_oracle."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    B, Hq, Hkv, S = 3, 16, 2, 60  # within one tile at every head_dim: one run
+    lens = np.array([60, 37, 0], np.int32)
+    x = synth.decode_inputs(140 + D, B, Hq, Hkv, D, S, lens=lens, outliers=True)
+    cache = tq.KVCache(B, Hkv, D, 64)
+    tq.tq_quantize_kv_append(cache, torch.from_numpy(x.k).cuda(), torch.from_numpy(x.v).cuda(),
+                             torch.zeros(B, dtype=torch.int32, device="cuda"), flags=tq.TQ_ROTATE_V)
+    q, lt = torch.from_numpy(x.q).cuda(), torch.from_numpy(lens).cuda()
+    a = 1 / math.sqrt(D)
+    assert tq.tq_sdpa_plan(cache, Hq, S)[0] == 1
+    out = tq.tq_sdpa_int4_decode(cache, q, lt, S, a, workspace_for(B, Hq, Hkv, D, S), flags=tq.TQ_ROTATE_V)
+    _, l, acc = tq.tq_sdpa_int4_partial(cache, q, lt, S, a, chunks_per_split=0)
+    l = l.cpu().numpy()[:, :, 0]
+    acc = acc.cpu().numpy()[:, :, 0, :]
+    z = np.float32(0.0)
+    t = (acc + z) + z  # the reduce's t = 0 + fmaf(1, acc, 0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        o = np.where(l[..., None] > 0, t / l[..., None], z).astype(np.float32)
+    rs = np.float32(1.0 / np.sqrt(np.float64(D)))
+    want = (sequential_transform_f32(o) * rs).astype(np.float16)
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), want.view(np.uint16))
+    assert np.all(want[2] == 0)
