@@ -217,6 +217,45 @@ def test_advance_after_separate_append(paged):
     assert np.array_equal(outs[0], outs[1])
 
 
+@pytest.mark.parametrize("paged", [False, True])
+@pytest.mark.parametrize("n_new", [1, 20])  # the append fused into phase 1; its own kernel
+def test_advance_with_rotation(paged, n_new):
+    """TQ_STEP_ADVANCE on a rotated cache (TQ_ROTATE_K | TQ_ROTATE_V): the
+    reduce both rotates the merged output and advances the lengths.  Same
+    output as the step without the flag (both plan without merging), the
+    rows stored the same, lengths advanced by n_new."""
+    torch = need_gpu()
+    import int4_kv_cache_gb300 as tq
+
+    B, Hq, Hkv, D, S = 2, 16, 2, 128, 1024
+    rot = tq.TQ_ROTATE_K | tq.TQ_ROTATE_V
+    x = synth.decode_inputs(185 + n_new, B, Hq, Hkv, D, S, outliers=True)
+    kn, vn = synth.append_tokens(185, 2, B, Hkv, D, n_new, outliers=x.outlier_channels)
+    pos = np.array([600, 1000 - n_new], np.int32)
+    outs, caches = [], []
+    for flags in (rot, rot | tq.TQ_STEP_ADVANCE):
+        if paged:
+            c, _ = _paged_like(tq, torch, B, Hkv, D, S, 128, seed=186)
+        else:
+            c = tq.KVCache(B, Hkv, D, S)
+        tq.tq_quantize_kv_append(c, torch.from_numpy(x.k).cuda(), torch.from_numpy(x.v).cuda(),
+                                 torch.zeros(B, dtype=torch.int32, device="cuda"), flags=rot)
+        wp, lt = torch.from_numpy(pos.copy()).cuda(), torch.from_numpy(pos + n_new).cuda()
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        o = tq.tq_decode_step(c, torch.from_numpy(kn).cuda(), torch.from_numpy(vn).cuda(), wp,
+                              torch.from_numpy(x.q).cuda(), lt, S, 0.088, workspace_for(B, Hq, Hkv, D, S),
+                              status=st, flags=flags)
+        outs.append(o.float().cpu().numpy())
+        caches.append(c)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        want = n_new if flags & tq.TQ_STEP_ADVANCE else 0
+        assert np.array_equal(wp.cpu().numpy(), pos + want)
+        assert np.array_equal(lt.cpu().numpy(), pos + n_new + want)
+    assert np.array_equal(outs[0], outs[1])
+    assert torch.equal(caches[0].buffer, caches[1].buffer)
+
+
 @pytest.mark.parametrize("flags,D,bits", [(3, 128, 4), (1, 64, 4), (2, 256, 8)])
 def test_paged_rotated_prefill_equals_oracle(flags, D, bits):
     """A rotated prefill large enough for the persistent TMA kernels, into a
