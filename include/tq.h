@@ -350,8 +350,9 @@ tq_status tq_decode_step(const tq_kv_cache* cache, const uint16_t* k_new,
 /* Decode over a cache written with rotation flags (the same flags as its
  * appends): TQ_ROTATE_K rotates the query (into the workspace) before phase
  * 1; TQ_ROTATE_V applies H to the merged output before its fp16 rounding.
- * Otherwise as tq_sdpa_int4_decode / tq_decode_step (a rotated append always
- * runs the append kernel, with the decode as its programmatic dependent). */
+ * Otherwise as tq_sdpa_int4_decode / tq_decode_step (a rotated step appends
+ * its rows inside the decode kernel like an unrotated one, rotating each row
+ * across the lanes that hold it). */
 tq_status tq_sdpa_int4_decode_ex(const tq_kv_cache* cache, const uint16_t* q,
                                  int32_t num_q_heads, const int32_t* seq_lens,
                                  int32_t max_seq_len, float attn_scale, int32_t chunk,

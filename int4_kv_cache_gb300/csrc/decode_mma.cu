@@ -350,11 +350,22 @@ __global__ void __launch_bounds__(Cfg<D, BITS, WIDE>::THREADS, Cfg<D, BITS, WIDE
     // finish); its latency overlaps the tile and Q loads.
     const int app_tasks = (app_hi - app_lo) * NG * 2;  // eight lanes per (row, group, K|V)
     const int app_part = threadIdx.x & 7;
+    // A row's 2 NG tasks are consecutive.  Up to head_dim 128 the K and V
+    // tasks of a group are neighbours; at head_dim 256 the row's four K
+    // groups come first, then its four V groups, so that each tensor's row
+    // fills the 32 lanes of one warp (which its rotation spans).
+    struct AppTask {
+        int kv, g, r;
+    };
+    auto app_task = [&](int task) -> AppTask {
+        if constexpr (NG == 4) return {(task >> 2) & 1, task & 3, app_lo + (task >> 3)};
+        else return {task & 1, (task >> 1) % NG, app_lo + (task >> 1) / NG};
+    };
     auto app_src = [&](int task) {
-        const int kv = task & 1, g = (task >> 1) % NG, r = app_lo + (task >> 1) / NG;
-        return (kv ? p.app.v_new : p.app.k_new) +
-               (((static_cast<long long>(b) * p.num_kv_heads + kvh) * p.app.n_new + (r - app_wp)) * D + g * kGroup +
-                app_part * 8);
+        const AppTask a = app_task(task);
+        return (a.kv ? p.app.v_new : p.app.k_new) +
+               (((static_cast<long long>(b) * p.num_kv_heads + kvh) * p.app.n_new + (a.r - app_wp)) * D +
+                a.g * kGroup + app_part * 8);
     };
     uint4 app_raw = make_uint4(0, 0, 0, 0);
     if (static_cast<int>(threadIdx.x >> 3) < app_tasks)
@@ -489,34 +500,38 @@ __global__ void __launch_bounds__(Cfg<D, BITS, WIDE>::THREADS, Cfg<D, BITS, WIDE
     // The fused append, part 2: quantize the rows this run owns, publish them
     // to the async proxy, then load the first tiles that use them.
     if (app_lo < app_hi) {  // the same for the whole CTA
+        static_assert((C::THREADS / 8) % (2 * NG) == 0, "a pass covers whole rows: a tensor's row starts a warp");
         for (int t0 = 0; t0 < app_tasks; t0 += C::THREADS / 8) {  // uniform trip count: shuffles inside
             const int task = t0 + (threadIdx.x >> 3);
             const bool valid = task < app_tasks;
             uint4 raw = app_raw;
             if (t0 > 0 && valid) raw = __ldcs(reinterpret_cast<const uint4*>(app_src(task)));
-            if constexpr (NG <= 2) {
-                if (p.app.flags != 0) {  // the same for the whole CTA: rows are stored rotated
-                    // A row's K (or V) sits in 8 NG lanes: element 64 g + 8 part + j.
-                    // Stages h = 1, 2, 4 in the lane, h = 8, 16, 32 across lane bits
-                    // 0-2 (part), h = 64 across lane bit 4 (g).  (Head dims above
-                    // 128 span two warps; their rotated appends run the append kernel.)
-                    float v[8];
-                    halves_to_floats<8>(&raw, v);
-                    hadamard_in_lane<8>(v);
+            if (p.app.flags != 0) {  // the same for the whole CTA: rows are stored rotated
+                // A row's K (or V) sits in 8 NG lanes of one warp: element
+                // 64 g + 8 part + j.  Stages h = 1, 2, 4 in the lane, h = 8, 16,
+                // 32 across lane bits 0-2 (part), then h = 64 across lane bit 4
+                // (g, head_dim 128: K and V interleaved) or h = 64, 128 across
+                // lane bits 3 and 4 (g, head_dim 256).
+                float v[8];
+                halves_to_floats<8>(&raw, v);
+                hadamard_in_lane<8>(v);
 #pragma unroll
-                    for (int hl = 1; hl < 8; hl <<= 1) hadamard_across_lanes<8>(v, lane, hl);
-                    if constexpr (NG == 2) hadamard_across_lanes<8>(v, lane, 16);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], p.app.rot_scale);
-                    uint4 rot;
-                    floats_to_halves<8>(v, &rot);
-                    const bool v_lane = ((threadIdx.x >> 3) & 1) != 0;  // task & 1
-                    if ((p.app.flags & (v_lane ? TQ_ROTATE_V : TQ_ROTATE_K)) != 0) raw = rot;
+                for (int hl = 1; hl < 8; hl <<= 1) hadamard_across_lanes<8>(v, lane, hl);
+                if constexpr (NG == 2) hadamard_across_lanes<8>(v, lane, 16);
+                if constexpr (NG == 4) {
+                    hadamard_across_lanes<8>(v, lane, 8);
+                    hadamard_across_lanes<8>(v, lane, 16);
                 }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], p.app.rot_scale);
+                uint4 rot;
+                floats_to_halves<8>(v, &rot);
+                if ((p.app.flags & (app_task(task).kv ? TQ_ROTATE_V : TQ_ROTATE_K)) != 0) raw = rot;
             }
             const GroupQ<BITS> gq = quantize_lane8<BITS>(raw);
             if (valid) {
-                const int kv = task & 1, g = (task >> 1) % NG, r = app_lo + (task >> 1) / NG;
+                const AppTask a = app_task(task);
+                const int kv = a.kv, g = a.g, r = a.r;
                 long long row;
                 if constexpr (PAGED) row = kv_row(p.map, p.num_kv_heads, b, kvh, r, p.status);
                 else row = row_base + r;

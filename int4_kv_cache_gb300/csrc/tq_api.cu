@@ -712,8 +712,7 @@ tq_status decode_path(const Store* cache, const uint16_t* k_new, const uint16_t*
     // wider heads, run the append kernel; the decode starts early and waits
     // only for the tiles that hold the new rows.
     const tq::AppendParams ap = append_params(cache, k_new, v_new, n_new, write_pos, status, flags);
-    const bool fused = n_new > 0 && n_new <= tq::kFusedAppendMaxRows && ph1 == TQ_IMPL_MMA &&
-                       (flags == 0 || cache->head_dim <= 128);
+    const bool fused = n_new > 0 && n_new <= tq::kFusedAppendMaxRows && ph1 == TQ_IMPL_MMA;
     if (n_new > 0 && !fused) {
         s = cuda_status(tq::launch_quantize_append_primary(ap, st));
         if (s != TQ_OK) return s;

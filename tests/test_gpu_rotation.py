@@ -105,13 +105,15 @@ def test_rotated_step_equals_append_then_decode():
 
 @pytest.mark.parametrize("D,bits,flags,n_new,paged", [
     (128, 4, 3, 1, False), (128, 4, 1, 3, False), (128, 4, 2, 1, False), (64, 4, 3, 2, False),
-    (128, 8, 3, 1, False), (64, 8, 1, 1, False), (256, 4, 3, 1, False), (128, 4, 3, 2, True)])
+    (128, 8, 3, 1, False), (64, 8, 1, 1, False), (256, 4, 3, 1, False), (128, 4, 3, 2, True),
+    (256, 8, 3, 2, False), (256, 4, 1, 3, True), (256, 4, 2, 16, False), (128, 4, 3, 17, False)])
 def test_rotated_step_stores_oracle_rows(D, bits, flags, n_new, paged):
-    # A rotated step appends its rows inside the decode kernel for head dims
-    # up to 128 (rotation across the lanes that hold a row) and through the
-    # append kernel above: either way the stored rows are the oracle's
-    # quantised fp16(H x / sqrt(D)) bit for bit, and the output is the
-    # rotated attention within the output tolerance.
+    # A rotated step of up to 16 rows appends them inside the decode kernel
+    # (each tensor's row rotated across the warp lanes that hold it; at
+    # head_dim 256 a whole warp), longer ones through the append kernel:
+    # either way the stored rows are the oracle's quantised fp16(H x /
+    # sqrt(D)) bit for bit, and the output is the rotated attention within the
+    # output tolerance.
     torch = need_gpu()
     import int4_kv_cache_gb300 as tq
 
